@@ -1,0 +1,421 @@
+"""Pins of the oracle against things other than itself: hand-worked closed
+forms, library routines for the number formats and norms, invariants of the
+routing rule, brute force on tiny experts. CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- formats
+
+def test_bf16_decode_matches_torch():
+    bits = np.arange(0, 65536, 7, dtype=np.uint32).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    got = O.bf16_to_f64(bits)
+    finite = np.isfinite(want)
+    assert np.array_equal(got[finite], want[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+
+
+def test_round_bf16_matches_torch_on_fp32_inputs():
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        np.array([0.0, -0.0, 1.0, 1.00390625, 1.005859375, 3e38, -3.4e38])])
+    v = v.astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
+    got = O.round_bf16(v.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_round_bf16_ties_to_even_on_exact_midpoints():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties go to the even mantissa (1.0);
+    # 1 + 3*2^-8 lies between 1 + 2^-7 (odd) and 1 + 2^-6 (even).
+    assert O.round_bf16(1 + 2.0 ** -8) == 1.0
+    assert O.round_bf16(1 + 3 * 2.0 ** -8) == 1 + 2.0 ** -6
+    assert O.round_bf16(1 + 2.0 ** -8 + 2.0 ** -40) == 1 + 2.0 ** -7
+    # a direct fp64 rounding (no detour through fp32, which would double-round)
+    assert O.round_bf16(1 + 2.0 ** -8 + 2.0 ** -30) == 1 + 2.0 ** -7
+
+
+def test_bf16_bits_roundtrip():
+    bits = np.arange(0, 0x7F80, 3, dtype=np.uint16)
+    assert np.array_equal(O.f64_to_bf16_bits(O.bf16_to_f64(bits)), bits)
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = O.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert O.e4m3_decode(np.array([0x7E]))[0] == 448.0
+    assert O.e4m3_decode(np.array([0x01]))[0] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(1)
+    v = (rng.standard_normal(50000) * 2.0 ** rng.integers(-12, 9, 50000)).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.e4m3_encode(v.astype(np.float64))
+    # torch keeps the sign of a value that rounds to zero; compare values for zeros
+    same = (got == want) | ((O.e4m3_decode(got) == 0) & (O.e4m3_decode(want) == 0))
+    assert same.all()
+
+
+def test_e4m3_encode_saturates():
+    assert list(O.e4m3_encode(np.array([448.0, 449.0, 470.0, 1e6, -1e6, -500.0]))) == [
+        0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+
+
+def test_e2m1_table_matches_the_minifloat_definition():
+    # e2m1: sign bit, 2 exponent bits with bias 1, 1 mantissa bit; exponent
+    # field 0 is subnormal with exponent 1 - bias = 0.
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        mag = 2.0 ** (e - 1) * (1 + m / 2) if e else (m / 2)
+        want = -mag if s else mag
+        assert O.e2m1_decode(np.array([code]))[0] == want
+        assert math.copysign(1, O.e2m1_decode(np.array([code]))[0]) == (-1 if s else 1)
+
+
+def test_ue8m0_decode_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e8m0fnu).double().numpy()
+    got = O.ue8m0_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_fp4_nibble_order():
+    # element 2j in the low nibble of byte j
+    assert list(O.unpack_fp4(np.array([[0x21, 0xF3]], np.uint8))[0]) == [1, 2, 3, 15]
+
+
+# ---------------------------------------------------------------- norms
+
+def test_rms_norm_matches_torch():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((5, 64)) * 3
+    w = 1 + 0.05 * rng.standard_normal(64)
+    want = torch.nn.functional.rms_norm(torch.from_numpy(v), (64,), torch.from_numpy(w),
+                                        eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(v, w, 1e-6), want, rtol=1e-13, atol=0)
+
+
+def test_rms_norm_invariants():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((3, 100))
+    eps = 1e-3
+    n = O.rms_norm(v, 1.0, eps)
+    ms = (v * v).mean(axis=-1)
+    np.testing.assert_allclose((n * n).mean(axis=-1), ms / (ms + eps), rtol=1e-12)
+    np.testing.assert_allclose(O.rms_norm(7.5 * v, 1.0, 0.0), O.rms_norm(v, 1.0, 0.0),
+                               rtol=1e-12)
+    assert np.all(O.rms_norm(np.zeros((1, 8)), 1.0, 1e-6) == 0)
+
+
+# ---------------------------------------------------------------- routing
+
+def _load_cases():
+    with open(os.path.join(GOLDEN, "routing_hand_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _load_cases(), ids=lambda c: c["name"])
+def test_routing_hand_cases(case):
+    r = O.route(O.round_f32(np.array(case["logits"])), np.array(case["bias"], np.float32),
+                case["top_k"], case["route_scale"], case["multiplier"], case["score"],
+                case["division_eps"])
+    assert r.ids.tolist() == case["ids"]
+    np.testing.assert_allclose(r.weights, case["weights"], rtol=2e-7, atol=0)
+
+
+def _random_logits(seed, b=16, E=32, scale=2.0):
+    rng = np.random.default_rng(seed)
+    return O.round_f32(rng.standard_normal((b, E)) * scale), rng
+
+
+@pytest.mark.parametrize("score", ["sigmoid", "softmax"])
+@pytest.mark.parametrize("eps", [None, 1e-20, 1e-3])
+def test_routing_weights_sum(score, eps):
+    logits, rng = _random_logits(4)
+    bias = rng.uniform(-0.1, 0.1, 32).astype(np.float32)
+    r = O.route(logits, bias, 6, 2.5, 0.5, score, eps)
+    rows = np.arange(16)[:, None]
+    S = r.scores[rows, r.ids].sum(axis=-1)
+    want = 2.5 * S / (S + (np.float32(eps) if eps is not None else 0.0))
+    np.testing.assert_allclose(r.weights.sum(axis=-1), want, rtol=1e-6)
+
+
+def test_routing_ids_unique_and_in_range():
+    logits, rng = _random_logits(5, b=64, E=128)
+    r = O.route(logits, rng.uniform(-0.1, 0.1, 128).astype(np.float32), 8, 2.5, None,
+                "sigmoid", None)
+    assert r.ids.dtype == np.int32
+    assert ((r.ids >= 0) & (r.ids < 128)).all()
+    assert all(len(set(row)) == 8 for row in r.ids.tolist())
+    # ids are in descending selection order, and every unselected score is lower
+    rows = np.arange(64)[:, None]
+    sel = r.selection[rows, r.ids]
+    assert (np.diff(sel, axis=-1) <= 0).all()
+    mask = np.ones_like(r.selection, dtype=bool)
+    mask[rows, r.ids] = False
+    assert (r.selection[mask].reshape(64, -1).max(axis=-1) <= sel[:, -1]).all()
+
+
+def test_bias_changes_selection_never_the_weight_formula():
+    logits, rng = _random_logits(6, b=32, E=16)
+    b1 = rng.uniform(-0.1, 0.1, 16).astype(np.float32)
+    b2 = b1.copy()
+    b2[3] += np.float32(0.5)                   # expert 3 becomes much easier to select
+    r1 = O.route(logits, b1, 4, 2.5, None, "sigmoid", 1e-20)
+    r2 = O.route(logits, b2, 4, 2.5, None, "sigmoid", 1e-20)
+    assert (r1.ids != r2.ids).any()            # the bias did move some selections
+    same = (r1.ids == r2.ids).all(axis=-1)
+    assert same.any()
+    np.testing.assert_array_equal(r1.weights[same], r2.weights[same])
+    # the weights only ever use the unbiased scores: gather them directly
+    rows = np.arange(32)[:, None]
+    s = r2.scores[rows, r2.ids]
+    np.testing.assert_allclose(r2.weights, 2.5 * s / s.sum(-1, keepdims=True), rtol=1e-6)
+
+
+def test_uniform_bias_shift_keeps_ids():
+    logits, rng = _random_logits(7, b=32, E=32)
+    bias = rng.uniform(-0.1, 0.1, 32).astype(np.float32)
+    r1 = O.route(logits, bias, 5, 2.5, None, "sigmoid", None)
+    r2 = O.route(logits, bias + np.float32(0.25), 5, 2.5, None, "sigmoid", None)
+    clear = r1.gap > 1e-5
+    np.testing.assert_array_equal(r1.ids[clear], r2.ids[clear])
+
+
+def test_routing_permutation_equivariance():
+    logits, rng = _random_logits(8, b=16, E=32)
+    bias = rng.uniform(-0.1, 0.1, 32).astype(np.float32)
+    perm = rng.permutation(32)
+    r1 = O.route(logits, bias, 4, 2.5, None, "softmax", 1e-6)
+    r2 = O.route(logits[:, perm], bias[perm], 4, 2.5, None, "softmax", 1e-6)
+    clear = r1.gap > 1e-6
+    np.testing.assert_array_equal(perm[r2.ids][clear], r1.ids[clear])
+    np.testing.assert_allclose(r2.weights[clear], r1.weights[clear], rtol=1e-6)
+
+
+def test_scores_match_scipy_and_full_topk_reduces_to_softmax():
+    logits, _ = _random_logits(9, b=8, E=16)
+    r = O.route(logits, np.zeros(16, np.float32), 16, 2.5, None, "softmax", 1e-6)
+    sm = scipy.special.softmax(logits, axis=-1)
+    np.testing.assert_allclose(r.scores, sm, rtol=1e-6)
+    rows = np.arange(8)[:, None]
+    # k = E: the weights are the softmax itself scaled by route_scale / (1 + eps)
+    np.testing.assert_allclose(r.weights, 2.5 * sm[rows, r.ids] / (1 + 1e-6), rtol=1e-6)
+    rs = O.route(logits, np.zeros(16, np.float32), 3, 1.0, 0.5, "sigmoid", None)
+    np.testing.assert_allclose(rs.scores, scipy.special.expit(0.5 * logits), rtol=1e-6)
+
+
+def test_invalid_score_raises():
+    with pytest.raises(ValueError):
+        O.route(np.zeros((1, 4)), np.zeros(4, np.float32), 1, 1.0, None, "relu", None)
+
+
+# ---------------------------------------------------------------- GEMVs
+
+def _bf16(v):
+    return O.f64_to_bf16_bits(O.round_bf16(v))
+
+
+def test_router_logits_one_hot_columns():
+    rng = np.random.default_rng(10)
+    W = rng.standard_normal((8, 32)).astype(np.float32)
+    x = np.zeros((3, 32))
+    x[0, 5], x[1, 17], x[2, 31] = 1.0, -2.0, 0.5
+    lg = O.router_logits(_bf16(x), W)
+    np.testing.assert_array_equal(lg[0], W[:, 5])
+    np.testing.assert_array_equal(lg[1], -2.0 * W[:, 17])
+    np.testing.assert_array_equal(lg[2], 0.5 * W[:, 31])
+
+
+def test_pooler_one_hot_without_and_with_norm():
+    rng = np.random.default_rng(11)
+    Wp = _bf16(rng.standard_normal((16, 24)) * 0.1)
+    wn = _bf16(1 + 0.05 * rng.standard_normal(16))
+    x = np.zeros((2, 24))
+    x[0, 3], x[1, 20] = 1.0, 1.0
+    h = O.pre_expert(_bf16(x), Wp, wn, 1e-6, pre_norm=False)
+    np.testing.assert_array_equal(h[0], O.bf16_to_f64(Wp[:, 3]))
+    np.testing.assert_array_equal(h[1], O.bf16_to_f64(Wp[:, 20]))
+    hn = O.pre_expert(_bf16(x), Wp, wn, 1e-6, pre_norm=True)
+    col = O.bf16_to_f64(Wp[:, 20])
+    want = torch.nn.functional.rms_norm(torch.from_numpy(col), (16,),
+                                        torch.from_numpy(O.bf16_to_f64(wn)), eps=1e-6)
+    np.testing.assert_array_equal(hn[1], O.round_bf16(want.numpy()))
+
+
+def test_unpool_one_hot():
+    rng = np.random.default_rng(12)
+    Wu = _bf16(rng.standard_normal((40, 16)) * 0.1)
+    m = np.zeros((1, 16))
+    m[0, 9] = 3.0
+    np.testing.assert_array_equal(O.unpool(m, Wu)[0], 3.0 * O.bf16_to_f64(Wu[:, 9]))
+
+
+# ---------------------------------------------------------------- experts
+
+def _decode_nibble_bits(c):
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    mag = 2.0 ** (e - 1) * (1 + m / 2) if e else m / 2
+    return -mag if s else mag
+
+
+def test_mxfp4_dequant_brute_force():
+    rng = np.random.default_rng(13)
+    t = {"w13": rng.integers(0, 256, (2, 64, 32), dtype=np.uint8),
+         "w13_scale": rng.integers(119, 124, (2, 64, 2), dtype=np.uint8),
+         "w2": rng.integers(0, 256, (2, 64, 16), dtype=np.uint8),
+         "w2_scale": rng.integers(119, 124, (2, 64, 1), dtype=np.uint8)}
+    w13, w2 = O.dequant_expert("mxfp4", t, 1)
+    for n in range(64):
+        for k in range(64):
+            byte = int(t["w13"][1, n, k // 2])
+            code = byte & 0xF if k % 2 == 0 else byte >> 4
+            want = _decode_nibble_bits(code) * 2.0 ** (int(t["w13_scale"][1, n, k // 32]) - 127)
+            assert w13[n, k] == want
+    assert w2.shape == (64, 32)
+    for n in range(64):
+        for k in range(32):
+            byte = int(t["w2"][1, n, k // 2])
+            code = byte & 0xF if k % 2 == 0 else byte >> 4
+            assert w2[n, k] == _decode_nibble_bits(code) * 2.0 ** (int(t["w2_scale"][1, n, 0]) - 127)
+
+
+def test_nvfp4_and_fp8_dequant_brute_force():
+    rng = np.random.default_rng(14)
+    sf = np.array([0x38, 0x30, 0x01, 0x7E], np.uint8)   # 1, 0.5, 2^-9, 448
+    t = {"w13": rng.integers(0, 256, (1, 4, 32), dtype=np.uint8),
+         "w13_scale": np.tile(sf, (1, 4, 1)).reshape(1, 4, 4),
+         "w13_gscale": np.array([1.25], np.float32),
+         "w2": rng.integers(0, 256, (1, 64, 8), dtype=np.uint8),
+         "w2_scale": np.full((1, 64, 1), 0x38, np.uint8),
+         "w2_gscale": np.array([0.75], np.float32)}
+    w13, _ = O.dequant_expert("nvfp4", t, 0)
+    sfv = [1.0, 0.5, 2.0 ** -9, 448.0]
+    for n in range(4):
+        for k in range(64):
+            byte = int(t["w13"][0, n, k // 2])
+            code = byte & 0xF if k % 2 == 0 else byte >> 4
+            assert w13[n, k] == _decode_nibble_bits(code) * sfv[k // 16] * 1.25
+    f = {"w13": np.array([[[0x38, 0xB8, 0x7E]]], np.uint8),
+         "w13_scale": np.array([[0.5]], np.float32),
+         "w2": np.array([[[0x40]]], np.uint8), "w2_scale": np.array([[3.0]], np.float32)}
+    w13, w2 = O.dequant_expert("fp8", f, 0)
+    assert w13.tolist() == [[0.5, -0.5, 224.0]] and w2.tolist() == [[6.0]]
+
+
+def _mx_expert(P, I, w13_vals, w2_vals):
+    """Pack exact e2m1 values (scale 2^0) into the plain MXFP4 layout."""
+    inv = {v: c for c, v in enumerate(O.E2M1[:8])}
+
+    def pack(vals):
+        vals = np.asarray(vals, dtype=np.float64)
+        codes = np.vectorize(lambda v: inv[abs(v)] | (8 if v < 0 else 0))(vals).astype(np.uint8)
+        return (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+
+    return {"w13": pack(w13_vals)[None], "w13_scale": np.full((1, 2 * I, P // 32), 127, np.uint8),
+            "w2": pack(w2_vals)[None], "w2_scale": np.full((1, P, I // 32), 127, np.uint8)}
+
+
+def test_expert_gate_up_order_and_transposes():
+    P, I = 32, 32
+    rng = np.random.default_rng(15)
+    vals = np.array([0, 0.5, 1, 1.5, 2, -1, -0.5, 3])
+    A = rng.choice(vals, (I, P))
+    B = rng.choice(vals, (I, P))
+    C = rng.choice(vals, (P, I))
+    t = _mx_expert(P, I, np.concatenate([A, B]), C)
+    h = O.round_bf16(rng.standard_normal((1, P)))
+    y = O.expert_outputs(h, np.array([[0]]), "mxfp4", t, I)
+    g, u = A @ h[0], B @ h[0]
+    a = O.round_bf16(g / (1 + np.exp(-g)) * u)
+    np.testing.assert_allclose(y[0, 0], C @ a, rtol=1e-12, atol=1e-12)
+
+
+def test_silu_matches_torch():
+    z = np.linspace(-20, 20, 101)
+    np.testing.assert_allclose(O.silu(z), torch.nn.functional.silu(torch.from_numpy(z)).numpy(),
+                               rtol=1e-14, atol=1e-300)
+
+
+def test_fp8_row_quant_maps_amax_to_448():
+    rng = np.random.default_rng(16)
+    v = O.round_bf16(rng.standard_normal((6, 128)) * 3)
+    q, s = O.quantize_rows_e4m3(v)
+    back = O.e4m3_decode(q) * s[:, None]
+    amax = np.abs(v).max(axis=-1)
+    assert (np.abs(O.e4m3_decode(q)).max(axis=-1) == 448.0).all()
+    np.testing.assert_allclose(np.abs(back).max(axis=-1), amax, rtol=2 ** -22)
+    # e4m3 keeps 4 significant bits: half an ulp is 2^-4 relative (normal range)
+    big = np.abs(v) > amax[:, None] * 2.0 ** -6
+    assert (np.abs(back - v)[big] <= np.abs(v)[big] * 2.0 ** -4 * (1 + 1e-6)).all()
+    q0, s0 = O.quantize_rows_e4m3(np.zeros((1, 8)))
+    assert s0[0] == 0 and (q0 == 0).all()
+
+
+# ---------------------------------------------------------------- tail and boundary
+
+def test_single_route_closed_form():
+    rng = np.random.default_rng(17)
+    y = rng.standard_normal((3, 1, 64))
+    wpost = _bf16(1 + 0.05 * rng.standard_normal(64))
+    w = np.array([[2.5 * 0.7 / (0.7 + 1e-20)]] * 3)
+    out = O.finalize(y, w, wpost, 1e-6)
+    want = O.round_bf16(w[:, 0:1] * O.rms_norm(y[:, 0], O.bf16_to_f64(wpost), 1e-6))
+    np.testing.assert_array_equal(out, want)
+
+
+def test_identical_experts_make_the_output_independent_of_routing():
+    cfg_rng = np.random.default_rng(18)
+    P, I, E, H = 64, 32, 6, 96
+    codes13 = cfg_rng.integers(0, 256, (1, 2 * I, P // 2), dtype=np.uint8)
+    codes2 = cfg_rng.integers(0, 256, (1, P, I // 2), dtype=np.uint8)
+    t = {"w13": np.repeat(codes13, E, 0), "w13_scale": np.full((E, 2 * I, P // 32), 121, np.uint8),
+         "w2": np.repeat(codes2, E, 0), "w2_scale": np.full((E, P, I // 32), 122, np.uint8)}
+    h = O.round_bf16(cfg_rng.standard_normal((4, P)))
+    ids_a = np.array([[0, 1], [2, 3], [4, 5], [1, 0]])
+    ids_b = np.array([[5, 4], [0, 2], [3, 1], [2, 5]])
+    ya = O.expert_outputs(h, ids_a, "mxfp4", t, I)
+    yb = O.expert_outputs(h, ids_b, "mxfp4", t, I)
+    np.testing.assert_array_equal(ya, yb)
+    wpost = _bf16(np.ones(P))
+    S = np.array([[0.6, 0.3]] * 4)
+    wts = O.round_f32(2.5 * S / (S.sum(-1, keepdims=True) + 1e-20))
+    out = O.finalize(ya, wts, wpost, 1e-6)
+    n = O.rms_norm(ya[:, 0], 1.0, 1e-6)
+    np.testing.assert_allclose(out, O.round_bf16(wts.sum(-1, keepdims=True) * n), rtol=2 ** -7)
+    assert H  # dims documented above
+
+
+def test_boundary_linearity_and_zero_gate():
+    rng = np.random.default_rng(19)
+    u = rng.standard_normal((2, 48))
+    stream = rng.standard_normal((2, 48)).astype(np.float32)
+    wf = _bf16(1 + 0.05 * rng.standard_normal(48))
+    wn = _bf16(1 + 0.05 * rng.standard_normal(48))
+    s1, out = O.boundary(u, stream, wf, 0.75, wn, 1e-6)
+    add = O.rms_norm(u, O.bf16_to_f64(wf), 1e-6)
+    np.testing.assert_allclose(s1 - stream, 0.75 * add, atol=4 * 2.0 ** -24 * np.abs(s1).max())
+    s0, _ = O.boundary(u, stream, wf, 0.0, wn, 1e-6)
+    np.testing.assert_array_equal(s0, stream.astype(np.float64))
+    want = torch.nn.functional.rms_norm(torch.from_numpy(s1), (48,),
+                                        torch.from_numpy(O.bf16_to_f64(wn)), eps=1e-6).numpy()
+    np.testing.assert_array_equal(out, O.round_bf16(want))
