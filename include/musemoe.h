@@ -1,0 +1,210 @@
+/*
+ * musemoe -- the MuseSpark1x MoE decode block on one GB300 (sm_103a).
+ *
+ * One call runs, for `rows` input rows (a small-batch decode / speculative
+ * verify step):
+ *   router GEMV (fp32 weight [E, H] x bf16 input [rows, H] -> fp32 logits)
+ *   routing rule: optional output multiplier -> sigmoid or softmax -> expert
+ *     bias added for SELECTION only -> top-k -> gather the UNBIASED scores ->
+ *     divide by (sum + division_eps) -> multiply by route_scale
+ *     (page "vllm.models.muse_spark.amd.muse_moe_runner", class
+ *     MuseSpark1xRouter, docstring and _compute_routing_native);
+ *   pooler GEMM H -> P and the pre-expert RMSNorm -> bf16 h
+ *     (page "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
+ *     MoEProvider docstring);
+ *   routed experts on MXFP4 / NVFP4 / FP8 weights: fused w13 (gate rows
+ *     first), SiLU(gate) * up -> bf16, w2; one UNWEIGHTED output per route
+ *     (muse_moe_runner page, MuseSparkAiterExperts: unit router weights);
+ *   per-route post-expert RMSNorm, then the router weight, summed over the
+ *     k routes -> bf16 moe_out (muse_moe_runner page,
+ *     MuseSparkTopKWeightAndReduce.apply);
+ *   unpooler GEMM P -> H;
+ *   FFN boundary: post_ffn_norm, gated add into the fp32 residual stream in
+ *     place, next pre-norm -> bf16 out (providers page, BoundaryProvider).
+ *
+ * Conventions (providers page, Provider: build once, then a run that
+ * allocates nothing and is CUDA-graph capturable):
+ *   - musemoe_create validates the configuration and allocates the handle's
+ *     device workspace (sized for dims.max_rows) on the current device. It
+ *     is the only call that allocates device memory.
+ *   - musemoe_route / musemoe_forward / musemoe_forward_debug allocate
+ *     nothing, never synchronize, launch only on the given stream and can be
+ *     captured in a CUDA graph. All tensors are caller-owned device memory
+ *     (e.g. PyTorch tensors); the library keeps no pointer after a call.
+ *   - Arguments are validated before anything is launched; on failure the
+ *     call returns MUSEMOE_EINVAL / MUSEMOE_EUNSUPPORTED, launches nothing and
+ *     musemoe_last_error(handle) says why. A failed launch returns
+ *     MUSEMOE_ECUDA.
+ *   - One handle serves one stream at a time (its workspace is shared by
+ *     consecutive calls). Use one handle per concurrent stream.
+ *   - bf16 tensors are passed as uint16_t bit patterns; all tensors are
+ *     row-major and contiguous, 16-byte aligned.
+ */
+#ifndef MUSEMOE_H
+#define MUSEMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *musemoe_stream_t; /* a cudaStream_t */
+typedef struct CUevent_st *musemoe_event_t;   /* a cudaEvent_t */
+typedef struct musemoe_handle musemoe_handle;
+
+typedef enum {
+  MUSEMOE_OK = 0,
+  MUSEMOE_EINVAL = 1,       /* bad argument: null, misaligned, out of range */
+  MUSEMOE_EUNSUPPORTED = 2, /* a configuration or device the kernels do not serve */
+  MUSEMOE_ECUDA = 3,        /* a CUDA runtime call or launch failed */
+  MUSEMOE_ENOMEM = 4,       /* workspace allocation failed (create only) */
+  MUSEMOE_ERANGE = 5,       /* health: an expert operand left the fp16 range */
+} musemoe_status;
+
+typedef enum {
+  /* e2m1 codes + UE8M0 scale per 32 along K (page
+   * "vllm.models.muse_spark.amd.mono.decoder", MonoDims.expert_shapes) */
+  MUSEMOE_MXFP4 = 0,
+  /* e2m1 codes + e4m3 scale per 16 along K + fp32 global scale per expert */
+  MUSEMOE_NVFP4 = 1,
+  /* e4m3 codes + fp32 scale per output row; expert inputs quantized to e4m3
+   * per row with a dynamic fp32 scale (amax / 448) */
+  MUSEMOE_FP8_W8A8 = 2,
+} musemoe_quant;
+
+typedef enum { MUSEMOE_SIGMOID = 0, MUSEMOE_SOFTMAX = 1 } musemoe_score;
+
+/* Block sizes. hidden H, pooled P, inter I (per expert), experts E. */
+typedef struct {
+  int32_t max_rows; /* largest `rows` any call of this handle will pass */
+  int32_t hidden;   /* H: multiple of 32 */
+  int32_t pooled;   /* P: multiple of 128 */
+  int32_t inter;    /* I: multiple of 128 */
+  int32_t experts;  /* E: 1..256 */
+  int32_t top_k;    /* k: 1..E */
+} musemoe_dims;
+
+/* Routing rule and norm parameters (MuseSpark1xRouter constructor). */
+typedef struct {
+  int32_t score;            /* musemoe_score */
+  float route_scale;
+  int32_t has_multiplier;   /* 0: router_output_multiplier is None */
+  float multiplier;
+  int32_t has_division_eps; /* 0: router_score_division_eps is None */
+  float division_eps;
+  float norm_eps;           /* epsilon of all four RMSNorms */
+  int32_t pre_expert_norm;  /* 1: apply the pre-expert RMSNorm (default) */
+} musemoe_config;
+
+/* One layer's weights: caller-owned device pointers, read in place.
+ * Expert codes must be in the kernel layout musemoe_pack_experts writes. */
+typedef struct {
+  const float *w_router;      /* fp32 [E, H] */
+  const float *expert_bias;   /* fp32 [E], selection only */
+  const uint16_t *w_pool;     /* bf16 [P, H] */
+  const uint16_t *w_pre_norm; /* bf16 [P] (effective weight) */
+  const uint8_t *w13;         /* MXFP4/NVFP4 packed [E, 2I, P/2]; FP8 [E, 2I, P] */
+  const void *w13_scale;      /* MX u8 [E, 2I, P/32]; NV e4m3 [E, 2I, P/16]; FP8 fp32 [E, 2I] */
+  const float *w13_gscale;    /* NVFP4 only: fp32 [E] */
+  const uint8_t *w2;          /* MXFP4/NVFP4 packed [E, P, I/2]; FP8 [E, P, I] */
+  const void *w2_scale;       /* MX u8 [E, P, I/32]; NV e4m3 [E, P, I/16]; FP8 fp32 [E, P] */
+  const float *w2_gscale;     /* NVFP4 only: fp32 [E] */
+  const uint16_t *w_post_norm; /* bf16 [P] */
+  const uint16_t *w_unpool;    /* bf16 [H, P] */
+  const uint16_t *w_ffn_norm;  /* bf16 [H] (post_ffn_norm) */
+  const uint16_t *w_next_norm; /* bf16 [H] (the next layer's pre-norm) */
+  const float *gate;           /* fp32 [1]: the gated add's per-layer gate */
+} musemoe_weights;
+
+/* Optional device buffers that musemoe_forward_debug fills (each may be
+ * NULL) and optional events recorded around every kernel. */
+typedef struct {
+  float *logits;          /* fp32 [rows, E] router logits */
+  int32_t *ids;           /* int32 [rows, k] selected experts, best first */
+  float *weights;         /* fp32 [rows, k] routing weights */
+  uint16_t *h;            /* bf16 [rows, P] pre-expert-normed pooled input */
+  uint16_t *act;          /* [rows * k, I] SiLU(gate) * up per route: f16 bits for
+                             MXFP4/NVFP4, bf16 bits for FP8 W8A8 */
+  float *y;               /* fp32 [rows * k, P] unweighted route outputs */
+  uint16_t *moe_out;      /* bf16 [rows, P] */
+  float *u;               /* fp32 [rows, H] unpooler output */
+  musemoe_event_t *events; /* 2 * musemoe_num_kernels(quant) existing events:
+                              start and end of kernel i at [2i] and [2i+1];
+                              an event that cannot be recorded gives EINVAL.
+                              With events the kernels run without programmatic
+                              dependent launch, so each is timed alone. */
+} musemoe_taps;
+
+/* Validates dims/quant/config against the kernels (every reason is listed
+ * in the error text) and allocates the workspace on the current device.
+ * Returns EUNSUPPORTED for dims the kernels do not serve or a device that is
+ * not sm_103, EINVAL for null/invalid arguments, ENOMEM/ECUDA on allocation
+ * failure. On failure *out is NULL and musemoe_last_error(NULL) says why. */
+musemoe_status musemoe_create(const musemoe_dims *dims, int32_t quant,
+                              const musemoe_config *config, musemoe_handle **out);
+
+/* Frees the workspace (synchronizes the device first). NULL is a no-op. */
+void musemoe_destroy(musemoe_handle *handle);
+
+/* The last error text of this handle; with NULL, the calling thread's last
+ * musemoe_create / musemoe_pack_experts error. Never NULL. */
+const char *musemoe_last_error(const musemoe_handle *handle);
+
+/* Device workspace bytes musemoe_create allocates for these dims. */
+size_t musemoe_workspace_bytes(const musemoe_dims *dims, int32_t quant);
+
+/* Kernels one musemoe_forward launches for this quant (for taps->events). */
+int32_t musemoe_num_kernels(int32_t quant);
+/* Name of kernel i of the forward ("front", "route", "w13", ...). */
+const char *musemoe_kernel_name(int32_t quant, int32_t i);
+
+/* Re-lays the packed e2m1 codes of MXFP4/NVFP4 expert tensors from the plain
+ * layout (row-major [E, N, K/2], element 2j in the low nibble of byte j) into
+ * the kernel layout: within every 64-byte group of a row, byte 8j + 2q + b
+ * moves to 16q + 2j + b (q < 4, j < 8, b < 2). w13: N = 2I, K = P; w2: N = P,
+ * K = I. src and dst may be the same buffer (in place). Scales are used as
+ * given. For FP8 the plain layout is the kernel layout and this copies. */
+musemoe_status musemoe_pack_experts(const musemoe_dims *dims, int32_t quant,
+                                    const uint8_t *w13_src, uint8_t *w13_dst,
+                                    const uint8_t *w2_src, uint8_t *w2_dst,
+                                    musemoe_stream_t stream);
+
+/* Router GEMV + routing rule only: ids_out int32 [rows, k] (descending
+ * selection score, equal scores to the lower expert id), weights_out fp32
+ * [rows, k]. Needs w->w_router and w->expert_bias. */
+musemoe_status musemoe_route(musemoe_handle *handle, const musemoe_weights *w,
+                             const uint16_t *x, int32_t rows, int32_t *ids_out,
+                             float *weights_out, musemoe_stream_t stream);
+
+/* The whole block: x bf16 [rows, H] in; stream fp32 [rows, H] updated in
+ * place; out bf16 [rows, H] (the next layer's input). 1 <= rows <= max_rows. */
+musemoe_status musemoe_forward(musemoe_handle *handle, const musemoe_weights *w,
+                               const uint16_t *x, float *stream, uint16_t *out,
+                               int32_t rows, musemoe_stream_t stream_);
+
+/* musemoe_forward plus the taps (any may be NULL). */
+musemoe_status musemoe_forward_debug(musemoe_handle *handle, const musemoe_weights *w,
+                                     const uint16_t *x, float *stream, uint16_t *out,
+                                     int32_t rows, musemoe_stream_t stream_,
+                                     const musemoe_taps *taps);
+
+/* musemoe_forward on HOST buffers (pinned memory recommended): copies x and
+ * stream to the workspace, runs the block, copies stream and out back and
+ * synchronizes the stream. Not graph-capturable. */
+musemoe_status musemoe_forward_host(musemoe_handle *handle, const musemoe_weights *w,
+                                    const uint16_t *x_host, float *stream_host,
+                                    uint16_t *out_host, int32_t rows,
+                                    musemoe_stream_t stream_);
+
+/* Reads (synchronously) and clears the handle's device health word. Returns
+ * MUSEMOE_ERANGE if a forward since the last poll produced an expert operand
+ * (h or the SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504),
+ * MUSEMOE_OK otherwise. */
+musemoe_status musemoe_poll_health(musemoe_handle *handle);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUSEMOE_H */

@@ -1,0 +1,336 @@
+// Routing, pre-expert norm and the token -> expert permute. One CTA per row.
+//
+// Routing rule (page "vllm.models.muse_spark.amd.muse_moe_runner", class
+// MuseSpark1xRouter, docstring and _compute_routing_native): optional output
+// multiplier -> sigmoid or softmax -> expert bias added for SELECTION only ->
+// top-k -> gather the UNBIASED scores -> divide by (sum + division_eps) ->
+// multiply by route_scale. All in fp32, as the recipe's torch ops are.
+// Top-k: one warp sorts the E (<= 256) keys (selection score, then lower id
+// first on equal scores) with a register bitonic network, 32 * EPL keys.
+//
+// Pre-expert norm (page "vllm.models.muse_spark.nvidia.specialized_decode.
+// runtime.providers", MoEProvider docstring): RMSNorm of the pooled row with
+// the effective bf16 weight, stored as bf16 h; the expert operand is h in
+// f16 (exact for |h| in [2^-14, 65504]) or, for FP8 W8A8, e4m3 codes with a
+// per-row dynamic scale amax / 448.
+//
+// Permute: the CTA that finishes last (atomic ticket, no waiting) counts the
+// routes per expert and writes them grouped by expert in route order (a
+// stable counting sort), then the token groups the expert kernels walk.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace musemoe {
+
+constexpr int kRouteThreads = 256;
+
+__device__ __forceinline__ uint32_t orderable(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Warp-wide descending bitonic sort of 32 * EPL 64-bit keys; key i lives in
+// lane i / EPL, register i % EPL.
+template <int EPL>
+__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&key)[EPL], int lane) {
+  constexpr int N = 32 * EPL;
+#pragma unroll
+  for (int kk = 2; kk <= N; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      if (j >= EPL) {
+        const int lj = j / EPL;
+#pragma unroll
+        for (int r = 0; r < EPL; ++r) {
+          const int i = lane * EPL + r;
+          const uint64_t other = __shfl_xor_sync(0xffffffffu, key[r], lj);
+          const bool lower = (i & j) == 0;
+          const bool desc = (i & kk) == 0;
+          const bool take_max = (lower == desc);
+          const uint64_t mx = key[r] > other ? key[r] : other;
+          const uint64_t mn = key[r] > other ? other : key[r];
+          key[r] = take_max ? mx : mn;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < EPL; ++r) {
+          const int r2 = r ^ j;
+          if (r2 > r) {
+            const int i = lane * EPL + r;
+            const bool desc = (i & kk) == 0;
+            const uint64_t a = key[r], b = key[r2];
+            const bool swap = desc ? (a < b) : (a > b);
+            key[r] = swap ? b : a;
+            key[r2] = swap ? a : b;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int EPL>
+__device__ void select_topk(const float* sel, int E, int k, int* top, int lane) {
+  uint64_t key[EPL];
+#pragma unroll
+  for (int r = 0; r < EPL; ++r) {
+    const int i = lane * EPL + r;
+    key[r] = (i < E) ? ((uint64_t)orderable(sel[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i)
+                     : 0ull;
+  }
+  warp_bitonic_desc<EPL>(key, lane);
+#pragma unroll
+  for (int r = 0; r < EPL; ++r) {
+    const int i = lane * EPL + r;
+    if (i < k) top[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[r] & 0xFFFFFFFFull));
+  }
+}
+
+// Exclusive scan of one int per thread (blockDim.x == kRouteThreads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < kRouteThreads / 32 ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kRouteThreads / 32) scratch[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int before = wid ? scratch[wid - 1] : 0;
+  *total = scratch[kRouteThreads / 32 - 1];
+  return before + x - v;
+}
+
+struct RouteSmem {
+  float g[256];     // scaled logits
+  float s[256];     // unbiased scores
+  float sel[256];   // selection scores
+  int top[256];
+  float scratch[32];
+  int iscratch[32];
+  int flag;
+};
+
+__device__ void permute_last_cta(const RouteParams& p, unsigned char* dyn) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int E = p.E, rt = p.rows * p.k;
+  const int nch = (rt + 31) / 32;
+  int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
+  uint8_t* rank_s = reinterpret_cast<uint8_t*>(ids_s + ((rt + 7) & ~7));
+  uint16_t* hist = reinterpret_cast<uint16_t*>(rank_s + ((rt + 15) & ~15));
+  __shared__ int cnt_s[256], off_s[257], goff_s[257];
+  __shared__ int scan_scratch[32];
+
+  for (int i = tid; i < rt; i += kRouteThreads) ids_s[i] = (int16_t)__ldcg(p.ids + i);
+  for (int i = tid; i < nch * E; i += kRouteThreads) hist[i] = 0;
+  __syncthreads();
+  // per 32-route chunk: rank of each route among equal experts, chunk counts
+  for (int c = wid; c < nch; c += kRouteThreads / 32) {
+    const int r = c * 32 + lane;
+    const int e = r < rt ? (int)ids_s[r] : E + lane;  // pads never match
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (r < rt) {
+      rank_s[r] = (uint8_t)rank;
+      if (rank == 0) hist[c * E + e] = (uint16_t)__popc(peers);
+    }
+  }
+  __syncthreads();
+  // per expert: exclusive prefix over chunks
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int run = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int t = hist[c * E + e];
+      hist[c * E + e] = (uint16_t)run;
+      run += t;
+    }
+    cnt_s[e] = run;
+  }
+  __syncthreads();
+  // offsets of experts, and of their token groups
+  {
+    const int e = tid;
+    const int c = e < E ? cnt_s[e] : 0;
+    const int ng = (c + p.token_group - 1) / p.token_group;
+    int tot;
+    const int off = block_exclusive_scan(c, scan_scratch, &tot);
+    if (e < E) off_s[e] = off;
+    if (e == 0) off_s[E] = tot;
+    int gtot;
+    const int goff = block_exclusive_scan(ng, scan_scratch, &gtot);
+    if (e < E) goff_s[e] = goff;
+    if (e == 0) goff_s[E] = gtot;
+  }
+  __syncthreads();
+  for (int r = tid; r < rt; r += kRouteThreads) {
+    const int e = ids_s[r];
+    p.route_list[off_s[e] + hist[(r >> 5) * E + e] + rank_s[r]] = r;
+  }
+  for (int e = tid; e < E; e += kRouteThreads) {
+    const int c = cnt_s[e];
+    for (int gi = 0, s = 0; s < c; ++gi, s += p.token_group) {
+      int4 gd = make_int4(e, off_s[e] + s, min(p.token_group, c - s), 0);
+      reinterpret_cast<int4*>(p.groups)[goff_s[e] + gi] = gd;
+    }
+  }
+  if (tid == 0) {
+    p.counters[kNumGroups] = goff_s[E];
+    p.counters[kTicket] = 0;
+  }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ RouteSmem sm;
+  extern __shared__ __align__(16) unsigned char dyn[];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int E = p.E, k = p.k;
+
+  // ---- logits, multiplier, scores, selection scores --------------------
+  float gmax = -INFINITY;
+  for (int e = tid; e < E; e += kRouteThreads) {
+    float l = 0.f;
+    for (int ks = 0; ks < p.ks_r; ++ks) l += __ldcg(p.logit_part + ((size_t)ks * p.rows + t) * E + e);
+    p.logits[(size_t)t * E + e] = l;
+    const float g = p.has_multiplier ? l * p.multiplier : l;
+    sm.g[e] = g;
+    gmax = fmaxf(gmax, g);
+  }
+  if (p.score == 1) {  // softmax over the experts
+    gmax = block_max(gmax, sm.scratch);
+    float part = 0.f;
+    for (int e = tid; e < E; e += kRouteThreads) {
+      const float z = expf(sm.g[e] - gmax);
+      sm.s[e] = z;
+      part += z;
+    }
+    const float tot = block_sum(part, sm.scratch);
+    for (int e = tid; e < E; e += kRouteThreads) sm.s[e] = sm.s[e] / tot;
+  } else {
+    for (int e = tid; e < E; e += kRouteThreads) sm.s[e] = 1.0f / (1.0f + expf(-sm.g[e]));
+  }
+  for (int e = tid; e < E; e += kRouteThreads) sm.sel[e] = sm.s[e] + __ldg(p.expert_bias + e);
+  __syncthreads();
+
+  // ---- top-k and weights (warp 0) -----------------------------------------
+  if (wid == 0) {
+    select_topk<EPL>(sm.sel, E, k, sm.top, lane);
+    __syncwarp();
+    float part = 0.f;
+    for (int i = lane; i < k; i += 32) part += sm.s[sm.top[i]];
+    float denom = warp_sum(part);
+    if (p.has_division_eps) denom += p.division_eps;
+    for (int i = lane; i < k; i += 32) {
+      const int e = sm.top[i];
+      p.ids[(size_t)t * k + i] = e;
+      p.weights[(size_t)t * k + i] = sm.s[e] / denom * p.route_scale;
+    }
+  }
+
+  // ---- pre-expert norm ----------------------------------------------------
+  if (p.pool_part != nullptr) {
+    float* hr = reinterpret_cast<float*>(dyn);
+    float ss = 0.f;
+    for (int i = tid; i < p.P; i += kRouteThreads) {
+      float v = 0.f;
+      for (int ks = 0; ks < p.ks_p; ++ks) v += __ldcg(p.pool_part + ((size_t)ks * p.rows + t) * p.P + i);
+      hr[i] = v;
+      ss += v * v;
+    }
+    ss = block_sum(ss, sm.scratch);
+    const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.P + p.norm_eps) : 1.0f;
+    float amax = 0.f;
+    int bad = 0;
+    for (int i = tid; i < p.P; i += kRouteThreads) {
+      float v = hr[i];
+      if (p.pre_norm) v = (v * rstd) * bf16_bits_to_f32(p.w_pre_norm[i]);
+      const float hb = round_bf16(v);
+      p.h[(size_t)t * p.P + i] = f32_to_bf16_bits(hb);
+      hr[i] = hb;
+      amax = fmaxf(amax, fabsf(hb));
+      if (p.quant != kFP8) {
+        reinterpret_cast<__half*>(p.h_op)[(size_t)t * p.P + i] = __float2half_rn(hb);
+        bad |= !(fabsf(hb) <= 65504.f);
+      }
+    }
+    if (p.quant == kFP8) {
+      amax = block_max(amax, sm.scratch);
+      const float s = amax / 448.0f;
+      for (int i = 2 * tid; i < p.P; i += 2 * kRouteThreads) {
+        const float a = s > 0.f ? hr[i] / s : 0.f;
+        const float b = s > 0.f ? hr[i + 1] / s : 0.f;
+        reinterpret_cast<uint16_t*>(p.h_op + (size_t)t * p.P)[i / 2] = f32x2_to_e4m3x2(a, b);
+      }
+      if (tid == 0) p.h_scale[t] = s;
+    }
+    if (bad) atomicOr(p.health, kHealthHRange);
+  }
+
+  if (p.route_list == nullptr) return;
+  // ---- last CTA: permute --------------------------------------------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(p.counters + kTicket, 1);
+    sm.flag = (prev == p.rows - 1);
+  }
+  __syncthreads();
+  if (!sm.flag) return;
+  __threadfence();
+  permute_last_cta(p, dyn);
+}
+
+static size_t route_dyn_smem(const RouteParams& p) {
+  size_t a = (p.pool_part != nullptr) ? (size_t)p.P * 4 : 0;
+  size_t b = 0;
+  if (p.route_list != nullptr) {
+    const size_t rt = (size_t)p.rows * p.k;
+    const size_t nch = (rt + 31) / 32;
+    b = ((rt + 7) & ~(size_t)7) * 2 + ((rt + 15) & ~(size_t)15) + nch * p.E * 2;
+  }
+  return ((a > b ? a : b) + 15) & ~(size_t)15;
+}
+
+template <int EPL>
+static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t s, bool pdl) {
+  const size_t smem = route_dyn_smem(p);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_route<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.rows);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_route<EPL>, p);
+}
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl) {
+  if (p.E <= 32) return launch_route_t<1>(p, s, pdl);
+  if (p.E <= 64) return launch_route_t<2>(p, s, pdl);
+  if (p.E <= 128) return launch_route_t<4>(p, s, pdl);
+  return launch_route_t<8>(p, s, pdl);
+}
+
+}  // namespace musemoe

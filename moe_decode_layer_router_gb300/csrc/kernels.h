@@ -1,0 +1,127 @@
+// Internal launch interface of the musemoe kernels (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace musemoe {
+
+enum Quant : int { kMXFP4 = 0, kNVFP4 = 1, kFP8 = 2 };
+
+// counters[] slots in the workspace
+enum Counter : int { kNumGroups = 0, kTicket = 1, kNumCounters = 8 };
+// health bits
+enum Health : int { kHealthHRange = 1, kHealthActRange = 2 };
+
+// ---- front: router GEMV (fp32 FFMA) + pooler GEMV (tensor cores) --------
+// The router part writes logit partial sums [ks_r][rows][E]; the GEMV part
+// writes partial sums [ks][rows][M] of Y = X W^T for bf16 W [M, K].
+struct FrontParams {
+  const uint16_t* x;  // bf16 [rows, K]
+  int rows;
+  // router (skipped when router_ctas == 0)
+  const float* w_router;  // fp32 [E, K]
+  float* logit_part;      // [ks_r, rows, E]
+  int E, ks_r, router_ctas;
+  // bf16 GEMV
+  const uint16_t* w;  // bf16 [M, K]
+  float* part;        // [ks, rows, M]
+  int M, K, ks;
+  int kchunks_per_split;  // 32-element chunks per split
+  int token_blocks;       // ceil(rows / (8 * NT))
+};
+cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl);
+int front_ctas(const FrontParams& p);
+
+// ---- route: routing rule + pre-expert norm + token->expert permute ------
+struct RouteParams {
+  const float* logit_part;  // [ks_r, rows, E]
+  const float* expert_bias;
+  float* logits;            // [rows, E]
+  int32_t* ids;             // [rows, k]
+  float* weights;           // [rows, k]
+  int rows, E, k, ks_r;
+  int score;  // 0 sigmoid, 1 softmax
+  int has_multiplier;
+  float multiplier;
+  int has_division_eps;
+  float division_eps;
+  float route_scale;
+  // pre-expert norm (skipped when pool_part == nullptr: routing only)
+  const float* pool_part;  // [ks_p, rows, P]
+  const uint16_t* w_pre_norm;
+  int P, ks_p, pre_norm;
+  float norm_eps;
+  int quant;
+  uint16_t* h;      // bf16 [rows, P]
+  uint8_t* h_op;    // f16 [rows, P] (FP4) or e4m3 [rows, P] (FP8)
+  float* h_scale;   // [rows] (FP8)
+  // permute (skipped when route_list == nullptr)
+  int32_t* route_list;  // [rows*k]
+  int32_t* groups;      // [max_groups, 4]: expert, first route slot, ntok, 0
+  int32_t* counters;
+  int32_t* health;
+  int token_group;  // routes per group (8 * NT of the expert kernels)
+};
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
+
+// ---- routed experts --------------------------------------------------------
+struct ExpertParams {
+  int quant;
+  int role;      // 0: w13 + SiLU*up -> act; 1: w2 -> y
+  int E, N, K;   // rows N and reduction K of the weight matrix
+  int I, P, k;
+  const uint8_t* w;        // codes [E, N, K/2] packed (FP4) or [E, N, K] (FP8)
+  const void* scale;       // see musemoe_weights
+  const float* gscale;     // NVFP4 [E]
+  const uint8_t* b;        // activation operand: f16 [*, K] or e4m3 [*, K]
+  const float* b_scale;    // FP8: per B row
+  int b_by_token;          // 1: B row = route / k (w13 reads h); 0: B row = route
+  const int32_t* route_list;
+  const int32_t* groups;
+  const int32_t* counters;
+  void* out;               // role 0: act f16/bf16 [rows*k, I]; role 1: y fp32 [rows*k, P]
+  int32_t* health;
+  int grid;
+};
+cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pdl);
+int expert_ctas_per_sm(int quant, int role, int nt);
+
+// FP8 only: per-route dynamic e4m3 quantization of the bf16 activation.
+struct ActQuantParams {
+  const uint16_t* act;  // bf16 [routes, I]
+  uint8_t* q;           // e4m3 [routes, I]
+  float* scale;         // [routes]
+  int routes, I;
+};
+cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl);
+
+// ---- tail: per-route post-expert norm, router weight, sum over k --------
+struct FinalizeParams {
+  const float* y;  // [rows*k, P]
+  const float* weights;
+  const uint16_t* w_post_norm;
+  uint16_t* moe_out;  // bf16 [rows, P]
+  int rows, k, P;
+  float eps;
+};
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl);
+
+// ---- FFN boundary ------------------------------------------------------------
+struct BoundaryParams {
+  const float* part;  // unpooler partials [ks, rows, H]
+  int ks;
+  float* stream;      // fp32 [rows, H], in place
+  uint16_t* out;      // bf16 [rows, H]
+  const uint16_t* w_ffn_norm;
+  const uint16_t* w_next_norm;
+  const float* gate;
+  float* u_tap;       // optional fp32 [rows, H]
+  int rows, H;
+  float eps;
+};
+cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
+
+// ---- weight re-layout ----------------------------------------------------
+cudaError_t launch_pack_fp4(const uint8_t* src, uint8_t* dst, size_t bytes, cudaStream_t s);
+
+}  // namespace musemoe

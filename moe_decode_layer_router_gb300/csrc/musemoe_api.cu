@@ -1,0 +1,669 @@
+// C ABI of the musemoe library: validation, workspace and the launch chain.
+// See include/musemoe.h for the contract of every entry point.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "musemoe.h"
+
+using namespace musemoe;
+
+namespace {
+
+thread_local std::string g_thread_err;
+
+std::string fmt(const char* f, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, f);
+  vsnprintf(buf, sizeof buf, f, ap);
+  va_end(ap);
+  return buf;
+}
+
+constexpr int kMaxRoutes = 4096;  // rows * top_k served by the permute
+constexpr size_t kAlign = 256;
+
+int nt_front(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
+int nt_expert(int rows) {
+  const int t = (rows + 7) / 8;
+  return t <= 1 ? 1 : t <= 2 ? 2 : t <= 4 ? 4 : 8;
+}
+int nt_index(int nt) { return nt == 1 ? 0 : nt == 2 ? 1 : nt == 4 ? 2 : 3; }
+
+struct GemvSplit {
+  int ks, kcps, tb;
+};
+// K-split of a bf16 GEMV so that the grid fills ~4 CTAs per SM.
+GemvSplit gemv_split(int M, int K, int rows, int sms) {
+  const int nt = nt_front(rows);
+  const int tb = (rows + 8 * nt - 1) / (8 * nt);
+  const int RB = M / 64, KC = K / 32;
+  int ks = (int)std::lround(4.0 * sms / std::max(1, RB * tb));
+  ks = std::max(1, std::min(ks, KC));
+  const int kcps = (KC + ks - 1) / ks;
+  ks = (KC + kcps - 1) / kcps;
+  return {ks, kcps, tb};
+}
+int router_split(int E, int H, int rows, int sms) {
+  const int EB = (E + 15) / 16, tb = (rows + 7) / 8;
+  const int K4 = H / 4;
+  int ks = (2 * sms) / std::max(1, EB * tb);
+  return std::max(1, std::min(ks, std::max(1, K4 / 32)));
+}
+int router_ctas(int E, int rows, int ks) { return ((E + 15) / 16) * ks * ((rows + 7) / 8); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct musemoe_handle {
+  musemoe_dims d{};
+  int quant = 0;
+  musemoe_config cfg{};
+  int device = -1, sms = 0;
+  int max_routes = 0, max_groups = 0;
+  int expert_grid[2][4] = {};
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  // workspace views
+  float *logit_part = nullptr, *pool_part = nullptr, *unpool_part = nullptr;
+  float *logits = nullptr, *weights = nullptr, *h_scale = nullptr, *act_scale = nullptr;
+  float *y = nullptr, *stream_stage = nullptr;
+  int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
+  int32_t* health = nullptr;
+  uint16_t *h = nullptr, *moe_out = nullptr, *x_stage = nullptr, *out_stage = nullptr;
+  uint8_t *h_op = nullptr, *act = nullptr, *act_q = nullptr;
+  std::string err;
+};
+
+namespace {
+
+struct Layout {
+  size_t off = 0;
+  std::vector<std::pair<void**, size_t>> items;
+  template <typename T>
+  void add(T** p, size_t bytes) {
+    items.push_back({reinterpret_cast<void**>(p), off});
+    off += (bytes + kAlign - 1) / kAlign * kAlign;
+  }
+};
+
+void plan(musemoe_handle* h, Layout& L) {
+  const musemoe_dims& d = h->d;
+  const size_t R = d.max_rows, E = d.experts, H = d.hidden, P = d.pooled, I = d.inter;
+  const size_t RT = R * d.top_k;
+  size_t pool_part = 0, unpool_part = 0, logit_part = 0;
+  for (int rows = 1; rows <= d.max_rows; ++rows) {
+    pool_part = std::max(pool_part, (size_t)gemv_split(d.pooled, d.hidden, rows, h->sms).ks * rows);
+    unpool_part =
+        std::max(unpool_part, (size_t)gemv_split(d.hidden, d.pooled, rows, h->sms).ks * rows);
+    logit_part = std::max(logit_part, (size_t)router_split(d.experts, d.hidden, rows, h->sms) * rows);
+  }
+  const bool fp8 = h->quant == kFP8;
+  L.add(&h->logit_part, logit_part * E * 4);
+  L.add(&h->pool_part, pool_part * P * 4);
+  L.add(&h->unpool_part, unpool_part * H * 4);
+  L.add(&h->logits, R * E * 4);
+  L.add(&h->ids, RT * 4);
+  L.add(&h->weights, RT * 4);
+  L.add(&h->h, R * P * 2);
+  L.add(&h->h_op, R * P * (fp8 ? 1 : 2));
+  L.add(&h->h_scale, R * 4);
+  L.add(&h->route_list, RT * 4);
+  L.add(&h->groups, (size_t)h->max_groups * 16);
+  L.add(&h->counters, kNumCounters * 4);
+  L.add(&h->health, 16);
+  L.add(&h->act, RT * I * 2);
+  if (fp8) {
+    L.add(&h->act_q, RT * I);
+    L.add(&h->act_scale, RT * 4);
+  }
+  L.add(&h->y, RT * P * 4);
+  L.add(&h->moe_out, R * P * 2);
+  L.add(&h->x_stage, R * H * 2);
+  L.add(&h->stream_stage, R * H * 4);
+  L.add(&h->out_stage, R * H * 2);
+}
+
+std::vector<std::string> refusals(const musemoe_dims* d, int32_t quant, const musemoe_config* c) {
+  std::vector<std::string> r;
+  if (d->max_rows < 1) r.push_back(fmt("max_rows %d < 1", d->max_rows));
+  if (d->hidden < 64 || d->hidden % 64) r.push_back(fmt("hidden %d is not a multiple of 64", d->hidden));
+  if (d->pooled < 128 || d->pooled % 128)
+    r.push_back(fmt("pooled %d is not a multiple of 128", d->pooled));
+  if (d->inter < 128 || d->inter % 128) r.push_back(fmt("inter %d is not a multiple of 128", d->inter));
+  if (d->experts < 1 || d->experts > 256)
+    r.push_back(fmt("experts %d outside 1..256 (the register top-k)", d->experts));
+  if (d->top_k < 1 || d->top_k > d->experts)
+    r.push_back(fmt("top_k %d outside 1..experts (%d)", d->top_k, d->experts));
+  if ((long long)d->max_rows * d->top_k > kMaxRoutes)
+    r.push_back(fmt("max_rows * top_k = %lld exceeds %d routes", (long long)d->max_rows * d->top_k,
+                    kMaxRoutes));
+  if ((size_t)d->pooled * 4 > 200 * 1024) r.push_back(fmt("pooled %d too large for one CTA row", d->pooled));
+  if ((size_t)d->hidden * 4 > 200 * 1024) r.push_back(fmt("hidden %d too large for one CTA row", d->hidden));
+  if (quant < 0 || quant > 2) r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1) or FP8_W8A8 (2)", quant));
+  if (c->score != 0 && c->score != 1) r.push_back(fmt("score %d is not sigmoid (0) or softmax (1)", c->score));
+  if (!std::isfinite(c->route_scale)) r.push_back("route_scale is not finite");
+  if (c->has_multiplier && !std::isfinite(c->multiplier)) r.push_back("multiplier is not finite");
+  if (c->has_division_eps && !(c->division_eps >= 0.f)) r.push_back("division_eps < 0");
+  if (!(c->norm_eps >= 0.f)) r.push_back("norm_eps < 0");
+  return r;
+}
+
+std::string join(const std::vector<std::string>& v) {
+  std::string s;
+  for (size_t i = 0; i < v.size(); ++i) s += (i ? "; " : "") + v[i];
+  return s;
+}
+
+musemoe_status set_err(musemoe_handle* h, musemoe_status st, const std::string& m) {
+  if (h) h->err = m;
+  else g_thread_err = m;
+  return st;
+}
+
+musemoe_status cuda_err(musemoe_handle* h, cudaError_t e, const char* what) {
+  return set_err(h, MUSEMOE_ECUDA, fmt("%s: %s", what, cudaGetErrorString(e)));
+}
+
+// Returns an error text, or empty when the weights are usable.
+std::string check_weights(const musemoe_handle* h, const musemoe_weights* w, bool route_only) {
+  if (!w) return "weights is NULL";
+  std::vector<std::string> bad;
+  auto need = [&](const void* p, const char* name) {
+    if (!p) bad.push_back(fmt("%s is NULL", name));
+    else if (!aligned16(p)) bad.push_back(fmt("%s is not 16-byte aligned", name));
+  };
+  need(w->w_router, "w_router");
+  need(w->expert_bias, "expert_bias");
+  if (!route_only) {
+    need(w->w_pool, "w_pool");
+    need(w->w_pre_norm, "w_pre_norm");
+    need(w->w13, "w13");
+    need(w->w13_scale, "w13_scale");
+    need(w->w2, "w2");
+    need(w->w2_scale, "w2_scale");
+    if (h->quant == kNVFP4) {
+      need(w->w13_gscale, "w13_gscale");
+      need(w->w2_gscale, "w2_gscale");
+    }
+    need(w->w_post_norm, "w_post_norm");
+    need(w->w_unpool, "w_unpool");
+    need(w->w_ffn_norm, "w_ffn_norm");
+    need(w->w_next_norm, "w_next_norm");
+    need(w->gate, "gate");
+  }
+  return join(bad);
+}
+
+musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const uint16_t* x,
+                            float* stream, uint16_t* out, int rows, cudaStream_t s,
+                            const musemoe_taps* taps) {
+  const musemoe_dims& d = h->d;
+  musemoe_event_t* ev = taps ? taps->events : nullptr;
+  const bool pdl = (ev == nullptr);
+  int ki = 0;
+  cudaError_t e = cudaSuccess;
+  bool bad_event = false;
+  auto before = [&]() {
+    if (ev && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * ki]), s) != cudaSuccess)
+      bad_event = true;
+  };
+  auto after = [&](cudaError_t r, const char* name) -> bool {
+    if (r == cudaSuccess) r = cudaGetLastError();
+    if (r != cudaSuccess) {
+      e = r;
+      h->err = fmt("launch of %s failed: %s", name, cudaGetErrorString(r));
+      return false;
+    }
+    if (ev && cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * ki + 1]), s) != cudaSuccess)
+      bad_event = true;
+    ++ki;
+    return true;
+  };
+
+  // 1. front: router GEMV + pooler GEMV
+  const GemvSplit sp = gemv_split(d.pooled, d.hidden, rows, h->sms);
+  const int ks_r = router_split(d.experts, d.hidden, rows, h->sms);
+  FrontParams fp{};
+  fp.x = x;
+  fp.rows = rows;
+  fp.w_router = w->w_router;
+  fp.logit_part = h->logit_part;
+  fp.E = d.experts;
+  fp.ks_r = ks_r;
+  fp.router_ctas = router_ctas(d.experts, rows, ks_r);
+  fp.w = w->w_pool;
+  fp.part = h->pool_part;
+  fp.M = d.pooled;
+  fp.K = d.hidden;
+  fp.ks = sp.ks;
+  fp.kchunks_per_split = sp.kcps;
+  fp.token_blocks = sp.tb;
+  before();
+  if (!after(launch_front(fp, nt_front(rows), s, pdl), "front")) return MUSEMOE_ECUDA;
+
+  // 2. routing + pre-expert norm + permute
+  const int nte = nt_expert(rows);
+  RouteParams rp{};
+  rp.logit_part = h->logit_part;
+  rp.expert_bias = w->expert_bias;
+  rp.logits = h->logits;
+  rp.ids = h->ids;
+  rp.weights = h->weights;
+  rp.rows = rows;
+  rp.E = d.experts;
+  rp.k = d.top_k;
+  rp.ks_r = ks_r;
+  rp.score = h->cfg.score;
+  rp.has_multiplier = h->cfg.has_multiplier;
+  rp.multiplier = h->cfg.multiplier;
+  rp.has_division_eps = h->cfg.has_division_eps;
+  rp.division_eps = h->cfg.division_eps;
+  rp.route_scale = h->cfg.route_scale;
+  rp.pool_part = h->pool_part;
+  rp.w_pre_norm = w->w_pre_norm;
+  rp.P = d.pooled;
+  rp.ks_p = sp.ks;
+  rp.pre_norm = h->cfg.pre_expert_norm;
+  rp.norm_eps = h->cfg.norm_eps;
+  rp.quant = h->quant;
+  rp.h = h->h;
+  rp.h_op = h->h_op;
+  rp.h_scale = h->h_scale;
+  rp.route_list = h->route_list;
+  rp.groups = h->groups;
+  rp.counters = h->counters;
+  rp.health = h->health;
+  rp.token_group = 8 * nte;
+  before();
+  if (!after(launch_route(rp, s, pdl), "route")) return MUSEMOE_ECUDA;
+
+  // 3. w13 + SiLU * up
+  ExpertParams ep{};
+  ep.quant = h->quant;
+  ep.role = 0;
+  ep.E = d.experts;
+  ep.N = 2 * d.inter;
+  ep.K = d.pooled;
+  ep.I = d.inter;
+  ep.P = d.pooled;
+  ep.k = d.top_k;
+  ep.w = w->w13;
+  ep.scale = w->w13_scale;
+  ep.gscale = w->w13_gscale;
+  ep.b = h->h_op;
+  ep.b_scale = h->h_scale;
+  ep.b_by_token = 1;
+  ep.route_list = h->route_list;
+  ep.groups = h->groups;
+  ep.counters = h->counters;
+  ep.out = h->act;
+  ep.health = h->health;
+  ep.grid = h->expert_grid[0][nt_index(nte)];
+  before();
+  if (!after(launch_expert(ep, nte, s, pdl), "w13")) return MUSEMOE_ECUDA;
+
+  // 3b. FP8: quantize the activation per route
+  if (h->quant == kFP8) {
+    ActQuantParams aq{};
+    aq.act = reinterpret_cast<const uint16_t*>(h->act);
+    aq.q = h->act_q;
+    aq.scale = h->act_scale;
+    aq.routes = rows * d.top_k;
+    aq.I = d.inter;
+    before();
+    if (!after(launch_act_quant(aq, s, pdl), "act_quant")) return MUSEMOE_ECUDA;
+  }
+
+  // 4. w2
+  ep.role = 1;
+  ep.N = d.pooled;
+  ep.K = d.inter;
+  ep.w = w->w2;
+  ep.scale = w->w2_scale;
+  ep.gscale = w->w2_gscale;
+  ep.b = h->quant == kFP8 ? h->act_q : h->act;
+  ep.b_scale = h->act_scale;
+  ep.b_by_token = 0;
+  ep.out = h->y;
+  ep.grid = h->expert_grid[1][nt_index(nte)];
+  before();
+  if (!after(launch_expert(ep, nte, s, pdl), "w2")) return MUSEMOE_ECUDA;
+
+  // 5. post-expert norm, weight, reduce
+  FinalizeParams fz{};
+  fz.y = h->y;
+  fz.weights = h->weights;
+  fz.w_post_norm = w->w_post_norm;
+  fz.moe_out = h->moe_out;
+  fz.rows = rows;
+  fz.k = d.top_k;
+  fz.P = d.pooled;
+  fz.eps = h->cfg.norm_eps;
+  before();
+  if (!after(launch_finalize(fz, s, pdl), "finalize")) return MUSEMOE_ECUDA;
+
+  // 6. unpooler GEMV
+  const GemvSplit su = gemv_split(d.hidden, d.pooled, rows, h->sms);
+  FrontParams up{};
+  up.x = h->moe_out;
+  up.rows = rows;
+  up.router_ctas = 0;
+  up.ks_r = 1;
+  up.w = w->w_unpool;
+  up.part = h->unpool_part;
+  up.M = d.hidden;
+  up.K = d.pooled;
+  up.ks = su.ks;
+  up.kchunks_per_split = su.kcps;
+  up.token_blocks = su.tb;
+  before();
+  if (!after(launch_front(up, nt_front(rows), s, pdl), "unpool")) return MUSEMOE_ECUDA;
+
+  // 7. FFN boundary
+  BoundaryParams bp{};
+  bp.part = h->unpool_part;
+  bp.ks = su.ks;
+  bp.stream = stream;
+  bp.out = out;
+  bp.w_ffn_norm = w->w_ffn_norm;
+  bp.w_next_norm = w->w_next_norm;
+  bp.gate = w->gate;
+  bp.u_tap = taps ? taps->u : nullptr;
+  bp.rows = rows;
+  bp.H = d.hidden;
+  bp.eps = h->cfg.norm_eps;
+  before();
+  if (!after(launch_boundary(bp, s, pdl), "boundary")) return MUSEMOE_ECUDA;
+
+  if (taps) {
+    struct Cp {
+      void* dst;
+      const void* src;
+      size_t bytes;
+    } cps[] = {
+        {taps->logits, h->logits, (size_t)rows * d.experts * 4},
+        {taps->ids, h->ids, (size_t)rows * d.top_k * 4},
+        {taps->weights, h->weights, (size_t)rows * d.top_k * 4},
+        {taps->h, h->h, (size_t)rows * d.pooled * 2},
+        {taps->act, h->act, (size_t)rows * d.top_k * d.inter * 2},
+        {taps->y, h->y, (size_t)rows * d.top_k * d.pooled * 4},
+        {taps->moe_out, h->moe_out, (size_t)rows * d.pooled * 2},
+    };
+    for (const Cp& c : cps)
+      if (c.dst) {
+        const cudaError_t r = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, s);
+        if (r != cudaSuccess) return cuda_err(h, r, "tap copy");
+      }
+  }
+  (void)e;
+  if (bad_event) {
+    cudaGetLastError();  // clear the failed record
+    return set_err(h, MUSEMOE_EINVAL, "taps->events holds an event that could not be recorded");
+  }
+  return MUSEMOE_OK;
+}
+
+musemoe_status check_call(musemoe_handle* h, const musemoe_weights* w, const void* x,
+                          const void* stream, const void* out, int32_t rows, bool route_only) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  if (rows < 1 || rows > h->d.max_rows)
+    return set_err(h, MUSEMOE_EINVAL, fmt("rows %d outside 1..max_rows (%d)", rows, h->d.max_rows));
+  std::vector<std::string> bad;
+  if (!x) bad.push_back("x is NULL");
+  else if (!aligned16(x)) bad.push_back("x is not 16-byte aligned");
+  if (!route_only) {
+    if (!stream) bad.push_back("stream is NULL");
+    else if (!aligned16(stream)) bad.push_back("stream is not 16-byte aligned");
+    if (!out) bad.push_back("out is NULL");
+    else if (!aligned16(out)) bad.push_back("out is not 16-byte aligned");
+  }
+  const std::string wb = check_weights(h, w, route_only);
+  if (!wb.empty()) bad.push_back(wb);
+  if (!bad.empty()) return set_err(h, MUSEMOE_EINVAL, join(bad));
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != h->device)
+    return set_err(h, MUSEMOE_EINVAL,
+                   fmt("current device %d is not the handle's device %d", dev, h->device));
+  return MUSEMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+musemoe_status musemoe_create(const musemoe_dims* dims, int32_t quant, const musemoe_config* config,
+                              musemoe_handle** out) {
+  if (out) *out = nullptr;
+  if (!dims || !config || !out) return set_err(nullptr, MUSEMOE_EINVAL, "dims, config and out must not be NULL");
+  const std::vector<std::string> r = refusals(dims, quant, config);
+  if (!r.empty()) return set_err(nullptr, MUSEMOE_EUNSUPPORTED, join(r));
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_err(nullptr, MUSEMOE_ECUDA, fmt("no CUDA device: %s", cudaGetErrorString(e)));
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return set_err(nullptr, MUSEMOE_ECUDA, fmt("cudaGetDeviceProperties: %s", cudaGetErrorString(e)));
+  if (!(prop.major == 10 && prop.minor == 3))
+    return set_err(nullptr, MUSEMOE_EUNSUPPORTED,
+                   fmt("device %d is sm_%d%d; the kernels are built for sm_103a", dev, prop.major,
+                       prop.minor));
+  musemoe_handle* h = new (std::nothrow) musemoe_handle();
+  if (!h) return set_err(nullptr, MUSEMOE_ENOMEM, "host allocation failed");
+  h->d = *dims;
+  h->quant = quant;
+  h->cfg = *config;
+  h->device = dev;
+  h->sms = prop.multiProcessorCount;
+  h->max_routes = dims->max_rows * dims->top_k;
+  h->max_groups = std::min(dims->experts, h->max_routes) + (h->max_routes + 7) / 8 + 1;
+  for (int role = 0; role < 2; ++role)
+    for (int i = 0; i < 4; ++i)
+      h->expert_grid[role][i] = h->sms * expert_ctas_per_sm(quant, role, 1 << i);
+  Layout L;
+  plan(h, L);
+  h->ws_bytes = L.off;
+  e = cudaMalloc(&h->ws, h->ws_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    return set_err(nullptr, MUSEMOE_ENOMEM,
+                   fmt("workspace of %zu bytes: %s", L.off, cudaGetErrorString(e)));
+  }
+  for (auto& it : L.items) *it.first = static_cast<char*>(h->ws) + it.second;
+  e = cudaMemset(h->ws, 0, h->ws_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return set_err(nullptr, MUSEMOE_ECUDA, fmt("workspace init: %s", cudaGetErrorString(e)));
+  }
+  *out = h;
+  return MUSEMOE_OK;
+}
+
+void musemoe_destroy(musemoe_handle* h) {
+  if (!h) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->ws);
+  if (cur >= 0) cudaSetDevice(cur);
+  delete h;
+}
+
+const char* musemoe_last_error(const musemoe_handle* h) {
+  return h ? h->err.c_str() : g_thread_err.c_str();
+}
+
+size_t musemoe_workspace_bytes(const musemoe_dims* dims, int32_t quant) {
+  if (!dims) return 0;
+  musemoe_config c{};
+  c.route_scale = 1.f;
+  if (!refusals(dims, quant, &c).empty()) return 0;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  musemoe_handle h;
+  h.d = *dims;
+  h.quant = quant;
+  h.sms = sms;
+  h.max_routes = dims->max_rows * dims->top_k;
+  h.max_groups = std::min(dims->experts, h.max_routes) + (h.max_routes + 7) / 8 + 1;
+  Layout L;
+  plan(&h, L);
+  return L.off;
+}
+
+int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 8 : 7; }
+
+const char* musemoe_kernel_name(int32_t quant, int32_t i) {
+  static const char* fp4[] = {"front", "route", "w13", "w2", "finalize", "unpool", "boundary"};
+  static const char* fp8[] = {"front", "route", "w13", "act_quant", "w2", "finalize", "unpool", "boundary"};
+  if (quant == kFP8) return (i >= 0 && i < 8) ? fp8[i] : "";
+  return (i >= 0 && i < 7) ? fp4[i] : "";
+}
+
+musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const uint8_t* w13_src,
+                                    uint8_t* w13_dst, const uint8_t* w2_src, uint8_t* w2_dst,
+                                    musemoe_stream_t stream) {
+  if (!d) return set_err(nullptr, MUSEMOE_EINVAL, "dims is NULL");
+  musemoe_config c{};
+  c.route_scale = 1.f;
+  const std::vector<std::string> r = refusals(d, quant, &c);
+  if (!r.empty()) return set_err(nullptr, MUSEMOE_EUNSUPPORTED, join(r));
+  if (!w13_src || !w13_dst || !w2_src || !w2_dst)
+    return set_err(nullptr, MUSEMOE_EINVAL, "expert tensor pointers must not be NULL");
+  if (!aligned16(w13_src) || !aligned16(w13_dst) || !aligned16(w2_src) || !aligned16(w2_dst))
+    return set_err(nullptr, MUSEMOE_EINVAL, "expert tensors must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t E = d->experts, P = d->pooled, I = d->inter;
+  const size_t b13 = E * 2 * I * (quant == kFP8 ? P : P / 2);
+  const size_t b2 = E * P * (quant == kFP8 ? I : I / 2);
+  cudaError_t e;
+  if (quant == kFP8) {
+    e = (w13_src == w13_dst) ? cudaSuccess
+                             : cudaMemcpyAsync(w13_dst, w13_src, b13, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && w2_src != w2_dst)
+      e = cudaMemcpyAsync(w2_dst, w2_src, b2, cudaMemcpyDeviceToDevice, s);
+  } else {
+    e = launch_pack_fp4(w13_src, w13_dst, b13, s);
+    if (e == cudaSuccess) e = launch_pack_fp4(w2_src, w2_dst, b2, s);
+  }
+  if (e != cudaSuccess) return set_err(nullptr, MUSEMOE_ECUDA, fmt("pack: %s", cudaGetErrorString(e)));
+  return MUSEMOE_OK;
+}
+
+musemoe_status musemoe_route(musemoe_handle* h, const musemoe_weights* w, const uint16_t* x,
+                             int32_t rows, int32_t* ids_out, float* weights_out,
+                             musemoe_stream_t stream) {
+  musemoe_status st = check_call(h, w, x, nullptr, nullptr, rows, true);
+  if (st != MUSEMOE_OK) return st;
+  if (!ids_out || !weights_out || !aligned16(ids_out) || !aligned16(weights_out))
+    return set_err(h, MUSEMOE_EINVAL, "ids_out and weights_out must be non-NULL and 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const musemoe_dims& d = h->d;
+  const int ks_r = router_split(d.experts, d.hidden, rows, h->sms);
+  FrontParams fp{};
+  fp.x = x;
+  fp.rows = rows;
+  fp.w_router = w->w_router;
+  fp.logit_part = h->logit_part;
+  fp.E = d.experts;
+  fp.ks_r = ks_r;
+  fp.router_ctas = router_ctas(d.experts, rows, ks_r);
+  fp.M = 0;
+  fp.K = d.hidden;
+  fp.ks = 1;
+  fp.kchunks_per_split = 1;
+  fp.token_blocks = 1;
+  cudaError_t e = launch_front(fp, 1, s, true);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_err(h, e, "launch of router");
+  RouteParams rp{};
+  rp.logit_part = h->logit_part;
+  rp.expert_bias = w->expert_bias;
+  rp.logits = h->logits;
+  rp.ids = ids_out;
+  rp.weights = weights_out;
+  rp.rows = rows;
+  rp.E = d.experts;
+  rp.k = d.top_k;
+  rp.ks_r = ks_r;
+  rp.score = h->cfg.score;
+  rp.has_multiplier = h->cfg.has_multiplier;
+  rp.multiplier = h->cfg.multiplier;
+  rp.has_division_eps = h->cfg.has_division_eps;
+  rp.division_eps = h->cfg.division_eps;
+  rp.route_scale = h->cfg.route_scale;
+  e = launch_route(rp, s, true);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_err(h, e, "launch of route");
+  return MUSEMOE_OK;
+}
+
+musemoe_status musemoe_forward(musemoe_handle* h, const musemoe_weights* w, const uint16_t* x,
+                               float* stream, uint16_t* out, int32_t rows, musemoe_stream_t s) {
+  musemoe_status st = check_call(h, w, x, stream, out, rows, false);
+  if (st != MUSEMOE_OK) return st;
+  return launch_chain(h, w, x, stream, out, rows, reinterpret_cast<cudaStream_t>(s), nullptr);
+}
+
+musemoe_status musemoe_forward_debug(musemoe_handle* h, const musemoe_weights* w, const uint16_t* x,
+                                     float* stream, uint16_t* out, int32_t rows, musemoe_stream_t s,
+                                     const musemoe_taps* taps) {
+  musemoe_status st = check_call(h, w, x, stream, out, rows, false);
+  if (st != MUSEMOE_OK) return st;
+  return launch_chain(h, w, x, stream, out, rows, reinterpret_cast<cudaStream_t>(s), taps);
+}
+
+musemoe_status musemoe_forward_host(musemoe_handle* h, const musemoe_weights* w,
+                                    const uint16_t* x_host, float* stream_host, uint16_t* out_host,
+                                    int32_t rows, musemoe_stream_t stream) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  if (!x_host || !stream_host || !out_host)
+    return set_err(h, MUSEMOE_EINVAL, "host buffers must not be NULL");
+  if (rows < 1 || rows > h->d.max_rows)
+    return set_err(h, MUSEMOE_EINVAL, fmt("rows %d outside 1..max_rows (%d)", rows, h->d.max_rows));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nh = (size_t)rows * h->d.hidden;
+  cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, nh * 2, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->stream_stage, stream_host, nh * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_err(h, e, "copy to device");
+  musemoe_status st = check_call(h, w, h->x_stage, h->stream_stage, h->out_stage, rows, false);
+  if (st != MUSEMOE_OK) return st;
+  st = launch_chain(h, w, h->x_stage, h->stream_stage, h->out_stage, rows, s, nullptr);
+  if (st != MUSEMOE_OK) return st;
+  e = cudaMemcpyAsync(stream_host, h->stream_stage, nh * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, h->out_stage, nh * 2, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_err(h, e, "copy to host");
+  return MUSEMOE_OK;
+}
+
+musemoe_status musemoe_poll_health(musemoe_handle* h) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpy(&word, h->health, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->health, 0, 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_err(h, e, "health read");
+  if (word) {
+    std::string m;
+    if (word & kHealthHRange) m += "h beyond the fp16 operand range; ";
+    if (word & kHealthActRange) m += "SiLU(gate)*up beyond the fp16 operand range; ";
+    return set_err(h, MUSEMOE_ERANGE, m);
+  }
+  return MUSEMOE_OK;
+}
+
+}  // extern "C"

@@ -76,6 +76,32 @@ def round_bf16(v) -> np.ndarray:
     return np.where(big, np.copysign(np.inf, r), r)
 
 
+# Width of the band, relative to the RMS of the row, inside which a rounding
+# decision counts as a near tie (a bound on the fp32 accumulation error of
+# the dot products and norms that feed the rounding points).
+NEAR_TIE_BAND = 2.0 ** -16
+
+
+def round_bf16_near(v, near=None, band=NEAR_TIE_BAND):
+    """round_bf16 with the near-tie rule of the rounding decision.
+
+    ``near`` holds another computation's bf16 values of the same quantity.
+    Where such a value is the bf16 rounding of some value within
+    ``band * RMS(row of v)`` of v, the rounding decision is a near tie (both
+    results are correct to working precision) and ``near`` is taken;
+    everywhere else the result is round_bf16(v). Returns (values, number of
+    elements taken from ``near`` that differ from round_bf16(v)).
+    """
+    r = round_bf16(v)
+    if near is None:
+        return r, 0
+    v = np.asarray(v, dtype=np.float64)
+    near = np.asarray(near, dtype=np.float64)
+    d = band * np.sqrt(np.mean(v * v, axis=-1, keepdims=True))
+    ok = (near >= round_bf16(v - d)) & (near <= round_bf16(v + d))
+    return np.where(ok, near, r), int(np.count_nonzero(ok & (near != r)))
+
+
 def f64_to_bf16_bits(v) -> np.ndarray:
     """bf16-representable float64 values -> their bit patterns."""
     f = np.asarray(v, dtype=np.float64).astype(np.float32)
@@ -182,6 +208,19 @@ class Routing:
     gap: np.ndarray        # [b] selection[k-th] - selection[(k+1)-th]; inf if k == E
 
 
+def weights_for_ids(scores, ids, route_scale: float, division_eps=None) -> np.ndarray:
+    """Gather the UNBIASED scores of the selected ids, divide by (their sum +
+    division_eps), multiply by route_scale; stored as fp32 (muse_moe_runner
+    page, MuseSpark1xRouter._compute_routing_native, after the top-k)."""
+    ids = np.asarray(ids, dtype=np.int64)
+    rows = np.arange(ids.shape[0])[:, None]
+    w = np.asarray(scores, dtype=np.float64)[rows, ids]
+    denom = w.sum(axis=-1, keepdims=True)
+    if division_eps is not None:
+        denom = denom + float(np.float32(division_eps))
+    return round_f32(w / denom * float(np.float32(route_scale)))
+
+
 def route(logits, expert_bias, top_k: int, route_scale: float,
           multiplier: float | None = None, score: str = "sigmoid",
           division_eps: float | None = None) -> Routing:
@@ -220,11 +259,7 @@ def route(logits, expert_bias, top_k: int, route_scale: float,
         gap = sel[rows[:, 0], ids[:, -1]] - sel[rows[:, 0], order[:, top_k]]
     else:
         gap = np.full(b, np.inf)
-    w = s[rows, ids]
-    denom = w.sum(axis=-1, keepdims=True)
-    if division_eps is not None:
-        denom = denom + float(np.float32(division_eps))
-    weights = round_f32(w / denom * float(np.float32(route_scale)))
+    weights = weights_for_ids(s, ids, route_scale, division_eps)
     return Routing(ids.astype(np.int32), weights, s, sel, gap)
 
 
@@ -234,7 +269,7 @@ def route(logits, expert_bias, top_k: int, route_scale: float,
 
 
 def pre_expert(x_bf16, w_pool_bf16, w_pre_norm_bf16, eps: float,
-               pre_norm: bool = True) -> np.ndarray:
+               pre_norm: bool = True, near=None, ties=None) -> np.ndarray:
     """Pooler GEMM H -> P, then pre_expert_norm (providers page, MoEProvider
     docstring: "pooler GEMM and gather + pre_expert_norm"). The pooled vector
     is not rounded before the norm (the pooler and the norm run fused); the
@@ -242,7 +277,10 @@ def pre_expert(x_bf16, w_pool_bf16, w_pre_norm_bf16, eps: float,
     h_raw = bf16_to_f64(x_bf16) @ bf16_to_f64(w_pool_bf16).T
     if pre_norm:
         h_raw = rms_norm(h_raw, bf16_to_f64(w_pre_norm_bf16), eps)
-    return round_bf16(h_raw)
+    h, n = round_bf16_near(h_raw, near)
+    if ties is not None:
+        ties["h"] = ties.get("h", 0) + n
+    return h
 
 
 def quantize_rows_e4m3(v: np.ndarray):
@@ -307,7 +345,8 @@ def silu(z):
 
 
 def expert_outputs(h: np.ndarray, ids: np.ndarray, quant: str, t: dict,
-                   inter: int) -> np.ndarray:
+                   inter: int, act_out: np.ndarray | None = None, near_act=None,
+                   ties=None) -> np.ndarray:
     """One unweighted output per selected route, y [b, k, P] (muse_moe_runner
     page, MuseSparkAiterExperts: the experts run with unit weights so that
     the router weighting happens after the post-expert norm).
@@ -316,7 +355,9 @@ def expert_outputs(h: np.ndarray, ids: np.ndarray, quant: str, t: dict,
     up = gu[I:] (reading: the vLLM fused-w13 order, gate rows first);
     a = bf16(silu(gate) * up) (the MoE activations are bf16); y = W2_e a.
     FP8 W8A8 quantizes both expert inputs per row (quantize_rows_e4m3) and
-    multiplies the e4m3 values back by their scales.
+    multiplies the e4m3 values back by their scales. ``act_out`` ([b, k, I]),
+    when given, receives the bf16 activations; ``near_act`` applies the
+    near-tie rule of round_bf16_near to their rounding.
     """
     b, k = ids.shape
     P = h.shape[-1]
@@ -330,7 +371,12 @@ def expert_outputs(h: np.ndarray, ids: np.ndarray, quant: str, t: dict,
         tok, slot = np.nonzero(ids == e)
         w13, w2 = dequant_expert(quant, t, int(e))
         gu = h_in[tok] @ w13.T                       # [n, 2I]
-        a = round_bf16(silu(gu[:, :inter]) * gu[:, inter:])
+        a, n = round_bf16_near(silu(gu[:, :inter]) * gu[:, inter:],
+                               None if near_act is None else near_act[tok, slot])
+        if ties is not None:
+            ties["act"] = ties.get("act", 0) + n
+        if act_out is not None:
+            act_out[tok, slot] = a
         if quant == "fp8":
             qa, sa = quantize_rows_e4m3(a)
             a = e4m3_decode(qa) * sa[:, None]
@@ -343,13 +389,18 @@ def expert_outputs(h: np.ndarray, ids: np.ndarray, quant: str, t: dict,
 # --------------------------------------------------------------------------
 
 
-def finalize(y: np.ndarray, weights: np.ndarray, w_post_bf16, eps: float) -> np.ndarray:
+def finalize(y: np.ndarray, weights: np.ndarray, w_post_bf16, eps: float, near=None,
+             ties=None) -> np.ndarray:
     """post_expert_norm of every route row, times its router weight, summed
     over the k routes (muse_moe_runner page, MuseSparkTopKWeightAndReduce.apply,
     unfused branch); the result moe_out is stored as bf16 (providers page,
     RoutedMoE buffer ``moe_out``)."""
     n = rms_norm(y, bf16_to_f64(w_post_bf16), eps)
-    return round_bf16((n * np.asarray(weights, dtype=np.float64)[..., None]).sum(axis=1))
+    out, c = round_bf16_near((n * np.asarray(weights, dtype=np.float64)[..., None]).sum(axis=1),
+                             near)
+    if ties is not None:
+        ties["moe_out"] = ties.get("moe_out", 0) + c
+    return out
 
 
 def unpool(moe_out: np.ndarray, w_unpool_bf16) -> np.ndarray:
@@ -359,7 +410,7 @@ def unpool(moe_out: np.ndarray, w_unpool_bf16) -> np.ndarray:
 
 
 def boundary(u: np.ndarray, stream, w_ffn_norm_bf16, gate: float,
-             w_next_norm_bf16, eps: float):
+             w_next_norm_bf16, eps: float, near=None, ties=None):
     """FFN boundary (providers page, BoundaryProvider docstring): post_ffn_norm
     of u, gated add into the fp32 stream in place, next pre-norm into bf16 out.
     Reading: the gated add is stream + gate * post_ffn_norm(u), one scalar gate
@@ -367,7 +418,9 @@ def boundary(u: np.ndarray, stream, w_ffn_norm_bf16, gate: float,
     Returns (new stream as fp32 values, out as bf16 values)."""
     add = rms_norm(u, bf16_to_f64(w_ffn_norm_bf16), eps)
     s_new = round_f32(np.asarray(stream, dtype=np.float64) + float(np.float32(gate)) * add)
-    out = round_bf16(rms_norm(s_new, bf16_to_f64(w_next_norm_bf16), eps))
+    out, c = round_bf16_near(rms_norm(s_new, bf16_to_f64(w_next_norm_bf16), eps), near)
+    if ties is not None:
+        ties["out"] = ties.get("out", 0) + c
     return s_new, out
 
 
@@ -378,34 +431,34 @@ def boundary(u: np.ndarray, stream, w_ffn_norm_bf16, gate: float,
 
 def block(x_bf16, stream, w: dict, *, top_k: int, route_scale: float,
           multiplier=None, score="sigmoid", division_eps=None, quant="mxfp4",
-          norm_eps=1e-6, pre_norm=True, force_ids=None) -> dict:
+          norm_eps=1e-6, pre_norm=True, force_ids=None, near=None) -> dict:
     """One MoE decode block followed by its FFN boundary.
 
     ``w`` holds the layer's tensors in storage form (see synth.layer_tensors).
     ``force_ids`` replaces the selected ids (same order) to continue the chain
     on another valid selection at a near tie; the weights are then recomputed
-    from those ids with the same rule.
+    from those ids with the same rule. ``near`` (dict with any of h, act,
+    moe_out, out) applies the near-tie rule of round_bf16_near at those
+    rounding points; result["near_ties"] counts the elements it decided.
     Returns every intermediate: logits, routing, h, y, moe_out, u, stream, out
     (and out_bits, the bf16 bit patterns of out).
     """
     logits = router_logits(x_bf16, w["w_router"])
     r = route(logits, w["expert_bias"], top_k, route_scale, multiplier, score, division_eps)
     if force_ids is not None:
-        ids = np.asarray(force_ids, dtype=np.int64)
-        rows = np.arange(ids.shape[0])[:, None]
-        ws = r.scores[rows, ids]
-        denom = ws.sum(axis=-1, keepdims=True)
-        if division_eps is not None:
-            denom = denom + float(np.float32(division_eps))
-        r = Routing(ids.astype(np.int32), round_f32(ws / denom * float(np.float32(route_scale))),
+        ids = np.asarray(force_ids, dtype=np.int32)
+        r = Routing(ids, weights_for_ids(r.scores, ids, route_scale, division_eps),
                     r.scores, r.selection, r.gap)
-    h = pre_expert(x_bf16, w["w_pool"], w["w_pre_norm"], norm_eps, pre_norm)
+    near = near or {}
+    ties: dict = {}
+    h = pre_expert(x_bf16, w["w_pool"], w["w_pre_norm"], norm_eps, pre_norm, near.get("h"), ties)
     inter = (w["w13"].shape[1]) // 2
-    y = expert_outputs(h, r.ids, quant, w, inter)
-    moe_out = finalize(y, r.weights, w["w_post_norm"], norm_eps)
+    act = np.zeros(r.ids.shape + (inter,))
+    y = expert_outputs(h, r.ids, quant, w, inter, act, near.get("act"), ties)
+    moe_out = finalize(y, r.weights, w["w_post_norm"], norm_eps, near.get("moe_out"), ties)
     u = unpool(moe_out, w["w_unpool"])
     s_new, out = boundary(u, stream, w["w_ffn_norm"], float(w["gate"][0]),
-                          w["w_next_norm"], norm_eps)
+                          w["w_next_norm"], norm_eps, near.get("out"), ties)
     return dict(logits=logits, routing=r, ids=r.ids, weights=r.weights, gap=r.gap,
-                h=h, y=y, moe_out=moe_out, u=u, stream=s_new, out=out,
-                out_bits=f64_to_bf16_bits(out))
+                h=h, act=act, y=y, moe_out=moe_out, u=u, stream=s_new, out=out,
+                out_bits=f64_to_bf16_bits(out), near_ties=ties)

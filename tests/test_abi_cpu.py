@@ -1,0 +1,70 @@
+"""The C ABI library builds, loads and exports every entry point the header
+declares; without a GPU, create fails cleanly with a status and a reason.
+CPU only (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_decode_layer_router_gb300 as mm
+from moe_decode_layer_router_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "musemoe.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(musemoe_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mm.library()
+
+
+def test_header_and_binding_agree():
+    assert _declared() == sorted(mm.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_workspace_bytes_and_names_need_no_gpu(lib):
+    d = mm.Dims(max_rows=8, hidden=5120, pooled=2048, inter=1024, experts=128, top_k=8)
+    assert mm.musemoe_workspace_bytes(d, mm.MUSEMOE_MXFP4) > 8 * 8 * 2048 * 4  # >= y
+    bad = mm.Dims(max_rows=8, hidden=5120, pooled=2000, inter=1024, experts=128, top_k=8)
+    assert mm.musemoe_workspace_bytes(bad, mm.MUSEMOE_MXFP4) == 0
+    assert mm.musemoe_kernel_name(mm.MUSEMOE_MXFP4, 2) == "w13"
+
+
+def test_create_rejects_bad_arguments_before_touching_a_device(lib):
+    d = mm.Dims(max_rows=0, hidden=100, pooled=256, inter=128, experts=16, top_k=2)
+    c = mm.Config(score=0, route_scale=2.5, norm_eps=1e-6, pre_expert_norm=1)
+    with pytest.raises(mm.MuseMoEError) as ei:
+        mm.musemoe_create(d, mm.MUSEMOE_MXFP4, c)
+    assert ei.value.status == mm.MUSEMOE_EUNSUPPORTED
+    assert "max_rows" in str(ei.value) and "hidden 100" in str(ei.value)
+
+
+def test_create_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    d = mm.Dims(max_rows=4, hidden=512, pooled=256, inter=128, experts=16, top_k=2)
+    c = mm.Config(score=0, route_scale=2.5, norm_eps=1e-6, pre_expert_norm=1)
+    with pytest.raises(mm.MuseMoEError) as ei:
+        mm.musemoe_create(d, mm.MUSEMOE_MXFP4, c)
+    assert ei.value.status == mm.MUSEMOE_ECUDA
+    assert mm.musemoe_last_error(None)
+
+
+def test_calls_with_null_handle_fail_cleanly(lib):
+    assert lib.musemoe_forward(None, None, None, None, None, 1, None) == mm.MUSEMOE_EINVAL
+    assert lib.musemoe_poll_health(None) == mm.MUSEMOE_EINVAL
+    lib.musemoe_destroy(None)

@@ -1,0 +1,205 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, element by
+element on the same seeded inputs: the full block on every single-layer
+workload at full size, its intermediates, and the edge cases."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import moe_decode_layer_router_gb300 as mm
+import oracle as O
+import synth
+from moe_decode_layer_router_gb300 import _build
+
+from . import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    _build.build()
+    mm.library()
+
+
+def _compare_block(cfg, w, x, st, run=None, pre_norm=True, report=None):
+    """Stage-wise parity (the oracle continues through the GPU's near-tie
+    decisions, so every stage is checked on the same inputs) and the
+    independent end-to-end parity of the block outputs."""
+    t, W = H.upload_layer(cfg, w)
+    own = run is None
+    run = run or H.Run(cfg, pre_norm=pre_norm)
+    try:
+        g = run.forward(W, x, st)
+        assert mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_OK
+    finally:
+        if own:
+            run.close()
+    rep = H.compare(cfg, w, x, st, g, pre_norm=pre_norm)
+    if report is not None:
+        report.update(rep)
+    return g, rep
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "verify", "large"])
+def test_block_parity_full_size(name, record_property):
+    cfg = synth.CONFIGS[name]
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    rep = {}
+    _compare_block(cfg, w, x, st, report=rep)
+    for k, v in rep.items():
+        record_property(k, v)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8])
+@pytest.mark.parametrize("score", [synth.SIGMOID, synth.SOFTMAX])
+def test_tiny_dims_every_quant_and_score(quant, score):
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, score=score, seed=11)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st)
+
+
+@pytest.mark.parametrize("rows", [1, 3, 13])
+def test_ragged_rows(rows):
+    # rows below the handle's max_rows, including a ragged tail of a token tile
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=16, seed=5)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    run = H.Run(cfg, max_rows=16)
+    try:
+        _compare_block(cfg, w, x[:rows].copy(), st[:rows].copy(), run=run)
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("top_k", [1, 16])
+def test_top_k_extremes(top_k):
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], top_k=top_k, seed=6)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st)
+
+
+def test_no_multiplier_no_eps_no_pre_norm():
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], multiplier=None, division_eps=None, seed=7)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st, pre_norm=False)
+
+
+def test_all_equal_scores_go_to_the_lowest_ids():
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], seed=8)
+    w = synth.layer_tensors(cfg)
+    w["expert_bias"][:] = 0.0
+    x, st = synth.activations(cfg)
+    x[:] = 0  # zero input: every logit 0, every score sigmoid(0)
+    g, _ = _compare_block(cfg, w, x, st)
+    assert (g["ids"] == np.arange(cfg.top_k)).all()
+    assert np.all(g["moe_out"] == 0)
+    np.testing.assert_array_equal(g["stream"], st.astype(np.float64))
+
+
+def test_large_rows_multiple_token_groups():
+    # 64 rows all routed to the same few experts: token groups of 64 routes
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=64, top_k=2, hot_experts=2,
+                              hot_bias=5.0, seed=9)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st)
+
+
+def test_route_entry_point_matches_oracle():
+    cfg = synth.CONFIGS["decode"]
+    d = synth.dense_tensors(cfg, 0)
+    x, _ = synth.activations(cfg)
+    wr, wb = H.to_dev(d["w_router"]), H.to_dev(d["expert_bias"])
+    W = mm.make_weights({"w_router": wr, "expert_bias": wb})
+    run = H.Run(cfg)
+    try:
+        ids = torch.empty((cfg.rows, cfg.top_k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((cfg.rows, cfg.top_k), dtype=torch.float32, device="cuda")
+        mm.musemoe_route(run.handle, W, H.to_dev(x), cfg.rows, ids, wts)
+        torch.cuda.synchronize()
+    finally:
+        run.close()
+    r = O.route(O.router_logits(x, d["w_router"]), d["expert_bias"], cfg.top_k, cfg.route_scale,
+                cfg.multiplier, cfg.score, cfg.division_eps)
+    gi = ids.cpu().numpy()
+    H.check_ids(gi, r, cfg.top_k)
+    want = O.weights_for_ids(r.scores, gi, cfg.route_scale, cfg.division_eps)
+    np.testing.assert_allclose(wts.cpu().numpy(), want, rtol=H.WEIGHT_RTOL, atol=0)
+
+
+def test_forward_is_deterministic_and_graph_capturable():
+    cfg = synth.CONFIGS["decode"]
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    t, W = H.upload_layer(cfg, w)
+    run = H.Run(cfg)
+    try:
+        xd = H.to_dev(x)
+        outs = []
+        for _ in range(2):
+            sd = H.to_dev(st)
+            out = torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16, device="cuda")
+            mm.musemoe_forward(run.handle, W, xd, sd, out, cfg.rows)
+            torch.cuda.synchronize()
+            outs.append((sd.clone(), out.clone()))
+        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+        # capture one forward in a CUDA graph and replay it
+        sd = H.to_dev(st)
+        out = torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16, device="cuda")
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            mm.musemoe_forward(run.handle, W, xd, sd, out, cfg.rows, s)  # warm
+        torch.cuda.synchronize()
+        sd.copy_(H.to_dev(st))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            mm.musemoe_forward(run.handle, W, xd, sd, out, cfg.rows, s)
+        sd.copy_(H.to_dev(st))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(sd, outs[0][0]) and torch.equal(out, outs[0][1])
+    finally:
+        run.close()
+
+
+def test_forward_host_matches_device_forward():
+    cfg = synth.CONFIGS["tiny"]
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    t, W = H.upload_layer(cfg, w)
+    run = H.Run(cfg)
+    try:
+        g = run.forward(W, x, st, taps=False)
+        xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+        sh = torch.from_numpy(st.copy()).pin_memory()
+        oh = torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16).pin_memory()
+        mm.musemoe_forward_host(run.handle, W, xh, sh, oh, cfg.rows)
+    finally:
+        run.close()
+    np.testing.assert_array_equal(oh.numpy().view(np.uint16), g["out_bits"])
+    np.testing.assert_array_equal(sh.numpy().astype(np.float64), g["stream"])
+
+
+def test_pack_out_of_place_equals_in_place():
+    cfg = synth.CONFIGS["tiny"]
+    e = synth.expert_tensors(cfg, 0)
+    a13, a2 = H.to_dev(e["w13"]), H.to_dev(e["w2"])
+    b13, b2 = torch.empty_like(a13), torch.empty_like(a2)
+    mm.musemoe_pack_experts(H.dims_of(cfg), mm.MUSEMOE_MXFP4, a13, b13, a2, b2)
+    mm.musemoe_pack_experts(H.dims_of(cfg), mm.MUSEMOE_MXFP4, a13, a13, a2, a2)
+    torch.cuda.synchronize()
+    assert torch.equal(a13, b13) and torch.equal(a2, b2)
+    # the documented byte permutation, checked on the host
+    src = e["w13"].reshape(-1, 64)
+    got = b13.cpu().numpy().reshape(-1, 64)
+    for qq in range(4):
+        for j in range(8):
+            for bb in range(2):
+                np.testing.assert_array_equal(got[:, 16 * qq + 2 * j + bb], src[:, 8 * j + 2 * qq + bb])

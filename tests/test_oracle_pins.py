@@ -419,3 +419,23 @@ def test_boundary_linearity_and_zero_gate():
     want = torch.nn.functional.rms_norm(torch.from_numpy(s1), (48,),
                                         torch.from_numpy(O.bf16_to_f64(wn)), eps=1e-6).numpy()
     np.testing.assert_array_equal(out, O.round_bf16(want))
+
+
+# ---------------------------------------------------------------- near-tie rounding rule
+
+def test_round_bf16_near_takes_only_values_inside_the_band():
+    row = np.array([[1.0 + 2.0 ** -8, 1.0 + 2.0 ** -6 + 1e-3, 3e-7, 1.0]])
+    # the first element is exactly a rounding midpoint: either neighbour is valid
+    near = np.array([[1.0 + 2.0 ** -7, 1.0 + 2.0 ** -6, 2.9e-7, 1.0]])
+    out, n = O.round_bf16_near(row, near, band=2.0 ** -16)
+    assert out[0, 0] == 1.0 + 2.0 ** -7 and n >= 1
+    # the second is far from a midpoint: the other neighbour is refused
+    assert out[0, 1] == O.round_bf16(row[0, 1])
+    # a near-zero element: any bf16 value within band * RMS(row) is accepted
+    assert out[0, 2] == 2.9e-7
+    far = np.array([[1.0 + 2.0 ** -8, 1.0 + 2.0 ** -6 + 1e-3, 5e-4, 1.0]])
+    out2, _ = O.round_bf16_near(row, far, band=2.0 ** -16)
+    assert out2[0, 2] == O.round_bf16(3e-7)
+    # without a hint it is plain round-to-nearest-even
+    out3, n3 = O.round_bf16_near(row)
+    assert n3 == 0 and np.array_equal(out3, O.round_bf16(row))
