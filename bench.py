@@ -1,0 +1,451 @@
+"""Benchmark of the MuseSpark1x MoE decode block on GB300 (one JSON line).
+
+A step is one pass of the whole block (router, routing, pooler + pre-expert
+norm, grouped experts, post-expert norm + weighted sum, unpooler, FFN
+boundary) over one batch of the decode workload: b=8 rows, H=5120, P=2048,
+I=1024, E=128, top-8, MXFP4 experts. Steps replay a CUDA graph of
+musemoe_forward; they rotate over 4 independent weight sets (about 1.9 GB,
+far beyond the 129 MB L2) so every step reads its weights from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun) runs N independent replicas, one per GPU (the block
+has no cross-GPU step): value = rows of all ranks / max over ranks of the
+timed region. --impl reference times the oracle (numpy, float64) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-block decode rows/s and achieved HBM GB/s vs roofline per bucket (1×GB300)"
+WORKLOAD = "decode"
+WEIGHT_SETS = 4
+
+# DRAM traffic of one launch of the dominant kernel, from the ncu capture
+# summarized in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
+# valid only for the kernel source it was taken on.
+NCU_TRAFFIC = {"kernel": None, "source_sha1": None, "bytes_per_launch": None}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ bytes model
+
+def algorithmic_bytes(cfg, ids_list):
+    """Minimal HBM bytes per kernel and per step: every weight byte the step
+    needs once (only the selected experts' codes and scales), every input
+    read once and every output written once, at their storage widths."""
+    import numpy as np
+    b, H, P, I, E, k = cfg.rows, cfg.hidden, cfg.pooled, cfg.inter, cfg.experts, cfg.top_k
+    w13_e = 2 * I * P // 2 + 2 * I * P // 32
+    w2_e = P * I // 2 + P * I // 32
+    routes = b * k
+    per = []
+    for ids in ids_list:
+        active = len(np.unique(ids))
+        per.append({
+            "front": E * H * 4 + P * H * 2 + b * H * 2 + b * E * 4 + b * P * 4,
+            "route": b * E * 4 + b * P * 4 + E * 4 + P * 2 + b * P * 4 + routes * 8,
+            "w13": active * w13_e + b * P * 2 + routes * I * 2,
+            "w2": active * w2_e + routes * I * 2 + routes * P * 4,
+            "finalize": routes * P * 4 + routes * 4 + P * 2 + b * P * 2,
+            "unpool": H * P * 2 + b * P * 2 + b * H * 4,
+            "boundary": b * H * 4 + 2 * b * H * 4 + 2 * H * 2 + b * H * 2,
+            "active_experts": active,
+            "expert_bytes": active * (w13_e + w2_e),
+        })
+    return per
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons of one GPU."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            rows.append(parts)
+        if not rows:
+            return None
+        mhz = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------ oracle leg
+
+ORACLE_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import synth, oracle as O
+cfg = synth.CONFIGS[{workload!r}]
+w = synth.layer_tensors(cfg)
+x, st = synth.activations(cfg)
+p = synth.routing_params(cfg)
+times = []
+deadline = time.perf_counter() + {budget}
+for i in range({steps}):
+    t0 = time.perf_counter()
+    O.block(x, st, w, quant=cfg.quant, norm_eps=cfg.norm_eps, **p)
+    times.append(time.perf_counter() - t0)
+    if time.perf_counter() > deadline:
+        break
+print(json.dumps({{"times": times, "rows": cfg.rows}}))
+"""
+
+
+def run_oracle(steps: int, budget_s: float, threads: int = 1) -> dict:
+    """Times the oracle on full decode steps (8 rows each) in a child
+    process pinned to `threads` BLAS/OpenMP threads."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    code = ORACLE_SNIPPET.format(root=ROOT, workload=WORKLOAD, steps=steps, budget=budget_s)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True)
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------ our arm
+
+def bench_ours(args):
+    import numpy as np
+    import torch
+
+    import moe_decode_layer_router_gb300 as mm
+    import synth
+    from moe_decode_layer_router_gb300 import _build
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _build.build()
+    synth.build()
+    cfg = synth.CONFIGS[WORKLOAD]
+    quant = mm.MUSEMOE_MXFP4
+    dims = mm.Dims(max_rows=cfg.rows, hidden=cfg.hidden, pooled=cfg.pooled, inter=cfg.inter,
+                   experts=cfg.experts, top_k=cfg.top_k)
+    conf = mm.Config(score=mm.MUSEMOE_SIGMOID, route_scale=cfg.route_scale, has_multiplier=1,
+                     multiplier=cfg.multiplier, has_division_eps=1,
+                     division_eps=cfg.division_eps, norm_eps=cfg.norm_eps, pre_expert_norm=1)
+    handle = mm.musemoe_create(dims, quant, conf)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # independent weight sets (different seeds: different weights and routes)
+    sets = []
+    for r in range(WEIGHT_SETS):
+        c = synth.Config(**{**cfg.__dict__, "seed": cfg.seed + 1000 * (r + 1) + 97 * rank})
+        t = {k: to_dev(v) for k, v in synth.layer_tensors(c).items()}
+        mm.musemoe_pack_experts(dims, quant, t["w13"], t["w13_scale"], t["w13"], t["w13_scale"],
+                                t["w2"], t["w2_scale"], t["w2"], t["w2_scale"])
+        x, st = synth.activations(c)
+        sets.append({"t": t, "w": mm.make_weights(t), "x": to_dev(x), "stream": to_dev(st),
+                     "out": torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16, device=dev),
+                     "x_host": torch.from_numpy(x.view(np.int16).copy()).pin_memory(),
+                     "stream_host": torch.from_numpy(st.copy()).pin_memory()})
+    torch.cuda.synchronize()
+    set_bytes = sum(v.numel() * v.element_size() for v in sets[0]["t"].values())
+
+    # CUDA graph per set
+    s = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(s):
+        for st_ in sets:
+            mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
+    torch.cuda.synchronize()
+    for st_ in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up (>= 3 steps)
+    with torch.cuda.stream(s):
+        for i in range(max(3, args.warmup)):
+            graphs[i % WEIGHT_SETS].replay()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.6)  # the sampler's first reading lands inside the timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for i in range(args.steps):
+            graphs[i % WEIGHT_SETS].replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        tmax = torch.tensor([ms], device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        ms = float(tmax.item())
+    kernels = mm.musemoe_num_kernels(quant)
+    ms_step = ms / args.steps
+    value = world * cfg.rows * args.steps / (ms / 1e3)
+
+    # per-kernel durations (each kernel timed alone with events) and the
+    # selected experts of each set, for the bytes model
+    n = kernels
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    for e in ev:
+        e.record(s)
+    taps_ids = [torch.empty((cfg.rows, cfg.top_k), dtype=torch.int32, device=dev)
+                for _ in sets]
+    reps = 50
+    dur = [[0.0] * n for _ in sets]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for rep in range(reps):
+            for si, st_ in enumerate(sets):
+                tp = mm.make_taps(events=ev, ids=taps_ids[si])
+                mm.musemoe_forward_debug(handle, st_["w"], st_["x"], st_["stream"], st_["out"],
+                                         cfg.rows, s, tp)
+                s.synchronize()
+                for i in range(n):
+                    dur[si][i] += ev[2 * i].elapsed_time(ev[2 * i + 1]) / reps
+    names = [mm.musemoe_kernel_name(quant, i) for i in range(n)]
+    ids_np = [t.cpu().numpy() for t in taps_ids]
+    model = algorithmic_bytes(cfg, ids_np)
+    kernel_ms = {nm: sum(dur[si][i] for si in range(len(sets))) / len(sets)
+                 for i, nm in enumerate(names)}
+    kernel_bytes = {nm: sum(m[nm] for m in model) / len(model) for nm in names}
+    share = {nm: kernel_ms[nm] / sum(kernel_ms.values()) for nm in names}
+    dom = max(names, key=lambda nm: kernel_ms[nm])
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    hbm_peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm_peak else "fallback"
+    hbm_peak = hbm_peak or 6800.0
+    achieved = kernel_bytes[dom] / (kernel_ms[dom] / 1e3) / 1e9
+    src = open(os.path.join(ROOT, "moe_decode_layer_router_gb300", "csrc", "k_experts.cu"),
+               "rb").read()
+    traffic = None
+    if (NCU_TRAFFIC["kernel"] == dom and NCU_TRAFFIC["source_sha1"] ==
+            hashlib.sha1(src).hexdigest()):
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    step_bytes = sum(sum(m[nm] for nm in names) for m in model) / len(model)
+    expert_bytes = sum(m["expert_bytes"] for m in model) / len(model)
+    expert_ms = kernel_ms["w13"] + kernel_ms["w2"]
+
+    # end to end through the public API with host buffers
+    e2e_steps = max(20, min(2000, args.steps // 10))
+    xh, sh = sets[0]["x_host"], sets[0]["stream_host"]
+    oh = torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16).pin_memory()
+    for i in range(5):
+        st_ = sets[i % WEIGHT_SETS]
+        mm.musemoe_forward_host(handle, st_["w"], st_["x_host"], st_["stream_host"], oh,
+                                cfg.rows, s)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        st_ = sets[i % WEIGHT_SETS]
+        mm.musemoe_forward_host(handle, st_["w"], st_["x_host"], st_["stream_host"], oh,
+                                cfg.rows, s)
+    t_e2e = time.perf_counter() - t0
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    del xh, sh
+    e2e_value = world * cfg.rows * e2e_steps / t_e2e
+    h2d = cfg.rows * cfg.hidden * (2 + 4)
+    d2h = cfg.rows * cfg.hidden * (4 + 2)
+
+    health = mm.musemoe_poll_health(handle)
+    mm.musemoe_destroy(handle)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = run_oracle(steps=6, budget_s=20.0, threads=1)
+        tot = sum(r["times"])
+        cpu = {"value": r["rows"] * len(r["times"]) / tot, "unit": "rows/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{len(r['times'])} full decode steps of {r['rows']} rows "
+                         f"({tot:.1f} s, numpy float64, 1 BLAS thread)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1xf16->f32 (MXFP4 experts), bf16 dense, fp32 router",
+        "data": "synthetic (seeded generator, random-init weights of the workload's shapes)",
+        "config": {"workload": "decode bucket: b=8 rows, H=5120, P=2048, I=1024, E=128, "
+                               "top-8, sigmoid, multiplier 0.5, MXFP4 experts",
+                   "rows_per_gpu": cfg.rows, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {WEIGHT_SETS} rotating weight sets of "
+                         f"{set_bytes / 1e6:.0f} MB",
+                   "cuda_graph": True},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kernel_bytes[dom]},
+        "block": {"algorithmic_bytes_per_step": step_bytes,
+                  "achieved_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+                  "frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm_peak,
+                  "expert_phase_gbs": expert_bytes / (expert_ms / 1e3) / 1e9,
+                  "expert_phase_frac": expert_bytes / (expert_ms / 1e3) / 1e9 / hbm_peak,
+                  "active_experts": sum(m["active_experts"] for m in model) / len(model),
+                  "kernel_us": {k_: v * 1e3 for k_, v in kernel_ms.items()},
+                  "kernel_share": share},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": kernels * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
+    }
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ------------------------------------------------------------ reference arm
+
+def bench_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    warm = max(3, args.warmup) if args.warmup < 3 else args.warmup
+    # bound the whole run to a few minutes: one oracle step is a full 8-row
+    # decode step (seconds on one core)
+    w_run = run_oracle(steps=min(warm, 3), budget_s=60.0, threads=1)
+    per = sum(w_run["times"]) / len(w_run["times"])
+    k = max(1, min(args.steps, int(120.0 / max(per, 1e-3))))
+    r = run_oracle(steps=k, budget_s=150.0, threads=1)
+    tot = sum(r["times"])
+    value = r["rows"] * len(r["times"]) / tot
+    sample = (f"{len(r['times'])} full decode steps of {r['rows']} rows (capped from "
+              f"{args.steps} to fit a few minutes; numpy float64, 1 BLAS thread)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": world, "steps": len(r["times"]), "warmup": warm,
+        "ms_per_step": tot / len(r["times"]) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator, random-init weights of the workload's shapes)",
+        "config": {"workload": "decode bucket: b=8 rows, H=5120, P=2048, I=1024, E=128, "
+                               "top-8, sigmoid, multiplier 0.5, MXFP4 experts",
+                   "rows_per_gpu": 8, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

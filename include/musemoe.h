@@ -61,6 +61,7 @@ typedef enum {
   MUSEMOE_ECUDA = 3,        /* a CUDA runtime call or launch failed */
   MUSEMOE_ENOMEM = 4,       /* workspace allocation failed (create only) */
   MUSEMOE_ERANGE = 5,       /* health: an expert operand left the fp16 range */
+  MUSEMOE_ETIMEOUT = 6,     /* health: a kernel's bounded wait ran out */
 } musemoe_status;
 
 typedef enum {
@@ -99,17 +100,18 @@ typedef struct {
 } musemoe_config;
 
 /* One layer's weights: caller-owned device pointers, read in place.
- * Expert codes must be in the kernel layout musemoe_pack_experts writes. */
+ * Expert codes and scales must be in the kernel layout musemoe_pack_experts
+ * writes. */
 typedef struct {
   const float *w_router;      /* fp32 [E, H] */
   const float *expert_bias;   /* fp32 [E], selection only */
   const uint16_t *w_pool;     /* bf16 [P, H] */
   const uint16_t *w_pre_norm; /* bf16 [P] (effective weight) */
-  const uint8_t *w13;         /* MXFP4/NVFP4 packed [E, 2I, P/2]; FP8 [E, 2I, P] */
-  const void *w13_scale;      /* MX u8 [E, 2I, P/32]; NV e4m3 [E, 2I, P/16]; FP8 fp32 [E, 2I] */
+  const uint8_t *w13;         /* kernel layout of [E, 2I, P/2] (FP4) / [E, 2I, P] (FP8) */
+  const void *w13_scale;      /* kernel layout: MX u8, NV e4m3; FP8 fp32 [E, 2I] */
   const float *w13_gscale;    /* NVFP4 only: fp32 [E] */
-  const uint8_t *w2;          /* MXFP4/NVFP4 packed [E, P, I/2]; FP8 [E, P, I] */
-  const void *w2_scale;       /* MX u8 [E, P, I/32]; NV e4m3 [E, P, I/16]; FP8 fp32 [E, P] */
+  const uint8_t *w2;          /* kernel layout of [E, P, I/2] (FP4) / [E, P, I] (FP8) */
+  const void *w2_scale;       /* kernel layout: MX u8, NV e4m3; FP8 fp32 [E, P] */
   const float *w2_gscale;     /* NVFP4 only: fp32 [E] */
   const uint16_t *w_post_norm; /* bf16 [P] */
   const uint16_t *w_unpool;    /* bf16 [H, P] */
@@ -160,15 +162,24 @@ int32_t musemoe_num_kernels(int32_t quant);
 /* Name of kernel i of the forward ("front", "route", "w13", ...). */
 const char *musemoe_kernel_name(int32_t quant, int32_t i);
 
-/* Re-lays the packed e2m1 codes of MXFP4/NVFP4 expert tensors from the plain
- * layout (row-major [E, N, K/2], element 2j in the low nibble of byte j) into
- * the kernel layout: within every 64-byte group of a row, byte 8j + 2q + b
- * moves to 16q + 2j + b (q < 4, j < 8, b < 2). w13: N = 2I, K = P; w2: N = P,
- * K = I. src and dst may be the same buffer (in place). Scales are used as
- * given. For FP8 the plain layout is the kernel layout and this copies. */
+/* Re-lays the expert tensors from their plain layout into the kernel layout
+ * the forward reads (done once, e.g. after loading weights).
+ * Plain layout: codes row-major [E, N, K/2] for MXFP4/NVFP4 (two e2m1 codes
+ * per byte, element 2j in the low nibble of byte j) or [E, N, K] e4m3 for FP8;
+ * scales [E, N, K/32] UE8M0 (MXFP4), [E, N, K/16] e4m3 (NVFP4), fp32 [E, N]
+ * (FP8). w13: N = 2I (gate rows first), K = P; w2: N = P, K = I.
+ * Kernel layout: every row is cut into 64-byte code chunks (128 FP4 or 64 FP8
+ * elements) and rows are taken in groups of 8, stored chunk by chunk:
+ * codes [E][N/8][chunk][8 rows][64 B], scales [E][N/8][chunk][8 rows][4 B]
+ * (MXFP4) or [..][8 B] (NVFP4); FP8 scales keep their layout. For FP4 the 64
+ * bytes of a chunk are also reordered: byte 8j + 2q + b moves to 16q + 2j + b
+ * (q < 4, j < 8, b < 2). Each src may be its dst (in place). The NVFP4 global
+ * scales need no re-layout. */
 musemoe_status musemoe_pack_experts(const musemoe_dims *dims, int32_t quant,
-                                    const uint8_t *w13_src, uint8_t *w13_dst,
-                                    const uint8_t *w2_src, uint8_t *w2_dst,
+                                    const uint8_t *w13_src, const void *w13_scale_src,
+                                    uint8_t *w13_dst, void *w13_scale_dst,
+                                    const uint8_t *w2_src, const void *w2_scale_src,
+                                    uint8_t *w2_dst, void *w2_scale_dst,
                                     musemoe_stream_t stream);
 
 /* Router GEMV + routing rule only: ids_out int32 [rows, k] (descending
@@ -199,9 +210,11 @@ musemoe_status musemoe_forward_host(musemoe_handle *handle, const musemoe_weight
                                     musemoe_stream_t stream_);
 
 /* Reads (synchronously) and clears the handle's device health word. Returns
- * MUSEMOE_ERANGE if a forward since the last poll produced an expert operand
- * (h or the SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504),
- * MUSEMOE_OK otherwise. */
+ * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
+ * ran out since the last poll (that forward's outputs are invalid),
+ * MUSEMOE_ERANGE if a forward produced an expert operand (h or the
+ * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504), MUSEMOE_OK
+ * otherwise. */
 musemoe_status musemoe_poll_health(musemoe_handle *handle);
 
 #ifdef __cplusplus

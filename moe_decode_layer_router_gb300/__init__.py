@@ -18,7 +18,7 @@ from . import _build
 
 __all__ = [
     "MUSEMOE_OK", "MUSEMOE_EINVAL", "MUSEMOE_EUNSUPPORTED", "MUSEMOE_ECUDA", "MUSEMOE_ENOMEM",
-    "MUSEMOE_ERANGE", "MUSEMOE_MXFP4", "MUSEMOE_NVFP4", "MUSEMOE_FP8_W8A8", "MUSEMOE_SIGMOID",
+    "MUSEMOE_ERANGE", "MUSEMOE_ETIMEOUT", "MUSEMOE_MXFP4", "MUSEMOE_NVFP4", "MUSEMOE_FP8_W8A8", "MUSEMOE_SIGMOID",
     "MUSEMOE_SOFTMAX", "Dims", "Config", "Weights", "Taps", "MuseMoEError", "library",
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
@@ -26,11 +26,12 @@ __all__ = [
     "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
 ]
 
-MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE = (
-    0, 1, 2, 3, 4, 5)
+(MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
+ MUSEMOE_ETIMEOUT) = (0, 1, 2, 3, 4, 5, 6)
 MUSEMOE_MXFP4, MUSEMOE_NVFP4, MUSEMOE_FP8_W8A8 = 0, 1, 2
 MUSEMOE_SIGMOID, MUSEMOE_SOFTMAX = 0, 1
-_STATUS = {0: "OK", 1: "EINVAL", 2: "EUNSUPPORTED", 3: "ECUDA", 4: "ENOMEM", 5: "ERANGE"}
+_STATUS = {0: "OK", 1: "EINVAL", 2: "EUNSUPPORTED", 3: "ECUDA", 4: "ENOMEM", 5: "ERANGE",
+           6: "ETIMEOUT"}
 
 c_i32, c_f32, c_vp = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
 
@@ -95,7 +96,7 @@ def library() -> ctypes.CDLL:
         lib.musemoe_num_kernels.argtypes = [c_i32]
         lib.musemoe_kernel_name.argtypes = [c_i32, c_i32]
         lib.musemoe_kernel_name.restype = ctypes.c_char_p
-        lib.musemoe_pack_experts.argtypes = [P(Dims), c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]
+        lib.musemoe_pack_experts.argtypes = [P(Dims), c_i32] + [c_vp] * 9
         lib.musemoe_route.argtypes = [c_vp, P(Weights), c_vp, c_i32, c_vp, c_vp, c_vp]
         lib.musemoe_forward.argtypes = [c_vp, P(Weights), c_vp, c_vp, c_vp, c_i32, c_vp]
         lib.musemoe_forward_debug.argtypes = [c_vp, P(Weights), c_vp, c_vp, c_vp, c_i32, c_vp,
@@ -159,11 +160,12 @@ def musemoe_kernel_name(quant: int, i: int) -> str:
     return library().musemoe_kernel_name(quant, i).decode()
 
 
-def musemoe_pack_experts(dims: Dims, quant: int, w13_src, w13_dst, w2_src, w2_dst,
-                         stream=None) -> None:
-    _check(library().musemoe_pack_experts(ctypes.byref(dims), quant, _addr(w13_src),
-                                          _addr(w13_dst), _addr(w2_src), _addr(w2_dst),
-                                          _stream(stream)))
+def musemoe_pack_experts(dims: Dims, quant: int, w13_src, w13_scale_src, w13_dst, w13_scale_dst,
+                         w2_src, w2_scale_src, w2_dst, w2_scale_dst, stream=None) -> None:
+    _check(library().musemoe_pack_experts(
+        ctypes.byref(dims), quant, _addr(w13_src), _addr(w13_scale_src), _addr(w13_dst),
+        _addr(w13_scale_dst), _addr(w2_src), _addr(w2_scale_src), _addr(w2_dst),
+        _addr(w2_scale_dst), _stream(stream)))
 
 
 def musemoe_route(handle, weights: Weights, x, rows: int, ids_out, weights_out,
@@ -194,10 +196,11 @@ def musemoe_forward_host(handle, weights: Weights, x_host, stream_host, out_host
 
 
 def musemoe_poll_health(handle) -> int:
-    """MUSEMOE_OK, or MUSEMOE_ERANGE when an expert operand left the fp16
-    range since the last poll; other failures raise."""
+    """MUSEMOE_OK, MUSEMOE_ERANGE (an expert operand left the fp16 range) or
+    MUSEMOE_ETIMEOUT (a bounded wait ran out) since the last poll; other
+    failures raise."""
     st = library().musemoe_poll_health(handle)
-    if st not in (MUSEMOE_OK, MUSEMOE_ERANGE):
+    if st not in (MUSEMOE_OK, MUSEMOE_ERANGE, MUSEMOE_ETIMEOUT):
         _check(st, handle)
     return st
 

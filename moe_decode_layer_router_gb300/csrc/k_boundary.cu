@@ -1,8 +1,7 @@
 // FFN boundary (page "vllm.models.muse_spark.nvidia.specialized_decode.runtime.
 // providers", BoundaryProvider docstring): post_ffn_norm of the unpooler
 // output, gated add into the fp32 residual stream in place, and the next
-// pre-norm into bf16 out. One CTA per row; the unpooler's K-split partial
-// sums are added here in a fixed order.
+// pre-norm into bf16 out. One CTA per row.
 // Gated add: stream += gate * post_ffn_norm(u), one scalar gate per layer
 // (the decoder page names add_ffn alpha/beta but prints no formula; this is
 // the plain reading with alpha = 1, beta = gate).
@@ -12,51 +11,74 @@
 namespace musemoe {
 
 constexpr int kBoundaryThreads = 512;
+constexpr int kBoundaryVec = 4;  // float4 columns per thread held in registers
 
+// One CTA per row; the row (H <= kBoundaryThreads * kBoundaryVec * 4) lives
+// in registers, every load of the row is issued before the first use.
 __global__ void __launch_bounds__(kBoundaryThreads) k_boundary(BoundaryParams p) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float scratch[32];
-  extern __shared__ float buf[];  // [H]
   const int t = blockIdx.x;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < p.H; i += kBoundaryThreads) {
-    float u = 0.f;
-    for (int ks = 0; ks < p.ks; ++ks) u += __ldcg(p.part + ((size_t)ks * p.rows + t) * p.H + i);
-    buf[i] = u;
-    if (p.u_tap) p.u_tap[(size_t)t * p.H + i] = u;
-    ss += u * u;
+  const int H4 = p.H / 4;
+  const float4* u4 = reinterpret_cast<const float4*>(p.u + (size_t)t * p.H);
+  float4* srow = reinterpret_cast<float4*>(p.stream + (size_t)t * p.H);
+  const uint2* wf = reinterpret_cast<const uint2*>(p.w_ffn_norm);
+  const uint2* wn = reinterpret_cast<const uint2*>(p.w_next_norm);
+  float4 u[kBoundaryVec], s0[kBoundaryVec];
+  uint2 f[kBoundaryVec], nx[kBoundaryVec];
+#pragma unroll
+  for (int r = 0; r < kBoundaryVec; ++r) {
+    const int i = threadIdx.x + r * kBoundaryThreads;
+    const bool v = i < H4;
+    u[r] = v ? __ldcg(u4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    s0[r] = v ? srow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    f[r] = v ? wf[i] : make_uint2(0, 0);
+    nx[r] = v ? wn[i] : make_uint2(0, 0);
   }
+  const float gate = __ldg(p.gate);
+  float ss = 0.f;
+#pragma unroll
+  for (int r = 0; r < kBoundaryVec; ++r)
+    ss += u[r].x * u[r].x + u[r].y * u[r].y + u[r].z * u[r].z + u[r].w * u[r].w;
   ss = block_sum(ss, scratch);
   const float rstd = 1.0f / sqrtf(ss / (float)p.H + p.eps);
-  const float gate = __ldg(p.gate);
-  float* srow = p.stream + (size_t)t * p.H;
   float ss2 = 0.f;
-  for (int i = threadIdx.x; i < p.H; i += kBoundaryThreads) {
-    const float add = (buf[i] * rstd) * bf16_bits_to_f32(p.w_ffn_norm[i]);
-    const float s = fmaf(gate, add, srow[i]);
-    srow[i] = s;
-    buf[i] = s;
-    ss2 += s * s;
+#pragma unroll
+  for (int r = 0; r < kBoundaryVec; ++r) {
+    float4 s1;
+    s1.x = fmaf(gate, (u[r].x * rstd) * bf16_bits_to_f32(f[r].x & 0xFFFFu), s0[r].x);
+    s1.y = fmaf(gate, (u[r].y * rstd) * bf16_bits_to_f32(f[r].x >> 16), s0[r].y);
+    s1.z = fmaf(gate, (u[r].z * rstd) * bf16_bits_to_f32(f[r].y & 0xFFFFu), s0[r].z);
+    s1.w = fmaf(gate, (u[r].w * rstd) * bf16_bits_to_f32(f[r].y >> 16), s0[r].w);
+    const int i = threadIdx.x + r * kBoundaryThreads;
+    if (i < H4) {
+      srow[i] = s1;
+      ss2 += s1.x * s1.x + s1.y * s1.y + s1.z * s1.z + s1.w * s1.w;
+    }
+    s0[r] = s1;
   }
   ss2 = block_sum(ss2, scratch);
   const float rstd2 = 1.0f / sqrtf(ss2 / (float)p.H + p.eps);
-  for (int i = threadIdx.x; i < p.H; i += kBoundaryThreads)
-    p.out[(size_t)t * p.H + i] =
-        f32_to_bf16_bits((buf[i] * rstd2) * bf16_bits_to_f32(p.w_next_norm[i]));
+  uint2* orow = reinterpret_cast<uint2*>(p.out + (size_t)t * p.H);
+#pragma unroll
+  for (int r = 0; r < kBoundaryVec; ++r) {
+    const int i = threadIdx.x + r * kBoundaryThreads;
+    if (i >= H4) continue;
+    const float4 s1 = s0[r];
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits((s1.x * rstd2) * bf16_bits_to_f32(nx[r].x & 0xFFFFu)) |
+          ((uint32_t)f32_to_bf16_bits((s1.y * rstd2) * bf16_bits_to_f32(nx[r].x >> 16)) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits((s1.z * rstd2) * bf16_bits_to_f32(nx[r].y & 0xFFFFu)) |
+          ((uint32_t)f32_to_bf16_bits((s1.w * rstd2) * bf16_bits_to_f32(nx[r].y >> 16)) << 16);
+    orow[i] = o;
+  }
 }
 
 cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl) {
-  const size_t smem = (size_t)p.H * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_boundary, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.rows);
   cfg.blockDim = dim3(kBoundaryThreads);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -1,19 +1,27 @@
 // Routed experts: grouped GEMV/GEMM over the selected experts only.
 //
-// Work item = (token group of one expert, tile of weight rows). A CTA of 8
-// warps splits the item's reduction dimension K across its warps and sums
-// the 8 partial tiles in shared memory (fixed order: deterministic). CTAs
-// take contiguous runs of items, so a CTA mostly stays on one expert group.
+// Work item = (token group of one expert, tile of weight rows). Each CTA
+// walks a contiguous run of items; its thread 0 streams the items' weight
+// codes and block scales into a ring of shared-memory stages with 1-D bulk
+// copies (cp.async.bulk, completion counted on one mbarrier per stage), a few
+// items ahead of the 8 consumer warps. Every wait is bounded: past the limit
+// the CTA raises a health bit and leaves. The consumer warps split the
+// item's reduction dimension K (chunk c goes to warp c % 8) and sum their 8
+// partial tiles in shared memory in a fixed order (deterministic).
 //
-// Weights are streamed once from HBM with 128-bit loads straight into
-// mma.sync fragments. Each thread's 16 bytes of a row cover:
-//  * FP4 (kernel layout, see musemoe_pack_experts): 8 k-steps of m16n8k16;
-//    k-step j of the 64-byte group holds elements 16j..16j+15 and thread q
-//    owns 16j+4q..16j+4q+3, so one k-step never crosses a scale block. The
-//    e2m1 pairs become f16 pairs with one cvt (exact). MXFP4 scales (UE8M0,
-//    per 32) multiply the fp32 partial of each pair of k-steps; NVFP4 scales
-//    (e4m3, per 16) multiply the f16 operand (e2m1 * e4m3 is exact in f16) and
-//    the fp32 global scale multiplies the result.
+// Kernel weight layout (written by musemoe_pack_experts): rows in groups of
+// 8, each group stored chunk by chunk, [E][N/8][NC][8 rows][64 B] for codes
+// and [E][N/8][NC][8 rows][SB B] for MXFP4 (SB = 4) / NVFP4 (SB = 8) scales,
+// so an item is one or two contiguous blocks and the 8 rows of a chunk are
+// 512 contiguous bytes (conflict-free 128-bit shared loads). Thread (g, q)
+// of a warp reads 16 bytes of row g and of row g + 8:
+//  * FP4: 8 k-steps of m16n8k16; within the 64-byte chunk, k-step j holds
+//    elements 16j..16j+15 and thread q owns 16j+4q..16j+4q+3, so one k-step
+//    never crosses a scale block. The e2m1 pairs become f16 pairs with one
+//    cvt (exact). MXFP4 scales (UE8M0, per 32) multiply the fp32 partial of
+//    each pair of k-steps; NVFP4 scales (e4m3, per 16) multiply the f16
+//    operand (e2m1 * e4m3 is exact in f16) and the fp32 global scale
+//    multiplies the result.
 //  * FP8: 2 k-steps of m16n8k32 e4m3 x e4m3; the per-row weight scale and the
 //    per-row activation scale multiply the fp32 result.
 // Activations (the N side, tokens) come from L1/L2: h or act rows in f16
@@ -34,8 +42,11 @@ namespace musemoe {
 
 constexpr int kExpertThreads = 256;
 constexpr int kExpertWarps = kExpertThreads / 32;
-constexpr int kChunkBytes = 64;  // bytes of one weight row per thread-quad
-constexpr int kCMax = 2;         // chunks loaded ahead per warp
+constexpr int kChunkBytes = 64;      // bytes of one weight row per thread-quad
+constexpr int kGroupChunk = 8 * 64;  // bytes of one chunk of a row group
+constexpr int kStageBudget = 100 * 1024;
+constexpr int kMetaGroups = 8;  // token groups whose metadata a CTA keeps in shared memory
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -45,62 +56,269 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the mbarrier phase to complete, at most `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase,
+                                          unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, phase))
+    if (globaltimer() - t0 > limit_ns) return false;
+  return true;
+}
+// 1-D bulk copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
-template <int Q, int ROLE, int NT, int RT>
+// Geometry of one work item's weights in a stage.
+struct StageGeo {
+  int NC;            // 64-byte chunks per row
+  int code_group;    // code bytes of one row group (NC * 512)
+  int scale_group;   // scale bytes of one row group
+  int groups;        // row groups per item
+  int stage_bytes;   // codes then scales, rounded up to 128
+};
+
+template <int Q, int ROLE, int RT>
+__host__ __device__ __forceinline__ StageGeo stage_geo(int K) {
+  StageGeo g;
+  const int rowbytes = (Q == kFP8) ? K : K / 2;
+  g.NC = rowbytes / kChunkBytes;
+  g.code_group = g.NC * kGroupChunk;
+  g.scale_group = (Q == kMXFP4) ? g.NC * 32 : (Q == kNVFP4) ? g.NC * 64 : 0;
+  g.groups = (ROLE == 0) ? 2 : 2 * RT;
+  g.stage_bytes = (g.groups * (g.code_group + g.scale_group) + 127) & ~127;
+  return g;
+}
+
+// Thread 0: start the copies of item `item` into stage buffer `dst`.
+template <int Q, int ROLE, int RT>
+__device__ __forceinline__ void issue_item(const ExpertParams& p, const StageGeo& G, int e,
+                                           int tile, uint32_t dst, uint32_t bar) {
+  const int NG = p.N / 8;  // row groups per expert
+  const uint8_t* sb = reinterpret_cast<const uint8_t*>(p.scale);
+  mbar_expect_tx(bar, G.groups * (G.code_group + G.scale_group));
+  if (ROLE == 0) {
+    const int rg[2] = {tile, p.I / 8 + tile};  // gate rows, up rows
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const size_t gi = (size_t)e * NG + rg[h];
+      bulk_g2s(dst + h * G.code_group, p.w + gi * G.code_group, G.code_group, bar);
+      if (G.scale_group)
+        bulk_g2s(dst + 2 * G.code_group + h * G.scale_group, sb + gi * G.scale_group,
+                 G.scale_group, bar);
+    }
+  } else {
+    const size_t gi = (size_t)e * NG + (size_t)tile * 2 * RT;
+    bulk_g2s(dst, p.w + gi * G.code_group, G.groups * G.code_group, bar);
+    if (G.scale_group)
+      bulk_g2s(dst + G.groups * G.code_group, sb + gi * G.scale_group,
+               G.groups * G.scale_group, bar);
+  }
+}
+
+// The mma work of one 64-byte chunk of the fragment rows g (codes L, scales
+// sl) and g + 8 (codes H, scales sh) against the n-tiles' B fragments, which
+// `bfrag(nt, j)` returns: for FP4 the uint2 of k-step j (0..7), for FP8 the
+// uint4 of both k-steps (j unused).
+template <int Q, int NT, typename BFrag>
+__device__ __forceinline__ void chunk_mma(float (&acc)[NT][4], const uint4& L, const uint4& H,
+                                          uint2 sl, uint2 sh, int ntile_act, BFrag&& bfrag) {
+  if constexpr (Q == kFP8) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (nt >= ntile_act) break;
+      const uint4 bv = bfrag(nt, 0);
+      mma_e4m3_16832(acc[nt], L.x, H.x, L.y, H.y, bv.x, bv.y);
+      mma_e4m3_16832(acc[nt], L.z, H.z, L.w, H.w, bv.z, bv.w);
+    }
+  } else if constexpr (Q == kMXFP4) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float fl = ue8m0_to_f32(sl.x >> (8 * b));
+      const float fh = ue8m0_to_f32(sh.x >> (8 * b));
+      const uint32_t wl = word_of(L, b), wh = word_of(H, b);
+      const uint32_t a00 = e2m1x2_to_f16x2(wl), a01 = e2m1x2_to_f16x2(wh);
+      const uint32_t a02 = e2m1x2_to_f16x2(wl >> 8), a03 = e2m1x2_to_f16x2(wh >> 8);
+      const uint32_t a10 = e2m1x2_to_f16x2(wl >> 16), a11 = e2m1x2_to_f16x2(wh >> 16);
+      const uint32_t a12 = e2m1x2_to_f16x2(wl >> 24), a13 = e2m1x2_to_f16x2(wh >> 24);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        if (nt >= ntile_act) break;
+        const uint2 b0 = bfrag(nt, 2 * b), b1 = bfrag(nt, 2 * b + 1);
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(t, a00, a01, a02, a03, b0.x, b0.y);
+        mma_f16_16816(t, a10, a11, a12, a13, b1.x, b1.y);
+        acc[nt][0] = fmaf(t[0], fl, acc[nt][0]);
+        acc[nt][1] = fmaf(t[1], fl, acc[nt][1]);
+        acc[nt][2] = fmaf(t[2], fh, acc[nt][2]);
+        acc[nt][3] = fmaf(t[3], fh, acc[nt][3]);
+      }
+    }
+  } else {  // NVFP4: one e4m3 scale per k-step
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t slw = (j < 4 ? sl.x : sl.y) >> (8 * (j & 3));
+      const uint32_t shw = (j < 4 ? sh.x : sh.y) >> (8 * (j & 3));
+      const uint32_t sfl = e4m3x2_to_f16x2(slw & 0xFFu);
+      const uint32_t sfh = e4m3x2_to_f16x2(shw & 0xFFu);
+      const uint32_t sl2 = __byte_perm(sfl, sfl, 0x1010);  // broadcast low half
+      const uint32_t sh2 = __byte_perm(sfh, sfh, 0x1010);
+      const uint32_t wl = word_of(L, j >> 1) >> (16 * (j & 1));
+      const uint32_t wh = word_of(H, j >> 1) >> (16 * (j & 1));
+      const uint32_t a0 = hmul2(e2m1x2_to_f16x2(wl), sl2);
+      const uint32_t a1 = hmul2(e2m1x2_to_f16x2(wh), sh2);
+      const uint32_t a2 = hmul2(e2m1x2_to_f16x2(wl >> 8), sl2);
+      const uint32_t a3 = hmul2(e2m1x2_to_f16x2(wh >> 8), sh2);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        if (nt >= ntile_act) break;
+        const uint2 bv = bfrag(nt, j);
+        mma_f16_16816(acc[nt], a0, a1, a2, a3, bv.x, bv.y);
+      }
+    }
+  }
+}
+
+// BC: the warp keeps the B fragments of its (at most CPW) chunks in
+// registers while consecutive items stay on one token group.
+template <int Q, int ROLE, int NT, int RT, bool BC, int CPW>
 __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  extern __shared__ __align__(16) float4 red[];  // [warps][RT][NT][32]
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) unsigned long long bars[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
+  const StageGeo G = stage_geo<Q, ROLE, RT>(p.K);
+  const int S = p.stages;
+  float4* red = reinterpret_cast<float4*>(smem + (size_t)S * G.stage_bytes);  // [warps][RT][NT][32]
   const int n_groups = __ldcg(p.counters + kNumGroups);
   const int tiles = (ROLE == 0) ? p.I / 8 : p.N / (16 * RT);
   const int n_items = n_groups * tiles;
   const int i0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
   const int i1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
-  const int rowbytes = (Q == kFP8) ? p.K : p.K / 2;
-  const int NC = rowbytes / kChunkBytes;
+  const int mine = i1 - i0;
   const int kel = (Q == kFP8) ? 1 : 2;  // bytes per activation element
-  const int nc_w = warp < NC ? (NC - warp + kExpertWarps - 1) / kExpertWarps : 0;
+  const uint32_t stage0 = smem_u32(smem);
 
-  for (int item = i0; item < i1; ++item) {
+  // metadata of the token groups this CTA's items touch (the first
+  // kMetaGroups of them; items of later groups read it from global memory)
+  __shared__ int4 meta_g[kMetaGroups];
+  __shared__ int meta_r[kMetaGroups][8 * NT];
+  const int g_first = mine > 0 ? i0 / tiles : 0;
+  const int g_count = mine > 0 ? min(kMetaGroups, (i1 - 1) / tiles - g_first + 1) : 0;
+  for (int i = threadIdx.x; i < g_count; i += kExpertThreads)
+    meta_g[i] = __ldcg(reinterpret_cast<const int4*>(p.groups) + g_first + i);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < S; ++st) mbar_init(smem_u32(&bars[st]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < g_count * 8 * NT; i += kExpertThreads) {
+    const int gi = i / (8 * NT), n = i % (8 * NT);
+    if (n < meta_g[gi].z) meta_r[gi][n] = __ldcg(p.route_list + meta_g[gi].y + n);
+  }
+  auto group_of = [&](int grp) -> int4 {
+    const int gi = grp - g_first;
+    return gi < kMetaGroups ? meta_g[gi] : __ldcg(reinterpret_cast<const int4*>(p.groups) + grp);
+  };
+  auto route_of = [&](int grp, int rbase, int n) -> int {
+    const int gi = grp - g_first;
+    return gi < kMetaGroups ? meta_r[gi][n] : __ldcg(p.route_list + rbase + n);
+  };
+  if (threadIdx.x == 0)
+    for (int st = 0; st < S && st < mine; ++st) {
+      const int it = i0 + st;
+      issue_item<Q, ROLE, RT>(p, G, group_of(it / tiles).x, it % tiles,
+                              stage0 + st * G.stage_bytes, smem_u32(&bars[st]));
+    }
+  __syncthreads();
+
+  int stop_at = -1;  // item counter at which a wait timed out
+  int cached_grp = -1;
+  uint2 bcache4[BC && Q != kFP8 ? CPW : 1][BC && Q != kFP8 ? NT : 1][8];
+  uint4 bcache8[BC && Q == kFP8 ? CPW : 1][BC && Q == kFP8 ? NT : 1];
+  (void)bcache4;
+  (void)bcache8;
+  for (int ii = 0; ii < mine; ++ii) {
+    const int item = i0 + ii;
+    const int st = ii % S;
+    const uint32_t phase = (uint32_t)(ii / S) & 1u;
     const int grp = item / tiles, tile = item % tiles;
-    const int4 gd = __ldcg(reinterpret_cast<const int4*>(p.groups) + grp);
+    const int4 gd = group_of(grp);
     const int e = gd.x, rbase = gd.y, ntok = gd.z;
     const int ntile_act = (ntok + 7) >> 3;
-
-    // activation row of this lane's B column in every n-tile
     const uint8_t* brow[NT];
+    if (!BC || grp != cached_grp) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n = nt * 8 + g;
-      brow[nt] = nullptr;
-      if (n < ntok) {
-        const int r = __ldcg(p.route_list + rbase + n);
-        const int br = p.b_by_token ? r / p.k : r;
-        brow[nt] = p.b + (size_t)br * p.K * kel;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int nn = nt * 8 + g;
+        brow[nt] = nullptr;
+        if (nn < ntok) {
+          const int r = route_of(grp, rbase, nn);
+          const int br = p.b_by_token ? r / p.k : r;
+          brow[nt] = p.b + (size_t)br * p.K * kel;
+        }
       }
     }
-    // weight rows of this lane
-    const uint8_t* wlo[RT];
-    const uint8_t* whi[RT];
-    int rlo[RT];
+    if constexpr (BC) {
+      if (grp != cached_grp) {  // fetch this warp's B fragments of the new group
+        cached_grp = grp;
 #pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-      int lo, hi;
-      if (ROLE == 0) {
-        lo = tile * 8 + g;
-        hi = p.I + tile * 8 + g;
-      } else {
-        lo = tile * 16 * RT + rt * 16 + g;
-        hi = lo + 8;
+        for (int u = 0; u < CPW; ++u) {
+          const int c = warp + kExpertWarps * u;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const bool v = c < G.NC && brow[nt] != nullptr;
+            if constexpr (Q == kFP8) {
+              bcache8[u][nt] = v ? ld_act_v4(brow[nt] + (size_t)c * 64 + q * 16) : make_uint4(0, 0, 0, 0);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                bcache4[u][nt][j] =
+                    v ? ld_act_v2(brow[nt] + ((size_t)c * 128 + 16 * j + 4 * q) * 2) : make_uint2(0, 0);
+            }
+          }
+        }
       }
-      rlo[rt] = lo;
-      wlo[rt] = p.w + ((size_t)e * p.N + lo) * rowbytes + q * 16;
-      whi[rt] = p.w + ((size_t)e * p.N + hi) * rowbytes + q * 16;
     }
-    const size_t srow = (Q == kMXFP4) ? p.K / 32 : (Q == kNVFP4) ? p.K / 16 : 0;
-    const uint8_t* sb = reinterpret_cast<const uint8_t*>(p.scale);
+    const bool ok = mbar_wait(smem_u32(&bars[st]), phase, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      stop_at = ii;
+      break;
+    }
+    const uint8_t* stg = smem + (size_t)st * G.stage_bytes;
 
     float acc[RT][NT][4];
 #pragma unroll
@@ -110,102 +328,50 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[rt][nt][i] = 0.f;
 
-    for (int cb = 0; cb < nc_w; cb += kCMax) {
-      uint4 L[kCMax][RT], H[kCMax][RT];
-      uint2 SL[kCMax][RT], SH[kCMax][RT];
-#pragma unroll
-      for (int u = 0; u < kCMax; ++u) {
-        if (cb + u < nc_w) {
-          const int c = warp + kExpertWarps * (cb + u);
-#pragma unroll
-          for (int rt = 0; rt < RT; ++rt) {
-            L[u][rt] = ld_stream_v4(wlo[rt] + (size_t)c * kChunkBytes);
-            H[u][rt] = ld_stream_v4(whi[rt] + (size_t)c * kChunkBytes);
-            if (Q == kMXFP4) {
-              const int lo = ROLE == 0 ? rlo[rt] : rlo[rt];
-              const int hi = ROLE == 0 ? p.I + rlo[rt] : rlo[rt] + 8;
-              SL[u][rt].x = ld_stream_u32(sb + ((size_t)e * p.N + lo) * srow + c * 4);
-              SH[u][rt].x = ld_stream_u32(sb + ((size_t)e * p.N + hi) * srow + c * 4);
-            } else if (Q == kNVFP4) {
-              const int lo = rlo[rt];
-              const int hi = ROLE == 0 ? p.I + rlo[rt] : rlo[rt] + 8;
-              SL[u][rt] = ld_stream_v2(sb + ((size_t)e * p.N + lo) * srow + c * 8);
-              SH[u][rt] = ld_stream_v2(sb + ((size_t)e * p.N + hi) * srow + c * 8);
-            }
-          }
-        }
+    // fragment rows g (lo) and g + 8 (hi) of row tile rt: their row groups
+    auto chunk = [&](int c, int rt, auto&& bfrag) {
+      const int glo = (ROLE == 0) ? 0 : 2 * rt, ghi = (ROLE == 0) ? 1 : 2 * rt + 1;
+      const uint4 L = *reinterpret_cast<const uint4*>(stg + glo * G.code_group + c * kGroupChunk +
+                                                      g * 64 + q * 16);
+      const uint4 Hh = *reinterpret_cast<const uint4*>(stg + ghi * G.code_group + c * kGroupChunk +
+                                                       g * 64 + q * 16);
+      const uint8_t* sc = stg + G.groups * G.code_group;
+      uint2 sl = make_uint2(0, 0), sh = make_uint2(0, 0);
+      if (Q == kMXFP4) {
+        sl.x = *reinterpret_cast<const uint32_t*>(sc + glo * G.scale_group + c * 32 + g * 4);
+        sh.x = *reinterpret_cast<const uint32_t*>(sc + ghi * G.scale_group + c * 32 + g * 4);
+      } else if (Q == kNVFP4) {
+        sl = *reinterpret_cast<const uint2*>(sc + glo * G.scale_group + c * 64 + g * 8);
+        sh = *reinterpret_cast<const uint2*>(sc + ghi * G.scale_group + c * 64 + g * 8);
       }
+      chunk_mma<Q, NT>(acc[rt], L, Hh, sl, sh, ntile_act, bfrag);
+    };
+    if constexpr (BC) {
 #pragma unroll
-      for (int u = 0; u < kCMax; ++u) {
-        if (cb + u >= nc_w) break;
-        const int c = warp + kExpertWarps * (cb + u);
+      for (int u = 0; u < CPW; ++u) {
+        const int c = warp + kExpertWarps * u;
+        if (c >= G.NC) break;
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt) {
-          if (Q == kFP8) {
-            // one chunk = 64 K = 2 k-steps of m16n8k32
+          if constexpr (Q == kFP8)
+            chunk(c, rt, [&](int nt, int) { return bcache8[u][nt]; });
+          else
+            chunk(c, rt, [&](int nt, int j) { return bcache4[u][nt][j]; });
+        }
+      }
+    } else {
+      for (int c = warp; c < G.NC; c += kExpertWarps) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              if (nt >= ntile_act) break;
-              uint4 bv = make_uint4(0, 0, 0, 0);
-              if (brow[nt]) bv = ld_act_v4(brow[nt] + (size_t)c * 64 + q * 16);
-              mma_e4m3_16832(acc[rt][nt], L[u][rt].x, H[u][rt].x, L[u][rt].y, H[u][rt].y, bv.x,
-                             bv.y);
-              mma_e4m3_16832(acc[rt][nt], L[u][rt].z, H[u][rt].z, L[u][rt].w, H[u][rt].w, bv.z,
-                             bv.w);
-            }
-          } else if (Q == kMXFP4) {
-            // one chunk = 128 K = 4 scale blocks of 32 = 8 k-steps
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const float fl = ue8m0_to_f32(SL[u][rt].x >> (8 * b));
-              const float fh = ue8m0_to_f32(SH[u][rt].x >> (8 * b));
-              const uint32_t wl = word_of(L[u][rt], b), wh = word_of(H[u][rt], b);
-              const uint32_t a00 = e2m1x2_to_f16x2(wl), a01 = e2m1x2_to_f16x2(wh);
-              const uint32_t a02 = e2m1x2_to_f16x2(wl >> 8), a03 = e2m1x2_to_f16x2(wh >> 8);
-              const uint32_t a10 = e2m1x2_to_f16x2(wl >> 16), a11 = e2m1x2_to_f16x2(wh >> 16);
-              const uint32_t a12 = e2m1x2_to_f16x2(wl >> 24), a13 = e2m1x2_to_f16x2(wh >> 24);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt >= ntile_act) break;
-                uint2 b0 = make_uint2(0, 0), b1 = make_uint2(0, 0);
-                if (brow[nt]) {
-                  const uint8_t* bp = brow[nt] + ((size_t)c * 128 + 32 * b + 4 * q) * 2;
-                  b0 = ld_act_v2(bp);
-                  b1 = ld_act_v2(bp + 32);
-                }
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16_16816(t, a00, a01, a02, a03, b0.x, b0.y);
-                mma_f16_16816(t, a10, a11, a12, a13, b1.x, b1.y);
-                acc[rt][nt][0] = fmaf(t[0], fl, acc[rt][nt][0]);
-                acc[rt][nt][1] = fmaf(t[1], fl, acc[rt][nt][1]);
-                acc[rt][nt][2] = fmaf(t[2], fh, acc[rt][nt][2]);
-                acc[rt][nt][3] = fmaf(t[3], fh, acc[rt][nt][3]);
-              }
-            }
-          } else {  // NVFP4: one chunk = 8 k-steps, one e4m3 scale per k-step
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t slw = (j < 4 ? SL[u][rt].x : SL[u][rt].y) >> (8 * (j & 3));
-              const uint32_t shw = (j < 4 ? SH[u][rt].x : SH[u][rt].y) >> (8 * (j & 3));
-              const uint32_t sfl = e4m3x2_to_f16x2(slw & 0xFFu);
-              const uint32_t sfh = e4m3x2_to_f16x2(shw & 0xFFu);
-              const uint32_t sl2 = __byte_perm(sfl, sfl, 0x1010);  // broadcast low half
-              const uint32_t sh2 = __byte_perm(sfh, sfh, 0x1010);
-              const uint32_t wl = word_of(L[u][rt], j >> 1) >> (16 * (j & 1));
-              const uint32_t wh = word_of(H[u][rt], j >> 1) >> (16 * (j & 1));
-              const uint32_t a0 = hmul2(e2m1x2_to_f16x2(wl), sl2);
-              const uint32_t a1 = hmul2(e2m1x2_to_f16x2(wh), sh2);
-              const uint32_t a2 = hmul2(e2m1x2_to_f16x2(wl >> 8), sl2);
-              const uint32_t a3 = hmul2(e2m1x2_to_f16x2(wh >> 8), sh2);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt >= ntile_act) break;
-                uint2 bv = make_uint2(0, 0);
-                if (brow[nt]) bv = ld_act_v2(brow[nt] + ((size_t)c * 128 + 16 * j + 4 * q) * 2);
-                mma_f16_16816(acc[rt][nt], a0, a1, a2, a3, bv.x, bv.y);
-              }
-            }
-          }
+        for (int rt = 0; rt < RT; ++rt) {
+          if constexpr (Q == kFP8)
+            chunk(c, rt, [&](int nt, int) {
+              return brow[nt] ? ld_act_v4(brow[nt] + (size_t)c * 64 + q * 16) : make_uint4(0, 0, 0, 0);
+            });
+          else
+            chunk(c, rt, [&](int nt, int j) {
+              return brow[nt] ? ld_act_v2(brow[nt] + ((size_t)c * 128 + 16 * j + 4 * q) * 2)
+                              : make_uint2(0, 0);
+            });
         }
       }
     }
@@ -218,7 +384,13 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         if (nt < ntile_act)
           red[((warp * RT + rt) * NT + nt) * 32 + lane] =
               make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]);
-    __syncthreads();
+    __syncthreads();  // stage st is free, the partial tiles are complete
+    if (threadIdx.x == 0 && ii + S < mine) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      const int it = item + S;
+      issue_item<Q, ROLE, RT>(p, G, group_of(it / tiles).x, it % tiles,
+                              stage0 + st * G.stage_bytes, smem_u32(&bars[st]));
+    }
     const int slots = RT * NT * 32;
     for (int s = threadIdx.x; s < slots; s += kExpertThreads) {
       const int ln = s & 31, nt = (s >> 5) % NT, rt = s / (32 * NT);
@@ -250,7 +422,7 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         for (int h = 0; h < 2; ++h) {
           const int n = n0 + h;
           if (n >= ntok) continue;
-          const int r = __ldcg(p.route_list + rbase + n);
+          const int r = route_of(grp, rbase, n);
           float gt = gate[h], ut = up[h];
           if (Q == kFP8) {
             const float bs = __ldcg(p.b_scale + r / p.k);
@@ -279,7 +451,7 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         for (int h = 0; h < 2; ++h) {
           const int n = n0 + h;
           if (n >= ntok) continue;
-          const int r = __ldcg(p.route_list + rbase + n);
+          const int r = route_of(grp, rbase, n);
           const float bs = (Q == kFP8) ? __ldcg(p.b_scale + r) : 1.f;
           float* y = reinterpret_cast<float*>(p.out) + (size_t)r * p.P;
           y[plo] = lo[h] * bs;
@@ -289,16 +461,52 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
     }
     __syncthreads();
   }
+  if (stop_at >= 0 && threadIdx.x == 0) {
+    // a wait ran out: report it, and let the copies already issued land
+    // (bounded) before the CTA's shared memory is released
+    atomicOr(p.health, kHealthTimeout);
+    for (int k = stop_at; k < stop_at + S && k < mine; ++k)
+      mbar_wait(smem_u32(&bars[k % S]), (uint32_t)(k / S) & 1u, kWaitLimitNs / 4);
+  }
+}
+
+template <int Q, int ROLE, int NT, int RT>
+static void expert_smem_t(int K, int* stages, size_t* smem) {
+  const StageGeo G = stage_geo<Q, ROLE, RT>(K);
+  const size_t red = (size_t)kExpertWarps * RT * NT * 32 * sizeof(float4);
+  int S = (int)((kStageBudget > (int)red ? kStageBudget - (int)red : 0) / G.stage_bytes);
+  S = S < 2 ? 2 : (S > 8 ? 8 : S);
+  *stages = S;
+  *smem = (size_t)S * G.stage_bytes + red;
+}
+
+using ExpertKernel = void (*)(ExpertParams);
+
+// The instantiation for reduction length K: B fragments cached in registers
+// when the token tile is small and the warp's chunks fit the cache.
+template <int Q, int ROLE, int NT, int RT>
+static ExpertKernel expert_kernel(int K) {
+  constexpr int CPW = (Q == kFP8) ? 4 : 2;
+  const int NC = stage_geo<Q, ROLE, RT>(K).NC;
+  if constexpr (NT <= 2) {
+    if (NC <= kExpertWarps * CPW) return k_expert<Q, ROLE, NT, RT, true, CPW>;
+  }
+  return k_expert<Q, ROLE, NT, RT, false, CPW>;
 }
 
 template <int Q, int ROLE, int NT, int RT>
 static cudaError_t launch_expert_t(const ExpertParams& p, cudaStream_t s, bool pdl) {
-  const size_t smem = (size_t)kExpertWarps * RT * NT * 32 * sizeof(float4);
+  int S;
+  size_t smem;
+  expert_smem_t<Q, ROLE, NT, RT>(p.K, &S, &smem);
+  const ExpertKernel kern = expert_kernel<Q, ROLE, NT, RT>(p.K);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_expert<Q, ROLE, NT, RT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  ExpertParams q = p;
+  q.stages = S;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(kExpertThreads);
@@ -309,7 +517,7 @@ static cudaError_t launch_expert_t(const ExpertParams& p, cudaStream_t s, bool p
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_expert<Q, ROLE, NT, RT>, p);
+  return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
 template <int Q, int ROLE>
@@ -324,8 +532,6 @@ static cudaError_t launch_expert_q(const ExpertParams& p, int nt, cudaStream_t s
   }
 }
 
-int expert_rows_per_tile(int role, int nt) { return role == 1 && nt <= 2 ? 32 : 16; }
-
 cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pdl) {
   switch (p.quant * 2 + p.role) {
     case 0: return launch_expert_q<kMXFP4, 0>(p, nt, s, pdl);
@@ -339,34 +545,34 @@ cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pd
 }
 
 template <int Q, int ROLE, int NT, int RT>
-static int occ_t() {
-  int n = 0;
-  const size_t smem = (size_t)kExpertWarps * RT * NT * 32 * sizeof(float4);
+static int occ_t(int K) {
+  int n = 0, S;
+  size_t smem;
+  expert_smem_t<Q, ROLE, NT, RT>(K, &S, &smem);
+  const ExpertKernel kern = expert_kernel<Q, ROLE, NT, RT>(K);
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(k_expert<Q, ROLE, NT, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_expert<Q, ROLE, NT, RT>, kExpertThreads,
-                                                    smem) != cudaSuccess)
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kExpertThreads, smem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 template <int Q, int ROLE>
-static int occ_q(int nt) {
+static int occ_q(int nt, int K) {
   switch (nt) {
-    case 1: return occ_t<Q, ROLE, 1, ROLE == 1 ? 2 : 1>();
-    case 2: return occ_t<Q, ROLE, 2, ROLE == 1 ? 2 : 1>();
-    case 4: return occ_t<Q, ROLE, 4, 1>();
-    default: return occ_t<Q, ROLE, 8, 1>();
+    case 1: return occ_t<Q, ROLE, 1, ROLE == 1 ? 2 : 1>(K);
+    case 2: return occ_t<Q, ROLE, 2, ROLE == 1 ? 2 : 1>(K);
+    case 4: return occ_t<Q, ROLE, 4, 1>(K);
+    default: return occ_t<Q, ROLE, 8, 1>(K);
   }
 }
-int expert_ctas_per_sm(int quant, int role, int nt) {
+int expert_ctas_per_sm(int quant, int role, int nt, int K) {
   switch (quant * 2 + role) {
-    case 0: return occ_q<kMXFP4, 0>(nt);
-    case 1: return occ_q<kMXFP4, 1>(nt);
-    case 2: return occ_q<kNVFP4, 0>(nt);
-    case 3: return occ_q<kNVFP4, 1>(nt);
-    case 4: return occ_q<kFP8, 0>(nt);
-    default: return occ_q<kFP8, 1>(nt);
+    case 0: return occ_q<kMXFP4, 0>(nt, K);
+    case 1: return occ_q<kMXFP4, 1>(nt, K);
+    case 2: return occ_q<kNVFP4, 0>(nt, K);
+    case 3: return occ_q<kNVFP4, 1>(nt, K);
+    case 4: return occ_q<kFP8, 0>(nt, K);
+    default: return occ_q<kFP8, 1>(nt, K);
   }
 }
 
@@ -411,88 +617,136 @@ cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl) 
 // (page "vllm.models.muse_spark.amd.muse_moe_runner",
 // MuseSparkTopKWeightAndReduce.apply: norm to fp32, times topk_weights, sum
 // over k; moe_out stored as bf16.)
-__global__ void __launch_bounds__(256) k_finalize(FinalizeParams p) {
+constexpr int kFinalizeThreads = 512;
+constexpr int kFinalizeUnroll = 8;
+
+// One CTA per token. All k route rows are read with every load of a round in
+// flight and kept in shared memory when they fit (`stash`), so the rows
+// leave HBM/L2 once.
+__global__ void __launch_bounds__(kFinalizeThreads) k_finalize(FinalizeParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float scratch[32];
-  extern __shared__ float rstd[];
-  const int t = blockIdx.x;
-  for (int j = 0; j < p.k; ++j) {
-    const float* y = p.y + ((size_t)t * p.k + j) * p.P;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < p.P; i += blockDim.x) {
-      const float v = __ldcg(y + i);
-      ss += v * v;
+  extern __shared__ __align__(16) float4 fsm4[];
+  __shared__ float part[kFinalizeUnroll * 2][kFinalizeThreads / 32];
+  __shared__ float rstd[256], wt[256];
+  const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NW = kFinalizeThreads / 32;
+  const int P4 = p.P / 4;
+  const bool stash = p.stash != 0;
+  const float4* y4 = reinterpret_cast<const float4*>(p.y) + (size_t)t * p.k * P4;
+  for (int j = threadIdx.x; j < p.k; j += kFinalizeThreads) wt[j] = __ldcg(p.weights + (size_t)t * p.k + j);
+  // sums of squares, kFinalizeUnroll routes per round, all their loads in flight
+  for (int j0 = 0; j0 < p.k; j0 += kFinalizeUnroll) {
+    float ss[kFinalizeUnroll];
+#pragma unroll
+    for (int u = 0; u < kFinalizeUnroll; ++u) ss[u] = 0.f;
+    for (int i0 = 0; i0 < P4; i0 += kFinalizeThreads) {
+      const int i = i0 + threadIdx.x;
+      float4 v[kFinalizeUnroll];
+#pragma unroll
+      for (int u = 0; u < kFinalizeUnroll; ++u)
+        v[u] = (j0 + u < p.k && i < P4) ? __ldcg(y4 + (size_t)(j0 + u) * P4 + i)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kFinalizeUnroll; ++u) {
+        ss[u] += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+        if (stash && j0 + u < p.k && i < P4) fsm4[(size_t)(j0 + u) * P4 + i] = v[u];
+      }
     }
-    ss = block_sum(ss, scratch);
-    if (threadIdx.x == 0) rstd[j] = 1.0f / sqrtf(ss / (float)p.P + p.eps);
+#pragma unroll
+    for (int u = 0; u < kFinalizeUnroll; ++u) {
+      const float w = warp_sum(ss[u]);
+      if (lane == 0) part[u][warp] = w;
+    }
+    __syncthreads();
+    if (threadIdx.x < kFinalizeUnroll && j0 + threadIdx.x < p.k) {
+      float a = 0.f;
+      for (int w = 0; w < NW; ++w) a += part[threadIdx.x][w];
+      rstd[j0 + threadIdx.x] = 1.0f / sqrtf(a / (float)p.P + p.eps);
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < p.P; i += blockDim.x) {
-    const float wp = bf16_bits_to_f32(p.w_post_norm[i]);
-    float acc = 0.f;
+  for (int i = threadIdx.x; i < P4; i += kFinalizeThreads) {
+    const uint2 wpb = *reinterpret_cast<const uint2*>(p.w_post_norm + 4 * i);
+    const float w0 = bf16_bits_to_f32(wpb.x & 0xFFFFu), w1 = bf16_bits_to_f32(wpb.x >> 16);
+    const float w2 = bf16_bits_to_f32(wpb.y & 0xFFFFu), w3 = bf16_bits_to_f32(wpb.y >> 16);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
     for (int j = 0; j < p.k; ++j) {
-      const float v = __ldcg(p.y + ((size_t)t * p.k + j) * p.P + i);
-      const float n = (v * rstd[j]) * wp;
-      acc = fmaf(__ldcg(p.weights + (size_t)t * p.k + j), n, acc);
+      const float4 v = stash ? fsm4[(size_t)j * P4 + i] : __ldcg(y4 + (size_t)j * P4 + i);
+      const float r = rstd[j], c = wt[j];
+      a0 = fmaf(c, (v.x * r) * w0, a0);
+      a1 = fmaf(c, (v.y * r) * w1, a1);
+      a2 = fmaf(c, (v.z * r) * w2, a2);
+      a3 = fmaf(c, (v.w * r) * w3, a3);
     }
-    p.moe_out[(size_t)t * p.P + i] = f32_to_bf16_bits(acc);
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(a0) | ((uint32_t)f32_to_bf16_bits(a1) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(a2) | ((uint32_t)f32_to_bf16_bits(a3) << 16);
+    reinterpret_cast<uint2*>(p.moe_out + (size_t)t * p.P)[i] = o;
   }
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl) {
+  FinalizeParams q = p;
+  const size_t stash = (size_t)p.k * p.P * sizeof(float);
+  q.stash = stash <= 160 * 1024;
+  const size_t smem = q.stash ? stash : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_finalize, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.rows);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = (size_t)p.k * sizeof(float);
+  cfg.blockDim = dim3(kFinalizeThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_finalize, p);
+  return cudaLaunchKernelEx(&cfg, k_finalize, q);
 }
 
-// ---- weight re-layout: plain FP4 rows -> kernel layout ---------------------
-// Within every 64-byte group: byte 8j + 2q + b -> byte 16q + 2j + b.
-__global__ void k_pack_fp4(const uint8_t* src, uint8_t* dst, size_t groups) {
-  const size_t gi = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gi >= groups) return;
-  const uint4* s4 = reinterpret_cast<const uint4*>(src + gi * 64);
-  uint32_t in[16];
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 x = s4[v];
-    in[4 * v] = x.x;
-    in[4 * v + 1] = x.y;
-    in[4 * v + 2] = x.z;
-    in[4 * v + 3] = x.w;
-  }
-  uint32_t out[16];
-#pragma unroll
-  for (int w = 0; w < 16; ++w) {
-    uint32_t o = 0;
-#pragma unroll
-    for (int bb = 0; bb < 4; ++bb) {
-      const int dpos = 4 * w + bb;               // = 16q + 2j + b
-      const int qq = dpos >> 4, j = (dpos >> 1) & 7, b = dpos & 1;
-      const int spos = 8 * j + 2 * qq + b;
-      const uint32_t byte = (in[spos >> 2] >> (8 * (spos & 3))) & 0xFFu;
-      o |= byte << (8 * bb);
+// ---- weight re-layout: plain rows -> kernel layout --------------------------
+// One CTA per group of 8 consecutive rows: the group's bytes are read into
+// shared memory, then written back interleaved, so src may equal dst.
+// Kernel layout of a [rows, row_bytes] tensor whose row is cut into `nc`
+// chunks of `cb` bytes: [rows / 8][nc][8][cb]. With `permute_fp4`, the 64
+// bytes of each chunk are also reordered (byte 8j + 2q + b -> 16q + 2j + b).
+__global__ void k_pack_rows(const uint8_t* src, uint8_t* dst, int row_bytes, int cb,
+                            int permute_fp4) {
+  extern __shared__ __align__(16) uint8_t blk[];
+  const size_t base = (size_t)blockIdx.x * 8 * row_bytes;
+  const int nbytes = 8 * row_bytes;
+  for (int i = threadIdx.x * 4; i < nbytes; i += blockDim.x * 4)
+    *reinterpret_cast<uint32_t*>(blk + i) = *reinterpret_cast<const uint32_t*>(src + base + i);
+  __syncthreads();
+  const int nc = row_bytes / cb;
+  for (int o = threadIdx.x; o < nbytes; o += blockDim.x) {
+    const int c = o / (8 * cb), r = (o / cb) % 8;
+    int b = o % cb;
+    if (permute_fp4) {  // o's byte within the chunk is 16q + 2j + bb
+      const int qq = b >> 4, j = (b >> 1) & 7, bb = b & 1;
+      b = 8 * j + 2 * qq + bb;
     }
-    out[w] = o;
+    dst[base + o] = blk[r * row_bytes + c * cb + b];
+    (void)nc;
   }
-  uint4* d4 = reinterpret_cast<uint4*>(dst + gi * 64);
-#pragma unroll
-  for (int v = 0; v < 4; ++v)
-    d4[v] = make_uint4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
 }
 
-cudaError_t launch_pack_fp4(const uint8_t* src, uint8_t* dst, size_t bytes, cudaStream_t s) {
-  const size_t groups = bytes / 64;
-  if (groups == 0) return cudaSuccess;
-  k_pack_fp4<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(src, dst, groups);
+cudaError_t launch_pack_rows(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
+                             bool permute_fp4, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const size_t smem = (size_t)8 * row_bytes;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_pack_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_pack_rows<<<(unsigned)(rows / 8), 256, smem, s>>>(src, dst, row_bytes, cb, permute_fp4 ? 1 : 0);
   return cudaGetLastError();
 }
 

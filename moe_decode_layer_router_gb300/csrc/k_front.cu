@@ -20,6 +20,42 @@ constexpr int kFrontThreads = 128;  // 4 warps
 constexpr int kRouterRowsPerCta = 16;
 constexpr int kGemvRowsPerCta = 64;
 
+// True in every thread of the CTA that finishes the last of `splits` CTAs
+// sharing `ticket`; that CTA resets the ticket. No thread waits on another CTA.
+__device__ __forceinline__ bool last_of_tile(int32_t* ticket, int splits) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(ticket, 1);
+    s_last = (prev == splits - 1);
+    if (s_last) *ticket = 0;
+  }
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last;
+}
+
+// Sum of `splits` partials spaced `stride` floats apart, in a fixed order,
+// with up to 8 loads in flight.
+__device__ __forceinline__ float sum_splits(const float* p, size_t stride, int splits) {
+  float v = 0.f;
+  int s = 0;
+  for (; s + 8 <= splits; s += 8) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = __ldcg(p + (size_t)(s + i) * stride);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v += a[i];
+  }
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = (s + i < splits) ? __ldcg(p + (size_t)(s + i) * stride) : 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v += a[i];
+  return v;
+}
+
 __device__ __forceinline__ void router_cta(const FrontParams& p, int task) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int EB = (p.E + kRouterRowsPerCta - 1) / kRouterRowsPerCta;
@@ -70,6 +106,16 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task) {
       if (lane == 0 && e0 + r < p.E && t0 + t < p.rows)
         p.logit_part[((size_t)ks * p.rows + t0 + t) * p.E + e0 + r] = v;
     }
+  // the last split of this (expert block, token block) adds the partials
+  if (!last_of_tile(p.router_tickets + eb + EB * tb, p.ks_r)) return;
+  const int ntok = min(8, p.rows - t0);
+  for (int idx = threadIdx.x; idx < kRouterRowsPerCta * ntok; idx += kFrontThreads) {
+    const int e = eb * kRouterRowsPerCta + idx % kRouterRowsPerCta;
+    const int t = t0 + idx / kRouterRowsPerCta;
+    if (e >= p.E) continue;
+    p.logits[(size_t)t * p.E + e] =
+        sum_splits(p.logit_part + (size_t)t * p.E + e, (size_t)p.rows * p.E, p.ks_r);
+  }
 }
 
 template <int NT>
@@ -104,34 +150,39 @@ __device__ __forceinline__ void gemv_cta(const FrontParams& p, int task) {
   constexpr int U = 4;
   int c = c0;
   for (; c + U <= c1; c += U) {
-    uint4 lo[U], hi[U];
+    uint4 lo[U], hi[U], bv[U][NT];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       lo[u] = ld_stream_v4(a_lo + (size_t)(c + u) * 32);
       hi[u] = ld_stream_v4(a_hi + (size_t)(c + u) * 32);
     }
 #pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        bv[u][nt] = bval[nt] ? ld_act_v4(bptr[nt] + (size_t)(c + u) * 32) : make_uint4(0, 0, 0, 0);
+#pragma unroll
     for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (tok0 + nt * 8 >= p.rows) break;
-        uint4 bv = make_uint4(0, 0, 0, 0);
-        if (bval[nt]) bv = ld_act_v4(bptr[nt] + (size_t)(c + u) * 32);
-        mma_bf16_16816(acc[nt], lo[u].x, hi[u].x, lo[u].y, hi[u].y, bv.x, bv.y);
-        mma_bf16_16816(acc[nt], lo[u].z, hi[u].z, lo[u].w, hi[u].w, bv.z, bv.w);
+        mma_bf16_16816(acc[nt], lo[u].x, hi[u].x, lo[u].y, hi[u].y, bv[u][nt].x, bv[u][nt].y);
+        mma_bf16_16816(acc[nt], lo[u].z, hi[u].z, lo[u].w, hi[u].w, bv[u][nt].z, bv[u][nt].w);
       }
     }
   }
   for (; c < c1; ++c) {
     const uint4 lo = ld_stream_v4(a_lo + (size_t)c * 32);
     const uint4 hi = ld_stream_v4(a_hi + (size_t)c * 32);
+    uint4 bv[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      bv[nt] = bval[nt] ? ld_act_v4(bptr[nt] + (size_t)c * 32) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       if (tok0 + nt * 8 >= p.rows) break;
-      uint4 bv = make_uint4(0, 0, 0, 0);
-      if (bval[nt]) bv = ld_act_v4(bptr[nt] + (size_t)c * 32);
-      mma_bf16_16816(acc[nt], lo.x, hi.x, lo.y, hi.y, bv.x, bv.y);
-      mma_bf16_16816(acc[nt], lo.z, hi.z, lo.w, hi.w, bv.z, bv.w);
+      mma_bf16_16816(acc[nt], lo.x, hi.x, lo.y, hi.y, bv[nt].x, bv[nt].y);
+      mma_bf16_16816(acc[nt], lo.z, hi.z, lo.w, hi.w, bv[nt].z, bv[nt].w);
     }
   }
   // D fragment: c0/c1 = (row g, tokens 2q, 2q+1), c2/c3 = (row g+8, same tokens)
@@ -147,6 +198,14 @@ __device__ __forceinline__ void gemv_cta(const FrontParams& p, int task) {
       base[(size_t)(n0 + 1) * p.M + row_lo] = acc[nt][1];
       base[(size_t)(n0 + 1) * p.M + row_lo + 8] = acc[nt][3];
     }
+  }
+  // the last split of this (row block, token block) adds the partials
+  if (!last_of_tile(p.tickets + rb + RB * tb, p.ks)) return;
+  const int ntok = min(8 * NT, p.rows - tok0);
+  for (int idx = threadIdx.x; idx < kGemvRowsPerCta * ntok; idx += kFrontThreads) {
+    const int row = rb * kGemvRowsPerCta + idx % kGemvRowsPerCta;
+    const int t = tok0 + idx / kGemvRowsPerCta;
+    p.y[(size_t)t * p.M + row] = sum_splits(p.part + (size_t)t * p.M + row, (size_t)p.rows * p.M, p.ks);
   }
 }
 

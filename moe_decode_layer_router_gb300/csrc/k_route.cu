@@ -69,23 +69,6 @@ __device__ __forceinline__ void warp_bitonic_desc(uint64_t (&key)[EPL], int lane
   }
 }
 
-template <int EPL>
-__device__ void select_topk(const float* sel, int E, int k, int* top, int lane) {
-  uint64_t key[EPL];
-#pragma unroll
-  for (int r = 0; r < EPL; ++r) {
-    const int i = lane * EPL + r;
-    key[r] = (i < E) ? ((uint64_t)orderable(sel[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i)
-                     : 0ull;
-  }
-  warp_bitonic_desc<EPL>(key, lane);
-#pragma unroll
-  for (int r = 0; r < EPL; ++r) {
-    const int i = lane * EPL + r;
-    if (i < k) top[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[r] & 0xFFFFFFFFull));
-  }
-}
-
 // Exclusive scan of one int per thread (blockDim.x == kRouteThreads).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -113,27 +96,83 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   return before + x - v;
 }
 
-struct RouteSmem {
-  float g[256];     // scaled logits
-  float s[256];     // unbiased scores
-  float sel[256];   // selection scores
-  int top[256];
-  float scratch[32];
-  int iscratch[32];
-  int flag;
-};
+// One warp routes row t: scores from the fp32 logits, selection keys, the
+// bitonic top-k, then the weights from the UNBIASED scores of the selected
+// ids. `s_w` (E floats) and `top` (k ints) are the warp's shared scratch.
+template <int EPL>
+__device__ void route_row_warp(const RouteParams& p, int t, int lane, float* s_w, int* top,
+                               int16_t* ids_smem) {
+  const int E = p.E, k = p.k;
+  float g[EPL];
+  float gmax = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < EPL; ++r) {
+    const int i = lane * EPL + r;
+    float l = (i < E) ? __ldcg(p.logits + (size_t)t * E + i) : -INFINITY;
+    if (p.has_multiplier && i < E) l = l * p.multiplier;
+    g[r] = l;
+    gmax = fmaxf(gmax, l);
+  }
+  float sc[EPL];
+  if (p.score == 1) {  // softmax over the experts
+    gmax = warp_max(gmax);
+    float part = 0.f;
+#pragma unroll
+    for (int r = 0; r < EPL; ++r) {
+      sc[r] = (lane * EPL + r < E) ? expf(g[r] - gmax) : 0.f;
+      part += sc[r];
+    }
+    const float tot = warp_sum(part);
+#pragma unroll
+    for (int r = 0; r < EPL; ++r) sc[r] = sc[r] / tot;
+  } else {
+#pragma unroll
+    for (int r = 0; r < EPL; ++r) sc[r] = 1.0f / (1.0f + expf(-g[r]));
+  }
+  uint64_t key[EPL];
+#pragma unroll
+  for (int r = 0; r < EPL; ++r) {
+    const int i = lane * EPL + r;
+    if (i < E) {
+      s_w[i] = sc[r];
+      const float sel = sc[r] + __ldg(p.expert_bias + i);  // selection only
+      key[r] = ((uint64_t)orderable(sel) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+    } else {
+      key[r] = 0ull;
+    }
+  }
+  warp_bitonic_desc<EPL>(key, lane);
+#pragma unroll
+  for (int r = 0; r < EPL; ++r) {
+    const int i = lane * EPL + r;
+    if (i < k) top[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[r] & 0xFFFFFFFFull));
+  }
+  __syncwarp();
+  float part = 0.f;
+  for (int i = lane; i < k; i += 32) part += s_w[top[i]];
+  float denom = warp_sum(part);
+  if (p.has_division_eps) denom += p.division_eps;
+  for (int i = lane; i < k; i += 32) {
+    const int e = top[i];
+    p.ids[(size_t)t * k + i] = e;
+    p.weights[(size_t)t * k + i] = s_w[e] / denom * p.route_scale;
+    if (ids_smem) ids_smem[(size_t)t * k + i] = (int16_t)e;
+  }
+  __syncwarp();
+}
 
-__device__ void permute_last_cta(const RouteParams& p, unsigned char* dyn) {
+// Token -> expert permute from the ids in ids_s (shared): counts per expert,
+// routes grouped by expert in route order (a stable counting sort), then the
+// token groups the expert kernels walk.
+__device__ void permute(const RouteParams& p, int16_t* ids_s, unsigned char* work) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int E = p.E, rt = p.rows * p.k;
   const int nch = (rt + 31) / 32;
-  int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
-  uint8_t* rank_s = reinterpret_cast<uint8_t*>(ids_s + ((rt + 7) & ~7));
+  uint8_t* rank_s = work;
   uint16_t* hist = reinterpret_cast<uint16_t*>(rank_s + ((rt + 15) & ~15));
   __shared__ int cnt_s[256], off_s[257], goff_s[257];
   __shared__ int scan_scratch[32];
 
-  for (int i = tid; i < rt; i += kRouteThreads) ids_s[i] = (int16_t)__ldcg(p.ids + i);
   for (int i = tid; i < nch * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
   // per 32-route chunk: rank of each route among equal experts, chunk counts
@@ -191,116 +230,107 @@ __device__ void permute_last_cta(const RouteParams& p, unsigned char* dyn) {
   }
 }
 
+// RMSNorm of the pooled row t with the effective bf16 weight -> bf16 h and
+// the expert operand (f16, or e4m3 + per-row scale for FP8).
+__device__ void pre_norm_row(const RouteParams& p, int t, float* hr, float* scratch) {
+  const int tid = threadIdx.x;
+  float ss = 0.f;
+  const float4* src = reinterpret_cast<const float4*>(p.h_raw + (size_t)t * p.P);
+#pragma unroll 4
+  for (int i = tid; i < p.P / 4; i += kRouteThreads) {
+    const float4 v = __ldcg(src + i);
+    reinterpret_cast<float4*>(hr)[i] = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = block_sum(ss, scratch);  // also orders the hr[] writes before the reads
+  const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.P + p.norm_eps) : 1.0f;
+  float amax = 0.f;
+  int bad = 0;
+  for (int i = tid; i < p.P; i += kRouteThreads) {
+    float v = hr[i];
+    if (p.pre_norm) v = (v * rstd) * bf16_bits_to_f32(p.w_pre_norm[i]);
+    const float hb = round_bf16(v);
+    p.h[(size_t)t * p.P + i] = f32_to_bf16_bits(hb);
+    hr[i] = hb;
+    amax = fmaxf(amax, fabsf(hb));
+    if (p.quant != kFP8) {
+      reinterpret_cast<__half*>(p.h_op)[(size_t)t * p.P + i] = __float2half_rn(hb);
+      bad |= !(fabsf(hb) <= 65504.f);
+    }
+  }
+  if (p.quant == kFP8) {
+    amax = block_max(amax, scratch);
+    const float sc = amax / 448.0f;
+    for (int i = 2 * tid; i < p.P; i += 2 * kRouteThreads) {
+      const float a = sc > 0.f ? hr[i] / sc : 0.f;
+      const float b = sc > 0.f ? hr[i + 1] / sc : 0.f;
+      reinterpret_cast<uint16_t*>(p.h_op + (size_t)t * p.P)[i / 2] = f32x2_to_e4m3x2(a, b);
+    }
+    if (tid == 0) p.h_scale[t] = sc;
+  }
+  if (bad) atomicOr(p.health, kHealthHRange);
+}
+
+// Grid: with p.central, rows + 1 CTAs: CTA `rows` routes every row (one warp
+// per row) and builds the permute from shared memory; CTAs 0..rows-1 normalize
+// their pooled row. Otherwise rows CTAs, each routing and normalizing its
+// row; the CTA that finishes last (atomic ticket, no waiting) builds the
+// permute. Without p.h_raw only the routing runs.
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ RouteSmem sm;
+  __shared__ float s_w[kRouteThreads / 32][256];
+  __shared__ int top[kRouteThreads / 32][256];
+  __shared__ float scratch[32];
+  __shared__ int flag;
   extern __shared__ __align__(16) unsigned char dyn[];
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int E = p.E, k = p.k;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
-  // ---- logits, multiplier, scores, selection scores --------------------
-  float gmax = -INFINITY;
-  for (int e = tid; e < E; e += kRouteThreads) {
-    float l = 0.f;
-    for (int ks = 0; ks < p.ks_r; ++ks) l += __ldcg(p.logit_part + ((size_t)ks * p.rows + t) * E + e);
-    p.logits[(size_t)t * E + e] = l;
-    const float g = p.has_multiplier ? l * p.multiplier : l;
-    sm.g[e] = g;
-    gmax = fmaxf(gmax, g);
-  }
-  if (p.score == 1) {  // softmax over the experts
-    gmax = block_max(gmax, sm.scratch);
-    float part = 0.f;
-    for (int e = tid; e < E; e += kRouteThreads) {
-      const float z = expf(sm.g[e] - gmax);
-      sm.s[e] = z;
-      part += z;
+  if (p.central) {
+    if ((int)blockIdx.x < p.rows) {
+      if (p.h_raw != nullptr) pre_norm_row(p, blockIdx.x, reinterpret_cast<float*>(dyn), scratch);
+      return;
     }
-    const float tot = block_sum(part, sm.scratch);
-    for (int e = tid; e < E; e += kRouteThreads) sm.s[e] = sm.s[e] / tot;
-  } else {
-    for (int e = tid; e < E; e += kRouteThreads) sm.s[e] = 1.0f / (1.0f + expf(-sm.g[e]));
-  }
-  for (int e = tid; e < E; e += kRouteThreads) sm.sel[e] = sm.s[e] + __ldg(p.expert_bias + e);
-  __syncthreads();
-
-  // ---- top-k and weights (warp 0) -----------------------------------------
-  if (wid == 0) {
-    select_topk<EPL>(sm.sel, E, k, sm.top, lane);
-    __syncwarp();
-    float part = 0.f;
-    for (int i = lane; i < k; i += 32) part += sm.s[sm.top[i]];
-    float denom = warp_sum(part);
-    if (p.has_division_eps) denom += p.division_eps;
-    for (int i = lane; i < k; i += 32) {
-      const int e = sm.top[i];
-      p.ids[(size_t)t * k + i] = e;
-      p.weights[(size_t)t * k + i] = sm.s[e] / denom * p.route_scale;
-    }
+    int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
+    const bool perm = p.route_list != nullptr;
+    for (int t = wid; t < p.rows; t += kRouteThreads / 32)
+      route_row_warp<EPL>(p, t, lane, s_w[wid], top[wid], perm ? ids_s : nullptr);
+    if (!perm) return;
+    __syncthreads();
+    const int rt = p.rows * p.k;
+    permute(p, ids_s, dyn + (((size_t)rt * 2 + 15) & ~(size_t)15));
+    return;
   }
 
-  // ---- pre-expert norm ----------------------------------------------------
-  if (p.pool_part != nullptr) {
-    float* hr = reinterpret_cast<float*>(dyn);
-    float ss = 0.f;
-    for (int i = tid; i < p.P; i += kRouteThreads) {
-      float v = 0.f;
-      for (int ks = 0; ks < p.ks_p; ++ks) v += __ldcg(p.pool_part + ((size_t)ks * p.rows + t) * p.P + i);
-      hr[i] = v;
-      ss += v * v;
-    }
-    ss = block_sum(ss, sm.scratch);
-    const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.P + p.norm_eps) : 1.0f;
-    float amax = 0.f;
-    int bad = 0;
-    for (int i = tid; i < p.P; i += kRouteThreads) {
-      float v = hr[i];
-      if (p.pre_norm) v = (v * rstd) * bf16_bits_to_f32(p.w_pre_norm[i]);
-      const float hb = round_bf16(v);
-      p.h[(size_t)t * p.P + i] = f32_to_bf16_bits(hb);
-      hr[i] = hb;
-      amax = fmaxf(amax, fabsf(hb));
-      if (p.quant != kFP8) {
-        reinterpret_cast<__half*>(p.h_op)[(size_t)t * p.P + i] = __float2half_rn(hb);
-        bad |= !(fabsf(hb) <= 65504.f);
-      }
-    }
-    if (p.quant == kFP8) {
-      amax = block_max(amax, sm.scratch);
-      const float s = amax / 448.0f;
-      for (int i = 2 * tid; i < p.P; i += 2 * kRouteThreads) {
-        const float a = s > 0.f ? hr[i] / s : 0.f;
-        const float b = s > 0.f ? hr[i + 1] / s : 0.f;
-        reinterpret_cast<uint16_t*>(p.h_op + (size_t)t * p.P)[i / 2] = f32x2_to_e4m3x2(a, b);
-      }
-      if (tid == 0) p.h_scale[t] = s;
-    }
-    if (bad) atomicOr(p.health, kHealthHRange);
-  }
-
+  const int t = blockIdx.x;
+  if (wid == 0) route_row_warp<EPL>(p, t, lane, s_w[0], top[0], nullptr);
+  if (p.h_raw != nullptr) pre_norm_row(p, t, reinterpret_cast<float*>(dyn), scratch);
   if (p.route_list == nullptr) return;
   // ---- last CTA: permute --------------------------------------------------
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const int prev = atomicAdd(p.counters + kTicket, 1);
-    sm.flag = (prev == p.rows - 1);
+    flag = (prev == p.rows - 1);
   }
   __syncthreads();
-  if (!sm.flag) return;
+  if (!flag) return;
   __threadfence();
-  permute_last_cta(p, dyn);
+  const int rt = p.rows * p.k;
+  int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
+  for (int i = tid; i < rt; i += kRouteThreads) ids_s[i] = (int16_t)__ldcg(p.ids + i);
+  __syncthreads();
+  permute(p, ids_s, dyn + (((size_t)rt * 2 + 15) & ~(size_t)15));
 }
 
 static size_t route_dyn_smem(const RouteParams& p) {
-  size_t a = (p.pool_part != nullptr) ? (size_t)p.P * 4 : 0;
+  size_t a = (p.h_raw != nullptr) ? (size_t)p.P * 4 : 0;
   size_t b = 0;
   if (p.route_list != nullptr) {
     const size_t rt = (size_t)p.rows * p.k;
     const size_t nch = (rt + 31) / 32;
-    b = ((rt + 7) & ~(size_t)7) * 2 + ((rt + 15) & ~(size_t)15) + nch * p.E * 2;
+    b = ((rt * 2 + 15) & ~(size_t)15) + ((rt + 15) & ~(size_t)15) + nch * p.E * 2;
   }
   return ((a > b ? a : b) + 15) & ~(size_t)15;
 }
@@ -314,7 +344,7 @@ static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t s, bool pdl
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.rows);
+  cfg.gridDim = dim3(p.central ? p.rows + 1 : p.rows);
   cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -10,21 +10,27 @@ enum Quant : int { kMXFP4 = 0, kNVFP4 = 1, kFP8 = 2 };
 // counters[] slots in the workspace
 enum Counter : int { kNumGroups = 0, kTicket = 1, kNumCounters = 8 };
 // health bits
-enum Health : int { kHealthHRange = 1, kHealthActRange = 2 };
+enum Health : int { kHealthHRange = 1, kHealthActRange = 2, kHealthTimeout = 4 };
 
 // ---- front: router GEMV (fp32 FFMA) + pooler GEMV (tensor cores) --------
 // The router part writes logit partial sums [ks_r][rows][E]; the GEMV part
 // writes partial sums [ks][rows][M] of Y = X W^T for bf16 W [M, K].
+// The CTA that finishes the last K-split of an output tile (atomic ticket,
+// no waiting) adds the partials in split order and writes the tile.
 struct FrontParams {
   const uint16_t* x;  // bf16 [rows, K]
   int rows;
   // router (skipped when router_ctas == 0)
   const float* w_router;  // fp32 [E, K]
   float* logit_part;      // [ks_r, rows, E]
+  float* logits;          // [rows, E]
+  int32_t* router_tickets;
   int E, ks_r, router_ctas;
   // bf16 GEMV
   const uint16_t* w;  // bf16 [M, K]
   float* part;        // [ks, rows, M]
+  float* y;           // [rows, M]
+  int32_t* tickets;
   int M, K, ks;
   int kchunks_per_split;  // 32-element chunks per split
   int token_blocks;       // ceil(rows / (8 * NT))
@@ -34,22 +40,21 @@ int front_ctas(const FrontParams& p);
 
 // ---- route: routing rule + pre-expert norm + token->expert permute ------
 struct RouteParams {
-  const float* logit_part;  // [ks_r, rows, E]
+  const float* logits;      // [rows, E]
   const float* expert_bias;
-  float* logits;            // [rows, E]
   int32_t* ids;             // [rows, k]
   float* weights;           // [rows, k]
-  int rows, E, k, ks_r;
+  int rows, E, k;
   int score;  // 0 sigmoid, 1 softmax
   int has_multiplier;
   float multiplier;
   int has_division_eps;
   float division_eps;
   float route_scale;
-  // pre-expert norm (skipped when pool_part == nullptr: routing only)
-  const float* pool_part;  // [ks_p, rows, P]
+  // pre-expert norm (skipped when h_raw == nullptr: routing only)
+  const float* h_raw;  // fp32 [rows, P] pooled rows
   const uint16_t* w_pre_norm;
-  int P, ks_p, pre_norm;
+  int P, pre_norm;
   float norm_eps;
   int quant;
   uint16_t* h;      // bf16 [rows, P]
@@ -61,6 +66,7 @@ struct RouteParams {
   int32_t* counters;
   int32_t* health;
   int token_group;  // routes per group (8 * NT of the expert kernels)
+  int central;      // 1: one extra CTA routes all rows (rows <= 32)
 };
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
 
@@ -70,8 +76,8 @@ struct ExpertParams {
   int role;      // 0: w13 + SiLU*up -> act; 1: w2 -> y
   int E, N, K;   // rows N and reduction K of the weight matrix
   int I, P, k;
-  const uint8_t* w;        // codes [E, N, K/2] packed (FP4) or [E, N, K] (FP8)
-  const void* scale;       // see musemoe_weights
+  const uint8_t* w;        // codes, kernel layout [E][N/8][NC][8][64]
+  const void* scale;       // MX/NV: kernel layout [E][N/8][NC][8][SB]; FP8: fp32 [E, N]
   const float* gscale;     // NVFP4 [E]
   const uint8_t* b;        // activation operand: f16 [*, K] or e4m3 [*, K]
   const float* b_scale;    // FP8: per B row
@@ -82,9 +88,10 @@ struct ExpertParams {
   void* out;               // role 0: act f16/bf16 [rows*k, I]; role 1: y fp32 [rows*k, P]
   int32_t* health;
   int grid;
+  int stages;  // set by launch_expert
 };
 cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pdl);
-int expert_ctas_per_sm(int quant, int role, int nt);
+int expert_ctas_per_sm(int quant, int role, int nt, int K);
 
 // FP8 only: per-route dynamic e4m3 quantization of the bf16 activation.
 struct ActQuantParams {
@@ -103,25 +110,28 @@ struct FinalizeParams {
   uint16_t* moe_out;  // bf16 [rows, P]
   int rows, k, P;
   float eps;
+  int stash;  // set by launch_finalize: route rows kept in shared memory
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl);
 
 // ---- FFN boundary ------------------------------------------------------------
 struct BoundaryParams {
-  const float* part;  // unpooler partials [ks, rows, H]
-  int ks;
+  const float* u;     // unpooler output fp32 [rows, H]
   float* stream;      // fp32 [rows, H], in place
   uint16_t* out;      // bf16 [rows, H]
   const uint16_t* w_ffn_norm;
   const uint16_t* w_next_norm;
   const float* gate;
-  float* u_tap;       // optional fp32 [rows, H]
   int rows, H;
   float eps;
 };
 cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
 
 // ---- weight re-layout ----------------------------------------------------
-cudaError_t launch_pack_fp4(const uint8_t* src, uint8_t* dst, size_t bytes, cudaStream_t s);
+// Interleaves groups of 8 rows of a [rows, row_bytes] tensor chunk by chunk
+// ([rows / 8][row_bytes / cb][8][cb]); permute_fp4 also reorders the bytes of
+// each 64-byte chunk for the FP4 mma fragments. src may equal dst.
+cudaError_t launch_pack_rows(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
+                             bool permute_fp4, cudaStream_t s);
 
 }  // namespace musemoe

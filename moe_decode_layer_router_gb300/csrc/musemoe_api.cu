@@ -77,6 +77,8 @@ struct musemoe_handle {
   // workspace views
   float *logit_part = nullptr, *pool_part = nullptr, *unpool_part = nullptr;
   float *logits = nullptr, *weights = nullptr, *h_scale = nullptr, *act_scale = nullptr;
+  float *h_raw = nullptr, *u = nullptr;
+  int32_t *router_tickets = nullptr, *pool_tickets = nullptr, *unpool_tickets = nullptr;
   float *y = nullptr, *stream_stage = nullptr;
   int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
   int32_t* health = nullptr;
@@ -113,6 +115,13 @@ void plan(musemoe_handle* h, Layout& L) {
   L.add(&h->pool_part, pool_part * P * 4);
   L.add(&h->unpool_part, unpool_part * H * 4);
   L.add(&h->logits, R * E * 4);
+  L.add(&h->h_raw, R * P * 4);
+  L.add(&h->u, R * H * 4);
+  // one ticket per output tile of the split GEMVs (tiles of 16 experts x 8
+  // tokens, 64 rows x 8 tokens)
+  L.add(&h->router_tickets, ((E + 15) / 16) * ((R + 7) / 8) * 4);
+  L.add(&h->pool_tickets, (P / 64) * ((R + 7) / 8) * 4);
+  L.add(&h->unpool_tickets, (H / 64) * ((R + 7) / 8) * 4);
   L.add(&h->ids, RT * 4);
   L.add(&h->weights, RT * 4);
   L.add(&h->h, R * P * 2);
@@ -149,8 +158,17 @@ std::vector<std::string> refusals(const musemoe_dims* d, int32_t quant, const mu
     r.push_back(fmt("max_rows * top_k = %lld exceeds %d routes", (long long)d->max_rows * d->top_k,
                     kMaxRoutes));
   if ((size_t)d->pooled * 4 > 200 * 1024) r.push_back(fmt("pooled %d too large for one CTA row", d->pooled));
-  if ((size_t)d->hidden * 4 > 200 * 1024) r.push_back(fmt("hidden %d too large for one CTA row", d->hidden));
+  if (d->hidden > 8192) r.push_back(fmt("hidden %d above 8192 (one CTA row in registers)", d->hidden));
   if (quant < 0 || quant > 2) r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1) or FP8_W8A8 (2)", quant));
+  else {
+    // two pipeline stages of the widest expert item (two 8-row groups of w13)
+    // plus the 32 KB reduction tile must fit in one CTA's shared memory
+    const long long chunk = quant == 2 ? 512 : 512 + (quant == 0 ? 32 : 64);
+    const long long nc = quant == 2 ? (long long)d->pooled / 64 : (long long)d->pooled / 128;
+    const long long stage = 2 * nc * chunk;
+    if (2 * stage + 32 * 1024 > 220 * 1024)
+      r.push_back(fmt("pooled %d too large for two expert pipeline stages", d->pooled));
+  }
   if (c->score != 0 && c->score != 1) r.push_back(fmt("score %d is not sigmoid (0) or softmax (1)", c->score));
   if (!std::isfinite(c->route_scale)) r.push_back("route_scale is not finite");
   if (c->has_multiplier && !std::isfinite(c->multiplier)) r.push_back("multiplier is not finite");
@@ -239,11 +257,15 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fp.rows = rows;
   fp.w_router = w->w_router;
   fp.logit_part = h->logit_part;
+  fp.logits = h->logits;
+  fp.router_tickets = h->router_tickets;
   fp.E = d.experts;
   fp.ks_r = ks_r;
   fp.router_ctas = router_ctas(d.experts, rows, ks_r);
   fp.w = w->w_pool;
   fp.part = h->pool_part;
+  fp.y = h->h_raw;
+  fp.tickets = h->pool_tickets;
   fp.M = d.pooled;
   fp.K = d.hidden;
   fp.ks = sp.ks;
@@ -255,25 +277,22 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   // 2. routing + pre-expert norm + permute
   const int nte = nt_expert(rows);
   RouteParams rp{};
-  rp.logit_part = h->logit_part;
-  rp.expert_bias = w->expert_bias;
   rp.logits = h->logits;
+  rp.expert_bias = w->expert_bias;
   rp.ids = h->ids;
   rp.weights = h->weights;
   rp.rows = rows;
   rp.E = d.experts;
   rp.k = d.top_k;
-  rp.ks_r = ks_r;
   rp.score = h->cfg.score;
   rp.has_multiplier = h->cfg.has_multiplier;
   rp.multiplier = h->cfg.multiplier;
   rp.has_division_eps = h->cfg.has_division_eps;
   rp.division_eps = h->cfg.division_eps;
   rp.route_scale = h->cfg.route_scale;
-  rp.pool_part = h->pool_part;
+  rp.h_raw = h->h_raw;
   rp.w_pre_norm = w->w_pre_norm;
   rp.P = d.pooled;
-  rp.ks_p = sp.ks;
   rp.pre_norm = h->cfg.pre_expert_norm;
   rp.norm_eps = h->cfg.norm_eps;
   rp.quant = h->quant;
@@ -285,6 +304,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   rp.counters = h->counters;
   rp.health = h->health;
   rp.token_group = 8 * nte;
+  rp.central = rows <= 32;
   before();
   if (!after(launch_route(rp, s, pdl), "route")) return MUSEMOE_ECUDA;
 
@@ -362,6 +382,8 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   up.ks_r = 1;
   up.w = w->w_unpool;
   up.part = h->unpool_part;
+  up.y = h->u;
+  up.tickets = h->unpool_tickets;
   up.M = d.hidden;
   up.K = d.pooled;
   up.ks = su.ks;
@@ -372,14 +394,12 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
 
   // 7. FFN boundary
   BoundaryParams bp{};
-  bp.part = h->unpool_part;
-  bp.ks = su.ks;
+  bp.u = h->u;
   bp.stream = stream;
   bp.out = out;
   bp.w_ffn_norm = w->w_ffn_norm;
   bp.w_next_norm = w->w_next_norm;
   bp.gate = w->gate;
-  bp.u_tap = taps ? taps->u : nullptr;
   bp.rows = rows;
   bp.H = d.hidden;
   bp.eps = h->cfg.norm_eps;
@@ -399,6 +419,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
         {taps->act, h->act, (size_t)rows * d.top_k * d.inter * 2},
         {taps->y, h->y, (size_t)rows * d.top_k * d.pooled * 4},
         {taps->moe_out, h->moe_out, (size_t)rows * d.pooled * 2},
+        {taps->u, h->u, (size_t)rows * d.hidden * 4},
     };
     for (const Cp& c : cps)
       if (c.dst) {
@@ -469,7 +490,8 @@ musemoe_status musemoe_create(const musemoe_dims* dims, int32_t quant, const mus
   h->max_groups = std::min(dims->experts, h->max_routes) + (h->max_routes + 7) / 8 + 1;
   for (int role = 0; role < 2; ++role)
     for (int i = 0; i < 4; ++i)
-      h->expert_grid[role][i] = h->sms * expert_ctas_per_sm(quant, role, 1 << i);
+      h->expert_grid[role][i] =
+          h->sms * expert_ctas_per_sm(quant, role, 1 << i, role == 0 ? dims->pooled : dims->inter);
   Layout L;
   plan(h, L);
   h->ws_bytes = L.off;
@@ -534,30 +556,47 @@ const char* musemoe_kernel_name(int32_t quant, int32_t i) {
 }
 
 musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const uint8_t* w13_src,
-                                    uint8_t* w13_dst, const uint8_t* w2_src, uint8_t* w2_dst,
+                                    const void* w13_scale_src, uint8_t* w13_dst,
+                                    void* w13_scale_dst, const uint8_t* w2_src,
+                                    const void* w2_scale_src, uint8_t* w2_dst, void* w2_scale_dst,
                                     musemoe_stream_t stream) {
   if (!d) return set_err(nullptr, MUSEMOE_EINVAL, "dims is NULL");
   musemoe_config c{};
   c.route_scale = 1.f;
   const std::vector<std::string> r = refusals(d, quant, &c);
   if (!r.empty()) return set_err(nullptr, MUSEMOE_EUNSUPPORTED, join(r));
-  if (!w13_src || !w13_dst || !w2_src || !w2_dst)
-    return set_err(nullptr, MUSEMOE_EINVAL, "expert tensor pointers must not be NULL");
-  if (!aligned16(w13_src) || !aligned16(w13_dst) || !aligned16(w2_src) || !aligned16(w2_dst))
-    return set_err(nullptr, MUSEMOE_EINVAL, "expert tensors must be 16-byte aligned");
+  const void* ptrs[8] = {w13_src, w13_scale_src, w13_dst, w13_scale_dst,
+                         w2_src,  w2_scale_src,  w2_dst,  w2_scale_dst};
+  for (const void* q : ptrs) {
+    if (!q) return set_err(nullptr, MUSEMOE_EINVAL, "expert tensor pointers must not be NULL");
+    if (!aligned16(q)) return set_err(nullptr, MUSEMOE_EINVAL, "expert tensors must be 16-byte aligned");
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t E = d->experts, P = d->pooled, I = d->inter;
-  const size_t b13 = E * 2 * I * (quant == kFP8 ? P : P / 2);
-  const size_t b2 = E * P * (quant == kFP8 ? I : I / 2);
-  cudaError_t e;
-  if (quant == kFP8) {
-    e = (w13_src == w13_dst) ? cudaSuccess
-                             : cudaMemcpyAsync(w13_dst, w13_src, b13, cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess && w2_src != w2_dst)
-      e = cudaMemcpyAsync(w2_dst, w2_src, b2, cudaMemcpyDeviceToDevice, s);
-  } else {
-    e = launch_pack_fp4(w13_src, w13_dst, b13, s);
-    if (e == cudaSuccess) e = launch_pack_fp4(w2_src, w2_dst, b2, s);
+  const bool fp8 = quant == kFP8;
+  const int sper = quant == kMXFP4 ? 4 : 8;  // scale bytes per 64-byte code chunk
+  struct M {
+    const uint8_t* src;
+    uint8_t* dst;
+    const void* ssrc;
+    void* sdst;
+    size_t rows;
+    size_t K;
+  } ms[2] = {{w13_src, w13_dst, w13_scale_src, w13_scale_dst, E * 2 * I, P},
+             {w2_src, w2_dst, w2_scale_src, w2_scale_dst, E * P, I}};
+  cudaError_t e = cudaSuccess;
+  for (const M& m : ms) {
+    const int rowbytes = (int)(fp8 ? m.K : m.K / 2);
+    if (e == cudaSuccess) e = launch_pack_rows(m.src, m.dst, m.rows, rowbytes, 64, !fp8, s);
+    if (e != cudaSuccess) break;
+    if (fp8) {  // per-row fp32 scales stay as they are
+      if (m.ssrc != m.sdst)
+        e = cudaMemcpyAsync(m.sdst, m.ssrc, m.rows * 4, cudaMemcpyDeviceToDevice, s);
+    } else {
+      const int srow = (int)(rowbytes / 64) * sper;
+      e = launch_pack_rows(reinterpret_cast<const uint8_t*>(m.ssrc),
+                           reinterpret_cast<uint8_t*>(m.sdst), m.rows, srow, sper, false, s);
+    }
   }
   if (e != cudaSuccess) return set_err(nullptr, MUSEMOE_ECUDA, fmt("pack: %s", cudaGetErrorString(e)));
   return MUSEMOE_OK;
@@ -578,6 +617,8 @@ musemoe_status musemoe_route(musemoe_handle* h, const musemoe_weights* w, const 
   fp.rows = rows;
   fp.w_router = w->w_router;
   fp.logit_part = h->logit_part;
+  fp.logits = h->logits;
+  fp.router_tickets = h->router_tickets;
   fp.E = d.experts;
   fp.ks_r = ks_r;
   fp.router_ctas = router_ctas(d.experts, rows, ks_r);
@@ -590,21 +631,20 @@ musemoe_status musemoe_route(musemoe_handle* h, const musemoe_weights* w, const 
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_err(h, e, "launch of router");
   RouteParams rp{};
-  rp.logit_part = h->logit_part;
-  rp.expert_bias = w->expert_bias;
   rp.logits = h->logits;
+  rp.expert_bias = w->expert_bias;
   rp.ids = ids_out;
   rp.weights = weights_out;
   rp.rows = rows;
   rp.E = d.experts;
   rp.k = d.top_k;
-  rp.ks_r = ks_r;
   rp.score = h->cfg.score;
   rp.has_multiplier = h->cfg.has_multiplier;
   rp.multiplier = h->cfg.multiplier;
   rp.has_division_eps = h->cfg.has_division_eps;
   rp.division_eps = h->cfg.division_eps;
   rp.route_scale = h->cfg.route_scale;
+  rp.central = rows <= 32;
   e = launch_route(rp, s, true);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_err(h, e, "launch of route");
@@ -659,9 +699,10 @@ musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (e != cudaSuccess) return cuda_err(h, e, "health read");
   if (word) {
     std::string m;
+    if (word & kHealthTimeout) m += "an expert kernel's bounded wait on its weight copies ran out; ";
     if (word & kHealthHRange) m += "h beyond the fp16 operand range; ";
     if (word & kHealthActRange) m += "SiLU(gate)*up beyond the fp16 operand range; ";
-    return set_err(h, MUSEMOE_ERANGE, m);
+    return set_err(h, (word & kHealthTimeout) ? MUSEMOE_ETIMEOUT : MUSEMOE_ERANGE, m);
   }
   return MUSEMOE_OK;
 }

@@ -51,7 +51,8 @@ def upload_layer(cfg: synth.Config, w: dict, device="cuda"):
     """Device copies of one layer's tensors (expert codes packed in place into
     the kernel layout) and the Weights struct pointing at them."""
     t = {k: to_dev(v, device) for k, v in w.items()}
-    mm.musemoe_pack_experts(dims_of(cfg), QUANT[cfg.quant], t["w13"], t["w13"], t["w2"], t["w2"])
+    mm.musemoe_pack_experts(dims_of(cfg), QUANT[cfg.quant], t["w13"], t["w13_scale"], t["w13"],
+                            t["w13_scale"], t["w2"], t["w2_scale"], t["w2"], t["w2_scale"])
     torch.cuda.synchronize()
     return t, mm.make_weights(t)
 
@@ -170,6 +171,24 @@ def check_ids(gpu_ids: np.ndarray, routing: "O.Routing", k: int) -> int:
             # only a near tie may separate the two selections
             assert routing.gap[t] < NEAR_TIE or len(set(g) ^ set(routing.ids[t].tolist())) == 0, t
     return differ
+
+
+def kernel_layout(a: np.ndarray, chunk_bytes: int, permute_fp4: bool) -> np.ndarray:
+    """Host restatement of the documented kernel layout of one plain expert
+    tensor [E, N, row_bytes] (bytes): [E][N/8][chunk][8 rows][chunk_bytes],
+    FP4 code chunks reordered byte 8j + 2q + b -> 16q + 2j + b."""
+    a = np.ascontiguousarray(a).view(np.uint8)
+    E, N, rb = a.shape
+    nc = rb // chunk_bytes
+    out = a.reshape(E, N // 8, 8, nc, chunk_bytes).transpose(0, 1, 3, 2, 4).copy()
+    if permute_fp4:
+        src = np.empty(64, np.int64)
+        for qq in range(4):
+            for j in range(8):
+                for bb in range(2):
+                    src[16 * qq + 2 * j + bb] = 8 * j + 2 * qq + bb
+        out = out[..., src]
+    return out.reshape(E, N, rb)
 
 
 def near_of(g: dict) -> dict:

@@ -187,19 +187,28 @@ def test_forward_host_matches_device_forward():
     np.testing.assert_array_equal(sh.numpy().astype(np.float64), g["stream"])
 
 
-def test_pack_out_of_place_equals_in_place():
-    cfg = synth.CONFIGS["tiny"]
+@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8])
+def test_pack_matches_the_documented_layout(quant):
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant)
     e = synth.expert_tensors(cfg, 0)
-    a13, a2 = H.to_dev(e["w13"]), H.to_dev(e["w2"])
-    b13, b2 = torch.empty_like(a13), torch.empty_like(a2)
-    mm.musemoe_pack_experts(H.dims_of(cfg), mm.MUSEMOE_MXFP4, a13, b13, a2, b2)
-    mm.musemoe_pack_experts(H.dims_of(cfg), mm.MUSEMOE_MXFP4, a13, a13, a2, a2)
+    src = {k: H.to_dev(v) for k, v in e.items()}
+    dst = {k: torch.empty_like(v) for k, v in src.items()}
+    d = H.dims_of(cfg)
+    q = H.QUANT[quant]
+    mm.musemoe_pack_experts(d, q, src["w13"], src["w13_scale"], dst["w13"], dst["w13_scale"],
+                            src["w2"], src["w2_scale"], dst["w2"], dst["w2_scale"])
+    mm.musemoe_pack_experts(d, q, src["w13"], src["w13_scale"], src["w13"], src["w13_scale"],
+                            src["w2"], src["w2_scale"], src["w2"], src["w2_scale"])
     torch.cuda.synchronize()
-    assert torch.equal(a13, b13) and torch.equal(a2, b2)
-    # the documented byte permutation, checked on the host
-    src = e["w13"].reshape(-1, 64)
-    got = b13.cpu().numpy().reshape(-1, 64)
-    for qq in range(4):
-        for j in range(8):
-            for bb in range(2):
-                np.testing.assert_array_equal(got[:, 16 * qq + 2 * j + bb], src[:, 8 * j + 2 * qq + bb])
+    for k in ("w13", "w13_scale", "w2", "w2_scale"):
+        assert torch.equal(src[k], dst[k]), k   # in place == out of place
+    fp4 = quant != synth.FP8
+    sc = 4 if quant == synth.MXFP4 else 8
+    for k in ("w13", "w2"):
+        want = H.kernel_layout(e[k], 64, fp4)
+        np.testing.assert_array_equal(dst[k].cpu().numpy().reshape(want.shape), want)
+        if fp4:
+            ws = H.kernel_layout(e[k + "_scale"], sc, False)
+            np.testing.assert_array_equal(dst[k + "_scale"].cpu().numpy(), ws)
+        else:
+            np.testing.assert_array_equal(dst[k + "_scale"].cpu().numpy(), e[k + "_scale"])

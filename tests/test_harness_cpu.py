@@ -33,3 +33,18 @@ def test_planted_mistakes_fail_the_comparison(tensor):
     flat[i] = flat[i] * 1.5 + 0.25
     with pytest.raises(AssertionError):
         H.compare(cfg, w, x, st, g)
+
+
+def test_kernel_layout_restatement_is_a_permutation():
+    cfg = synth.CONFIGS["tiny"]
+    e = synth.expert_tensors(cfg, 0, e0=0, ne=2)
+    k = H.kernel_layout(e["w13"], 64, True)
+    assert k.shape == e["w13"].shape
+    assert np.array_equal(np.sort(k.ravel()), np.sort(e["w13"].ravel()))
+    # row 9 of expert 1 (group 1, row 1), chunk 0: its 64 plain bytes land at
+    # [1][1][0][1] of [E][N/8][chunk][8][64] in permuted order
+    flat = k.reshape(2, -1)
+    nc = e["w13"].shape[2] // 64
+    blk = flat[1, (1 * nc + 0) * 512 + 1 * 64:(1 * nc + 0) * 512 + 2 * 64]
+    assert np.array_equal(np.sort(blk), np.sort(e["w13"][1, 9, :64]))
+    assert blk[16 * 1 + 2 * 3 + 1] == e["w13"][1, 9, 8 * 3 + 2 * 1 + 1]
