@@ -174,7 +174,9 @@ const char *musemoe_kernel_name(int32_t quant, int32_t i);
  * (MXFP4) or [..][8 B] (NVFP4); FP8 scales keep their layout. For FP4 the 64
  * bytes of a chunk are also reordered: byte 8j + 2q + b moves to 16q + 2j + b
  * (q < 4, j < 8, b < 2). Each src may be its dst (in place). The NVFP4 global
- * scales need no re-layout. */
+ * scales need no re-layout. MXFP4 scales must be UE8M0 codes 0x01..0xFE
+ * (0x00 = 2^-127 and 0xFF = NaN give EUNSUPPORTED, nothing is re-laid); with
+ * MXFP4 the call synchronizes the stream to read that check. */
 musemoe_status musemoe_pack_experts(const musemoe_dims *dims, int32_t quant,
                                     const uint8_t *w13_src, const void *w13_scale_src,
                                     uint8_t *w13_dst, void *w13_scale_dst,

@@ -94,6 +94,21 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Eight e2m1 codes (one 32-bit word, byte i = elements 2i (low nibble) and
+// 2i+1) -> four f16x2 (exact), f16x2 i from byte i.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t& a, uint32_t& b,
+                                                  uint32_t& c, uint32_t& d) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+      : "r"(w));
+}
+// UE8M0 scale byte i (0..3) of a word -> 2^(s-127) as fp32, for s in
+// 1..254 (musemoe_pack_experts refuses the codes 0x00 and 0xFF).
+__device__ __forceinline__ float ue8m0_byte_to_f32(uint32_t w, int i) {
+  return __uint_as_float(((w >> (8 * i)) & 0xFFu) << 23);
+}
 // UE8M0 scale byte -> 2^(s-127) as fp32 (s = 0 gives 2^-127, 0xFF NaN).
 __device__ __forceinline__ float ue8m0_to_f32(uint32_t s) {
   s &= 0xFFu;
@@ -112,6 +127,17 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D(16x8, f32) = A(16x16, f16, row) * B(16x8, f16, col)  (C = 0)
+__device__ __forceinline__ void mma_f16_16816_zc(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  const float z = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+      "{%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 // D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,

@@ -40,11 +40,12 @@
 
 namespace musemoe {
 
-constexpr int kExpertThreads = 256;
-constexpr int kExpertWarps = kExpertThreads / 32;
+constexpr int kComputeWarps = 8;
+constexpr int kExpertWarps = kComputeWarps;          // warps sharing one item's K
+constexpr int kExpertThreads = (kComputeWarps + 2) * 32;  // + producer + epilogue
 constexpr int kChunkBytes = 64;      // bytes of one weight row per thread-quad
 constexpr int kGroupChunk = 8 * 64;  // bytes of one chunk of a row group
-constexpr int kStageBudget = 100 * 1024;
+constexpr int kStageBudget = 64 * 1024;  // three CTAs per SM
 constexpr int kMetaGroups = 8;  // token groups whose metadata a CTA keeps in shared memory
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
 
@@ -71,13 +72,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// One bounded sleep on the mbarrier phase: the thread is woken when the phase
+// completes, or after about kSuspendNs.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(phase)
+      : "r"(bar), "r"(phase), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -165,19 +169,17 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[NT][4], const uint4& L, c
   } else if constexpr (Q == kMXFP4) {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const float fl = ue8m0_to_f32(sl.x >> (8 * b));
-      const float fh = ue8m0_to_f32(sh.x >> (8 * b));
-      const uint32_t wl = word_of(L, b), wh = word_of(H, b);
-      const uint32_t a00 = e2m1x2_to_f16x2(wl), a01 = e2m1x2_to_f16x2(wh);
-      const uint32_t a02 = e2m1x2_to_f16x2(wl >> 8), a03 = e2m1x2_to_f16x2(wh >> 8);
-      const uint32_t a10 = e2m1x2_to_f16x2(wl >> 16), a11 = e2m1x2_to_f16x2(wh >> 16);
-      const uint32_t a12 = e2m1x2_to_f16x2(wl >> 24), a13 = e2m1x2_to_f16x2(wh >> 24);
+      const float fl = ue8m0_byte_to_f32(sl.x, b);
+      const float fh = ue8m0_byte_to_f32(sh.x, b);
+      uint32_t a00, a02, a10, a12, a01, a03, a11, a13;
+      e2m1x8_to_f16x2x4(word_of(L, b), a00, a02, a10, a12);
+      e2m1x8_to_f16x2x4(word_of(H, b), a01, a03, a11, a13);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (nt >= ntile_act) break;
         const uint2 b0 = bfrag(nt, 2 * b), b1 = bfrag(nt, 2 * b + 1);
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16_16816(t, a00, a01, a02, a03, b0.x, b0.y);
+        float t[4];
+        mma_f16_16816_zc(t, a00, a01, a02, a03, b0.x, b0.y);
         mma_f16_16816(t, a10, a11, a12, a13, b1.x, b1.y);
         acc[nt][0] = fmaf(t[0], fl, acc[nt][0]);
         acc[nt][1] = fmaf(t[1], fl, acc[nt][1]);
@@ -194,12 +196,13 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[NT][4], const uint4& L, c
       const uint32_t sfh = e4m3x2_to_f16x2(shw & 0xFFu);
       const uint32_t sl2 = __byte_perm(sfl, sfl, 0x1010);  // broadcast low half
       const uint32_t sh2 = __byte_perm(sfh, sfh, 0x1010);
-      const uint32_t wl = word_of(L, j >> 1) >> (16 * (j & 1));
-      const uint32_t wh = word_of(H, j >> 1) >> (16 * (j & 1));
-      const uint32_t a0 = hmul2(e2m1x2_to_f16x2(wl), sl2);
-      const uint32_t a1 = hmul2(e2m1x2_to_f16x2(wh), sh2);
-      const uint32_t a2 = hmul2(e2m1x2_to_f16x2(wl >> 8), sl2);
-      const uint32_t a3 = hmul2(e2m1x2_to_f16x2(wh >> 8), sh2);
+      uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+      e2m1x8_to_f16x2x4(word_of(L, j >> 1), l0, l1, l2, l3);
+      e2m1x8_to_f16x2x4(word_of(H, j >> 1), h0, h1, h2, h3);
+      const uint32_t a0 = hmul2((j & 1) ? l2 : l0, sl2);
+      const uint32_t a1 = hmul2((j & 1) ? h2 : h0, sh2);
+      const uint32_t a2 = hmul2((j & 1) ? l3 : l1, sl2);
+      const uint32_t a3 = hmul2((j & 1) ? h3 : h1, sh2);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (nt >= ntile_act) break;
@@ -210,19 +213,42 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[NT][4], const uint4& L, c
   }
 }
 
-// BC: the warp keeps the B fragments of its (at most CPW) chunks in
+// Waits for the mbarrier phase, at most `limit_ns`; gives up early when
+// another warp of the CTA has aborted. False when it did not complete.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t phase,
+                                                   volatile int* abort_flag) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, phase)) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Warp roles: warps 0..7 compute (each owns the chunks c with c % 8 == warp),
+// warp 8 produces (its lane 0 issues the bulk copies), warp 9 finishes items
+// (sums the 8 partial tiles, applies scales / SiLU * up, stores). Hand-offs:
+// full[s] (copies landed), empty[s] (8 compute warps done with stage s),
+// ready[r] / freed[r] for the two partial-tile buffers.
+// BC: a compute warp keeps the B fragments of its (at most CPW) chunks in
 // registers while consecutive items stay on one token group.
 template <int Q, int ROLE, int NT, int RT, bool BC, int CPW>
-__global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
+__global__ void __launch_bounds__(kExpertThreads, (NT <= 2 && ROLE == 0 ? 3 : 1)) k_expert(ExpertParams p) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) unsigned long long bars[8];
+  __shared__ __align__(8) unsigned long long full_b[8], empty_b[8], ready_b[2], freed_b[2];
+  __shared__ int abort_flag;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const StageGeo G = stage_geo<Q, ROLE, RT>(p.K);
   const int S = p.stages;
-  float4* red = reinterpret_cast<float4*>(smem + (size_t)S * G.stage_bytes);  // [warps][RT][NT][32]
+  constexpr int kSlots = RT * NT * 32;  // float4 slots of one warp's partial tile
+  float4* red = reinterpret_cast<float4*>(smem + (size_t)S * G.stage_bytes);  // [2][8][slots]
   const int n_groups = __ldcg(p.counters + kNumGroups);
   const int tiles = (ROLE == 0) ? p.I / 8 : p.N / (16 * RT);
   const int n_items = n_groups * tiles;
@@ -241,7 +267,15 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
   for (int i = threadIdx.x; i < g_count; i += kExpertThreads)
     meta_g[i] = __ldcg(reinterpret_cast<const int4*>(p.groups) + g_first + i);
   if (threadIdx.x == 0) {
-    for (int st = 0; st < S; ++st) mbar_init(smem_u32(&bars[st]), 1);
+    for (int st = 0; st < S; ++st) {
+      mbar_init(smem_u32(&full_b[st]), 1);
+      mbar_init(smem_u32(&empty_b[st]), kComputeWarps);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(smem_u32(&ready_b[r]), kComputeWarps);
+      mbar_init(smem_u32(&freed_b[r]), 1);
+    }
+    abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -249,6 +283,7 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
     const int gi = i / (8 * NT), n = i % (8 * NT);
     if (n < meta_g[gi].z) meta_r[gi][n] = __ldcg(p.route_list + meta_g[gi].y + n);
   }
+  __syncthreads();  // the last CTA-wide barrier
   auto group_of = [&](int grp) -> int4 {
     const int gi = grp - g_first;
     return gi < kMetaGroups ? meta_g[gi] : __ldcg(reinterpret_cast<const int4*>(p.groups) + grp);
@@ -257,27 +292,139 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
     const int gi = grp - g_first;
     return gi < kMetaGroups ? meta_r[gi][n] : __ldcg(p.route_list + rbase + n);
   };
-  if (threadIdx.x == 0)
-    for (int st = 0; st < S && st < mine; ++st) {
-      const int it = i0 + st;
-      issue_item<Q, ROLE, RT>(p, G, group_of(it / tiles).x, it % tiles,
-                              stage0 + st * G.stage_bytes, smem_u32(&bars[st]));
-    }
-  __syncthreads();
+  auto fail = [&]() {
+    abort_flag = 1;
+    atomicOr(p.health, kHealthTimeout);
+  };
 
-  int stop_at = -1;  // item counter at which a wait timed out
+  if (warp == kComputeWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      for (int n = 0; n < mine; ++n) {
+        const int st = n % S, use = n / S;
+        if (use > 0 && !mbar_wait_or_abort(smem_u32(&empty_b[st]), (uint32_t)(use - 1) & 1u,
+                                           &abort_flag)) {
+          if (!abort_flag) fail();
+          break;
+        }
+        if (use > 0) asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        const int it = i0 + n;
+        issue_item<Q, ROLE, RT>(p, G, group_of(it / tiles).x, it % tiles,
+                                stage0 + st * G.stage_bytes, smem_u32(&full_b[st]));
+      }
+      // the copies still in flight must land before the CTA leaves
+      for (int st = 0; st < S && st < mine; ++st) {
+        const int last = st + ((mine - 1 - st) / S) * S;  // last item issued into stage st
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&full_b[st]), (uint32_t)(last / S) & 1u))
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+      }
+    }
+    return;
+  }
+
+  if (warp == kComputeWarps + 1) {
+    // ---------------- epilogue ----------------
+    for (int n = 0; n < mine; ++n) {
+      const int r = n & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&ready_b[r]),
+                                                                (uint32_t)(n >> 1) & 1u, &abort_flag));
+      if (!ok) {
+        if (lane == 0 && !abort_flag) fail();
+        break;
+      }
+      const int item = i0 + n;
+      const int grp = item / tiles, tile = item % tiles;
+      const int4 gd = group_of(grp);
+      const int e = gd.x, rbase = gd.y, ntok = gd.z;
+      const int ntile_act = (ntok + 7) >> 3;
+      const float4* rb = red + (size_t)r * kComputeWarps * kSlots;
+      for (int sl = lane; sl < kSlots; sl += 32) {
+        const int ln = sl & 31, nt = (sl >> 5) % NT, rt = sl / (32 * NT);
+        if (nt >= ntile_act) continue;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) {
+          const float4 x = rb[w * kSlots + sl];
+          v.x += x.x;
+          v.y += x.y;
+          v.z += x.z;
+          v.w += x.w;
+        }
+        const int ge = ln >> 2, qe = ln & 3;
+        const int n0 = nt * 8 + 2 * qe;
+        float gsc = 1.f;
+        if (Q == kNVFP4) gsc = __ldg(p.gscale + e);
+        if (ROLE == 0) {
+          const int i = tile * 8 + ge;
+          float sg = gsc, su = gsc;
+          if (Q == kFP8) {
+            const float* ws = reinterpret_cast<const float*>(p.scale);
+            sg = __ldg(ws + (size_t)e * p.N + i);
+            su = __ldg(ws + (size_t)e * p.N + p.I + i);
+          }
+          const float gate[2] = {v.x * sg, v.y * sg};
+          const float up[2] = {v.z * su, v.w * su};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int nn = n0 + h;
+            if (nn >= ntok) continue;
+            const int ro = route_of(grp, rbase, nn);
+            float gt = gate[h], ut = up[h];
+            if (Q == kFP8) {
+              const float bs = __ldcg(p.b_scale + ro / p.k);
+              gt *= bs;
+              ut *= bs;
+            }
+            const float a = round_bf16(silu(gt) * ut);
+            if (Q == kFP8) {
+              reinterpret_cast<uint16_t*>(p.out)[(size_t)ro * p.I + i] = f32_to_bf16_bits(a);
+            } else {
+              reinterpret_cast<__half*>(p.out)[(size_t)ro * p.I + i] = __float2half_rn(a);
+              if (!(fabsf(a) <= 65504.f)) atomicOr(p.health, kHealthActRange);
+            }
+          }
+        } else {
+          const int plo = tile * 16 * RT + rt * 16 + ge, phi = plo + 8;
+          float sl2 = gsc, sh2 = gsc;
+          if (Q == kFP8) {
+            const float* ws = reinterpret_cast<const float*>(p.scale);
+            sl2 = __ldg(ws + (size_t)e * p.N + plo);
+            sh2 = __ldg(ws + (size_t)e * p.N + phi);
+          }
+          const float lo[2] = {v.x * sl2, v.y * sl2};
+          const float hi[2] = {v.z * sh2, v.w * sh2};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int nn = n0 + h;
+            if (nn >= ntok) continue;
+            const int ro = route_of(grp, rbase, nn);
+            const float bs = (Q == kFP8) ? __ldcg(p.b_scale + ro) : 1.f;
+            float* y = reinterpret_cast<float*>(p.out) + (size_t)ro * p.P;
+            y[plo] = lo[h] * bs;
+            y[phi] = hi[h] * bs;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&freed_b[r]));
+    }
+    return;
+  }
+
+  // ---------------- compute warps ----------------
   int cached_grp = -1;
   uint2 bcache4[BC && Q != kFP8 ? CPW : 1][BC && Q != kFP8 ? NT : 1][8];
   uint4 bcache8[BC && Q == kFP8 ? CPW : 1][BC && Q == kFP8 ? NT : 1];
   (void)bcache4;
   (void)bcache8;
-  for (int ii = 0; ii < mine; ++ii) {
-    const int item = i0 + ii;
-    const int st = ii % S;
-    const uint32_t phase = (uint32_t)(ii / S) & 1u;
-    const int grp = item / tiles, tile = item % tiles;
+  for (int n = 0; n < mine; ++n) {
+    const int item = i0 + n;
+    const int st = n % S;
+    const uint32_t phase = (uint32_t)(n / S) & 1u;
+    const int grp = item / tiles;
     const int4 gd = group_of(grp);
-    const int e = gd.x, rbase = gd.y, ntok = gd.z;
+    const int rbase = gd.y, ntok = gd.z;
     const int ntile_act = (ntok + 7) >> 3;
     const uint8_t* brow[NT];
     if (!BC || grp != cached_grp) {
@@ -286,8 +433,8 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         const int nn = nt * 8 + g;
         brow[nt] = nullptr;
         if (nn < ntok) {
-          const int r = route_of(grp, rbase, nn);
-          const int br = p.b_by_token ? r / p.k : r;
+          const int ro = route_of(grp, rbase, nn);
+          const int br = p.b_by_token ? ro / p.k : ro;
           brow[nt] = p.b + (size_t)br * p.K * kel;
         }
       }
@@ -297,7 +444,7 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         cached_grp = grp;
 #pragma unroll
         for (int u = 0; u < CPW; ++u) {
-          const int c = warp + kExpertWarps * u;
+          const int c = warp + kComputeWarps * u;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const bool v = c < G.NC && brow[nt] != nullptr;
@@ -313,9 +460,8 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         }
       }
     }
-    const bool ok = mbar_wait(smem_u32(&bars[st]), phase, kWaitLimitNs);
-    if (__syncthreads_or(!ok)) {
-      stop_at = ii;
+    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&full_b[st]), phase, &abort_flag))) {
+      if (lane == 0 && !abort_flag) fail();
       break;
     }
     const uint8_t* stg = smem + (size_t)st * G.stage_bytes;
@@ -349,7 +495,7 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
     if constexpr (BC) {
 #pragma unroll
       for (int u = 0; u < CPW; ++u) {
-        const int c = warp + kExpertWarps * u;
+        const int c = warp + kComputeWarps * u;
         if (c >= G.NC) break;
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt) {
@@ -360,7 +506,7 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         }
       }
     } else {
-      for (int c = warp; c < G.NC; c += kExpertWarps) {
+      for (int c = warp; c < G.NC; c += kComputeWarps) {
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt) {
           if constexpr (Q == kFP8)
@@ -375,105 +521,34 @@ __global__ void __launch_bounds__(kExpertThreads) k_expert(ExpertParams p) {
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_b[st]));  // stage st may be refilled
 
-    // ---- reduce the 8 K-slices -------------------------------------------
+    // hand the partial tile to the epilogue warp
+    const int r = n & 1;
+    if (n >= 2 && !__all_sync(0xffffffffu,
+                              mbar_wait_or_abort(smem_u32(&freed_b[r]),
+                                                 (uint32_t)((n >> 1) - 1) & 1u, &abort_flag))) {
+      if (lane == 0 && !abort_flag) fail();
+      break;
+    }
+    float4* mine_red = red + ((size_t)r * kComputeWarps + warp) * kSlots;
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         if (nt < ntile_act)
-          red[((warp * RT + rt) * NT + nt) * 32 + lane] =
+          mine_red[(rt * NT + nt) * 32 + lane] =
               make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]);
-    __syncthreads();  // stage st is free, the partial tiles are complete
-    if (threadIdx.x == 0 && ii + S < mine) {
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      const int it = item + S;
-      issue_item<Q, ROLE, RT>(p, G, group_of(it / tiles).x, it % tiles,
-                              stage0 + st * G.stage_bytes, smem_u32(&bars[st]));
-    }
-    const int slots = RT * NT * 32;
-    for (int s = threadIdx.x; s < slots; s += kExpertThreads) {
-      const int ln = s & 31, nt = (s >> 5) % NT, rt = s / (32 * NT);
-      if (nt >= ntile_act) continue;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kExpertWarps; ++w) {
-        const float4 x = red[((w * RT + rt) * NT + nt) * 32 + ln];
-        v.x += x.x;
-        v.y += x.y;
-        v.z += x.z;
-        v.w += x.w;
-      }
-      const int ge = ln >> 2, qe = ln & 3;
-      const int n0 = nt * 8 + 2 * qe;
-      float gsc = 1.f;
-      if (Q == kNVFP4) gsc = __ldg(p.gscale + e);
-      if (ROLE == 0) {
-        const int i = tile * 8 + ge;
-        float sg = gsc, su = gsc;
-        if (Q == kFP8) {
-          const float* ws = reinterpret_cast<const float*>(p.scale);
-          sg = __ldg(ws + (size_t)e * p.N + i);
-          su = __ldg(ws + (size_t)e * p.N + p.I + i);
-        }
-        const float gate[2] = {v.x * sg, v.y * sg};
-        const float up[2] = {v.z * su, v.w * su};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = n0 + h;
-          if (n >= ntok) continue;
-          const int r = route_of(grp, rbase, n);
-          float gt = gate[h], ut = up[h];
-          if (Q == kFP8) {
-            const float bs = __ldcg(p.b_scale + r / p.k);
-            gt *= bs;
-            ut *= bs;
-          }
-          const float a = round_bf16(silu(gt) * ut);
-          if (Q == kFP8) {
-            reinterpret_cast<uint16_t*>(p.out)[(size_t)r * p.I + i] = f32_to_bf16_bits(a);
-          } else {
-            reinterpret_cast<__half*>(p.out)[(size_t)r * p.I + i] = __float2half_rn(a);
-            if (!(fabsf(a) <= 65504.f)) atomicOr(p.health, kHealthActRange);
-          }
-        }
-      } else {
-        const int plo = tile * 16 * RT + rt * 16 + ge, phi = plo + 8;
-        float sl = gsc, sh = gsc;
-        if (Q == kFP8) {
-          const float* ws = reinterpret_cast<const float*>(p.scale);
-          sl = __ldg(ws + (size_t)e * p.N + plo);
-          sh = __ldg(ws + (size_t)e * p.N + phi);
-        }
-        const float lo[2] = {v.x * sl, v.y * sl};
-        const float hi[2] = {v.z * sh, v.w * sh};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = n0 + h;
-          if (n >= ntok) continue;
-          const int r = route_of(grp, rbase, n);
-          const float bs = (Q == kFP8) ? __ldcg(p.b_scale + r) : 1.f;
-          float* y = reinterpret_cast<float*>(p.out) + (size_t)r * p.P;
-          y[plo] = lo[h] * bs;
-          y[phi] = hi[h] * bs;
-        }
-      }
-    }
-    __syncthreads();
-  }
-  if (stop_at >= 0 && threadIdx.x == 0) {
-    // a wait ran out: report it, and let the copies already issued land
-    // (bounded) before the CTA's shared memory is released
-    atomicOr(p.health, kHealthTimeout);
-    for (int k = stop_at; k < stop_at + S && k < mine; ++k)
-      mbar_wait(smem_u32(&bars[k % S]), (uint32_t)(k / S) & 1u, kWaitLimitNs / 4);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ready_b[r]));
   }
 }
 
 template <int Q, int ROLE, int NT, int RT>
 static void expert_smem_t(int K, int* stages, size_t* smem) {
   const StageGeo G = stage_geo<Q, ROLE, RT>(K);
-  const size_t red = (size_t)kExpertWarps * RT * NT * 32 * sizeof(float4);
+  const size_t red = (size_t)2 * kComputeWarps * RT * NT * 32 * sizeof(float4);
   int S = (int)((kStageBudget > (int)red ? kStageBudget - (int)red : 0) / G.stage_bytes);
   S = S < 2 ? 2 : (S > 8 ? 8 : S);
   *stages = S;
@@ -716,6 +791,19 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl) {
 // Kernel layout of a [rows, row_bytes] tensor whose row is cut into `nc`
 // chunks of `cb` bytes: [rows / 8][nc][8][cb]. With `permute_fp4`, the 64
 // bytes of each chunk are also reordered (byte 8j + 2q + b -> 16q + 2j + b).
+// Raises *bad when a byte of [p, p + n) is 0x00 or 0xFF (UE8M0 codes the
+// kernels do not take).
+__global__ void k_check_ue8m0(const uint8_t* p, size_t n, int* bad) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    if (p[i] == 0x00 || p[i] == 0xFF) *bad = 1;
+}
+
+cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s) {
+  k_check_ue8m0<<<1024, 256, 0, s>>>(p, n, bad_dev);
+  return cudaGetLastError();
+}
+
 __global__ void k_pack_rows(const uint8_t* src, uint8_t* dst, int row_bytes, int cb,
                             int permute_fp4) {
   extern __shared__ __align__(16) uint8_t blk[];

@@ -131,6 +131,8 @@ cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
 // Interleaves groups of 8 rows of a [rows, row_bytes] tensor chunk by chunk
 // ([rows / 8][row_bytes / cb][8][cb]); permute_fp4 also reorders the bytes of
 // each 64-byte chunk for the FP4 mma fragments. src may equal dst.
+// Sets *bad_dev to 1 if any of the n UE8M0 bytes is 0x00 or 0xFF.
+cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s);
 cudaError_t launch_pack_rows(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
                              bool permute_fp4, cudaStream_t s);
 

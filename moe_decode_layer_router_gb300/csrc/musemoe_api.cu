@@ -585,6 +585,24 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
   } ms[2] = {{w13_src, w13_dst, w13_scale_src, w13_scale_dst, E * 2 * I, P},
              {w2_src, w2_dst, w2_scale_src, w2_scale_dst, E * P, I}};
   cudaError_t e = cudaSuccess;
+  if (quant == kMXFP4) {
+    // the kernels decode UE8M0 as a bare exponent: 0x00 (2^-127) and 0xFF
+    // (NaN) are refused here, before anything is re-laid
+    int* bad = nullptr;
+    int bad_h = 0;
+    e = cudaMalloc(&bad, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), s);
+    for (const M& m : ms)
+      if (e == cudaSuccess)
+        e = check_ue8m0(reinterpret_cast<const uint8_t*>(m.ssrc), m.rows * (m.K / 32), bad, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&bad_h, bad, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (bad) cudaFree(bad);
+    if (e != cudaSuccess) return set_err(nullptr, MUSEMOE_ECUDA, fmt("pack: %s", cudaGetErrorString(e)));
+    if (bad_h)
+      return set_err(nullptr, MUSEMOE_EUNSUPPORTED,
+                     "an MXFP4 scale is UE8M0 0x00 (2^-127) or 0xFF (NaN); the kernels take 0x01..0xFE");
+  }
   for (const M& m : ms) {
     const int rowbytes = (int)(fp8 ? m.K : m.K / 2);
     if (e == cudaSuccess) e = launch_pack_rows(m.src, m.dst, m.rows, rowbytes, 64, !fp8, s);

@@ -105,3 +105,19 @@ def test_events_time_every_kernel():
         assert all(m > 0 for m in ms)
     finally:
         run.close()
+
+
+def test_pack_refuses_special_ue8m0_codes():
+    cfg = synth.CONFIGS["tiny"]
+    e = synth.expert_tensors(cfg, 0)
+    for bad in (0x00, 0xFF):
+        t = {k: H.to_dev(v) for k, v in e.items()}
+        t["w2_scale"][3, 5, 1] = bad
+        before = t["w13"].clone()
+        with pytest.raises(mm.MuseMoEError) as ei:
+            mm.musemoe_pack_experts(H.dims_of(cfg), mm.MUSEMOE_MXFP4, t["w13"], t["w13_scale"],
+                                    t["w13"], t["w13_scale"], t["w2"], t["w2_scale"], t["w2"],
+                                    t["w2_scale"])
+        assert ei.value.status == mm.MUSEMOE_EUNSUPPORTED and "UE8M0" in str(ei.value)
+        torch.cuda.synchronize()
+        assert torch.equal(before, t["w13"])  # nothing was re-laid
