@@ -211,6 +211,33 @@ musemoe_status musemoe_forward_host(musemoe_handle *handle, const musemoe_weight
                                     uint16_t *out_host, int32_t rows,
                                     musemoe_stream_t stream_);
 
+/* No allocation: the router GEMV + routing rule of musemoe_route without a
+ * handle, for callers that cannot allocate device memory (their memory
+ * belongs to another allocator, such as a serving engine's pooled one, or a
+ * new allocation is not allowed where they run). The paper has no
+ * counterpart: it is a calling convention of this library. Inputs and
+ * outputs as musemoe_route (w_router fp32 [experts, hidden], expert_bias
+ * fp32 [experts], x bf16 [rows, hidden] -> ids_out int32 [rows, top_k],
+ * weights_out fp32 [rows, top_k]); hidden a multiple of 64, experts 1..256,
+ * rows 1..MUSEMOE_STATIC_MAX_ROWS (larger gives EINVAL with the reason in
+ * musemoe_last_error(NULL)).
+ * The scratch (logit partial sums, logits, split counters) is one fixed
+ * device array of MUSEMOE_STATIC_SCRATCH_BYTES inside the library, held on
+ * every device that loads the library until the process exits; the call
+ * makes no cudaMalloc/cudaFree or other allocation. The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress, with
+ * the device current): make it before any stream capture. Every call shares
+ * the array and the array keeps the last call's contents; the call clears
+ * what must start at zero. Calls that overlap on the GPU (e.g. on two
+ * streams) race on the array: serialize them. */
+#define MUSEMOE_STATIC_MAX_ROWS 64
+#define MUSEMOE_STATIC_SCRATCH_BYTES (256 * 1024)
+musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, int32_t top_k,
+                                    const musemoe_config *config, const float *w_router,
+                                    const float *expert_bias, const uint16_t *x, int32_t rows,
+                                    int32_t *ids_out, float *weights_out,
+                                    musemoe_stream_t stream);
+
 /* Reads (synchronously) and clears the handle's device health word. Returns
  * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
  * ran out since the last poll (that forward's outputs are invalid),

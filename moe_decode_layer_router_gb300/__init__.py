@@ -23,7 +23,7 @@ __all__ = [
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
-    "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
+    "musemoe_route_static", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
 ]
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
@@ -65,7 +65,10 @@ EXPORTED_SYMBOLS = [
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
+    "musemoe_route_static",
 ]
+MUSEMOE_STATIC_MAX_ROWS = 64
+MUSEMOE_STATIC_SCRATCH_BYTES = 256 * 1024
 
 
 class MuseMoEError(RuntimeError):
@@ -103,6 +106,8 @@ def library() -> ctypes.CDLL:
                                               P(Taps)]
         lib.musemoe_forward_host.argtypes = [c_vp, P(Weights), c_vp, c_vp, c_vp, c_i32, c_vp]
         lib.musemoe_poll_health.argtypes = [c_vp]
+        lib.musemoe_route_static.argtypes = [c_i32, c_i32, c_i32, P(Config), c_vp, c_vp, c_vp,
+                                             c_i32, c_vp, c_vp, c_vp]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int:  # ctypes default
@@ -203,6 +208,15 @@ def musemoe_poll_health(handle) -> int:
     if st not in (MUSEMOE_OK, MUSEMOE_ERANGE, MUSEMOE_ETIMEOUT):
         _check(st, handle)
     return st
+
+
+def musemoe_route_static(hidden: int, experts: int, top_k: int, config: Config, w_router,
+                         expert_bias, x, rows: int, ids_out, weights_out, stream=None) -> None:
+    """musemoe_route without a handle: the library's fixed static scratch,
+    no device allocation (see include/musemoe.h)."""
+    _check(library().musemoe_route_static(hidden, experts, top_k, ctypes.byref(config),
+                                          _addr(w_router), _addr(expert_bias), _addr(x), rows,
+                                          _addr(ids_out), _addr(weights_out), _stream(stream)))
 
 
 def make_weights(tensors: dict) -> Weights:

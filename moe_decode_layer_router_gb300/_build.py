@@ -15,7 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmusemoe.so")
 
-SOURCES = ["musemoe_api.cu", "k_front.cu", "k_route.cu", "k_experts.cu", "k_boundary.cu"]
+SOURCES = ["musemoe_api.cu", "musemoe_static.cu", "k_front.cu", "k_route.cu", "k_experts.cu",
+           "k_boundary.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

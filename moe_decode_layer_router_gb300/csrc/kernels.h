@@ -3,9 +3,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace musemoe {
 
 enum Quant : int { kMXFP4 = 0, kNVFP4 = 1, kFP8 = 2 };
+
+// The calling thread's error text that musemoe_last_error(NULL) returns.
+void set_thread_error(const std::string& m);
 
 // counters[] slots in the workspace
 enum Counter : int { kNumGroups = 0, kTicket = 1, kNumCounters = 8 };

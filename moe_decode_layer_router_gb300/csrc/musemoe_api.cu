@@ -65,6 +65,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+void musemoe::set_thread_error(const std::string& m) { g_thread_err = m; }
+
 struct musemoe_handle {
   musemoe_dims d{};
   int quant = 0;

@@ -1,0 +1,139 @@
+// musemoe_route_static: the router GEMV + routing rule for callers that
+// cannot allocate device memory. Its scratch (K-split logit partials, the
+// summed logits, the split tickets) is a fixed file-scope device array, so
+// the call needs no handle and makes no allocation.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+#include "musemoe.h"
+
+using namespace musemoe;
+
+namespace {
+
+constexpr size_t kLogitsBytes = 64 * 1024;   // rows * E * 4 <= 64 * 256 * 4
+constexpr size_t kTicketBytes = 4 * 1024;    // (E / 16) * (rows / 8) tickets
+constexpr size_t kPartialBytes = MUSEMOE_STATIC_SCRATCH_BYTES - kLogitsBytes - kTicketBytes;
+constexpr int kMaxDevices = 64;
+
+// The scratch. In host code this name is only a stand-in for the device
+// array: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_route_scratch[MUSEMOE_STATIC_SCRATCH_BYTES];
+
+std::mutex g_mu;
+void* g_scratch_dev[kMaxDevices] = {};
+
+musemoe_status fail(musemoe_status st, const std::string& m) {
+  set_thread_error(m);  // read back with musemoe_last_error(NULL)
+  return st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, int32_t top_k,
+                                               const musemoe_config* config,
+                                               const float* w_router, const float* expert_bias,
+                                               const uint16_t* x, int32_t rows,
+                                               int32_t* ids_out, float* weights_out,
+                                               musemoe_stream_t stream) {
+  if (!config) return fail(MUSEMOE_EINVAL, "config is NULL");
+  if (rows < 1 || rows > MUSEMOE_STATIC_MAX_ROWS)
+    return fail(MUSEMOE_EINVAL, "rows " + std::to_string(rows) + " outside 1.." +
+                                    std::to_string(MUSEMOE_STATIC_MAX_ROWS) +
+                                    " (the static scratch holds at most that many rows)");
+  if (experts < 1 || experts > 256)
+    return fail(MUSEMOE_EUNSUPPORTED, "experts " + std::to_string(experts) + " outside 1..256");
+  if (top_k < 1 || top_k > experts)
+    return fail(MUSEMOE_EINVAL, "top_k " + std::to_string(top_k) + " outside 1..experts");
+  if (hidden < 64 || hidden % 64)
+    return fail(MUSEMOE_EUNSUPPORTED, "hidden " + std::to_string(hidden) + " is not a multiple of 64");
+  if (config->score != 0 && config->score != 1)
+    return fail(MUSEMOE_EINVAL, "score is not sigmoid (0) or softmax (1)");
+  const void* ptrs[] = {w_router, expert_bias, x, ids_out, weights_out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return fail(MUSEMOE_EINVAL, "tensors must be non-NULL and 16-byte aligned");
+
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MUSEMOE_EUNSUPPORTED, "device index out of range");
+  void* base = nullptr;
+  {
+    // first call on this device: look up the array's device address (with
+    // the device current); later calls reuse it
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_dev[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_route_scratch);
+      if (e != cudaSuccess)
+        return fail(MUSEMOE_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+      g_scratch_dev[dev] = ptr;
+    }
+    base = g_scratch_dev[dev];
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("device query: ") + cudaGetErrorString(e));
+
+  unsigned char* s = static_cast<unsigned char*>(base);
+  float* logits = reinterpret_cast<float*>(s);
+  int32_t* tickets = reinterpret_cast<int32_t*>(s + kLogitsBytes);
+  float* part = reinterpret_cast<float*>(s + kLogitsBytes + kTicketBytes);
+  // K-split of the router GEMV: as the handle path chooses it, shortened
+  // until the partial sums fit the scratch
+  const int EB = (experts + 15) / 16, tb = (rows + 7) / 8;
+  int ks = (2 * sms) / (EB * tb);
+  ks = ks < 1 ? 1 : ks;
+  const int kmax = (hidden / 4) / 32;
+  if (ks > kmax) ks = kmax < 1 ? 1 : kmax;
+  const size_t per_split = (size_t)rows * experts * sizeof(float);
+  if ((size_t)ks * per_split > kPartialBytes) ks = (int)(kPartialBytes / per_split);
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // every call shares the array: the split tickets must start at zero
+  e = cudaMemsetAsync(tickets, 0, (size_t)EB * tb * sizeof(int32_t), st);
+  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("clear: ") + cudaGetErrorString(e));
+
+  FrontParams fp{};
+  fp.x = x;
+  fp.rows = rows;
+  fp.w_router = w_router;
+  fp.logit_part = part;
+  fp.logits = logits;
+  fp.router_tickets = tickets;
+  fp.E = experts;
+  fp.ks_r = ks;
+  fp.router_ctas = EB * ks * tb;
+  fp.M = 0;
+  fp.K = hidden;
+  fp.ks = 1;
+  fp.kchunks_per_split = 1;
+  fp.token_blocks = 1;
+  e = launch_front(fp, 1, st, false);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("launch of router: ") + cudaGetErrorString(e));
+  RouteParams rp{};
+  rp.logits = logits;
+  rp.expert_bias = expert_bias;
+  rp.ids = ids_out;
+  rp.weights = weights_out;
+  rp.rows = rows;
+  rp.E = experts;
+  rp.k = top_k;
+  rp.score = config->score;
+  rp.has_multiplier = config->has_multiplier;
+  rp.multiplier = config->multiplier;
+  rp.has_division_eps = config->has_division_eps;
+  rp.division_eps = config->division_eps;
+  rp.route_scale = config->route_scale;
+  rp.central = rows <= 32;
+  e = launch_route(rp, st, true);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("launch of route: ") + cudaGetErrorString(e));
+  return MUSEMOE_OK;
+}
