@@ -59,6 +59,24 @@ def _dist():
 
 # ------------------------------------------------------------ bytes model
 
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The largest of the ranks' values (the job ends when its slowest rank
+    does). Collective over the default process group when world > 1."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, rows_per_rank: int, steps: int, seconds: float) -> float:
+    """Rows per second of the whole job: every rank runs `steps` steps of
+    `rows_per_rank` rows (weak scaling), timed by the slowest rank."""
+    return world * rows_per_rank * steps / seconds
+
+
 def algorithmic_bytes(cfg, ids_list):
     """Minimal HBM bytes per kernel and per step: every weight byte the step
     needs once (only the selected experts' codes and scales), every input
@@ -274,15 +292,10 @@ def bench_ours(args):
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        tmax = torch.tensor([ms], device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        ms = float(tmax.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     kernels = mm.musemoe_num_kernels(quant)
     ms_step = ms / args.steps
-    value = world * cfg.rows * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, cfg.rows, args.steps, ms / 1e3)
 
     # per-kernel durations (each kernel timed alone with events) and the
     # selected experts of each set, for the bytes model
@@ -344,14 +357,9 @@ def bench_ours(args):
         st_ = sets[i % WEIGHT_SETS]
         mm.musemoe_forward_host(handle, st_["w"], st_["x_host"], st_["stream_host"], oh,
                                 cfg.rows, s)
-    t_e2e = time.perf_counter() - t0
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
     del xh, sh
-    e2e_value = world * cfg.rows * e2e_steps / t_e2e
+    e2e_value = whole_job_rate(world, cfg.rows, e2e_steps, t_e2e)
     h2d = cfg.rows * cfg.hidden * (2 + 4)
     d2h = cfg.rows * cfg.hidden * (4 + 2)
 

@@ -8,7 +8,7 @@ It is a plain, slow, step-by-step restatement of what the pages fix:
 
 * router GEMV and routing rule -- page "vllm.models.muse_spark.amd.muse_moe_runner",
   class MuseSpark1xRouter (its docstring and ``_compute_routing_native``,
-  "the kernel's reference, and the CPU path");
+  which the page presents as the torch reference of the routing kernel);
 * pooler + pre_expert_norm, routed experts, tail, unpooler -- page
   "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
   MoEProvider docstring and RoutedMoE.run;
@@ -26,7 +26,7 @@ Every value is float64 unless a rounding is named. The rounding points are
 the storage dtypes the pages show: fp32 router logits and routing scores
 (the routing recipe runs on fp32 tensors), bf16 ``h`` and bf16 MoE
 activations (decoder page, _K5Bucket buffers ``h`` bf16; mono page,
-maybe_attach_mono: "MoE activations in bf16"), bf16 ``moe_out`` (providers
+maybe_attach_mono, which keeps the MoE activations in bf16), bf16 ``moe_out`` (providers
 page, RoutedMoE buffers), fp32 ``stream`` and bf16 ``out`` (BoundaryProvider).
 Where the pages are silent the module states the reading it takes.
 
@@ -115,7 +115,8 @@ E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
 
 def unpack_fp4(packed: np.ndarray) -> np.ndarray:
     """[..., K/2] bytes -> [..., K] 4-bit codes; element 2j sits in the low
-    nibble of byte j (reading: the pages say only "two e2m1 codes per byte")."""
+    nibble of byte j (reading: the pages pack two e2m1 codes into each byte
+    but fix no order)."""
     p = np.asarray(packed, dtype=np.uint8)
     out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.uint8)
     out[..., 0::2] = p & 0x0F
@@ -271,7 +272,8 @@ def route(logits, expert_bias, top_k: int, route_scale: float,
 def pre_expert(x_bf16, w_pool_bf16, w_pre_norm_bf16, eps: float,
                pre_norm: bool = True, near=None, ties=None) -> np.ndarray:
     """Pooler GEMM H -> P, then pre_expert_norm (providers page, MoEProvider
-    docstring: "pooler GEMM and gather + pre_expert_norm"). The pooled vector
+    docstring, which lists the pooler GEMM, the gather and pre_expert_norm as
+    one stage). The pooled vector
     is not rounded before the norm (the pooler and the norm run fused); the
     result h is stored as bf16 (decoder page, _K5Bucket buffer ``h`` bf16)."""
     h_raw = bf16_to_f64(x_bf16) @ bf16_to_f64(w_pool_bf16).T
