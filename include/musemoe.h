@@ -169,14 +169,19 @@ const char *musemoe_kernel_name(int32_t quant, int32_t i);
  * scales [E, N, K/32] UE8M0 (MXFP4), [E, N, K/16] e4m3 (NVFP4), fp32 [E, N]
  * (FP8). w13: N = 2I (gate rows first), K = P; w2: N = P, K = I.
  * Kernel layout: every row is cut into 64-byte code chunks (128 FP4 or 64 FP8
- * elements) and rows are taken in groups of 8, stored chunk by chunk:
- * codes [E][N/8][chunk][8 rows][64 B], scales [E][N/8][chunk][8 rows][4 B]
- * (MXFP4) or [..][8 B] (NVFP4); FP8 scales keep their layout. For FP4 the 64
- * bytes of a chunk are also reordered: byte 8j + 2q + b moves to 16q + 2j + b
- * (q < 4, j < 8, b < 2). Each src may be its dst (in place). The NVFP4 global
- * scales need no re-layout. MXFP4 scales must be UE8M0 codes 0x01..0xFE
- * (0x00 = 2^-127 and 0xFF = NaN give EUNSUPPORTED, nothing is re-laid); with
- * MXFP4 the call synchronizes the stream to read that check. */
+ * elements); rows are taken in tiles of 64, each tile is stored K-slice by
+ * K-slice (4 chunks; the last slice holds the remaining 1..4), each slice by
+ * group of 8 rows, then chunk, then row: codes
+ * [E][N/64][slice][8 groups][chunks of the slice][8 rows][64 B]; scales the
+ * same with the 4 (MXFP4) or 8 (NVFP4) scale bytes of a row's chunk in place
+ * of its 64 code bytes; FP8 scales keep their layout. For FP4 the 64 bytes of
+ * a chunk are also reordered: byte 8j + 2q + b moves to 16q + 2j + b (q < 4,
+ * j < 8, b < 2). Each src may be its dst (in place): the tensors then pass
+ * through a temporary device buffer of at most 64 MB, allocated and freed by
+ * this call, which synchronizes the stream before it returns. The NVFP4
+ * global scales need no re-layout. MXFP4 scales must be UE8M0 codes
+ * 0x01..0xFE (0x00 = 2^-127 and 0xFF = NaN give EUNSUPPORTED, nothing is
+ * re-laid); with MXFP4 the call synchronizes the stream to read that check. */
 musemoe_status musemoe_pack_experts(const musemoe_dims *dims, int32_t quant,
                                     const uint8_t *w13_src, const void *w13_scale_src,
                                     uint8_t *w13_dst, void *w13_scale_dst,

@@ -16,8 +16,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmusemoe.so")
 
 SOURCES = ["musemoe_api.cu", "musemoe_static.cu", "k_front.cu", "k_route.cu", "k_experts.cu",
-           "k_boundary.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+           "k_tail.cu", "k_pack.cu", "k_boundary.cu"]
+HEADERS = ["common.cuh", "kernels.h", "pipeline.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -1,0 +1,81 @@
+// Weight re-layout of the expert tensors (plain rows -> kernel layout) and
+// the UE8M0 scale check that precedes it.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace musemoe {
+
+// ---- weight re-layout: plain rows -> kernel layout --------------------------
+// One CTA per group of 8 consecutive rows: the group's bytes are read into
+// shared memory, then written back interleaved, so src may equal dst.
+// Kernel layout of a [rows, row_bytes] tensor whose row is cut into `nc`
+// chunks of `cb` bytes: [rows / 8][nc][8][cb]. With `permute_fp4`, the 64
+// bytes of each chunk are also reordered (byte 8j + 2q + b -> 16q + 2j + b).
+// Raises *bad when a byte of [p, p + n) is 0x00 or 0xFF (UE8M0 codes the
+// kernels do not take).
+__global__ void k_check_ue8m0(const uint8_t* p, size_t n, int* bad) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    if (p[i] == 0x00 || p[i] == 0xFF) *bad = 1;
+}
+
+cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s) {
+  k_check_ue8m0<<<1024, 256, 0, s>>>(p, n, bad_dev);
+  return cudaGetLastError();
+}
+
+// One output byte per thread step: output offset o of the kernel layout
+// [tiles][slice][8 groups][chunks of the slice][8 rows][cb] takes source
+// byte (row, byte) of the plain row-major [rows, row_bytes] tensor; FP4 code
+// chunks also reorder their bytes (output 16q + 2j + b <- chunk byte 8j + 2q + b).
+__global__ void k_pack_tiles(const uint8_t* src, uint8_t* dst, size_t bytes, int row_bytes, int cb,
+                             int permute_fp4) {
+  const int NC = row_bytes / cb;
+  const size_t tile_bytes = (size_t)64 * row_bytes;
+  const size_t full = (size_t)64 * kSliceChunks * cb;  // a full slice of a tile
+  for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < bytes;
+       o += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = o / tile_bytes, ot = o % tile_bytes;
+    const int s = (int)(ot / full);
+    const int rem = (int)(ot - (size_t)s * full);
+    const int ncs = min(kSliceChunks, NC - kSliceChunks * s);
+    const int gi = rem / (ncs * 8 * cb);
+    const int r2 = rem % (ncs * 8 * cb);
+    const int c = r2 / (8 * cb), r = (r2 / cb) % 8;
+    int b = r2 % cb;
+    if (permute_fp4) {
+      const int qq = b >> 4, j = (b >> 1) & 7, bb = b & 1;
+      b = 8 * j + 2 * qq + bb;
+    }
+    dst[o] = src[t * tile_bytes + (size_t)(gi * 8 + r) * row_bytes +
+                 (size_t)(kSliceChunks * s + c) * cb + b];
+  }
+}
+
+cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
+                              bool permute_fp4, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s) {
+  const size_t tile_bytes = (size_t)64 * row_bytes;
+  const size_t tiles = rows / 64;
+  const bool in_place = (src == dst);
+  const size_t batch = in_place ? std::max<size_t>(1, tmp_bytes / tile_bytes) : tiles;
+  if (in_place && tmp_bytes < tile_bytes) return cudaErrorInvalidValue;
+  for (size_t t0 = 0; t0 < tiles; t0 += batch) {
+    const size_t n = std::min(batch, tiles - t0);
+    const size_t off = t0 * tile_bytes, bytes = n * tile_bytes;
+    const uint8_t* from = src + off;
+    if (in_place) {
+      cudaError_t e = cudaMemcpyAsync(tmp, src + off, bytes, cudaMemcpyDeviceToDevice, s);
+      if (e != cudaSuccess) return e;
+      from = tmp;
+    }
+    const unsigned grid = (unsigned)std::min<size_t>((bytes + 255) / 256, 16384);
+    k_pack_tiles<<<grid, 256, 0, s>>>(from, dst + off, bytes, row_bytes, cb, permute_fp4 ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace musemoe

@@ -1,0 +1,143 @@
+// Tail of the expert phase: the FP8 per-route requantization of the bf16
+// activation between w13 and w2, and the per-route post-expert norm, router
+// weighting and sum over the k routes of each token.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace musemoe {
+
+// ---- FP8: per-route dynamic quantization of the bf16 activation ------------
+__global__ void __launch_bounds__(256) k_act_quant(ActQuantParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= p.routes) return;
+  const uint16_t* a = p.act + (size_t)r * p.I;
+  float amax = 0.f;
+  for (int i = lane * 2; i < p.I; i += 64) {
+    const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(a + i));
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(v & 0xFFFFu)), fabsf(bf16_bits_to_f32(v >> 16))));
+  }
+  amax = warp_max(amax);
+  const float s = amax / 448.0f;
+  for (int i = lane * 2; i < p.I; i += 64) {
+    const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(a + i));
+    const float x0 = bf16_bits_to_f32(v & 0xFFFFu), x1 = bf16_bits_to_f32(v >> 16);
+    const uint16_t qv = f32x2_to_e4m3x2(s > 0.f ? x0 / s : 0.f, s > 0.f ? x1 / s : 0.f);
+    reinterpret_cast<uint16_t*>(p.q + (size_t)r * p.I)[i / 2] = qv;
+  }
+  if (lane == 0) p.scale[r] = s;
+}
+
+cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.routes + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_act_quant, p);
+}
+
+// ---- tail: post-expert norm of each route, router weight, sum over k ------
+// (page "vllm.models.muse_spark.amd.muse_moe_runner",
+// MuseSparkTopKWeightAndReduce.apply: norm to fp32, times topk_weights, sum
+// over k; moe_out stored as bf16.)
+constexpr int kFinalizeThreads = 512;
+constexpr int kFinalizeUnroll = 8;
+
+// One CTA per token. All k route rows are read with every load of a round in
+// flight and kept in shared memory when they fit (`stash`), so the rows
+// leave HBM/L2 once.
+__global__ void __launch_bounds__(kFinalizeThreads) k_finalize(FinalizeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ __align__(16) float4 fsm4[];
+  __shared__ float part[kFinalizeUnroll * 2][kFinalizeThreads / 32];
+  __shared__ float rstd[256], wt[256];
+  const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NW = kFinalizeThreads / 32;
+  const int P4 = p.P / 4;
+  const bool stash = p.stash != 0;
+  const float4* y4 = reinterpret_cast<const float4*>(p.y) + (size_t)t * p.k * P4;
+  for (int j = threadIdx.x; j < p.k; j += kFinalizeThreads) wt[j] = __ldcg(p.weights + (size_t)t * p.k + j);
+  // sums of squares, kFinalizeUnroll routes per round, all their loads in flight
+  for (int j0 = 0; j0 < p.k; j0 += kFinalizeUnroll) {
+    float ss[kFinalizeUnroll];
+#pragma unroll
+    for (int u = 0; u < kFinalizeUnroll; ++u) ss[u] = 0.f;
+    for (int i0 = 0; i0 < P4; i0 += kFinalizeThreads) {
+      const int i = i0 + threadIdx.x;
+      float4 v[kFinalizeUnroll];
+#pragma unroll
+      for (int u = 0; u < kFinalizeUnroll; ++u)
+        v[u] = (j0 + u < p.k && i < P4) ? __ldcg(y4 + (size_t)(j0 + u) * P4 + i)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kFinalizeUnroll; ++u) {
+        ss[u] += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+        if (stash && j0 + u < p.k && i < P4) fsm4[(size_t)(j0 + u) * P4 + i] = v[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kFinalizeUnroll; ++u) {
+      const float w = warp_sum(ss[u]);
+      if (lane == 0) part[u][warp] = w;
+    }
+    __syncthreads();
+    if (threadIdx.x < kFinalizeUnroll && j0 + threadIdx.x < p.k) {
+      float a = 0.f;
+      for (int w = 0; w < NW; ++w) a += part[threadIdx.x][w];
+      rstd[j0 + threadIdx.x] = 1.0f / sqrtf(a / (float)p.P + p.eps);
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < P4; i += kFinalizeThreads) {
+    const uint2 wpb = *reinterpret_cast<const uint2*>(p.w_post_norm + 4 * i);
+    const float w0 = bf16_bits_to_f32(wpb.x & 0xFFFFu), w1 = bf16_bits_to_f32(wpb.x >> 16);
+    const float w2 = bf16_bits_to_f32(wpb.y & 0xFFFFu), w3 = bf16_bits_to_f32(wpb.y >> 16);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < p.k; ++j) {
+      const float4 v = stash ? fsm4[(size_t)j * P4 + i] : __ldcg(y4 + (size_t)j * P4 + i);
+      const float r = rstd[j], c = wt[j];
+      a0 = fmaf(c, (v.x * r) * w0, a0);
+      a1 = fmaf(c, (v.y * r) * w1, a1);
+      a2 = fmaf(c, (v.z * r) * w2, a2);
+      a3 = fmaf(c, (v.w * r) * w3, a3);
+    }
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(a0) | ((uint32_t)f32_to_bf16_bits(a1) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(a2) | ((uint32_t)f32_to_bf16_bits(a3) << 16);
+    reinterpret_cast<uint2*>(p.moe_out + (size_t)t * p.P)[i] = o;
+  }
+}
+
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl) {
+  FinalizeParams q = p;
+  const size_t stash = (size_t)p.k * p.P * sizeof(float);
+  q.stash = stash <= 160 * 1024;
+  const size_t smem = q.stash ? stash : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_finalize, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.rows);
+  cfg.blockDim = dim3(kFinalizeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_finalize, q);
+}
+
+}  // namespace musemoe

@@ -81,8 +81,8 @@ struct ExpertParams {
   int role;      // 0: w13 + SiLU*up -> act; 1: w2 -> y
   int E, N, K;   // rows N and reduction K of the weight matrix
   int I, P, k;
-  const uint8_t* w;        // codes, kernel layout [E][N/8][NC][8][64]
-  const void* scale;       // MX/NV: kernel layout [E][N/8][NC][8][SB]; FP8: fp32 [E, N]
+  const uint8_t* w;        // codes, kernel layout (launch_pack_tiles, cb = 64)
+  const void* scale;       // MX/NV: kernel layout (cb = 4 / 8); FP8: fp32 [E, N]
   const float* gscale;     // NVFP4 [E]
   const uint8_t* b;        // activation operand: f16 [*, K] or e4m3 [*, K]
   const float* b_scale;    // FP8: per B row
@@ -92,11 +92,15 @@ struct ExpertParams {
   const int32_t* counters;
   void* out;               // role 0: act f16/bf16 [rows*k, I]; role 1: y fp32 [rows*k, P]
   int32_t* health;
+  float* part;             // partial sums of tiles split across CTAs (expert_part_bytes)
+  int32_t* tickets;        // tile tickets (expert_tickets), zero between launches
   int grid;
-  int stages;  // set by launch_expert
+  int stages;  // set by the launcher
 };
 cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pdl);
-int expert_ctas_per_sm(int quant, int role, int nt, int K);
+int expert_ctas_per_sm(int quant, int role, int nt, int K, int N);
+size_t expert_part_bytes(int grid, int nt);
+size_t expert_tickets(int max_groups, int quant, int role, int K, int N);
 
 // FP8 only: per-route dynamic e4m3 quantization of the bf16 activation.
 struct ActQuantParams {
@@ -133,12 +137,17 @@ struct BoundaryParams {
 cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
 
 // ---- weight re-layout ----------------------------------------------------
-// Interleaves groups of 8 rows of a [rows, row_bytes] tensor chunk by chunk
-// ([rows / 8][row_bytes / cb][8][cb]); permute_fp4 also reorders the bytes of
-// each 64-byte chunk for the FP4 mma fragments. src may equal dst.
+// Kernel layout of a [rows, row_bytes] expert tensor cut into cb-byte chunks
+// (cb = 64 for codes, the scale bytes of one code chunk for scales): tiles of
+// 64 rows, each stored K-slice by K-slice (kSliceChunks chunks, the last
+// slice the remainder), each slice by 8-row group, chunk, row:
+// [rows / 64][slice][8][chunks of the slice][8][cb]. permute_fp4 also
+// reorders the bytes of each 64-byte code chunk for the FP4 mma fragments.
+// src may equal dst: the tiles then pass through `tmp` (at least one tile).
 // Sets *bad_dev to 1 if any of the n UE8M0 bytes is 0x00 or 0xFF.
+constexpr int kSliceChunks = 4;
 cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s);
-cudaError_t launch_pack_rows(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
-                             bool permute_fp4, cudaStream_t s);
+cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
+                              bool permute_fp4, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s);
 
 }  // namespace musemoe

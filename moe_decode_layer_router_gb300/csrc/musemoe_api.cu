@@ -31,12 +31,14 @@ std::string fmt(const char* f, ...) {
 
 constexpr int kMaxRoutes = 4096;  // rows * top_k served by the permute
 constexpr size_t kAlign = 256;
+constexpr int kExpertCtasPerSm = 2;  // expert kernels: resident CTAs per SM, at most
+constexpr size_t kPackTmpBytes = 64ull << 20;  // in-place pack: tiles per pass
 
 int nt_front(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
-int nt_expert(int rows) {
-  const int t = (rows + 7) / 8;
-  return t <= 1 ? 1 : t <= 2 ? 2 : t <= 4 ? 4 : 8;
-}
+// Token tile of the expert kernels (8 * NT routes per group). Up to 32 rows
+// an expert rarely gets more than 8 routes, and one that does becomes two
+// groups (its weights stream twice), cheaper than wider, mostly empty tiles.
+int nt_expert(int rows) { return rows <= 32 ? 1 : rows <= 64 ? 4 : 8; }
 int nt_index(int nt) { return nt == 1 ? 0 : nt == 2 ? 1 : nt == 4 ? 2 : 3; }
 
 struct GemvSplit {
@@ -81,7 +83,8 @@ struct musemoe_handle {
   float *logits = nullptr, *weights = nullptr, *h_scale = nullptr, *act_scale = nullptr;
   float *h_raw = nullptr, *u = nullptr;
   int32_t *router_tickets = nullptr, *pool_tickets = nullptr, *unpool_tickets = nullptr;
-  float *y = nullptr, *stream_stage = nullptr;
+  float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
+  int32_t* expert_tickets[2] = {nullptr, nullptr};
   int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
   int32_t* health = nullptr;
   uint16_t *h = nullptr, *moe_out = nullptr, *x_stage = nullptr, *out_stage = nullptr;
@@ -139,6 +142,14 @@ void plan(musemoe_handle* h, Layout& L) {
     L.add(&h->act_scale, RT * 4);
   }
   L.add(&h->y, RT * P * 4);
+  // Stream-K partial sums (shared by w13 and w2, which run one after the
+  // other) for the widest token tile, and one ticket array per matrix; at
+  // most kExpertCtasPerSm CTAs per SM
+  const int nt_max = nt_expert(d.max_rows);
+  L.add(&h->expert_part, expert_part_bytes(kExpertCtasPerSm * h->sms, nt_max));
+  L.add(&h->expert_tickets[0],
+        expert_tickets(h->max_groups, h->quant, 0, d.pooled, 2 * d.inter) * 4);
+  L.add(&h->expert_tickets[1], expert_tickets(h->max_groups, h->quant, 1, d.inter, d.pooled) * 4);
   L.add(&h->moe_out, R * P * 2);
   L.add(&h->x_stage, R * H * 2);
   L.add(&h->stream_stage, R * H * 4);
@@ -162,15 +173,6 @@ std::vector<std::string> refusals(const musemoe_dims* d, int32_t quant, const mu
   if ((size_t)d->pooled * 4 > 200 * 1024) r.push_back(fmt("pooled %d too large for one CTA row", d->pooled));
   if (d->hidden > 8192) r.push_back(fmt("hidden %d above 8192 (one CTA row in registers)", d->hidden));
   if (quant < 0 || quant > 2) r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1) or FP8_W8A8 (2)", quant));
-  else {
-    // two pipeline stages of the widest expert item (two 8-row groups of w13)
-    // plus the 32 KB reduction tile must fit in one CTA's shared memory
-    const long long chunk = quant == 2 ? 512 : 512 + (quant == 0 ? 32 : 64);
-    const long long nc = quant == 2 ? (long long)d->pooled / 64 : (long long)d->pooled / 128;
-    const long long stage = 2 * nc * chunk;
-    if (2 * stage + 32 * 1024 > 220 * 1024)
-      r.push_back(fmt("pooled %d too large for two expert pipeline stages", d->pooled));
-  }
   if (c->score != 0 && c->score != 1) r.push_back(fmt("score %d is not sigmoid (0) or softmax (1)", c->score));
   if (!std::isfinite(c->route_scale)) r.push_back("route_scale is not finite");
   if (c->has_multiplier && !std::isfinite(c->multiplier)) r.push_back("multiplier is not finite");
@@ -331,6 +333,8 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.counters = h->counters;
   ep.out = h->act;
   ep.health = h->health;
+  ep.part = h->expert_part;
+  ep.tickets = h->expert_tickets[0];
   ep.grid = h->expert_grid[0][nt_index(nte)];
   before();
   if (!after(launch_expert(ep, nte, s, pdl), "w13")) return MUSEMOE_ECUDA;
@@ -358,6 +362,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.b_scale = h->act_scale;
   ep.b_by_token = 0;
   ep.out = h->y;
+  ep.tickets = h->expert_tickets[1];
   ep.grid = h->expert_grid[1][nt_index(nte)];
   before();
   if (!after(launch_expert(ep, nte, s, pdl), "w2")) return MUSEMOE_ECUDA;
@@ -493,7 +498,10 @@ musemoe_status musemoe_create(const musemoe_dims* dims, int32_t quant, const mus
   for (int role = 0; role < 2; ++role)
     for (int i = 0; i < 4; ++i)
       h->expert_grid[role][i] =
-          h->sms * expert_ctas_per_sm(quant, role, 1 << i, role == 0 ? dims->pooled : dims->inter);
+          h->sms * std::min(kExpertCtasPerSm,
+                            expert_ctas_per_sm(quant, role, 1 << i,
+                                                  role == 0 ? dims->pooled : dims->inter,
+                                                  role == 0 ? 2 * dims->inter : dims->pooled));
   Layout L;
   plan(h, L);
   h->ws_bytes = L.off;
@@ -605,18 +613,38 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
       return set_err(nullptr, MUSEMOE_EUNSUPPORTED,
                      "an MXFP4 scale is UE8M0 0x00 (2^-127) or 0xFF (NaN); the kernels take 0x01..0xFE");
   }
+  // in-place re-layouts pass through a temporary buffer of whole row tiles
+  size_t tmp_bytes = 0;
+  for (const M& m : ms) {
+    const size_t rowbytes = fp8 ? m.K : m.K / 2;
+    const size_t total = m.rows * rowbytes, tile = 64 * rowbytes;
+    if (m.src == m.dst) tmp_bytes = std::max(tmp_bytes, std::max(tile, std::min(total, kPackTmpBytes)));
+    if (!fp8 && m.ssrc == m.sdst) tmp_bytes = std::max(tmp_bytes, 64 * (rowbytes / 64) * sper);
+  }
+  uint8_t* tmp = nullptr;
+  if (tmp_bytes) {
+    e = cudaMalloc(&tmp, tmp_bytes);
+    if (e != cudaSuccess)
+      return set_err(nullptr, MUSEMOE_ENOMEM, fmt("pack: temporary of %zu bytes: %s", tmp_bytes,
+                                                  cudaGetErrorString(e)));
+  }
   for (const M& m : ms) {
     const int rowbytes = (int)(fp8 ? m.K : m.K / 2);
-    if (e == cudaSuccess) e = launch_pack_rows(m.src, m.dst, m.rows, rowbytes, 64, !fp8, s);
+    if (e == cudaSuccess) e = launch_pack_tiles(m.src, m.dst, m.rows, rowbytes, 64, !fp8, tmp, tmp_bytes, s);
     if (e != cudaSuccess) break;
     if (fp8) {  // per-row fp32 scales stay as they are
       if (m.ssrc != m.sdst)
         e = cudaMemcpyAsync(m.sdst, m.ssrc, m.rows * 4, cudaMemcpyDeviceToDevice, s);
     } else {
       const int srow = (int)(rowbytes / 64) * sper;
-      e = launch_pack_rows(reinterpret_cast<const uint8_t*>(m.ssrc),
-                           reinterpret_cast<uint8_t*>(m.sdst), m.rows, srow, sper, false, s);
+      e = launch_pack_tiles(reinterpret_cast<const uint8_t*>(m.ssrc), reinterpret_cast<uint8_t*>(m.sdst),
+                            m.rows, srow, sper, false, tmp, tmp_bytes, s);
     }
+  }
+  if (tmp) {
+    const cudaError_t e2 = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = e2;
+    cudaFree(tmp);
   }
   if (e != cudaSuccess) return set_err(nullptr, MUSEMOE_ECUDA, fmt("pack: %s", cudaGetErrorString(e)));
   return MUSEMOE_OK;

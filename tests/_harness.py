@@ -175,20 +175,24 @@ def check_ids(gpu_ids: np.ndarray, routing: "O.Routing", k: int) -> int:
 
 def kernel_layout(a: np.ndarray, chunk_bytes: int, permute_fp4: bool) -> np.ndarray:
     """Host restatement of the documented kernel layout of one plain expert
-    tensor [E, N, row_bytes] (bytes): [E][N/8][chunk][8 rows][chunk_bytes],
-    FP4 code chunks reordered byte 8j + 2q + b -> 16q + 2j + b."""
+    tensor [E, N, row_bytes] (bytes): rows in tiles of 64, each tile K-slice
+    by K-slice (4 chunks of chunk_bytes, the last slice the remainder), each
+    slice [8 groups][chunks of the slice][8 rows][chunk_bytes]; FP4 code
+    chunks reordered byte 8j + 2q + b -> 16q + 2j + b."""
     a = np.ascontiguousarray(a).view(np.uint8)
     E, N, rb = a.shape
     nc = rb // chunk_bytes
-    out = a.reshape(E, N // 8, 8, nc, chunk_bytes).transpose(0, 1, 3, 2, 4).copy()
+    x = a.reshape(E, N // 64, 8, 8, nc, chunk_bytes)  # [E][tile][group][row][chunk][byte]
     if permute_fp4:
         src = np.empty(64, np.int64)
         for qq in range(4):
             for j in range(8):
                 for bb in range(2):
                     src[16 * qq + 2 * j + bb] = 8 * j + 2 * qq + bb
-        out = out[..., src]
-    return out.reshape(E, N, rb)
+        x = x[..., src]
+    slices = [x[:, :, :, :, s0:s0 + 4, :].transpose(0, 1, 2, 4, 3, 5).reshape(E, N // 64, -1)
+              for s0 in range(0, nc, 4)]
+    return np.concatenate(slices, axis=2).reshape(E, N, rb)
 
 
 def near_of(g: dict) -> dict:

@@ -63,6 +63,17 @@ def test_tiny_dims_every_quant_and_score(quant, score):
     _compare_block(cfg, w, x, st)
 
 
+@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8])
+def test_ragged_k_slices(quant):
+    # P = 640, I = 384: w13 rows of 5 (FP4) / 10 (FP8) 64-byte chunks and w2
+    # rows of 3 / 6 chunks, so the last K-slice of a tile is ragged and tiles
+    # are split across CTAs
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], pooled=640, inter=384, quant=quant, seed=12)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st)
+
+
 @pytest.mark.parametrize("rows", [1, 3, 13])
 def test_ragged_rows(rows):
     # rows below the handle's max_rows, including a ragged tail of a token tile
@@ -187,9 +198,10 @@ def test_forward_host_matches_device_forward():
     np.testing.assert_array_equal(sh.numpy().astype(np.float64), g["stream"])
 
 
+@pytest.mark.parametrize("dims", [(256, 128), (640, 384)])
 @pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8])
-def test_pack_matches_the_documented_layout(quant):
-    cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant)
+def test_pack_matches_the_documented_layout(quant, dims):
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, pooled=dims[0], inter=dims[1])
     e = synth.expert_tensors(cfg, 0)
     src = {k: H.to_dev(v) for k, v in e.items()}
     dst = {k: torch.empty_like(v) for k, v in src.items()}

@@ -36,15 +36,30 @@ def test_planted_mistakes_fail_the_comparison(tensor):
 
 
 def test_kernel_layout_restatement_is_a_permutation():
-    cfg = synth.CONFIGS["tiny"]
-    e = synth.expert_tensors(cfg, 0, e0=0, ne=2)
-    k = H.kernel_layout(e["w13"], 64, True)
-    assert k.shape == e["w13"].shape
-    assert np.array_equal(np.sort(k.ravel()), np.sort(e["w13"].ravel()))
-    # row 9 of expert 1 (group 1, row 1), chunk 0: its 64 plain bytes land at
-    # [1][1][0][1] of [E][N/8][chunk][8][64] in permuted order
-    flat = k.reshape(2, -1)
-    nc = e["w13"].shape[2] // 64
-    blk = flat[1, (1 * nc + 0) * 512 + 1 * 64:(1 * nc + 0) * 512 + 2 * 64]
-    assert np.array_equal(np.sort(blk), np.sort(e["w13"][1, 9, :64]))
-    assert blk[16 * 1 + 2 * 3 + 1] == e["w13"][1, 9, 8 * 3 + 2 * 1 + 1]
+    rng = np.random.default_rng(0)
+    plain = rng.integers(0, 256, size=(2, 128, 512), dtype=np.uint8)
+    k = H.kernel_layout(plain, 64, True)
+    assert k.shape == plain.shape
+    assert np.array_equal(np.sort(k.ravel()), np.sort(plain.ravel()))
+    # expert 1, row 73 = tile 1, group 1, row 1; chunk 5 = slice 1, chunk 1 of
+    # the slice (8 chunks per row, 4 per slice): offset within the expert
+    # 64*512 (tile 1) + 64*4*64 (slice 1) + (1*4 + 1)*512 + 1*64
+    off = 64 * 512 + 64 * 4 * 64 + (1 * 4 + 1) * 512 + 64
+    blk = k[1].reshape(-1)[off:off + 64]
+    row = plain[1, 73, 5 * 64:6 * 64]
+    assert np.array_equal(np.sort(blk), np.sort(row))
+    # chunk byte 8j + 2q + b sits at 16q + 2j + b (q = 1, j = 3, b = 1)
+    assert blk[16 * 1 + 2 * 3 + 1] == row[8 * 3 + 2 * 1 + 1]
+
+
+def test_kernel_layout_ragged_last_slice():
+    rng = np.random.default_rng(1)
+    plain = rng.integers(0, 256, size=(1, 64, 5 * 4), dtype=np.uint8)  # 5 chunks of 4 bytes
+    k = H.kernel_layout(plain, 4, False)
+    # row 9 = group 1, row 1; chunk 4 = the ragged slice 1 holding one chunk:
+    # 64*4*4 (slice 0) + (1*1 + 0)*8*4 + 1*4
+    off = 64 * 4 * 4 + (1 * 1 + 0) * 8 * 4 + 1 * 4
+    assert np.array_equal(k.reshape(-1)[off:off + 4], plain[0, 9, 16:20])
+    # and chunk 2 of row 9 in the full slice 0: (1*4 + 2)*8*4 + 1*4
+    off = (1 * 4 + 2) * 8 * 4 + 1 * 4
+    assert np.array_equal(k.reshape(-1)[off:off + 4], plain[0, 9, 8:12])
