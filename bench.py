@@ -90,7 +90,8 @@ def algorithmic_bytes(cfg, ids_list):
     for ids in ids_list:
         active = len(np.unique(ids))
         per.append({
-            "front": E * H * 4 + P * H * 2 + b * H * 2 + b * E * 4 + b * P * 4,
+            "router": E * H * 4 + b * H * 2 + b * E * 4,
+            "pool": P * H * 2 + b * H * 2 + b * P * 4,
             "route": b * E * 4 + b * P * 4 + E * 4 + P * 2 + b * P * 4 + routes * 8,
             "w13": active * w13_e + b * P * 2 + routes * I * 2,
             "w2": active * w2_e + routes * I * 2 + routes * P * 4,

@@ -159,7 +159,7 @@ size_t musemoe_workspace_bytes(const musemoe_dims *dims, int32_t quant);
 
 /* Kernels one musemoe_forward launches for this quant (for taps->events). */
 int32_t musemoe_num_kernels(int32_t quant);
-/* Name of kernel i of the forward ("front", "route", "w13", ...). */
+/* Name of kernel i of the forward ("router", "pool", "route", "w13", ...). */
 const char *musemoe_kernel_name(int32_t quant, int32_t i);
 
 /* Re-lays the expert tensors from their plain layout into the kernel layout
@@ -226,17 +226,18 @@ musemoe_status musemoe_forward_host(musemoe_handle *handle, const musemoe_weight
  * weights_out fp32 [rows, top_k]); hidden a multiple of 64, experts 1..256,
  * rows 1..MUSEMOE_STATIC_MAX_ROWS (larger gives EINVAL with the reason in
  * musemoe_last_error(NULL)).
- * The scratch (logit partial sums, logits, split counters) is one fixed
- * device array of MUSEMOE_STATIC_SCRATCH_BYTES inside the library, held on
- * every device that loads the library until the process exits; the call
- * makes no cudaMalloc/cudaFree or other allocation. The first call on a
- * device looks up that array's device address (cudaGetSymbolAddress, with
- * the device current): make it before any stream capture. Every call shares
- * the array and the array keeps the last call's contents; the call clears
- * what must start at zero. Calls that overlap on the GPU (e.g. on two
- * streams) race on the array: serialize them. */
+ * The scratch (the fp32 logits) is one fixed device array of
+ * MUSEMOE_STATIC_SCRATCH_BYTES inside the library, held on every device
+ * that loads the library until the process exits; the call makes no
+ * cudaMalloc/cudaFree or other allocation. The first call on a device looks
+ * up that array's device address (cudaGetSymbolAddress, with the device
+ * current): make it before any stream capture. Every call shares the array
+ * and the array keeps the last call's contents; nothing in it has to start
+ * at zero (the router writes every logit the routing reads). Calls that
+ * overlap on the GPU (e.g. on two streams) race on the array: serialize
+ * them. */
 #define MUSEMOE_STATIC_MAX_ROWS 64
-#define MUSEMOE_STATIC_SCRATCH_BYTES (256 * 1024)
+#define MUSEMOE_STATIC_SCRATCH_BYTES (64 * 1024)
 musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, int32_t top_k,
                                     const musemoe_config *config, const float *w_router,
                                     const float *expert_bias, const uint16_t *x, int32_t rows,

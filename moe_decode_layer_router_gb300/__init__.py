@@ -68,7 +68,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_route_static",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
-MUSEMOE_STATIC_SCRATCH_BYTES = 256 * 1024
+MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
 
 
 class MuseMoEError(RuntimeError):

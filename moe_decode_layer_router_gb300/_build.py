@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmusemoe.so")
 
-SOURCES = ["musemoe_api.cu", "musemoe_static.cu", "k_front.cu", "k_route.cu", "k_experts.cu",
+SOURCES = ["musemoe_api.cu", "musemoe_static.cu", "k_gemv.cu", "k_route.cu", "k_experts.cu",
            "k_tail.cu", "k_pack.cu", "k_boundary.cu"]
 HEADERS = ["common.cuh", "kernels.h", "pipeline.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

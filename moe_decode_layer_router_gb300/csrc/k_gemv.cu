@@ -1,0 +1,395 @@
+// Front of the block and the unpooler: dense bf16 GEMVs Y = X W^T with the
+// weight tile streamed in by the tensor memory accelerator, and the fp32
+// router GEMV.
+//
+// Router: fp32 weight [E, H] times the bf16 input (page
+// "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
+// MoEProvider docstring: the router is an fp32 linear layer from [b, H] to
+// one logit per expert), fp32 FFMA so the logits keep fp32 products. It is
+// its own launch, just before the pooler's.
+//
+// Pooler [P, H] / unpooler [H, P] (bf16, row-major as the caller holds
+// them): one CTA per 16-row tile (and token block) holds the tile's whole
+// reduction length in shared memory. Weights never depend on the previous
+// kernel, so thread 0 issues every [16 rows x 64] box of the tile (2-D
+// tensor copies, 128-byte swizzle, one mbarrier per box) before the kernel
+// waits for its predecessor; the copies overlap the predecessor's tail. The
+// 8 warps then split K, read conflict-free A fragments with ldmatrix, take
+// the activation fragments (at most 8 NT tokens) from L1/L2, accumulate
+// with mma.sync (bf16 in, fp32 out) and add their 8 partials in a fixed
+// order in shared memory. Rows and tokens past the end are never stored.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pipeline.cuh"
+
+namespace musemoe {
+
+constexpr int kGWarps = 8;
+constexpr int kGThreads = kGWarps * 32;
+constexpr int kGTileRows = 16;                 // weight rows per CTA
+constexpr int kGBoxK = 64;                     // elements per box row (128 B)
+constexpr int kGBoxBytes = kGTileRows * 128;   // one [16 x 64] bf16 box
+constexpr int kGMaxK = 6144;                   // reduction length held in shared memory
+constexpr int kRouterRowsPerCta = 16;
+
+__host__ __device__ constexpr int g_red_bytes(int nt) { return kGWarps * nt * 32 * 16; }
+// boxes (64-element chunks of the reduction) per warp
+__host__ __device__ constexpr int g_chunks_per_warp(int K) { return (K / kGBoxK + kGWarps - 1) / kGWarps; }
+__host__ __device__ constexpr size_t g_smem_bytes(int K, int nt) {
+  return (size_t)kGWarps * g_chunks_per_warp(K) * kGBoxBytes + g_red_bytes(nt) + 1024;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// Byte offset of 16-byte unit u of row r in a box of 128-byte rows written
+// with the 128-byte swizzle (the box starts on a 1024-byte boundary).
+__device__ __forceinline__ uint32_t swz(int r, int u) { return r * 128 + ((u ^ (r & 7)) << 4); }
+
+// Router CTA: expert e = blockIdx % E for tokens [8 tb, 8 tb + 8). Thread 0
+// copies the tokens' input rows into shared memory (1-D bulk copies, one
+// mbarrier); meanwhile every thread loads its float4 columns t, t + 256, ...
+// of the expert's fp32 weight row (at most kRouterCols). Then each thread
+// accumulates its columns for every token, and the CTA adds its threads'
+// sums (warp shuffles, then the 8 warps in order).
+constexpr int kRouterCols = 8;  // float4 columns per thread: K <= 8192
+__device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8_t* smem) {
+  __shared__ float red[kGWarps][8];
+  __shared__ __align__(8) unsigned long long xbar;
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = task % p.E, t0 = (task / p.E) * 8;
+  const int ntok = min(8, p.rows - t0);
+  const int K4 = p.K / 4;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&xbar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  // the weight row does not depend on the previous kernel
+  const float4* wr = reinterpret_cast<const float4*>(p.w_router + (size_t)e * p.K);
+  float4 wv[kRouterCols];
+#pragma unroll
+  for (int u = 0; u < kRouterCols; ++u) {
+    const int c = threadIdx.x + u * kGThreads;
+    wv[u] = c < K4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();  // x may be the previous kernel's output
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(smem_u32(&xbar), (uint32_t)(ntok * p.K * 2));
+    for (int t = 0; t < ntok; ++t)
+      bulk_g2s(smem_u32(smem) + t * p.K * 2, p.x + (size_t)(t0 + t) * p.K, p.K * 2, smem_u32(&xbar));
+  }
+  float acc[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+  const bool ok = mbar_wait_or_abort(smem_u32(&xbar), 0u, &abort_flag);
+  if (ok) {
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem);
+#pragma unroll
+    for (int u = 0; u < kRouterCols; ++u) {
+      const int c = threadIdx.x + u * kGThreads;
+      if (c >= K4) break;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (t >= ntok) break;
+        const uint2 xv = *reinterpret_cast<const uint2*>(xs + t * p.K + 4 * c);
+        float a = acc[t];
+        a = fmaf(wv[u].x, bf16_bits_to_f32(xv.x & 0xFFFFu), a);
+        a = fmaf(wv[u].y, bf16_bits_to_f32(xv.x >> 16), a);
+        a = fmaf(wv[u].z, bf16_bits_to_f32(xv.y & 0xFFFFu), a);
+        a = fmaf(wv[u].w, bf16_bits_to_f32(xv.y >> 16), a);
+        acc[t] = a;
+      }
+    }
+  } else if (!abort_flag) {
+    abort_flag = 1;
+    if (p.health) atomicOr(p.health, kHealthTimeout);
+  }
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const float v = warp_sum(acc[t]);
+    if (lane == 0) red[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < ntok) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGWarps; ++w) v += red[w][threadIdx.x];
+    p.logits[(size_t)(t0 + threadIdx.x) * p.E + e] = v;
+  }
+  // the copies must have landed before the CTA leaves (after a timeout)
+  if (threadIdx.x == 0 && !ok) {
+    const unsigned long long tw0 = globaltimer();
+    while (!mbar_try_wait(smem_u32(&xbar), 0u))
+      if (globaltimer() - tw0 > kWaitLimitNs) break;
+  }
+}
+
+// BPW > 0: every warp holds the B fragments of its (at most BPW) boxes in
+// registers, loaded right after the wait for the previous kernel; BPW = 0:
+// the fragments of the next box load while the current one runs.
+template <int NT, int BPW>
+__device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParams& p,
+                                         uint8_t* smem_raw) {
+  __shared__ __align__(8) unsigned long long warp_b[kGWarps];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int tiles = (p.M + kGTileRows - 1) / kGTileRows;
+  const int tile = blockIdx.x % tiles, tbk = blockIdx.x / tiles;
+  const int nbox = p.K / kGBoxK, nch = g_chunks_per_warp(p.K);
+  // 1024-byte aligned tile (the 128-byte swizzle repeats every 1024 bytes)
+  const uint32_t wt = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float4* red = reinterpret_cast<float4*>(smem_raw + (wt - smem_u32(smem_raw)) +
+                                          (size_t)kGWarps * nch * kGBoxBytes);
+
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kGWarps; ++w) mbar_init(smem_u32(&warp_b[w]), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // the weight tile does not depend on the previous kernel: load it now,
+    // one copy per warp of its nch chunks x 16 rows x 64 (past the end of
+    // the reduction the copy engine fills zeros; those chunks are skipped)
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tw)) : "memory");
+    for (int w = 0; w < kGWarps; ++w) {
+      if (w * nch >= nbox) break;
+      mbar_expect_tx(smem_u32(&warp_b[w]), (uint32_t)(nch * kGBoxBytes));
+      tma_load_3d(wt + w * nch * kGBoxBytes, tw, 0, tile * kGTileRows, w * nch, smem_u32(&warp_b[w]));
+    }
+  }
+  pdl_wait();  // x may be the previous kernel's output
+
+  // activation rows of this lane's tokens (lanes past the last token read the
+  // last token's row; their results are never stored)
+  const uint16_t* xr[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+    xr[nt] = p.x + (size_t)min(tbk * 8 * NT + nt * 8 + g, p.rows - 1) * p.K + 2 * q;
+  // B fragments of box b's 4 k-steps: k 2q, 2q+1 and 2q+8, 2q+9 of token g
+  auto load_b = [&](uint32_t (&f)[NT][4][2], int b) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const uint16_t* xp = xr[nt] + b * kGBoxK + s4 * 16;
+        f[nt][s4][0] = *reinterpret_cast<const uint32_t*>(xp);
+        f[nt][s4][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
+      }
+  };
+  const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_u = lane >> 4;
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+  auto box_mma = [&](int b, const uint32_t (&f)[NT][4][2]) {
+    const uint32_t box = wt + b * kGBoxBytes;
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(box + swz(a_row, 2 * s4 + a_u), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, f[nt][s4][0], f[nt][s4][1]);
+    }
+  };
+  const int b0 = warp * nch, b1 = min(b0 + nch, nbox);
+  bool ok = true;
+  if constexpr (BPW > 0) {
+    uint32_t bf[BPW][NT][4][2];
+#pragma unroll
+    for (int i = 0; i < BPW; ++i)
+      if (b0 + i < b1) load_b(bf[i], b0 + i);
+    if (b0 < b1) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&warp_b[warp]), 0u, &abort_flag));
+#pragma unroll
+    for (int i = 0; i < BPW; ++i) {
+      if (b0 + i >= b1 || !ok) break;
+      box_mma(b0 + i, bf[i]);
+    }
+  } else {
+    uint32_t bf[2][NT][4][2];
+    if (b0 < b1) {
+      load_b(bf[0], b0);
+      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&warp_b[warp]), 0u, &abort_flag));
+    }
+    for (int b = b0; b < b1 && ok; b += 2) {
+      if (b + 1 < b1) load_b(bf[1], b + 1);
+      box_mma(b, bf[0]);
+      if (b + 1 >= b1) break;
+      if (b + 2 < b1) load_b(bf[0], b + 2);
+      box_mma(b + 1, bf[1]);
+    }
+  }
+  if (!ok && lane == 0 && !abort_flag) {
+    abort_flag = 1;
+    atomicOr(p.health, kHealthTimeout);
+  }
+  // the 8 warps' partial tiles, added in warp order
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+    red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+  __syncthreads();
+  if (warp < NT) {
+    const int nt = warp;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kGWarps; ++w) {
+      const float4 x = red[(w * NT + nt) * 32 + lane];
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    const int r_lo = tile * kGTileRows + g, r_hi = r_lo + 8;
+    const float lo[2] = {v.x, v.y}, hi[2] = {v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = tbk * 8 * NT + nt * 8 + 2 * q + h;
+      if (t >= p.rows) continue;
+      if (r_lo < p.M) p.y[(size_t)t * p.M + r_lo] = lo[h];
+      if (r_hi < p.M) p.y[(size_t)t * p.M + r_hi] = hi[h];
+    }
+  }
+  // copies still in flight (after a timeout) must land before the CTA leaves
+  if (threadIdx.x == 0 && abort_flag) {
+    for (int w = 0; w < kGWarps && w * nch < nbox; ++w) {
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&warp_b[w]), 0u))
+        if (globaltimer() - t0 > kWaitLimitNs) break;
+    }
+  }
+}
+
+template <int NT, int BPW>
+__global__ void __launch_bounds__(kGThreads)
+    k_gemv(const __grid_constant__ CUtensorMap tw, FrontParams p) {
+  pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t smem[];
+  gemv_cta<NT, BPW>(&tw, p, smem);
+}
+
+__global__ void __launch_bounds__(kGThreads) k_router(FrontParams p) {
+  pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t smem[];
+  router_cta(p, blockIdx.x, smem);
+}
+
+// ---- host ------------------------------------------------------------------
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// 3-D bf16 view of a row-major [rows, K] tensor: (64 elements of a chunk,
+// row, chunk), strides K * 2 bytes for a row and 128 bytes for a chunk; box
+// (64, 16 rows, nch chunks) lands as nch [16 x 64] boxes, 128-byte swizzle;
+// zero fill out of bounds.
+cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t nch) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kGBoxK, rows, K / kGBoxK};
+  const cuuint64_t strides[2] = {K * 2, (cuuint64_t)kGBoxK * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kGBoxK, (cuuint32_t)kGTileRows, nch};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int NT, int BPW>
+cudaError_t launch_t(const FrontParams& p, cudaStream_t s, bool pdl) {
+  CUtensorMap tw{};
+  cudaError_t e = make_map(&tw, p.w, (uint64_t)p.K, (uint64_t)p.M, (uint32_t)g_chunks_per_warp(p.K));
+  if (e != cudaSuccess) return e;
+  const size_t smem = g_smem_bytes(p.K, NT);
+  e = cudaFuncSetAttribute(k_gemv<NT, BPW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.gemv_ctas);
+  cfg.blockDim = dim3(kGThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_gemv<NT, BPW>, tw, p);
+}
+}  // namespace
+
+int front_gemv_ctas(int M, int rows, int nt) {
+  return ((M + kGTileRows - 1) / kGTileRows) * ((rows + 8 * nt - 1) / (8 * nt));
+}
+int front_ctas_per_sm(int K, int nt) {
+  const size_t per = g_smem_bytes(K, nt);
+  const size_t budget = 227 * 1024;
+  return (int)std::max<size_t>(1, std::min<size_t>(budget / per, 2048 / kGThreads));
+}
+int front_max_k() { return kGMaxK; }
+
+// The bf16 GEMV: the activation fragments of a warp's boxes stay in
+// registers when a token tile is one 8-token group and a warp has at most
+// 12 boxes (K <= 6144); otherwise they stream one box ahead.
+cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl) {
+  if (p.gemv_ctas == 0) return cudaSuccess;
+  const int bpw = (p.K / kGBoxK + kGWarps - 1) / kGWarps;
+  switch (nt) {
+    case 1:
+      return bpw <= 4 ? launch_t<1, 4>(p, s, pdl) : bpw <= 8 ? launch_t<1, 8>(p, s, pdl)
+                                                              : launch_t<1, 12>(p, s, pdl);
+    case 2: return launch_t<2, 0>(p, s, pdl);
+    case 4: return launch_t<4, 0>(p, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl) {
+  if (p.router_ctas == 0) return cudaSuccess;
+  if (p.K / 4 > kRouterCols * kGThreads) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)8 * p.K * 2;  // the 8 tokens' input rows
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.router_ctas);
+  cfg.blockDim = dim3(kGThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_router, p);
+}
+
+}  // namespace musemoe

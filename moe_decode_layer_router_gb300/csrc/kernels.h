@@ -17,31 +17,30 @@ enum Counter : int { kNumGroups = 0, kTicket = 1, kNumCounters = 8 };
 // health bits
 enum Health : int { kHealthHRange = 1, kHealthActRange = 2, kHealthTimeout = 4 };
 
-// ---- front: router GEMV (fp32 FFMA) + pooler GEMV (tensor cores) --------
-// The router part writes logit partial sums [ks_r][rows][E]; the GEMV part
-// writes partial sums [ks][rows][M] of Y = X W^T for bf16 W [M, K].
-// The CTA that finishes the last K-split of an output tile (atomic ticket,
-// no waiting) adds the partials in split order and writes the tile.
+// ---- router GEMV (fp32 FFMA) and pooler / unpooler GEMV ------------------
+// The router runs router_ctas = E * ceil(rows / 8) CTAs, one per (expert,
+// 8-token block), each over the whole reduction. The bf16 GEMV Y = X W^T
+// (W [M, K] row-major, K a multiple of 64 and at most front_max_k()) runs on
+// front_gemv_ctas(M, rows, nt) CTAs, one per 16-row tile and token block.
 struct FrontParams {
   const uint16_t* x;  // bf16 [rows, K]
   int rows;
   // router (skipped when router_ctas == 0)
   const float* w_router;  // fp32 [E, K]
-  float* logit_part;      // [ks_r, rows, E]
   float* logits;          // [rows, E]
-  int32_t* router_tickets;
-  int E, ks_r, router_ctas;
-  // bf16 GEMV
+  int E, router_ctas;
+  // bf16 GEMV (skipped when gemv_ctas == 0)
   const uint16_t* w;  // bf16 [M, K]
-  float* part;        // [ks, rows, M]
-  float* y;           // [rows, M]
-  int32_t* tickets;
-  int M, K, ks;
-  int kchunks_per_split;  // 32-element chunks per split
-  int token_blocks;       // ceil(rows / (8 * NT))
+  float* y;           // fp32 [rows, M]
+  int32_t* health;
+  int M, K;
+  int gemv_ctas;
 };
-cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl);
-int front_ctas(const FrontParams& p);
+cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl);   // GEMV
+cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl);          // router
+int front_gemv_ctas(int M, int rows, int nt);
+int front_ctas_per_sm(int K, int nt);
+int front_max_k();
 
 // ---- route: routing rule + pre-expert norm + token->expert permute ------
 struct RouteParams {

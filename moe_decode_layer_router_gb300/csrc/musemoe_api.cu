@@ -41,27 +41,8 @@ int nt_front(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
 int nt_expert(int rows) { return rows <= 32 ? 1 : rows <= 64 ? 4 : 8; }
 int nt_index(int nt) { return nt == 1 ? 0 : nt == 2 ? 1 : nt == 4 ? 2 : 3; }
 
-struct GemvSplit {
-  int ks, kcps, tb;
-};
-// K-split of a bf16 GEMV so that the grid fills ~4 CTAs per SM.
-GemvSplit gemv_split(int M, int K, int rows, int sms) {
-  const int nt = nt_front(rows);
-  const int tb = (rows + 8 * nt - 1) / (8 * nt);
-  const int RB = M / 64, KC = K / 32;
-  int ks = (int)std::lround(4.0 * sms / std::max(1, RB * tb));
-  ks = std::max(1, std::min(ks, KC));
-  const int kcps = (KC + ks - 1) / ks;
-  ks = (KC + kcps - 1) / kcps;
-  return {ks, kcps, tb};
-}
-int router_split(int E, int H, int rows, int sms) {
-  const int EB = (E + 15) / 16, tb = (rows + 7) / 8;
-  const int K4 = H / 4;
-  int ks = (2 * sms) / std::max(1, EB * tb);
-  return std::max(1, std::min(ks, std::max(1, K4 / 32)));
-}
-int router_ctas(int E, int rows, int ks) { return ((E + 15) / 16) * ks * ((rows + 7) / 8); }
+// Router CTAs: one per (expert, block of 8 tokens).
+int router_ctas(int E, int rows) { return E * ((rows + 7) / 8); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -79,10 +60,8 @@ struct musemoe_handle {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   // workspace views
-  float *logit_part = nullptr, *pool_part = nullptr, *unpool_part = nullptr;
   float *logits = nullptr, *weights = nullptr, *h_scale = nullptr, *act_scale = nullptr;
   float *h_raw = nullptr, *u = nullptr;
-  int32_t *router_tickets = nullptr, *pool_tickets = nullptr, *unpool_tickets = nullptr;
   float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
   int32_t* expert_tickets[2] = {nullptr, nullptr};
   int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
@@ -108,25 +87,10 @@ void plan(musemoe_handle* h, Layout& L) {
   const musemoe_dims& d = h->d;
   const size_t R = d.max_rows, E = d.experts, H = d.hidden, P = d.pooled, I = d.inter;
   const size_t RT = R * d.top_k;
-  size_t pool_part = 0, unpool_part = 0, logit_part = 0;
-  for (int rows = 1; rows <= d.max_rows; ++rows) {
-    pool_part = std::max(pool_part, (size_t)gemv_split(d.pooled, d.hidden, rows, h->sms).ks * rows);
-    unpool_part =
-        std::max(unpool_part, (size_t)gemv_split(d.hidden, d.pooled, rows, h->sms).ks * rows);
-    logit_part = std::max(logit_part, (size_t)router_split(d.experts, d.hidden, rows, h->sms) * rows);
-  }
   const bool fp8 = h->quant == kFP8;
-  L.add(&h->logit_part, logit_part * E * 4);
-  L.add(&h->pool_part, pool_part * P * 4);
-  L.add(&h->unpool_part, unpool_part * H * 4);
   L.add(&h->logits, R * E * 4);
   L.add(&h->h_raw, R * P * 4);
   L.add(&h->u, R * H * 4);
-  // one ticket per output tile of the split GEMVs (tiles of 16 experts x 8
-  // tokens, 64 rows x 8 tokens)
-  L.add(&h->router_tickets, ((E + 15) / 16) * ((R + 7) / 8) * 4);
-  L.add(&h->pool_tickets, (P / 64) * ((R + 7) / 8) * 4);
-  L.add(&h->unpool_tickets, (H / 64) * ((R + 7) / 8) * 4);
   L.add(&h->ids, RT * 4);
   L.add(&h->weights, RT * 4);
   L.add(&h->h, R * P * 2);
@@ -171,7 +135,10 @@ std::vector<std::string> refusals(const musemoe_dims* d, int32_t quant, const mu
     r.push_back(fmt("max_rows * top_k = %lld exceeds %d routes", (long long)d->max_rows * d->top_k,
                     kMaxRoutes));
   if ((size_t)d->pooled * 4 > 200 * 1024) r.push_back(fmt("pooled %d too large for one CTA row", d->pooled));
-  if (d->hidden > 8192) r.push_back(fmt("hidden %d above 8192 (one CTA row in registers)", d->hidden));
+  if (d->hidden > front_max_k())
+    r.push_back(fmt("hidden %d above %d (a pooler row tile held in shared memory)", d->hidden, front_max_k()));
+  if (d->pooled > front_max_k())
+    r.push_back(fmt("pooled %d above %d (an unpooler row tile held in shared memory)", d->pooled, front_max_k()));
   if (quant < 0 || quant > 2) r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1) or FP8_W8A8 (2)", quant));
   if (c->score != 0 && c->score != 1) r.push_back(fmt("score %d is not sigmoid (0) or softmax (1)", c->score));
   if (!std::isfinite(c->route_scale)) r.push_back("route_scale is not finite");
@@ -253,30 +220,25 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     return true;
   };
 
-  // 1. front: router GEMV + pooler GEMV
-  const GemvSplit sp = gemv_split(d.pooled, d.hidden, rows, h->sms);
-  const int ks_r = router_split(d.experts, d.hidden, rows, h->sms);
+  // 1. router GEMV, then the pooler GEMV (its weight loads overlap the router)
+  const int ntf = nt_front(rows);
   FrontParams fp{};
   fp.x = x;
   fp.rows = rows;
   fp.w_router = w->w_router;
-  fp.logit_part = h->logit_part;
   fp.logits = h->logits;
-  fp.router_tickets = h->router_tickets;
   fp.E = d.experts;
-  fp.ks_r = ks_r;
-  fp.router_ctas = router_ctas(d.experts, rows, ks_r);
+  fp.router_ctas = router_ctas(d.experts, rows);
   fp.w = w->w_pool;
-  fp.part = h->pool_part;
   fp.y = h->h_raw;
-  fp.tickets = h->pool_tickets;
+  fp.health = h->health;
   fp.M = d.pooled;
   fp.K = d.hidden;
-  fp.ks = sp.ks;
-  fp.kchunks_per_split = sp.kcps;
-  fp.token_blocks = sp.tb;
+  fp.gemv_ctas = front_gemv_ctas(d.pooled, rows, ntf);
   before();
-  if (!after(launch_front(fp, nt_front(rows), s, pdl), "front")) return MUSEMOE_ECUDA;
+  if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
+  before();
+  if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
 
   // 2. routing + pre-expert norm + permute
   const int nte = nt_expert(rows);
@@ -381,23 +343,18 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   if (!after(launch_finalize(fz, s, pdl), "finalize")) return MUSEMOE_ECUDA;
 
   // 6. unpooler GEMV
-  const GemvSplit su = gemv_split(d.hidden, d.pooled, rows, h->sms);
   FrontParams up{};
   up.x = h->moe_out;
   up.rows = rows;
   up.router_ctas = 0;
-  up.ks_r = 1;
   up.w = w->w_unpool;
-  up.part = h->unpool_part;
   up.y = h->u;
-  up.tickets = h->unpool_tickets;
+  up.health = h->health;
   up.M = d.hidden;
   up.K = d.pooled;
-  up.ks = su.ks;
-  up.kchunks_per_split = su.kcps;
-  up.token_blocks = su.tb;
+  up.gemv_ctas = front_gemv_ctas(d.hidden, rows, ntf);
   before();
-  if (!after(launch_front(up, nt_front(rows), s, pdl), "unpool")) return MUSEMOE_ECUDA;
+  if (!after(launch_front(up, ntf, s, pdl), "unpool")) return MUSEMOE_ECUDA;
 
   // 7. FFN boundary
   BoundaryParams bp{};
@@ -556,13 +513,14 @@ size_t musemoe_workspace_bytes(const musemoe_dims* dims, int32_t quant) {
   return L.off;
 }
 
-int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 8 : 7; }
+int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 9 : 8; }
 
 const char* musemoe_kernel_name(int32_t quant, int32_t i) {
-  static const char* fp4[] = {"front", "route", "w13", "w2", "finalize", "unpool", "boundary"};
-  static const char* fp8[] = {"front", "route", "w13", "act_quant", "w2", "finalize", "unpool", "boundary"};
-  if (quant == kFP8) return (i >= 0 && i < 8) ? fp8[i] : "";
-  return (i >= 0 && i < 7) ? fp4[i] : "";
+  static const char* fp4[] = {"router", "pool", "route", "w13", "w2", "finalize", "unpool", "boundary"};
+  static const char* fp8[] = {"router", "pool", "route", "w13", "act_quant", "w2", "finalize", "unpool",
+                              "boundary"};
+  if (quant == kFP8) return (i >= 0 && i < 9) ? fp8[i] : "";
+  return (i >= 0 && i < 8) ? fp4[i] : "";
 }
 
 musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const uint8_t* w13_src,
@@ -659,23 +617,17 @@ musemoe_status musemoe_route(musemoe_handle* h, const musemoe_weights* w, const 
     return set_err(h, MUSEMOE_EINVAL, "ids_out and weights_out must be non-NULL and 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const musemoe_dims& d = h->d;
-  const int ks_r = router_split(d.experts, d.hidden, rows, h->sms);
   FrontParams fp{};
   fp.x = x;
   fp.rows = rows;
   fp.w_router = w->w_router;
-  fp.logit_part = h->logit_part;
   fp.logits = h->logits;
-  fp.router_tickets = h->router_tickets;
   fp.E = d.experts;
-  fp.ks_r = ks_r;
-  fp.router_ctas = router_ctas(d.experts, rows, ks_r);
+  fp.health = h->health;
+  fp.router_ctas = router_ctas(d.experts, rows);
   fp.M = 0;
   fp.K = d.hidden;
-  fp.ks = 1;
-  fp.kchunks_per_split = 1;
-  fp.token_blocks = 1;
-  cudaError_t e = launch_front(fp, 1, s, true);
+  cudaError_t e = launch_router(fp, s, true);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_err(h, e, "launch of router");
   RouteParams rp{};

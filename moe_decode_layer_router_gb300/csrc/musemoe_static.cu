@@ -1,7 +1,8 @@
 // musemoe_route_static: the router GEMV + routing rule for callers that
-// cannot allocate device memory. Its scratch (K-split logit partials, the
-// summed logits, the split tickets) is a fixed file-scope device array, so
-// the call needs no handle and makes no allocation.
+// cannot allocate device memory. Its scratch (the fp32 logits) is a fixed
+// file-scope device array, so the call needs no handle and makes no
+// allocation. Nothing in it has to start at zero: the router writes every
+// logit the routing kernel reads.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -14,9 +15,8 @@ using namespace musemoe;
 
 namespace {
 
-constexpr size_t kLogitsBytes = 64 * 1024;   // rows * E * 4 <= 64 * 256 * 4
-constexpr size_t kTicketBytes = 4 * 1024;    // (E / 16) * (rows / 8) tickets
-constexpr size_t kPartialBytes = MUSEMOE_STATIC_SCRATCH_BYTES - kLogitsBytes - kTicketBytes;
+constexpr size_t kLogitsBytes = 64 * 1024;  // rows * E * 4 <= 64 * 256 * 4
+static_assert(kLogitsBytes <= MUSEMOE_STATIC_SCRATCH_BYTES, "scratch too small");
 constexpr int kMaxDevices = 64;
 
 // The scratch. In host code this name is only a stand-in for the device
@@ -76,45 +76,17 @@ extern "C" musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, 
     }
     base = g_scratch_dev[dev];
   }
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("device query: ") + cudaGetErrorString(e));
-
-  unsigned char* s = static_cast<unsigned char*>(base);
-  float* logits = reinterpret_cast<float*>(s);
-  int32_t* tickets = reinterpret_cast<int32_t*>(s + kLogitsBytes);
-  float* part = reinterpret_cast<float*>(s + kLogitsBytes + kTicketBytes);
-  // K-split of the router GEMV: as the handle path chooses it, shortened
-  // until the partial sums fit the scratch
-  const int EB = (experts + 15) / 16, tb = (rows + 7) / 8;
-  int ks = (2 * sms) / (EB * tb);
-  ks = ks < 1 ? 1 : ks;
-  const int kmax = (hidden / 4) / 32;
-  if (ks > kmax) ks = kmax < 1 ? 1 : kmax;
-  const size_t per_split = (size_t)rows * experts * sizeof(float);
-  if ((size_t)ks * per_split > kPartialBytes) ks = (int)(kPartialBytes / per_split);
-
+  float* logits = static_cast<float*>(base);  // [rows, experts]
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // every call shares the array: the split tickets must start at zero
-  e = cudaMemsetAsync(tickets, 0, (size_t)EB * tb * sizeof(int32_t), st);
-  if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("clear: ") + cudaGetErrorString(e));
-
   FrontParams fp{};
   fp.x = x;
   fp.rows = rows;
   fp.w_router = w_router;
-  fp.logit_part = part;
   fp.logits = logits;
-  fp.router_tickets = tickets;
   fp.E = experts;
-  fp.ks_r = ks;
-  fp.router_ctas = EB * ks * tb;
-  fp.M = 0;
+  fp.router_ctas = experts * ((rows + 7) / 8);
   fp.K = hidden;
-  fp.ks = 1;
-  fp.kchunks_per_split = 1;
-  fp.token_blocks = 1;
-  e = launch_front(fp, 1, st, false);
+  e = launch_router(fp, st, false);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("launch of router: ") + cudaGetErrorString(e));
   RouteParams rp{};
