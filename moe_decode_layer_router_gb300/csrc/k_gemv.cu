@@ -33,16 +33,27 @@ constexpr int kGThreads = kGWarps * 32;
 constexpr int kGTileRows = 16;                 // weight rows per CTA
 constexpr int kGBoxK = 64;                     // elements per box row (128 B)
 constexpr int kGBoxBytes = kGTileRows * 128;   // one [16 x 64] bf16 box
-constexpr int kGMaxK = 6144;                   // reduction length held in shared memory
-constexpr int kRouterRowsPerCta = 16;
+constexpr int kGMaxK = 5632;                   // reduction length held in shared memory
 
 __host__ __device__ constexpr int g_red_bytes(int nt) { return kGWarps * nt * 32 * 16; }
 // boxes (64-element chunks of the reduction) per warp
 __host__ __device__ constexpr int g_chunks_per_warp(int K) { return (K / kGBoxK + kGWarps - 1) / kGWarps; }
+constexpr int kGXRing = 4;          // activation boxes in flight per warp (one token tile)
+constexpr int kGXBox = 8 * 128;     // one [8 tokens x 64] bf16 box
 __host__ __device__ constexpr size_t g_smem_bytes(int K, int nt) {
-  return (size_t)kGWarps * g_chunks_per_warp(K) * kGBoxBytes + g_red_bytes(nt) + 1024;
+  return (size_t)kGWarps * g_chunks_per_warp(K) * kGBoxBytes +
+         (nt == 1 ? (size_t)kGWarps * kGXRing * kGXBox : 0) + g_red_bytes(nt) + 1024;
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and its groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             int z, uint32_t bar) {
   asm volatile(
@@ -142,10 +153,12 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
   }
 }
 
-// BPW > 0: every warp holds the B fragments of its (at most BPW) boxes in
-// registers, loaded right after the wait for the previous kernel; BPW = 0:
-// the fragments of the next box load while the current one runs.
-template <int NT, int BPW>
+// NT = 1: every warp streams its activation boxes ([8 tokens x 64], 16-byte
+// asynchronous copies to the 128-byte-swizzled addresses, issued right after
+// the wait for the previous kernel) through a ring of kGXRing shared-memory
+// slots and reads its B fragments with ldmatrix. NT > 1: the fragments of the next box load from L1/L2 while the
+// current one runs.
+template <int NT>
 __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParams& p,
                                          uint8_t* smem_raw) {
   __shared__ __align__(8) unsigned long long warp_b[kGWarps];
@@ -157,8 +170,10 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
   const int nbox = p.K / kGBoxK, nch = g_chunks_per_warp(p.K);
   // 1024-byte aligned tile (the 128-byte swizzle repeats every 1024 bytes)
   const uint32_t wt = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t xring = wt + kGWarps * nch * kGBoxBytes + warp * kGXRing * kGXBox;
   float4* red = reinterpret_cast<float4*>(smem_raw + (wt - smem_u32(smem_raw)) +
-                                          (size_t)kGWarps * nch * kGBoxBytes);
+                                          (size_t)kGWarps * nch * kGBoxBytes +
+                                          (NT == 1 ? (size_t)kGWarps * kGXRing * kGXBox : 0));
 
   if (threadIdx.x == 0) {
     for (int w = 0; w < kGWarps; ++w) mbar_init(smem_u32(&warp_b[w]), 1);
@@ -179,55 +194,83 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
   }
   pdl_wait();  // x may be the previous kernel's output
 
-  // activation rows of this lane's tokens (lanes past the last token read the
-  // last token's row; their results are never stored)
-  const uint16_t* xr[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-    xr[nt] = p.x + (size_t)min(tbk * 8 * NT + nt * 8 + g, p.rows - 1) * p.K + 2 * q;
-  // B fragments of box b's 4 k-steps: k 2q, 2q+1 and 2q+8, 2q+9 of token g
-  auto load_b = [&](uint32_t (&f)[NT][4][2], int b) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) {
-        const uint16_t* xp = xr[nt] + b * kGBoxK + s4 * 16;
-        f[nt][s4][0] = *reinterpret_cast<const uint32_t*>(xp);
-        f[nt][s4][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
-      }
-  };
   const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_u = lane >> 4;
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-  auto box_mma = [&](int b, const uint32_t (&f)[NT][4][2]) {
-    const uint32_t box = wt + b * kGBoxBytes;
-#pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(box + swz(a_row, 2 * s4 + a_u), a0, a1, a2, a3);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, f[nt][s4][0], f[nt][s4][1]);
-    }
-  };
-  const int b0 = warp * nch, b1 = min(b0 + nch, nbox);
+  const int b0 = warp * nch, b1 = min(b0 + nch, nbox), nb = max(0, b1 - b0);
   bool ok = true;
-  if constexpr (BPW > 0) {
-    uint32_t bf[BPW][NT][4][2];
+  if constexpr (NT == 1) {
+    // box b0 + i into slot i % kGXRing: lane l copies the 16-byte units l and
+    // l + 32 (token row u / 8, unit u % 8); rows past the last token repeat it
+    auto issue_x = [&](int i) {
+      if (i < nb) {
+        const uint32_t slot = xring + (i % kGXRing) * kGXBox;
 #pragma unroll
-    for (int i = 0; i < BPW; ++i)
-      if (b0 + i < b1) load_b(bf[i], b0 + i);
-    if (b0 < b1) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&warp_b[warp]), 0u, &abort_flag));
+        for (int h = 0; h < 2; ++h) {
+          const int pc = lane + 32 * h, r = pc >> 3, u = pc & 7;
+          const uint16_t* src = p.x + (size_t)min(tbk * 8 + r, p.rows - 1) * p.K + (b0 + i) * kGBoxK + u * 8;
+          cp_async16(slot + swz(r, u), src);
+        }
+      }
+      cp_async_commit();
+    };
 #pragma unroll
-    for (int i = 0; i < BPW; ++i) {
-      if (b0 + i >= b1 || !ok) break;
-      box_mma(b0 + i, bf[i]);
+    for (int i = 0; i < kGXRing; ++i) issue_x(i);
+    if (nb > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&warp_b[warp]), 0u, &abort_flag));
+    const int b_row = lane & 7, b_u = lane >> 3;
+    for (int i = 0; i < nb && ok; ++i) {
+      cp_async_wait<kGXRing - 1>();  // box i has landed
+      __syncwarp();
+      const uint32_t box = wt + (b0 + i) * kGBoxBytes, xs = xring + (i % kGXRing) * kGXBox;
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        uint32_t bf[4];
+        ldsm_x4(xs + swz(b_row, 4 * s2 + b_u), bf[0], bf[1], bf[2], bf[3]);
+#pragma unroll
+        for (int s1 = 0; s1 < 2; ++s1) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(box + swz(a_row, 2 * (2 * s2 + s1) + a_u), a0, a1, a2, a3);
+          mma_bf16_16816(acc[0], a0, a1, a2, a3, bf[2 * s1], bf[2 * s1 + 1]);
+        }
+      }
+      __syncwarp();
+      issue_x(i + kGXRing);  // the slot just read
     }
+    cp_async_wait<0>();
   } else {
+    // activation rows of this lane's tokens (lanes past the last token read
+    // the last token's row; their results are never stored)
+    const uint16_t* xr[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      xr[nt] = p.x + (size_t)min(tbk * 8 * NT + nt * 8 + g, p.rows - 1) * p.K + 2 * q;
+    // B fragments of box b's 4 k-steps: k 2q, 2q+1 and 2q+8, 2q+9 of token g
+    auto load_b = [&](uint32_t (&f)[NT][4][2], int b) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const uint16_t* xp = xr[nt] + b * kGBoxK + s4 * 16;
+          f[nt][s4][0] = *reinterpret_cast<const uint32_t*>(xp);
+          f[nt][s4][1] = *reinterpret_cast<const uint32_t*>(xp + 8);
+        }
+    };
+    auto box_mma = [&](int b, const uint32_t (&f)[NT][4][2]) {
+      const uint32_t box = wt + b * kGBoxBytes;
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(box + swz(a_row, 2 * s4 + a_u), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, f[nt][s4][0], f[nt][s4][1]);
+      }
+    };
     uint32_t bf[2][NT][4][2];
-    if (b0 < b1) {
+    if (nb > 0) {
       load_b(bf[0], b0);
       ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&warp_b[warp]), 0u, &abort_flag));
     }
@@ -269,7 +312,6 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
       if (r_hi < p.M) p.y[(size_t)t * p.M + r_hi] = hi[h];
     }
   }
-  // copies still in flight (after a timeout) must land before the CTA leaves
   if (threadIdx.x == 0 && abort_flag) {
     for (int w = 0; w < kGWarps && w * nch < nbox; ++w) {
       const unsigned long long t0 = globaltimer();
@@ -279,12 +321,12 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
   }
 }
 
-template <int NT, int BPW>
+template <int NT>
 __global__ void __launch_bounds__(kGThreads)
     k_gemv(const __grid_constant__ CUtensorMap tw, FrontParams p) {
   pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
-  gemv_cta<NT, BPW>(&tw, p, smem);
+  gemv_cta<NT>(&tw, p, smem);
 }
 
 __global__ void __launch_bounds__(kGThreads) k_router(FrontParams p) {
@@ -323,13 +365,13 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NT, int BPW>
+template <int NT>
 cudaError_t launch_t(const FrontParams& p, cudaStream_t s, bool pdl) {
   CUtensorMap tw{};
   cudaError_t e = make_map(&tw, p.w, (uint64_t)p.K, (uint64_t)p.M, (uint32_t)g_chunks_per_warp(p.K));
   if (e != cudaSuccess) return e;
   const size_t smem = g_smem_bytes(p.K, NT);
-  e = cudaFuncSetAttribute(k_gemv<NT, BPW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(k_gemv<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.gemv_ctas);
@@ -341,7 +383,7 @@ cudaError_t launch_t(const FrontParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_gemv<NT, BPW>, tw, p);
+  return cudaLaunchKernelEx(&cfg, k_gemv<NT>, tw, p);
 }
 }  // namespace
 
@@ -355,18 +397,12 @@ int front_ctas_per_sm(int K, int nt) {
 }
 int front_max_k() { return kGMaxK; }
 
-// The bf16 GEMV: the activation fragments of a warp's boxes stay in
-// registers when a token tile is one 8-token group and a warp has at most
-// 12 boxes (K <= 6144); otherwise they stream one box ahead.
 cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl) {
   if (p.gemv_ctas == 0) return cudaSuccess;
-  const int bpw = (p.K / kGBoxK + kGWarps - 1) / kGWarps;
   switch (nt) {
-    case 1:
-      return bpw <= 4 ? launch_t<1, 4>(p, s, pdl) : bpw <= 8 ? launch_t<1, 8>(p, s, pdl)
-                                                              : launch_t<1, 12>(p, s, pdl);
-    case 2: return launch_t<2, 0>(p, s, pdl);
-    case 4: return launch_t<4, 0>(p, s, pdl);
+    case 1: return launch_t<1>(p, s, pdl);
+    case 2: return launch_t<2>(p, s, pdl);
+    case 4: return launch_t<4>(p, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
