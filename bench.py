@@ -37,7 +37,8 @@ WEIGHT_SETS = 4
 # DRAM traffic of one launch of the dominant kernel, from the ncu capture
 # summarized in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"kernel": None, "source_sha1": None, "bytes_per_launch": None}
+NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "c788341bbc8f7f26cbf399451507c5826ad05da1",
+               "bytes_per_launch": 102667776 + 2970624}
 
 
 def _args():
@@ -47,6 +48,8 @@ def _args():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step's kernels directly instead of replaying a CUDA graph")
     return ap.parse_args()
 
 
@@ -256,10 +259,15 @@ def bench_ours(args):
             mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
     torch.cuda.synchronize()
     for st_ in sets:
+        if args.eager:
+            def step(st_=st_):
+                mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
+            graphs.append(step)
+            continue
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
-        graphs.append(g)
+        graphs.append(g.replay)
     torch.cuda.synchronize()
 
     def barrier():
@@ -270,7 +278,7 @@ def bench_ours(args):
     # warm-up (>= 3 steps)
     with torch.cuda.stream(s):
         for i in range(max(3, args.warmup)):
-            graphs[i % WEIGHT_SETS].replay()
+            graphs[i % WEIGHT_SETS]()
     torch.cuda.synchronize()
 
     uuid = None
@@ -288,7 +296,7 @@ def bench_ours(args):
     with torch.cuda.stream(s):
         e0.record(s)
         for i in range(args.steps):
-            graphs[i % WEIGHT_SETS].replay()
+            graphs[i % WEIGHT_SETS]()
         e1.record(s)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
@@ -387,7 +395,7 @@ def bench_ours(args):
                    "rows_per_gpu": cfg.rows, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {WEIGHT_SETS} rotating weight sets of "
                          f"{set_bytes / 1e6:.0f} MB",
-                   "cuda_graph": True},
+                   "cuda_graph": not args.eager},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic,
