@@ -114,6 +114,58 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
   const long long u1 = blockIdx.x < GE ? x_start(blockIdx.x + 1, U, GE) : 0;
   const int kel = (Q == kFP8) ? 1 : 2;  // bytes per activation element
   const uint32_t stage0 = smem_u32(smem);
+  // Processing order of the CTA's units: its whole tiles [b0, b1), then the
+  // units [b1, u1) of the tile it shares with the next CTA (it holds that
+  // tile's first units and only leaves a partial), then the units [u0, b0)
+  // of the tile it shares with the previous CTA (it holds that tile's last
+  // unit: it waits for the other partials and finishes the tile). A range
+  // inside one tile is a single leave-a-partial part. Only owners wait, and
+  // an owner's part comes after everything the CTA's own partials need, so
+  // no wait depends on a waiting CTA.
+  // (unit indices fit in 32 bits: groups x tiles x slices)
+  const int U0 = (int)u0, U1 = (int)u1, KS = G.KS, PG = (int)per_group;
+  int b0 = (U0 + KS - 1) / KS * KS, b1 = U1 / KS * KS;
+  if (b0 > b1) b0 = b1 = U0;  // inside one tile: [u0, u1) is the "next-CTA" part
+  const int nM = b1 - b0, nE = U1 - b1;
+  const int count = U1 - U0;
+  // the three parts as (first unit, end) in processing order
+  const int part_a[3] = {b0, b1, U0}, part_e[3] = {b1, U1, b0};
+  // walks the units in processing order: unit index, its group, tile and
+  // slice, and the bounds of its part; divisions only where a part starts
+  struct Walk {
+    int u, grp, tile, slice, lo, hi, part, left;
+  };
+  auto walk_begin = [&](Walk& w) {
+    w.part = -1;
+    w.left = 0;
+  };
+  auto walk_next = [&](Walk& w) {
+    if (w.left == 0) {
+      do {
+        ++w.part;
+      } while (w.part < 3 && part_e[w.part] <= part_a[w.part]);
+      w.lo = part_a[w.part];
+      w.hi = part_e[w.part];
+      w.left = w.hi - w.lo;
+      w.u = w.lo;
+      w.grp = w.u / PG;
+      const int rem = w.u - w.grp * PG;
+      w.tile = rem / KS;
+      w.slice = rem - w.tile * KS;
+    } else {
+      ++w.u;
+      if (++w.slice == KS) {
+        w.slice = 0;
+        if (++w.tile == G.tiles) {
+          w.tile = 0;
+          ++w.grp;
+        }
+      }
+    }
+    --w.left;
+  };
+  (void)nM;
+  (void)nE;
 
   const int g_first = (u1 > u0) ? (int)(u0 / per_group) : 0;
   const int g_count = (u1 > u0) ? min(kXMeta, (int)((u1 - 1) / per_group) - g_first + 1) : 0;
@@ -155,12 +207,18 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       const int NRT = p.N / 64;  // row tiles per expert
       const size_t tile_codes = (size_t)G.NC * 4096, tile_scales = (size_t)G.NC * 64 * G.SB;
       const uint8_t* sb = reinterpret_cast<const uint8_t*>(p.scale);
-      int grp = (int)(u0 / per_group);
-      int rem = (int)(u0 % per_group);
-      int tile = rem / G.KS, slice = rem % G.KS;
-      int4 gd = (u1 > u0) ? group_of(grp) : make_int4(0, 0, 0, 0);
       int n = 0;
-      for (long long u = u0; u < u1; ++u, ++n) {
+      Walk wk;
+      walk_begin(wk);
+      int gcur = -1;
+      int4 gd = make_int4(0, 0, 0, 0);
+      for (; n < count; ++n) {
+        walk_next(wk);
+        const int grp = wk.grp, tile = wk.tile, slice = wk.slice;
+        if (grp != gcur) {
+          gd = group_of(grp);
+          gcur = grp;
+        }
         const int st = n % S, use = n / S;
         if (use > 0 && !mbar_wait_or_abort(smem_u32(&empty_b[st]), (uint32_t)(use - 1) & 1u,
                                            &abort_flag)) {
@@ -191,14 +249,6 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
                      b_row(route_of(grp, gd.y, t)) + (size_t)slice * kSliceChunks * G.cbB,
                      nc * G.cbB, bar);
         }
-        if (++slice == G.KS) {
-          slice = 0;
-          if (++tile == G.tiles) {
-            tile = 0;
-            ++grp;
-            if (u + 1 < u1) gd = group_of(grp);
-          }
-        }
       }
       // the copies still in flight must land before the CTA leaves
       const int issued = n;
@@ -213,9 +263,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
   }
 
   // ---------------- compute warps ----------------
-  int grp = (int)(u0 / per_group);
-  int rem = (int)(u0 % per_group);
-  int tile = rem / G.KS, slice = rem % G.KS;
+  int grp = 0, tile = 0, slice = 0;
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -273,8 +321,14 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
     }
   };
 
-  int n = 0;
-  for (long long u = u0; u < u1; ++u, ++n) {
+  Walk wk;
+  walk_begin(wk);
+  for (int n = 0; n < count; ++n) {
+    walk_next(wk);
+    const int u = wk.u;
+    grp = wk.grp;
+    tile = wk.tile;
+    slice = wk.slice;
     const int st = n % S;
     if (fresh) {
       const int4 gd = group_of(grp);
@@ -380,13 +434,15 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
     if (lane == 0) mbar_arrive(smem_u32(&empty_b[st]));  // stage st may be refilled
 
     const bool tile_end = (slice == G.KS - 1);
-    if (tile_end || u + 1 == u1) {
-      const long long tb = u - slice;  // first unit of the tile
-      if (tb >= u0 && tile_end) {
+    if (tile_end || u + 1 == wk.hi) {
+      const int tb = u - slice;  // first unit of the tile
+      if (tile_end && tb >= wk.lo) {
         finish(acc);
       } else {
-        // the tile spans several CTAs: leave this CTA's partial; the last
-        // warp to arrive adds them all in CTA order
+        // the tile spans several CTAs; the one holding its last unit (tile_end)
+        // owns it. A CTA without the last unit stores its partial and signals
+        // (no fence, no wait); the owner waits for the others' signals and
+        // adds all partials in CTA order.
         const int c_first = x_cta_of(tb, U, GE);
         const int c_last = x_cta_of(tb + G.KS - 1, U, GE);
         const int slot_sz = kXWarps * NT * 32;
@@ -395,28 +451,43 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
           return ((size_t)c * 2 + which) * slot_sz + (size_t)warp * NT * 32;
         };
         float4* part = reinterpret_cast<float4*>(p.part);
-        const size_t mine = slot_of(blockIdx.x);
+        int32_t* flag = p.tickets + ((size_t)grp * G.tiles + tile) * kXWarps + warp;
+        if (!tile_end) {
+          const size_t mine = slot_of(blockIdx.x);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          if (nt < ntile_act)
-            part[mine + nt * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-          int32_t* t = p.tickets + ((size_t)grp * G.tiles + tile) * kXWarps + warp;
-          last = (atomicAdd(t, 1) == c_last - c_first);
-          if (last) *t = 0;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
+          for (int nt = 0; nt < NT; ++nt)
+            if (nt < ntile_act)
+              part[mine + nt * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+          __syncwarp();  // orders the lanes' stores before lane 0's release
+          if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;\n" ::"l"(flag) : "memory");
+        } else {
+          int got = 1;
+          if (lane == 0) {
+            const int want = c_last - c_first;
+            int v = 0;
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+            if (v < want) {
+              const unsigned long long t0 = globaltimer();
+              do {
+                __nanosleep(256);
+                asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+              } while (v < want && globaltimer() - t0 <= kWaitLimitNs && !abort_flag);
+            }
+            got = (v >= want);
+            if (got) *flag = 0;  // ready for the next launch
+          }
+          got = __shfl_sync(0xffffffffu, got, 0);
+          __syncwarp();
+          if (!got) {
+            if (lane == 0 && !abort_flag) fail();
+            break;
+          }
           float v[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[nt][i] = 0.f;
-          for (int c = c_first; c <= c_last; ++c) {
+          for (int c = c_first; c < c_last; ++c) {
             const size_t sc = slot_of(c);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -428,6 +499,10 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
               v[nt][3] += x.w;
             }
           }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[nt][i] += acc[nt][i];
           finish(v);
         }
       }
@@ -436,13 +511,6 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
       fresh = true;
-    }
-    if (++slice == G.KS) {
-      slice = 0;
-      if (++tile == G.tiles) {
-        tile = 0;
-        ++grp;
-      }
     }
   }
 }
