@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       walk_begin(wk);
       int gcur = -1;
       int4 gd = make_int4(0, 0, 0, 0);
+      // the weights are read once: their lines leave L2 first
+      const uint64_t pol_first = l2_policy_evict_first();
       for (; n < count; ++n) {
         walk_next(wk);
         const int grp = wk.grp, tile = wk.tile, slice = wk.slice;
@@ -236,12 +238,13 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
         for (int blk = 0; blk < 2; ++blk) {
           const int rt = (ROLE == 0) ? (blk == 0 ? tile : p.I / 64 + tile) : 2 * tile + blk;
           const size_t ti = (size_t)gd.x * NRT + rt;
-          bulk_g2s(dst + blk * kXCodeBlock,
-                   p.w + ti * tile_codes + (size_t)slice * kSliceChunks * 4096, nc * 4096, bar);
+          bulk_g2s_hint(dst + blk * kXCodeBlock,
+                        p.w + ti * tile_codes + (size_t)slice * kSliceChunks * 4096, nc * 4096, bar,
+                        pol_first);
           if (G.SB)
-            bulk_g2s(dst + G.scale_off + blk * 8 * kSliceChunks * 8 * G.SB,
-                     sb + ti * tile_scales + (size_t)slice * kSliceChunks * 64 * G.SB,
-                     nc * 64 * G.SB, bar);
+            bulk_g2s_hint(dst + G.scale_off + blk * 8 * kSliceChunks * 8 * G.SB,
+                          sb + ti * tile_scales + (size_t)slice * kSliceChunks * 64 * G.SB,
+                          nc * 64 * G.SB, bar, pol_first);
         }
         if (NT == 1) {
           for (int t = 0; t < gd.z; ++t)
