@@ -5,8 +5,9 @@
 // multiplier -> sigmoid or softmax -> expert bias added for SELECTION only ->
 // top-k -> gather the UNBIASED scores -> divide by (sum + division_eps) ->
 // multiply by route_scale. All in fp32, as the recipe's torch ops are.
-// Top-k: one warp sorts the E (<= 256) keys (selection score, then lower id
-// first on equal scores) with a register bitonic network, 32 * EPL keys.
+// Top-k: one warp per row takes k rounds of a warp-wide argmax over the E
+// (<= 256) selection keys (largest score first, the lower id on equal
+// scores).
 //
 // Pre-expert norm (page "vllm.models.muse_spark.nvidia.specialized_decode.
 // runtime.providers", MoEProvider docstring): RMSNorm of the pooled row with
@@ -27,46 +28,6 @@ constexpr int kRouteThreads = 256;
 __device__ __forceinline__ uint32_t orderable(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Warp-wide descending bitonic sort of 32 * EPL 64-bit keys; key i lives in
-// lane i / EPL, register i % EPL.
-template <int EPL>
-__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&key)[EPL], int lane) {
-  constexpr int N = 32 * EPL;
-#pragma unroll
-  for (int kk = 2; kk <= N; kk <<= 1) {
-#pragma unroll
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      if (j >= EPL) {
-        const int lj = j / EPL;
-#pragma unroll
-        for (int r = 0; r < EPL; ++r) {
-          const int i = lane * EPL + r;
-          const uint64_t other = __shfl_xor_sync(0xffffffffu, key[r], lj);
-          const bool lower = (i & j) == 0;
-          const bool desc = (i & kk) == 0;
-          const bool take_max = (lower == desc);
-          const uint64_t mx = key[r] > other ? key[r] : other;
-          const uint64_t mn = key[r] > other ? other : key[r];
-          key[r] = take_max ? mx : mn;
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < EPL; ++r) {
-          const int r2 = r ^ j;
-          if (r2 > r) {
-            const int i = lane * EPL + r;
-            const bool desc = (i & kk) == 0;
-            const uint64_t a = key[r], b = key[r2];
-            const bool swap = desc ? (a < b) : (a > b);
-            key[r] = swap ? b : a;
-            key[r2] = swap ? a : b;
-          }
-        }
-      }
-    }
-  }
 }
 
 // Exclusive scan of one int per thread (blockDim.x == kRouteThreads).
@@ -103,15 +64,20 @@ template <int EPL>
 __device__ void route_row_warp(const RouteParams& p, int t, int lane, float* s_w, int* top,
                                int16_t* ids_smem) {
   const int E = p.E, k = p.k;
-  float g[EPL];
+  float g[EPL], bias[EPL];
+  // the logits and the selection bias in one round trip
+#pragma unroll
+  for (int r = 0; r < EPL; ++r) {
+    const int i = lane * EPL + r;
+    g[r] = (i < E) ? __ldcg(p.logits + (size_t)t * E + i) : -INFINITY;
+    bias[r] = (i < E) ? __ldg(p.expert_bias + i) : 0.f;
+  }
   float gmax = -INFINITY;
 #pragma unroll
   for (int r = 0; r < EPL; ++r) {
     const int i = lane * EPL + r;
-    float l = (i < E) ? __ldcg(p.logits + (size_t)t * E + i) : -INFINITY;
-    if (p.has_multiplier && i < E) l = l * p.multiplier;
-    g[r] = l;
-    gmax = fmaxf(gmax, l);
+    if (p.has_multiplier && i < E) g[r] = g[r] * p.multiplier;
+    gmax = fmaxf(gmax, g[r]);
   }
   float sc[EPL];
   if (p.score == 1) {  // softmax over the experts
@@ -129,23 +95,36 @@ __device__ void route_row_warp(const RouteParams& p, int t, int lane, float* s_w
 #pragma unroll
     for (int r = 0; r < EPL; ++r) sc[r] = 1.0f / (1.0f + expf(-g[r]));
   }
-  uint64_t key[EPL];
+  // selection keys; 0 marks padding and experts already taken (a real key
+  // is at least 1)
+  uint32_t key[EPL];
 #pragma unroll
   for (int r = 0; r < EPL; ++r) {
     const int i = lane * EPL + r;
     if (i < E) {
       s_w[i] = sc[r];
-      const float sel = sc[r] + __ldg(p.expert_bias + i);  // selection only
-      key[r] = ((uint64_t)orderable(sel) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+      const float sel = sc[r] + bias[r];  // selection only
+      key[r] = max(orderable(sel), 1u);
     } else {
-      key[r] = 0ull;
+      key[r] = 0u;
     }
   }
-  warp_bitonic_desc<EPL>(key, lane);
+  // top-k: k rounds of a warp argmax, the largest key and, among equal
+  // keys, the lowest id (the order a descending sort by (key, -id) gives)
+  for (int j = 0; j < k; ++j) {
+    uint32_t lm = 0u;
 #pragma unroll
-  for (int r = 0; r < EPL; ++r) {
-    const int i = lane * EPL + r;
-    if (i < k) top[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[r] & 0xFFFFFFFFull));
+    for (int r = 0; r < EPL; ++r) lm = max(lm, key[r]);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, lm);
+    uint32_t cand = 0xffffffffu;
+#pragma unroll
+    for (int r = EPL - 1; r >= 0; --r)
+      if (key[r] == m) cand = (uint32_t)(lane * EPL + r);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+#pragma unroll
+    for (int r = 0; r < EPL; ++r)
+      if ((uint32_t)(lane * EPL + r) == win) key[r] = 0u;
+    if (lane == 0) top[j] = (int)win;
   }
   __syncwarp();
   float part = 0.f;
@@ -234,29 +213,62 @@ __device__ void permute(const RouteParams& p, int16_t* ids_s, unsigned char* wor
 // the expert operand (f16, or e4m3 + per-row scale for FP8).
 __device__ void pre_norm_row(const RouteParams& p, int t, float* hr, float* scratch) {
   const int tid = threadIdx.x;
+  constexpr int kV = 4;  // float4s of the row per thread and pass
   float ss = 0.f;
   const float4* src = reinterpret_cast<const float4*>(p.h_raw + (size_t)t * p.P);
-#pragma unroll 4
-  for (int i = tid; i < p.P / 4; i += kRouteThreads) {
-    const float4 v = __ldcg(src + i);
-    reinterpret_cast<float4*>(hr)[i] = v;
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  const int n4 = p.P / 4;
+  for (int base = 0; base < n4; base += kV * kRouteThreads) {
+    float4 v[kV];
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      const int i = base + j * kRouteThreads + tid;
+      v[j] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      const int i = base + j * kRouteThreads + tid;
+      if (i < n4) reinterpret_cast<float4*>(hr)[i] = v[j];
+      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    }
   }
   ss = block_sum(ss, scratch);  // also orders the hr[] writes before the reads
   const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.P + p.norm_eps) : 1.0f;
   float amax = 0.f;
   int bad = 0;
-  for (int i = tid; i < p.P; i += kRouteThreads) {
-    float v = hr[i];
-    if (p.pre_norm) v = (v * rstd) * bf16_bits_to_f32(p.w_pre_norm[i]);
-    const float hb = round_bf16(v);
-    p.h[(size_t)t * p.P + i] = f32_to_bf16_bits(hb);
-    hr[i] = hb;
-    amax = fmaxf(amax, fabsf(hb));
-    if (p.quant != kFP8) {
-      reinterpret_cast<__half*>(p.h_op)[(size_t)t * p.P + i] = __float2half_rn(hb);
-      bad |= !(fabsf(hb) <= 65504.f);
+  // four elements per thread and step: the norm weights are loaded before
+  // any store of the step
+  for (int i0 = 4 * tid; i0 < p.P; i0 += 4 * kRouteThreads) {
+    float wv[4] = {1.f, 1.f, 1.f, 1.f};
+    if (p.pre_norm) {
+      const uint2 wb = __ldg(reinterpret_cast<const uint2*>(p.w_pre_norm + i0));
+      wv[0] = bf16_bits_to_f32(wb.x & 0xFFFFu);
+      wv[1] = bf16_bits_to_f32(wb.x >> 16);
+      wv[2] = bf16_bits_to_f32(wb.y & 0xFFFFu);
+      wv[3] = bf16_bits_to_f32(wb.y >> 16);
     }
+    const float4 x = *reinterpret_cast<const float4*>(hr + i0);
+    const float xv[4] = {x.x, x.y, x.z, x.w};
+    float hb[4];
+    uint32_t hbits[2], opbits[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v = xv[j];
+      if (p.pre_norm) v = (v * rstd) * wv[j];
+      hb[j] = round_bf16(v);
+      amax = fmaxf(amax, fabsf(hb[j]));
+      bad |= !(fabsf(hb[j]) <= 65504.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      hbits[j] = f32_to_bf16_bits(hb[2 * j]) | ((uint32_t)f32_to_bf16_bits(hb[2 * j + 1]) << 16);
+      const __half2 h2 = __floats2half2_rn(hb[2 * j], hb[2 * j + 1]);
+      opbits[j] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint2*>(p.h + (size_t)t * p.P + i0) = make_uint2(hbits[0], hbits[1]);
+    *reinterpret_cast<float4*>(hr + i0) = make_float4(hb[0], hb[1], hb[2], hb[3]);
+    if (p.quant != kFP8)
+      *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(p.h_op) + (size_t)t * p.P + i0) =
+          make_uint2(opbits[0], opbits[1]);
   }
   if (p.quant == kFP8) {
     amax = block_max(amax, scratch);
@@ -267,6 +279,7 @@ __device__ void pre_norm_row(const RouteParams& p, int t, float* hr, float* scra
       reinterpret_cast<uint16_t*>(p.h_op + (size_t)t * p.P)[i / 2] = f32x2_to_e4m3x2(a, b);
     }
     if (tid == 0) p.h_scale[t] = sc;
+    bad = 0;  // the e4m3 operand is scaled: no f16 range limit
   }
   if (bad) atomicOr(p.health, kHealthHRange);
 }
