@@ -3,9 +3,10 @@
 A step is one pass of the whole block (router, routing, pooler + pre-expert
 norm, grouped experts, post-expert norm + weighted sum, unpooler, FFN
 boundary) over one batch of the decode workload: b=8 rows, H=5120, P=2048,
-I=1024, E=128, top-8, MXFP4 experts. Steps replay a CUDA graph of
-musemoe_forward; they rotate over 4 independent weight sets (about 1.9 GB,
-far beyond the 129 MB L2) so every step reads its weights from HBM.
+I=1024, E=128, top-8, MXFP4 experts. Steps rotate over 4 independent
+weight sets (about 1.9 GB, far beyond the 129 MB L2) so every step reads its
+weights from HBM; one CUDA graph holds the 4 forwards in turn, so a replay
+runs 4 steps, chained on the device as consecutive layers' blocks would be.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -94,8 +95,8 @@ def algorithmic_bytes(cfg, ids_list):
         active = len(np.unique(ids))
         per.append({
             "router": E * H * 4 + b * H * 2 + b * E * 4,
-            "pool": P * H * 2 + b * H * 2 + b * P * 4,
-            "route": b * E * 4 + b * P * 4 + E * 4 + P * 2 + b * P * 4 + routes * 8,
+            "route": b * E * 4 + E * 4 + routes * 12,
+            "pool": P * H * 2 + b * H * 2 + b * P * 4 + P * 2 + 2 * b * P * 2,
             "w13": active * w13_e + b * P * 2 + routes * I * 2,
             "w2": active * w2_e + routes * I * 2 + routes * P * 4,
             "finalize": routes * P * 4 + routes * 4 + P * 2 + b * P * 2,
@@ -268,7 +269,31 @@ def bench_ours(args):
         with torch.cuda.graph(g, stream=s):
             mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
         graphs.append(g.replay)
+    # one graph of the WEIGHT_SETS forwards in turn: a replay runs that many
+    # steps, the launches of consecutive forwards chain on the device and
+    # the host issues one replay per WEIGHT_SETS steps
+    if args.eager:
+        def group():
+            for f in graphs:
+                f()
+    else:
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gg, stream=s):
+            for st_ in sets:
+                mm.musemoe_forward(handle, st_["w"], st_["x"], st_["stream"], st_["out"], cfg.rows, s)
+        group = gg.replay
     torch.cuda.synchronize()
+
+    def run_steps(count):
+        """count forwards, set i % WEIGHT_SETS for the i-th"""
+        i = 0
+        while i < count:
+            if count - i >= WEIGHT_SETS:
+                group()
+                i += WEIGHT_SETS
+            else:
+                graphs[i % WEIGHT_SETS]()
+                i += 1
 
     def barrier():
         if world > 1:
@@ -277,8 +302,7 @@ def bench_ours(args):
 
     # warm-up (>= 3 steps)
     with torch.cuda.stream(s):
-        for i in range(max(3, args.warmup)):
-            graphs[i % WEIGHT_SETS]()
+        run_steps(max(3, args.warmup))
     torch.cuda.synchronize()
 
     uuid = None
@@ -295,8 +319,7 @@ def bench_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
         e0.record(s)
-        for i in range(args.steps):
-            graphs[i % WEIGHT_SETS]()
+        run_steps(args.steps)
         e1.record(s)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
@@ -395,7 +418,8 @@ def bench_ours(args):
                    "rows_per_gpu": cfg.rows, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {WEIGHT_SETS} rotating weight sets of "
                          f"{set_bytes / 1e6:.0f} MB",
-                   "cuda_graph": not args.eager},
+                   "cuda_graph": (f"{WEIGHT_SETS} forwards per graph" if not args.eager
+                                  else False)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic,

@@ -93,8 +93,13 @@ constexpr int x_min_blocks() {
 
 template <int Q, int ROLE, int NT>
 __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(ExpertParams p) {
+  // The groups, route lists and counters below are the route kernel's
+  // output, complete before this launch starts: the kernel launched between
+  // the two (the pooler, or w13 for w2) signals its dependents only after it
+  // has waited for its own predecessor. What the previous kernel writes (the
+  // activations) is read only after pdl_wait: by the producer before its
+  // activation copies, by the compute warps before anything else.
   pdl_launch_dependents();
-  pdl_wait();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) unsigned long long full_b[8], empty_b[8];
   __shared__ int abort_flag;
@@ -214,30 +219,14 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       int4 gd = make_int4(0, 0, 0, 0);
       // the weights are read once: their lines leave L2 first
       const uint64_t pol_first = l2_policy_evict_first();
-      for (; n < count; ++n) {
-        walk_next(wk);
-        const int grp = wk.grp, tile = wk.tile, slice = wk.slice;
-        if (grp != gcur) {
-          gd = group_of(grp);
-          gcur = grp;
-        }
-        const int st = n % S, use = n / S;
-        if (use > 0 && !mbar_wait_or_abort(smem_u32(&empty_b[st]), (uint32_t)(use - 1) & 1u,
-                                           &abort_flag)) {
-          if (!abort_flag) fail();
-          break;
-        }
-        if (use > 0) asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        const int nc = min(kSliceChunks, G.NC - slice * kSliceChunks);
+      // the weight tiles and block scales of a unit into stage st
+      auto issue_w = [&](int st, int e_id, int tile, int slice, int nc) {
         const uint32_t dst = stage0 + st * G.stage_bytes;
         const uint32_t bar = smem_u32(&full_b[st]);
-        uint32_t bytes = 2u * nc * (4096 + 64 * G.SB);
-        if (NT == 1) bytes += (uint32_t)(gd.z * nc * G.cbB);
-        mbar_expect_tx(bar, bytes);
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
           const int rt = (ROLE == 0) ? (blk == 0 ? tile : p.I / 64 + tile) : 2 * tile + blk;
-          const size_t ti = (size_t)gd.x * NRT + rt;
+          const size_t ti = (size_t)e_id * NRT + rt;
           bulk_g2s_hint(dst + blk * kXCodeBlock,
                         p.w + ti * tile_codes + (size_t)slice * kSliceChunks * 4096, nc * 4096, bar,
                         pol_first);
@@ -246,11 +235,77 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
                           sb + ti * tile_scales + (size_t)slice * kSliceChunks * 64 * G.SB,
                           nc * 64 * G.SB, bar, pol_first);
         }
+      };
+      // the activation rows of a unit (one token tile) into stage st
+      auto issue_b = [&](int st, int grp, const int4& g4, int slice, int nc) {
+        const uint32_t dst = stage0 + st * G.stage_bytes;
+        const uint32_t bar = smem_u32(&full_b[st]);
+        for (int t = 0; t < g4.z; ++t)
+          bulk_g2s(dst + G.b_off + t * G.RS,
+                   b_row(route_of(grp, g4.y, t)) + (size_t)slice * kSliceChunks * G.cbB, nc * G.cbB,
+                   bar);
+      };
+      // The first S units' weights go out before the wait for the previous
+      // kernel (they depend only on the routing); their activation rows
+      // after it.
+      const int n_early = min(S, count);
+      int e_grp[8], e_slice[8];
+      bool waited = false;
+      for (; n < count; ++n) {
+        walk_next(wk);
+        const int grp = wk.grp, tile = wk.tile, slice = wk.slice;
+        if (grp != gcur) {
+          gd = group_of(grp);
+          gcur = grp;
+        }
+        const int st = n % S, use = n / S;
+        if (n == n_early && !waited) {
+          pdl_wait();
+          waited = true;
+          if (NT == 1) {
+            int gc = -1;
+            int4 g4 = make_int4(0, 0, 0, 0);
+            for (int m = 0; m < n_early; ++m) {
+              if (e_grp[m] != gc) {
+                gc = e_grp[m];
+                g4 = group_of(gc);
+              }
+              issue_b(m, gc, g4, e_slice[m], min(kSliceChunks, G.NC - e_slice[m] * kSliceChunks));
+            }
+          }
+        }
+        if (use > 0 && !mbar_wait_or_abort(smem_u32(&empty_b[st]), (uint32_t)(use - 1) & 1u,
+                                           &abort_flag)) {
+          if (!abort_flag) fail();
+          break;
+        }
+        if (use > 0) asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        const int nc = min(kSliceChunks, G.NC - slice * kSliceChunks);
+        uint32_t bytes = 2u * nc * (4096 + 64 * G.SB);
+        if (NT == 1) bytes += (uint32_t)(gd.z * nc * G.cbB);
+        mbar_expect_tx(smem_u32(&full_b[st]), bytes);
+        issue_w(st, gd.x, tile, slice, nc);
+        if (n < n_early) {
+          e_grp[n] = grp;
+          e_slice[n] = slice;
+        } else if (NT == 1) {
+          issue_b(st, grp, gd, slice, nc);
+        }
+      }
+      if (!waited && n == n_early) {
+        // every unit was early (count <= S)
+        pdl_wait();
+        waited = true;
         if (NT == 1) {
-          for (int t = 0; t < gd.z; ++t)
-            bulk_g2s(dst + G.b_off + t * G.RS,
-                     b_row(route_of(grp, gd.y, t)) + (size_t)slice * kSliceChunks * G.cbB,
-                     nc * G.cbB, bar);
+          int gc = -1;
+          int4 g4 = make_int4(0, 0, 0, 0);
+          for (int m = 0; m < n_early; ++m) {
+            if (e_grp[m] != gc) {
+              gc = e_grp[m];
+              g4 = group_of(gc);
+            }
+            issue_b(m, gc, g4, e_slice[m], min(kSliceChunks, G.NC - e_slice[m] * kSliceChunks));
+          }
         }
       }
       // the copies still in flight must land before the CTA leaves
@@ -266,6 +321,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
   }
 
   // ---------------- compute warps ----------------
+  pdl_wait();  // the activations, partial slots and outputs of the previous kernel
   int grp = 0, tile = 0, slice = 0;
   float acc[NT][4];
 #pragma unroll

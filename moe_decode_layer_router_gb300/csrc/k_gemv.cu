@@ -18,6 +18,8 @@
 // the activation fragments (at most 8 NT tokens) from L1/L2, accumulate
 // with mma.sync (bf16 in, fp32 out) and add their 8 partials in a fixed
 // order in shared memory. Rows and tokens past the end are never stored.
+// For the pooler, the CTA that stores a token block's last tile applies the
+// pre-expert norm to the block's rows (no separate launch, no waiting).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -102,6 +104,9 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
     wv[u] = c < K4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   pdl_wait();  // x may be the previous kernel's output
+  // dependents launch only now: the pooler two launches on reads x without
+  // a wait of its own
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_expect_tx(smem_u32(&xbar), (uint32_t)(ntok * p.K * 2));
     for (int t = 0; t < ntok; ++t)
@@ -153,12 +158,138 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
   }
 }
 
+// Pre-expert RMSNorm (page "vllm.models.muse_spark.nvidia.specialized_decode.
+// runtime.providers", MoEProvider docstring) of the pooled rows [t0, t1) of
+// y, one warp per row: the bf16 h, and the expert operand, h in f16 (exact
+// for |h| in [2^-14, 65504]) or, for FP8 W8A8, e4m3 codes with the per-row
+// dynamic scale amax / 448. A row of at most kNV * 128 elements is held in
+// registers (its loads and its norm weights' issued together); a longer one
+// is read from L2 once per pass.
+constexpr int kNV = 16;
+__device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n4 = p.M / 4;
+  const uint2* wsrc = reinterpret_cast<const uint2*>(p.w_pre_norm);
+  int bad = 0;
+  for (int t = t0 + warp; t < t1; t += kGWarps) {
+    const float4* src = reinterpret_cast<const float4*>(p.y + (size_t)t * p.M);
+    uint2* hdst = reinterpret_cast<uint2*>(p.h + (size_t)t * p.M);
+    // float4 i of the row: its loads, and the bf16 h, (x * rstd) * w rounded
+    auto load = [&](int i, float4& v, uint2& wb) {
+      v = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      wb = (i < n4 && p.pre_norm) ? __ldg(wsrc + i) : make_uint2(0u, 0u);
+    };
+    auto h4 = [&](const float4& x, const uint2& wb, float rstd, float (&hb)[4]) {
+      const float xv[4] = {x.x, x.y, x.z, x.w};
+      const float wv[4] = {bf16_bits_to_f32(wb.x & 0xFFFFu), bf16_bits_to_f32(wb.x >> 16),
+                           bf16_bits_to_f32(wb.y & 0xFFFFu), bf16_bits_to_f32(wb.y >> 16)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) hb[j] = round_bf16(p.pre_norm ? (xv[j] * rstd) * wv[j] : xv[j]);
+    };
+    // stores h (and the f16 operand) of float4 i; returns its amax
+    auto put = [&](int i, const float (&hb)[4]) -> float {
+      uint32_t hbits[2], opbits[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        hbits[c] = f32_to_bf16_bits(hb[2 * c]) | ((uint32_t)f32_to_bf16_bits(hb[2 * c + 1]) << 16);
+        const __half2 h2 = __floats2half2_rn(hb[2 * c], hb[2 * c + 1]);
+        opbits[c] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      float am = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        am = fmaxf(am, fabsf(hb[c]));
+        if (p.quant != kFP8) bad |= !(fabsf(hb[c]) <= 65504.f);
+      }
+      hdst[i] = make_uint2(hbits[0], hbits[1]);
+      if (p.quant != kFP8)
+        reinterpret_cast<uint2*>(p.h_op + (size_t)t * p.M * 2)[i] = make_uint2(opbits[0], opbits[1]);
+      return am;
+    };
+    auto put_q = [&](int i, const float (&hb)[4], float sc) {
+      uint16_t q[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        q[c] = f32x2_to_e4m3x2(sc > 0.f ? hb[2 * c] / sc : 0.f, sc > 0.f ? hb[2 * c + 1] / sc : 0.f);
+      reinterpret_cast<uint32_t*>(p.h_op + (size_t)t * p.M)[i] = (uint32_t)q[0] | ((uint32_t)q[1] << 16);
+    };
+    float ss = 0.f, amax = 0.f;
+    if (n4 <= kNV * 32) {
+      float4 v[kNV];
+      uint2 wb[kNV];
+#pragma unroll
+      for (int j = 0; j < kNV; ++j) load(j * 32 + lane, v[j], wb[j]);
+#pragma unroll
+      for (int j = 0; j < kNV; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+      ss = warp_sum(ss);
+      const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.M + p.norm_eps) : 1.0f;
+#pragma unroll
+      for (int j = 0; j < kNV; ++j) {
+        const int i = j * 32 + lane;
+        if (i < n4) {
+          float hb[4];
+          h4(v[j], wb[j], rstd, hb);
+          amax = fmaxf(amax, put(i, hb));
+        }
+      }
+      if (p.quant == kFP8) {
+        amax = warp_max(amax);
+        const float sc = amax / 448.0f;
+#pragma unroll
+        for (int j = 0; j < kNV; ++j) {
+          const int i = j * 32 + lane;
+          if (i < n4) {
+            float hb[4];
+            h4(v[j], wb[j], rstd, hb);
+            put_q(i, hb, sc);
+          }
+        }
+        if (lane == 0) p.h_scale[t] = sc;
+      }
+    } else {
+      constexpr int kB = 4;  // float4s per lane in flight
+      for (int base = 0; base < n4; base += kB * 32) {
+        float4 v[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int i = base + j * 32 + lane;
+          v[j] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+      }
+      ss = warp_sum(ss);
+      const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.M + p.norm_eps) : 1.0f;
+      for (int pass = 0; pass < (p.quant == kFP8 ? 2 : 1); ++pass) {
+        const float sc = pass ? warp_max(amax) / 448.0f : 0.f;
+        for (int base = 0; base < n4; base += kB * 32) {
+          float4 v[kB];
+          uint2 wb[kB];
+#pragma unroll
+          for (int j = 0; j < kB; ++j) load(base + j * 32 + lane, v[j], wb[j]);
+#pragma unroll
+          for (int j = 0; j < kB; ++j) {
+            const int i = base + j * 32 + lane;
+            if (i >= n4) break;
+            float hb[4];
+            h4(v[j], wb[j], rstd, hb);
+            if (pass == 0) amax = fmaxf(amax, put(i, hb));
+            else put_q(i, hb, sc);
+          }
+        }
+        if (pass == 1 && lane == 0) p.h_scale[t] = sc;
+      }
+    }
+  }
+  if (bad) atomicOr(p.health, kHealthHRange);
+}
+
 // NT = 1: every warp streams its activation boxes ([8 tokens x 64], 16-byte
 // asynchronous copies to the 128-byte-swizzled addresses, issued right after
 // the wait for the previous kernel) through a ring of kGXRing shared-memory
 // slots and reads its B fragments with ldmatrix. NT > 1: the fragments of the next box load from L1/L2 while the
 // current one runs.
-template <int NT>
+template <int NT, bool POOL>
 __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParams& p,
                                          uint8_t* smem_raw) {
   __shared__ __align__(8) unsigned long long warp_b[kGWarps];
@@ -192,7 +323,14 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
       tma_load_3d(wt + w * nch * kGBoxBytes, tw, 0, tile * kGTileRows, w * nch, smem_u32(&warp_b[w]));
     }
   }
-  pdl_wait();  // x may be the previous kernel's output
+  if constexpr (!POOL) {
+    pdl_wait();  // x is the previous kernel's output
+    pdl_launch_dependents();
+  }
+  // The pooler reads x without waiting: x is the router's input, final
+  // before this launch starts (the router signals its dependents only after
+  // its own wait for the kernel that writes x). It waits for the route
+  // kernel before it exits.
 
   const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_u = lane >> 4;
   float acc[NT][4];
@@ -319,18 +457,36 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
         if (globaltimer() - t0 > kWaitLimitNs) break;
     }
   }
+  if constexpr (POOL) {
+    // the CTA that stores a token block's last tile (atomic ticket, no
+    // waiting) normalizes the block's rows
+    __shared__ int last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      last = (atomicAdd(p.norm_ticket + tbk, 1) == tiles - 1);
+      if (last) p.norm_ticket[tbk] = 0;  // for the next launch
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      norm_rows(p, tbk * 8 * NT, min(p.rows, (tbk + 1) * 8 * NT));
+    }
+    // The expert kernel after this one reads the routing before its own
+    // wait: dependents launch only once the route kernel has completed.
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 }
 
-template <int NT>
+template <int NT, bool POOL>
 __global__ void __launch_bounds__(kGThreads)
     k_gemv(const __grid_constant__ CUtensorMap tw, FrontParams p) {
-  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
-  gemv_cta<NT>(&tw, p, smem);
+  gemv_cta<NT, POOL>(&tw, p, smem);
 }
 
 __global__ void __launch_bounds__(kGThreads) k_router(FrontParams p) {
-  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   router_cta(p, blockIdx.x, smem);
 }
@@ -365,13 +521,13 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NT>
+template <int NT, bool POOL>
 cudaError_t launch_t(const FrontParams& p, cudaStream_t s, bool pdl) {
   CUtensorMap tw{};
   cudaError_t e = make_map(&tw, p.w, (uint64_t)p.K, (uint64_t)p.M, (uint32_t)g_chunks_per_warp(p.K));
   if (e != cudaSuccess) return e;
   const size_t smem = g_smem_bytes(p.K, NT);
-  e = cudaFuncSetAttribute(k_gemv<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(k_gemv<NT, POOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.gemv_ctas);
@@ -383,7 +539,7 @@ cudaError_t launch_t(const FrontParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_gemv<NT>, tw, p);
+  return cudaLaunchKernelEx(&cfg, k_gemv<NT, POOL>, tw, p);
 }
 }  // namespace
 
@@ -400,9 +556,9 @@ int front_max_k() { return kGMaxK; }
 cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl) {
   if (p.gemv_ctas == 0) return cudaSuccess;
   switch (nt) {
-    case 1: return launch_t<1>(p, s, pdl);
-    case 2: return launch_t<2>(p, s, pdl);
-    case 4: return launch_t<4>(p, s, pdl);
+    case 1: return p.h ? launch_t<1, true>(p, s, pdl) : launch_t<1, false>(p, s, pdl);
+    case 2: return p.h ? launch_t<2, true>(p, s, pdl) : launch_t<2, false>(p, s, pdl);
+    case 4: return p.h ? launch_t<4, true>(p, s, pdl) : launch_t<4, false>(p, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

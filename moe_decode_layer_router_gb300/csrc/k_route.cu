@@ -1,4 +1,4 @@
-// Routing, pre-expert norm and the token -> expert permute. One CTA per row.
+// Routing and the token -> expert permute.
 //
 // Routing rule (page "vllm.models.muse_spark.amd.muse_moe_runner", class
 // MuseSpark1xRouter, docstring and _compute_routing_native): optional output
@@ -9,15 +9,11 @@
 // (<= 256) selection keys (largest score first, the lower id on equal
 // scores).
 //
-// Pre-expert norm (page "vllm.models.muse_spark.nvidia.specialized_decode.
-// runtime.providers", MoEProvider docstring): RMSNorm of the pooled row with
-// the effective bf16 weight, stored as bf16 h; the expert operand is h in
-// f16 (exact for |h| in [2^-14, 65504]) or, for FP8 W8A8, e4m3 codes with a
-// per-row dynamic scale amax / 448.
+// The routing needs only the router's logits, so the launch runs before the
+// pooler's: the pooler's weight copies overlap it.
 //
-// Permute: the CTA that finishes last (atomic ticket, no waiting) counts the
-// routes per expert and writes them grouped by expert in route order (a
-// stable counting sort), then the token groups the expert kernels walk.
+// Permute: the routes per expert, written grouped by expert in route order
+// (a stable counting sort), then the token groups the expert kernels walk.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -209,143 +205,57 @@ __device__ void permute(const RouteParams& p, int16_t* ids_s, unsigned char* wor
   }
 }
 
-// RMSNorm of the pooled row t with the effective bf16 weight -> bf16 h and
-// the expert operand (f16, or e4m3 + per-row scale for FP8).
-__device__ void pre_norm_row(const RouteParams& p, int t, float* hr, float* scratch) {
-  const int tid = threadIdx.x;
-  constexpr int kV = 4;  // float4s of the row per thread and pass
-  float ss = 0.f;
-  const float4* src = reinterpret_cast<const float4*>(p.h_raw + (size_t)t * p.P);
-  const int n4 = p.P / 4;
-  for (int base = 0; base < n4; base += kV * kRouteThreads) {
-    float4 v[kV];
-#pragma unroll
-    for (int j = 0; j < kV; ++j) {
-      const int i = base + j * kRouteThreads + tid;
-      v[j] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int j = 0; j < kV; ++j) {
-      const int i = base + j * kRouteThreads + tid;
-      if (i < n4) reinterpret_cast<float4*>(hr)[i] = v[j];
-      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-    }
-  }
-  ss = block_sum(ss, scratch);  // also orders the hr[] writes before the reads
-  const float rstd = p.pre_norm ? 1.0f / sqrtf(ss / (float)p.P + p.norm_eps) : 1.0f;
-  float amax = 0.f;
-  int bad = 0;
-  // four elements per thread and step: the norm weights are loaded before
-  // any store of the step
-  for (int i0 = 4 * tid; i0 < p.P; i0 += 4 * kRouteThreads) {
-    float wv[4] = {1.f, 1.f, 1.f, 1.f};
-    if (p.pre_norm) {
-      const uint2 wb = __ldg(reinterpret_cast<const uint2*>(p.w_pre_norm + i0));
-      wv[0] = bf16_bits_to_f32(wb.x & 0xFFFFu);
-      wv[1] = bf16_bits_to_f32(wb.x >> 16);
-      wv[2] = bf16_bits_to_f32(wb.y & 0xFFFFu);
-      wv[3] = bf16_bits_to_f32(wb.y >> 16);
-    }
-    const float4 x = *reinterpret_cast<const float4*>(hr + i0);
-    const float xv[4] = {x.x, x.y, x.z, x.w};
-    float hb[4];
-    uint32_t hbits[2], opbits[2];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float v = xv[j];
-      if (p.pre_norm) v = (v * rstd) * wv[j];
-      hb[j] = round_bf16(v);
-      amax = fmaxf(amax, fabsf(hb[j]));
-      bad |= !(fabsf(hb[j]) <= 65504.f);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      hbits[j] = f32_to_bf16_bits(hb[2 * j]) | ((uint32_t)f32_to_bf16_bits(hb[2 * j + 1]) << 16);
-      const __half2 h2 = __floats2half2_rn(hb[2 * j], hb[2 * j + 1]);
-      opbits[j] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint2*>(p.h + (size_t)t * p.P + i0) = make_uint2(hbits[0], hbits[1]);
-    *reinterpret_cast<float4*>(hr + i0) = make_float4(hb[0], hb[1], hb[2], hb[3]);
-    if (p.quant != kFP8)
-      *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(p.h_op) + (size_t)t * p.P + i0) =
-          make_uint2(opbits[0], opbits[1]);
-  }
-  if (p.quant == kFP8) {
-    amax = block_max(amax, scratch);
-    const float sc = amax / 448.0f;
-    for (int i = 2 * tid; i < p.P; i += 2 * kRouteThreads) {
-      const float a = sc > 0.f ? hr[i] / sc : 0.f;
-      const float b = sc > 0.f ? hr[i + 1] / sc : 0.f;
-      reinterpret_cast<uint16_t*>(p.h_op + (size_t)t * p.P)[i / 2] = f32x2_to_e4m3x2(a, b);
-    }
-    if (tid == 0) p.h_scale[t] = sc;
-    bad = 0;  // the e4m3 operand is scaled: no f16 range limit
-  }
-  if (bad) atomicOr(p.health, kHealthHRange);
-}
-
-// Grid: with p.central, rows + 1 CTAs: CTA `rows` routes every row (one warp
-// per row) and builds the permute from shared memory; CTAs 0..rows-1 normalize
-// their pooled row. Otherwise rows CTAs, each routing and normalizing its
-// row; the CTA that finishes last (atomic ticket, no waiting) builds the
-// permute. Without p.h_raw only the routing runs.
+// Grid: with p.central one CTA routes every row (one warp per row) and
+// builds the permute from shared memory. Otherwise one CTA per 8 rows, one
+// warp per row; the CTA that finishes last (atomic ticket, no waiting)
+// builds the permute.
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams p) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float s_w[kRouteThreads / 32][256];
   __shared__ int top[kRouteThreads / 32][256];
-  __shared__ float scratch[32];
   __shared__ int flag;
   extern __shared__ __align__(16) unsigned char dyn[];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int rt = p.rows * p.k;
+  int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
+  unsigned char* work = dyn + (((size_t)rt * 2 + 15) & ~(size_t)15);
 
   if (p.central) {
-    if ((int)blockIdx.x < p.rows) {
-      if (p.h_raw != nullptr) pre_norm_row(p, blockIdx.x, reinterpret_cast<float*>(dyn), scratch);
-      return;
-    }
-    int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
     const bool perm = p.route_list != nullptr;
     for (int t = wid; t < p.rows; t += kRouteThreads / 32)
       route_row_warp<EPL>(p, t, lane, s_w[wid], top[wid], perm ? ids_s : nullptr);
     if (!perm) return;
     __syncthreads();
-    const int rt = p.rows * p.k;
-    permute(p, ids_s, dyn + (((size_t)rt * 2 + 15) & ~(size_t)15));
+    permute(p, ids_s, work);
     return;
   }
 
-  const int t = blockIdx.x;
-  if (wid == 0) route_row_warp<EPL>(p, t, lane, s_w[0], top[0], nullptr);
-  if (p.h_raw != nullptr) pre_norm_row(p, t, reinterpret_cast<float*>(dyn), scratch);
+  const int t = blockIdx.x * (kRouteThreads / 32) + wid;
+  if (t < p.rows) route_row_warp<EPL>(p, t, lane, s_w[wid], top[wid], nullptr);
   if (p.route_list == nullptr) return;
   // ---- last CTA: permute --------------------------------------------------
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const int prev = atomicAdd(p.counters + kTicket, 1);
-    flag = (prev == p.rows - 1);
+    flag = (prev == (int)gridDim.x - 1);
   }
   __syncthreads();
   if (!flag) return;
   __threadfence();
-  const int rt = p.rows * p.k;
-  int16_t* ids_s = reinterpret_cast<int16_t*>(dyn);
   for (int i = tid; i < rt; i += kRouteThreads) ids_s[i] = (int16_t)__ldcg(p.ids + i);
   __syncthreads();
-  permute(p, ids_s, dyn + (((size_t)rt * 2 + 15) & ~(size_t)15));
+  permute(p, ids_s, work);
 }
 
 static size_t route_dyn_smem(const RouteParams& p) {
-  size_t a = (p.h_raw != nullptr) ? (size_t)p.P * 4 : 0;
-  size_t b = 0;
-  if (p.route_list != nullptr) {
-    const size_t rt = (size_t)p.rows * p.k;
-    const size_t nch = (rt + 31) / 32;
-    b = ((rt * 2 + 15) & ~(size_t)15) + ((rt + 15) & ~(size_t)15) + nch * p.E * 2;
-  }
-  return ((a > b ? a : b) + 15) & ~(size_t)15;
+  if (p.route_list == nullptr) return 16;
+  const size_t rt = (size_t)p.rows * p.k;
+  const size_t nch = (rt + 31) / 32;
+  return ((((rt * 2 + 15) & ~(size_t)15) + ((rt + 15) & ~(size_t)15) + nch * p.E * 2) + 15) &
+         ~(size_t)15;
 }
 
 template <int EPL>
@@ -357,7 +267,7 @@ static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t s, bool pdl
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.central ? p.rows + 1 : p.rows);
+  cfg.gridDim = dim3(p.central ? 1 : (p.rows + kRouteThreads / 32 - 1) / (kRouteThreads / 32));
   cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

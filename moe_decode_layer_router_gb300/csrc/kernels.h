@@ -35,6 +35,15 @@ struct FrontParams {
   int32_t* health;
   int M, K;
   int gemv_ctas;
+  // pooler only (skipped when h == nullptr): the last CTA of each token
+  // block applies the pre-expert RMSNorm to the block's rows of y
+  const uint16_t* w_pre_norm;  // bf16 [M]
+  int pre_norm, quant;
+  float norm_eps;
+  uint16_t* h;          // bf16 [rows, M]
+  uint8_t* h_op;        // f16 [rows, M] (FP4) or e4m3 [rows, M] (FP8)
+  float* h_scale;       // [rows] (FP8)
+  int32_t* norm_ticket; // [token blocks], zero between launches
 };
 cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl);   // GEMV
 cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl);          // router
@@ -42,7 +51,7 @@ int front_gemv_ctas(int M, int rows, int nt);
 int front_ctas_per_sm(int K, int nt);
 int front_max_k();
 
-// ---- route: routing rule + pre-expert norm + token->expert permute ------
+// ---- route: routing rule + token->expert permute ---------------------------
 struct RouteParams {
   const float* logits;      // [rows, E]
   const float* expert_bias;
@@ -55,22 +64,13 @@ struct RouteParams {
   int has_division_eps;
   float division_eps;
   float route_scale;
-  // pre-expert norm (skipped when h_raw == nullptr: routing only)
-  const float* h_raw;  // fp32 [rows, P] pooled rows
-  const uint16_t* w_pre_norm;
-  int P, pre_norm;
-  float norm_eps;
-  int quant;
-  uint16_t* h;      // bf16 [rows, P]
-  uint8_t* h_op;    // f16 [rows, P] (FP4) or e4m3 [rows, P] (FP8)
-  float* h_scale;   // [rows] (FP8)
   // permute (skipped when route_list == nullptr)
   int32_t* route_list;  // [rows*k]
   int32_t* groups;      // [max_groups, 4]: expert, first route slot, ntok, 0
   int32_t* counters;
   int32_t* health;
   int token_group;  // routes per group (8 * NT of the expert kernels)
-  int central;      // 1: one extra CTA routes all rows (rows <= 32)
+  int central;      // 1: one CTA routes every row and permutes (rows <= 32)
 };
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
 

@@ -64,6 +64,7 @@ struct musemoe_handle {
   float *h_raw = nullptr, *u = nullptr;
   float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
   int32_t* expert_tickets[2] = {nullptr, nullptr};
+  int32_t* norm_ticket = nullptr;
   int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
   int32_t* health = nullptr;
   uint16_t *h = nullptr, *moe_out = nullptr, *x_stage = nullptr, *out_stage = nullptr;
@@ -99,6 +100,7 @@ void plan(musemoe_handle* h, Layout& L) {
   L.add(&h->route_list, RT * 4);
   L.add(&h->groups, (size_t)h->max_groups * 16);
   L.add(&h->counters, kNumCounters * 4);
+  L.add(&h->norm_ticket, (R + 7) / 8 * 4);  // one per pooler token block
   L.add(&h->health, 16);
   L.add(&h->act, RT * I * 2);
   if (fp8) {
@@ -220,7 +222,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     return true;
   };
 
-  // 1. router GEMV, then the pooler GEMV (its weight loads overlap the router)
+  // 1. router GEMV
   const int ntf = nt_front(rows);
   FrontParams fp{};
   fp.x = x;
@@ -235,12 +237,19 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fp.M = d.pooled;
   fp.K = d.hidden;
   fp.gemv_ctas = front_gemv_ctas(d.pooled, rows, ntf);
+  fp.w_pre_norm = w->w_pre_norm;
+  fp.pre_norm = h->cfg.pre_expert_norm;
+  fp.quant = h->quant;
+  fp.norm_eps = h->cfg.norm_eps;
+  fp.h = h->h;
+  fp.h_op = h->h_op;
+  fp.h_scale = h->h_scale;
+  fp.norm_ticket = h->norm_ticket;
   before();
   if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
-  before();
-  if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
 
-  // 2. routing + pre-expert norm + permute
+  // 2. routing + permute: it needs only the logits, so it runs before the
+  // pooler, whose weight copies overlap it
   const int nte = nt_expert(rows);
   RouteParams rp{};
   rp.logits = h->logits;
@@ -256,15 +265,6 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   rp.has_division_eps = h->cfg.has_division_eps;
   rp.division_eps = h->cfg.division_eps;
   rp.route_scale = h->cfg.route_scale;
-  rp.h_raw = h->h_raw;
-  rp.w_pre_norm = w->w_pre_norm;
-  rp.P = d.pooled;
-  rp.pre_norm = h->cfg.pre_expert_norm;
-  rp.norm_eps = h->cfg.norm_eps;
-  rp.quant = h->quant;
-  rp.h = h->h;
-  rp.h_op = h->h_op;
-  rp.h_scale = h->h_scale;
   rp.route_list = h->route_list;
   rp.groups = h->groups;
   rp.counters = h->counters;
@@ -273,6 +273,11 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   rp.central = rows <= 32;
   before();
   if (!after(launch_route(rp, s, pdl), "route")) return MUSEMOE_ECUDA;
+
+  // 2b. pooler GEMV; the last CTA of each token block applies the
+  // pre-expert norm to the block's rows
+  before();
+  if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
 
   // 3. w13 + SiLU * up
   ExpertParams ep{};
@@ -516,8 +521,8 @@ size_t musemoe_workspace_bytes(const musemoe_dims* dims, int32_t quant) {
 int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 9 : 8; }
 
 const char* musemoe_kernel_name(int32_t quant, int32_t i) {
-  static const char* fp4[] = {"router", "pool", "route", "w13", "w2", "finalize", "unpool", "boundary"};
-  static const char* fp8[] = {"router", "pool", "route", "w13", "act_quant", "w2", "finalize", "unpool",
+  static const char* fp4[] = {"router", "route", "pool", "w13", "w2", "finalize", "unpool", "boundary"};
+  static const char* fp8[] = {"router", "route", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
                               "boundary"};
   if (quant == kFP8) return (i >= 0 && i < 9) ? fp8[i] : "";
   return (i >= 0 && i < 8) ? fp4[i] : "";

@@ -83,7 +83,7 @@ def test_num_kernels_and_names():
     assert mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4) == 8
     assert mm.musemoe_num_kernels(mm.MUSEMOE_FP8_W8A8) == 9
     names = [mm.musemoe_kernel_name(mm.MUSEMOE_FP8_W8A8, i) for i in range(9)]
-    assert names == ["router", "pool", "route", "w13", "act_quant", "w2", "finalize", "unpool",
+    assert names == ["router", "route", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
                      "boundary"]
 
 
