@@ -179,31 +179,40 @@ __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) 
       v = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       wb = (i < n4 && p.pre_norm) ? __ldg(wsrc + i) : make_uint2(0u, 0u);
     };
-    auto h4 = [&](const float4& x, const uint2& wb, float rstd, float (&hb)[4]) {
+    // (x * rstd) * w rounded to bf16, one conversion per pair: the packed
+    // bits in hbits, the values in hb
+    auto h4 = [&](const float4& x, const uint2& wb, float rstd, float (&hb)[4], uint32_t (&hbits)[2]) {
       const float xv[4] = {x.x, x.y, x.z, x.w};
       const float wv[4] = {bf16_bits_to_f32(wb.x & 0xFFFFu), bf16_bits_to_f32(wb.x >> 16),
                            bf16_bits_to_f32(wb.y & 0xFFFFu), bf16_bits_to_f32(wb.y >> 16)};
+      float v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) hb[j] = round_bf16(p.pre_norm ? (xv[j] * rstd) * wv[j] : xv[j]);
-    };
-    // stores h (and the f16 operand) of float4 i; returns its amax
-    auto put = [&](int i, const float (&hb)[4]) -> float {
-      uint32_t hbits[2], opbits[2];
+      for (int j = 0; j < 4; ++j) v[j] = p.pre_norm ? (xv[j] * rstd) * wv[j] : xv[j];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        hbits[c] = f32_to_bf16_bits(hb[2 * c]) | ((uint32_t)f32_to_bf16_bits(hb[2 * c + 1]) << 16);
-        const __half2 h2 = __floats2half2_rn(hb[2 * c], hb[2 * c + 1]);
-        opbits[c] = *reinterpret_cast<const uint32_t*>(&h2);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * c], v[2 * c + 1]);
+        hbits[c] = *reinterpret_cast<const uint32_t*>(&b2);
+        hb[2 * c] = __uint_as_float(hbits[c] << 16);
+        hb[2 * c + 1] = __uint_as_float(hbits[c] & 0xFFFF0000u);
       }
+    };
+    // stores h (and the f16 operand) of float4 i; returns its amax
+    auto put = [&](int i, const float (&hb)[4], const uint32_t (&hbits)[2]) -> float {
       float am = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        am = fmaxf(am, fabsf(hb[c]));
-        if (p.quant != kFP8) bad |= !(fabsf(hb[c]) <= 65504.f);
-      }
+      for (int c = 0; c < 4; ++c) am = fmaxf(am, fabsf(hb[c]));
       hdst[i] = make_uint2(hbits[0], hbits[1]);
-      if (p.quant != kFP8)
+      if (p.quant != kFP8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) bad |= !(fabsf(hb[c]) <= 65504.f);  // NaN too
+        uint32_t opbits[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const __half2 h2 = __floats2half2_rn(hb[2 * c], hb[2 * c + 1]);
+          opbits[c] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
         reinterpret_cast<uint2*>(p.h_op + (size_t)t * p.M * 2)[i] = make_uint2(opbits[0], opbits[1]);
+      }
       return am;
     };
     auto put_q = [&](int i, const float (&hb)[4], float sc) {
@@ -228,8 +237,9 @@ __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) 
         const int i = j * 32 + lane;
         if (i < n4) {
           float hb[4];
-          h4(v[j], wb[j], rstd, hb);
-          amax = fmaxf(amax, put(i, hb));
+          uint32_t hbits[2];
+          h4(v[j], wb[j], rstd, hb, hbits);
+          amax = fmaxf(amax, put(i, hb, hbits));
         }
       }
       if (p.quant == kFP8) {
@@ -240,7 +250,8 @@ __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) 
           const int i = j * 32 + lane;
           if (i < n4) {
             float hb[4];
-            h4(v[j], wb[j], rstd, hb);
+            uint32_t hbits[2];
+            h4(v[j], wb[j], rstd, hb, hbits);
             put_q(i, hb, sc);
           }
         }
@@ -272,8 +283,9 @@ __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) 
             const int i = base + j * 32 + lane;
             if (i >= n4) break;
             float hb[4];
-            h4(v[j], wb[j], rstd, hb);
-            if (pass == 0) amax = fmaxf(amax, put(i, hb));
+            uint32_t hbits[2];
+            h4(v[j], wb[j], rstd, hb, hbits);
+            if (pass == 0) amax = fmaxf(amax, put(i, hb, hbits));
             else put_q(i, hb, sc);
           }
         }
@@ -312,6 +324,12 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
+  if (POOL && blockIdx.x == 0 && threadIdx.x == 32) {
+    // the norm weights, read by the last CTA of each token block, into L2
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.w_pre_norm),
+                 "r"((uint32_t)(p.M * 2))
+                 : "memory");
+  }
   if (threadIdx.x == 0) {
     // the weight tile does not depend on the previous kernel: load it now,
     // one copy per warp of its nch chunks x 16 rows x 64 (past the end of
@@ -459,19 +477,21 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
   }
   if constexpr (POOL) {
     // the CTA that stores a token block's last tile (atomic ticket, no
-    // waiting) normalizes the block's rows
+    // waiting) normalizes the block's rows: the barrier orders the CTA's y
+    // stores before thread 0's fence and ticket; the last CTA's thread 0
+    // fences after the ticket, and the barrier orders its reads after that
     __shared__ int last;
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
+      __threadfence();
       last = (atomicAdd(p.norm_ticket + tbk, 1) == tiles - 1);
-      if (last) p.norm_ticket[tbk] = 0;  // for the next launch
+      if (last) {
+        p.norm_ticket[tbk] = 0;  // for the next launch
+        __threadfence();
+      }
     }
     __syncthreads();
-    if (last) {
-      __threadfence();
-      norm_rows(p, tbk * 8 * NT, min(p.rows, (tbk + 1) * 8 * NT));
-    }
+    if (last) norm_rows(p, tbk * 8 * NT, min(p.rows, (tbk + 1) * 8 * NT));
     // The expert kernel after this one reads the routing before its own
     // wait: dependents launch only once the route kernel has completed.
     pdl_wait();

@@ -205,6 +205,34 @@ __device__ void permute(const RouteParams& p, int16_t* ids_s, unsigned char* wor
   }
 }
 
+// The permute for at most kRouteThreads routes (and experts): one pass over
+// the ids in shared memory gives each route its slot (routes of lower
+// experts, then earlier routes of its own expert) and each expert its count
+// and first slot; the same stable counting sort as permute().
+__device__ void permute_small(const RouteParams& p, const int16_t* ids_s) {
+  const int tid = threadIdx.x;
+  const int E = p.E, rt = p.rows * p.k;
+  __shared__ int scan_scratch[32];
+  const int my_e = tid < rt ? (int)ids_s[tid] : -1;
+  int rank = 0, cnt = 0, first = 0;
+  for (int r = 0; r < rt; ++r) {
+    const int e2 = ids_s[r];
+    rank += (e2 < my_e) | ((e2 == my_e) & (r < tid));
+    cnt += (e2 == tid);
+    first += (e2 < tid);
+  }
+  if (tid < rt) p.route_list[rank] = tid;
+  const int ng = tid < E ? (cnt + p.token_group - 1) / p.token_group : 0;
+  int gtot;
+  const int goff = block_exclusive_scan(ng, scan_scratch, &gtot);
+  for (int gi = 0, s = 0; s < cnt && tid < E; ++gi, s += p.token_group)
+    reinterpret_cast<int4*>(p.groups)[goff + gi] = make_int4(tid, first + s, min(p.token_group, cnt - s), 0);
+  if (tid == 0) {
+    p.counters[kNumGroups] = gtot;
+    p.counters[kTicket] = 0;
+  }
+}
+
 // Grid: with p.central one CTA routes every row (one warp per row) and
 // builds the permute from shared memory. Otherwise one CTA per 8 rows, one
 // warp per row; the CTA that finishes last (atomic ticket, no waiting)
@@ -228,7 +256,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams p) {
       route_row_warp<EPL>(p, t, lane, s_w[wid], top[wid], perm ? ids_s : nullptr);
     if (!perm) return;
     __syncthreads();
-    permute(p, ids_s, work);
+    if (rt <= kRouteThreads && p.E <= kRouteThreads) permute_small(p, ids_s);
+    else permute(p, ids_s, work);
     return;
   }
 
