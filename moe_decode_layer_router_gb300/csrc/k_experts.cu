@@ -133,8 +133,6 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
   if (b0 > b1) b0 = b1 = U0;  // inside one tile: [u0, u1) is the "next-CTA" part
   const int nM = b1 - b0, nE = U1 - b1;
   const int count = U1 - U0;
-  // the three parts as (first unit, end) in processing order
-  const int part_a[3] = {b0, b1, U0}, part_e[3] = {b1, U1, b0};
   // walks the units in processing order: unit index, its group, tile and
   // slice, and the bounds of its part; divisions only where a part starts
   struct Walk {
@@ -144,13 +142,17 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
     w.part = -1;
     w.left = 0;
   };
+  // the three parts as (first unit, end) in processing order: [b0, b1),
+  // [b1, U1), [U0, b0) (selects, not an indexed array: no local memory)
+  auto part_lo = [&](int i) { return i == 0 ? b0 : (i == 1 ? b1 : U0); };
+  auto part_hi = [&](int i) { return i == 0 ? b1 : (i == 1 ? U1 : b0); };
   auto walk_next = [&](Walk& w) {
     if (w.left == 0) {
       do {
         ++w.part;
-      } while (w.part < 3 && part_e[w.part] <= part_a[w.part]);
-      w.lo = part_a[w.part];
-      w.hi = part_e[w.part];
+      } while (w.part < 3 && part_hi(w.part) <= part_lo(w.part));
+      w.lo = part_lo(w.part);
+      w.hi = part_hi(w.part);
       w.left = w.hi - w.lo;
       w.u = w.lo;
       w.grp = w.u / PG;
@@ -192,11 +194,17 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
   __syncthreads();  // the last CTA-wide barrier
   auto group_of = [&](int grp) -> int4 {
     const int gi = grp - g_first;
-    return gi < kXMeta ? meta_g[gi] : __ldcg(reinterpret_cast<const int4*>(p.groups) + grp);
+    int4 r;
+    if (gi < kXMeta) r = meta_g[gi];
+    else r = __ldcg(reinterpret_cast<const int4*>(p.groups) + grp);
+    return r;
   };
   auto route_of = [&](int grp, int rbase, int n) -> int {
     const int gi = grp - g_first;
-    return gi < kXMeta ? meta_r[gi][n] : __ldcg(p.route_list + rbase + n);
+    int r;
+    if (gi < kXMeta) r = meta_r[gi][n];
+    else r = __ldcg(p.route_list + rbase + n);
+    return r;
   };
   auto b_row = [&](int ro) -> const uint8_t* {  // activation row of route ro
     return p.b + (size_t)(p.b_by_token ? ro / p.k : ro) * p.K * kel;
@@ -249,8 +257,24 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       // kernel (they depend only on the routing); their activation rows
       // after it.
       const int n_early = min(S, count);
-      int e_grp[8], e_slice[8];
       bool waited = false;
+      // after the wait: the activation rows of the early units, found by a
+      // second walk over them
+      auto issue_early_b = [&]() {
+        Walk w2;
+        walk_begin(w2);
+        int gc = -1;
+        int4 g4 = make_int4(0, 0, 0, 0);
+        for (int m = 0; m < n_early; ++m) {
+          walk_next(w2);
+          if (w2.grp != gc) {
+            gc = w2.grp;
+            g4 = group_of(gc);
+          }
+          issue_b(m, gc, g4, w2.slice, min(kSliceChunks, G.NC - w2.slice * kSliceChunks));
+        }
+      };
+      int st = -1, use = 0;  // stage of unit n and how often it was filled before
       for (; n < count; ++n) {
         walk_next(wk);
         const int grp = wk.grp, tile = wk.tile, slice = wk.slice;
@@ -258,21 +282,14 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
           gd = group_of(grp);
           gcur = grp;
         }
-        const int st = n % S, use = n / S;
+        if (++st == S) {
+          st = 0;
+          ++use;
+        }
         if (n == n_early && !waited) {
           pdl_wait();
           waited = true;
-          if (NT == 1) {
-            int gc = -1;
-            int4 g4 = make_int4(0, 0, 0, 0);
-            for (int m = 0; m < n_early; ++m) {
-              if (e_grp[m] != gc) {
-                gc = e_grp[m];
-                g4 = group_of(gc);
-              }
-              issue_b(m, gc, g4, e_slice[m], min(kSliceChunks, G.NC - e_slice[m] * kSliceChunks));
-            }
-          }
+          if (NT == 1) issue_early_b();
         }
         if (use > 0 && !mbar_wait_or_abort(smem_u32(&empty_b[st]), (uint32_t)(use - 1) & 1u,
                                            &abort_flag)) {
@@ -285,28 +302,13 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
         if (NT == 1) bytes += (uint32_t)(gd.z * nc * G.cbB);
         mbar_expect_tx(smem_u32(&full_b[st]), bytes);
         issue_w(st, gd.x, tile, slice, nc);
-        if (n < n_early) {
-          e_grp[n] = grp;
-          e_slice[n] = slice;
-        } else if (NT == 1) {
-          issue_b(st, grp, gd, slice, nc);
-        }
+        if (n >= n_early && NT == 1) issue_b(st, grp, gd, slice, nc);
       }
       if (!waited && n == n_early) {
         // every unit was early (count <= S)
         pdl_wait();
         waited = true;
-        if (NT == 1) {
-          int gc = -1;
-          int4 g4 = make_int4(0, 0, 0, 0);
-          for (int m = 0; m < n_early; ++m) {
-            if (e_grp[m] != gc) {
-              gc = e_grp[m];
-              g4 = group_of(gc);
-            }
-            issue_b(m, gc, g4, e_slice[m], min(kSliceChunks, G.NC - e_slice[m] * kSliceChunks));
-          }
-        }
+        if (NT == 1) issue_early_b();
       }
       // the copies still in flight must land before the CTA leaves
       const int issued = n;
@@ -382,13 +384,18 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
 
   Walk wk;
   walk_begin(wk);
+  int st = -1;          // stage of unit n
+  uint32_t phase = 0u;  // parity of the stage's fill: (n / S) & 1
   for (int n = 0; n < count; ++n) {
     walk_next(wk);
     const int u = wk.u;
     grp = wk.grp;
     tile = wk.tile;
     slice = wk.slice;
-    const int st = n % S;
+    if (++st == S) {
+      st = 0;
+      phase ^= 1u;
+    }
     if (fresh) {
       const int4 gd = group_of(grp);
       e = gd.x;
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       }
     };
     const bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&full_b[st]),
-                                                               (uint32_t)(n / S) & 1u, &abort_flag));
+                                                               phase, &abort_flag));
     if (!ok) {
       if (lane == 0 && !abort_flag) fail();
       break;
