@@ -38,8 +38,8 @@ WEIGHT_SETS = 4
 # DRAM traffic of one launch of the dominant kernel, from the ncu capture
 # summarized in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "c788341bbc8f7f26cbf399451507c5826ad05da1",
-               "bytes_per_launch": 102667776 + 2970624}
+NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "7577fa771b5411edc4d7b1b66efa13eb0f49a681",
+               "bytes_per_launch": 102624000 + 2681344}
 
 
 def _args():
