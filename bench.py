@@ -375,6 +375,33 @@ def bench_ours(args):
     expert_bytes = sum(m["expert_bytes"] for m in model) / len(model)
     expert_ms = kernel_ms["w13"] + kernel_ms["w2"]
 
+    # the attention boundary before the block (a separate entry point, not
+    # part of the step above): one launch on the workload's rows, timed alone
+    ab = synth.attention_boundary_inputs(cfg)
+    ab_t = {k: to_dev(v) for k, v in ab.items()}
+    ab_out = torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16, device=dev)
+    ab_reps = 200
+    with torch.cuda.stream(s):
+        for _ in range(10):
+            mm.musemoe_attention_boundary(ab_t["partial"], ab_t["stream"], ab_out,
+                                          ab_t["w_pre_ffn_norm"], ab_t["gate"], cfg.rows,
+                                          cfg.hidden, cfg.norm_eps, s)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(s)
+        for _ in range(ab_reps):
+            mm.musemoe_attention_boundary(ab_t["partial"], ab_t["stream"], ab_out,
+                                          ab_t["w_pre_ffn_norm"], ab_t["gate"], cfg.rows,
+                                          cfg.hidden, cfg.norm_eps, s)
+        a1.record(s)
+    torch.cuda.synchronize()
+    ab_us = a0.elapsed_time(a1) * 1e3 / ab_reps
+    ab_bytes = 12 * cfg.rows * cfg.hidden + 2 * cfg.hidden
+    attn_boundary = {"us_per_launch": ab_us, "algorithmic_bytes": ab_bytes,
+                     "achieved_gbs": ab_bytes / (ab_us / 1e6) / 1e9,
+                     "frac": ab_bytes / (ab_us / 1e6) / 1e9 / hbm_peak,
+                     "note": f"{ab_reps} back-to-back launches on the same 0.5 MB (L2-warm); "
+                             "latency-bound"}
+
     # end to end through the public API with host buffers
     e2e_steps = max(20, min(2000, args.steps // 10))
     xh, sh = sets[0]["x_host"], sets[0]["stream_host"]
@@ -438,6 +465,7 @@ def bench_ours(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
+        "next": {"attention_boundary": attn_boundary},
     }
     if world > 1:
         import torch.distributed as dist

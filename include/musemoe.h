@@ -244,6 +244,25 @@ musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, int32_t top
                                     int32_t *ids_out, float *weights_out,
                                     musemoe_stream_t stream);
 
+/* Attention boundary, the step before the block (page
+ * "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
+ * AttentionBoundaryProvider docstring; post_attn_norm has no weight: page
+ * "vllm.models.muse_spark.amd.mono.decoder", the weight check of each
+ * layer): stream += gate * RMSNorm(partial) (weightless) into the fp32
+ * residual stream in place, then out = bf16(RMSNorm(stream) * w_pre_ffn_norm),
+ * the block's input x. partial bf16 [rows, hidden] is the o_proj output
+ * already summed over ranks (this library has no all-reduce). gate: one fp32
+ * on the device; w_pre_ffn_norm: the effective bf16 weight [hidden]. Every
+ * pointer is device memory, 16-byte aligned; the caller owns all of them.
+ * hidden a multiple of 4, at most 8192; rows >= 1; eps >= 0. No handle and
+ * no allocation; asynchronous on stream. EINVAL with the reason in
+ * musemoe_last_error(NULL) on bad arguments (nothing launched), ECUDA if the
+ * launch fails. */
+musemoe_status musemoe_attention_boundary(const uint16_t *partial, float *stream_io,
+                                          uint16_t *out, const uint16_t *w_pre_ffn_norm,
+                                          const float *gate, int32_t rows, int32_t hidden,
+                                          float eps, musemoe_stream_t stream);
+
 /* Reads (synchronously) and clears the handle's device health word. Returns
  * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
  * ran out since the last poll (that forward's outputs are invalid),

@@ -23,7 +23,7 @@ __all__ = [
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
-    "musemoe_route_static", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
+    "musemoe_route_static", "musemoe_attention_boundary", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
 ]
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
@@ -65,7 +65,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
-    "musemoe_route_static",
+    "musemoe_route_static", "musemoe_attention_boundary",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
 MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
@@ -108,6 +108,8 @@ def library() -> ctypes.CDLL:
         lib.musemoe_poll_health.argtypes = [c_vp]
         lib.musemoe_route_static.argtypes = [c_i32, c_i32, c_i32, P(Config), c_vp, c_vp, c_vp,
                                              c_i32, c_vp, c_vp, c_vp]
+        lib.musemoe_attention_boundary.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
+                                                   c_f32, c_vp]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int:  # ctypes default
@@ -217,6 +219,16 @@ def musemoe_route_static(hidden: int, experts: int, top_k: int, config: Config, 
     _check(library().musemoe_route_static(hidden, experts, top_k, ctypes.byref(config),
                                           _addr(w_router), _addr(expert_bias), _addr(x), rows,
                                           _addr(ids_out), _addr(weights_out), _stream(stream)))
+
+
+def musemoe_attention_boundary(partial, stream_io, out, w_pre_ffn_norm, gate, rows: int,
+                               hidden: int, eps: float, stream=None) -> None:
+    """The attention boundary before the block (see include/musemoe.h):
+    stream_io += gate * RMSNorm(partial); out = bf16(RMSNorm(stream_io) *
+    w_pre_ffn_norm). Device tensors; no handle."""
+    _check(library().musemoe_attention_boundary(_addr(partial), _addr(stream_io), _addr(out),
+                                                _addr(w_pre_ffn_norm), _addr(gate), rows, hidden,
+                                                eps, _stream(stream)))
 
 
 def make_weights(tensors: dict) -> Weights:

@@ -5,6 +5,10 @@
 // Gated add: stream += gate * post_ffn_norm(u), one scalar gate per layer
 // (the decoder page names add_ffn alpha/beta but prints no formula; this is
 // the plain reading with alpha = 1, beta = gate).
+// The same kernel is the attention boundary (providers page,
+// AttentionBoundaryProvider docstring): the bf16 o_proj output, the
+// weightless post_attn_norm (decoder page: post_attn_norm has no weight), the
+// gated add into the stream and pre_ffn_norm into the bf16 block input.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -12,9 +16,13 @@ namespace musemoe {
 
 constexpr int kBoundaryThreads = 512;
 constexpr int kBoundaryVec = 4;  // float4 columns per thread held in registers
+static_assert(kBoundaryMaxH == kBoundaryThreads * kBoundaryVec * 4, "row held in registers");
 
 // One CTA per row; the row (H <= kBoundaryThreads * kBoundaryVec * 4) lives
 // in registers, every load of the row is issued before the first use.
+// ATTN: the attention boundary's form (bf16 input, weightless first norm);
+// otherwise the FFN boundary's (fp32 input, weighted first norm).
+template <bool ATTN>
 __global__ void __launch_bounds__(kBoundaryThreads) k_boundary(BoundaryParams p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -31,9 +39,17 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_boundary(BoundaryParams p)
   for (int r = 0; r < kBoundaryVec; ++r) {
     const int i = threadIdx.x + r * kBoundaryThreads;
     const bool v = i < H4;
-    u[r] = v ? __ldcg(u4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (ATTN) {
+      const uint2 b = v ? __ldcg(reinterpret_cast<const uint2*>(p.u_bf16 + (size_t)t * p.H) + i)
+                        : make_uint2(0, 0);
+      u[r] = make_float4(bf16_bits_to_f32(b.x & 0xFFFFu), bf16_bits_to_f32(b.x >> 16),
+                         bf16_bits_to_f32(b.y & 0xFFFFu), bf16_bits_to_f32(b.y >> 16));
+      f[r] = make_uint2(0x3F803F80u, 0x3F803F80u);  // weightless: 1.0 in bf16
+    } else {
+      u[r] = v ? __ldcg(u4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      f[r] = v ? wf[i] : make_uint2(0, 0);
+    }
     s0[r] = v ? srow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    f[r] = v ? wf[i] : make_uint2(0, 0);
     nx[r] = v ? wn[i] : make_uint2(0, 0);
   }
   const float gate = __ldg(p.gate);
@@ -85,7 +101,8 @@ cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_boundary, p);
+  if (p.u_bf16 != nullptr) return cudaLaunchKernelEx(&cfg, k_boundary<true>, p);
+  return cudaLaunchKernelEx(&cfg, k_boundary<false>, p);
 }
 
 }  // namespace musemoe

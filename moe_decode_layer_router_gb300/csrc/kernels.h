@@ -124,15 +124,17 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl);
 
 // ---- FFN boundary ------------------------------------------------------------
 struct BoundaryParams {
-  const float* u;     // unpooler output fp32 [rows, H]
-  float* stream;      // fp32 [rows, H], in place
-  uint16_t* out;      // bf16 [rows, H]
-  const uint16_t* w_ffn_norm;
-  const uint16_t* w_next_norm;
+  const float* u;          // unpooler output fp32 [rows, H] (FFN boundary), or
+  const uint16_t* u_bf16;  // the o_proj output bf16 [rows, H] (attention boundary)
+  float* stream;           // fp32 [rows, H], in place
+  uint16_t* out;           // bf16 [rows, H]
+  const uint16_t* w_ffn_norm;   // weight of the first norm; nullptr: weightless
+  const uint16_t* w_next_norm;  // weight of the second norm
   const float* gate;
   int rows, H;
   float eps;
 };
+constexpr int kBoundaryMaxH = 8192;  // the row held in registers
 cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
 
 // ---- weight re-layout ----------------------------------------------------

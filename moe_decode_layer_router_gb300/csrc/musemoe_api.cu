@@ -695,6 +695,41 @@ musemoe_status musemoe_forward_host(musemoe_handle* h, const musemoe_weights* w,
   return MUSEMOE_OK;
 }
 
+musemoe_status musemoe_attention_boundary(const uint16_t* partial, float* stream_io, uint16_t* out,
+                                          const uint16_t* w_pre_ffn_norm, const float* gate,
+                                          int32_t rows, int32_t hidden, float eps,
+                                          musemoe_stream_t stream) {
+  std::vector<std::string> bad;
+  if (rows < 1) bad.push_back(fmt("rows %d < 1", rows));
+  if (hidden < 4 || hidden % 4 || hidden > kBoundaryMaxH)
+    bad.push_back(fmt("hidden %d is not a multiple of 4 in 4..%d", hidden, kBoundaryMaxH));
+  if (!(eps >= 0.f)) bad.push_back("eps < 0");
+  auto need = [&](const void* q, const char* name) {
+    if (!q) bad.push_back(fmt("%s is NULL", name));
+    else if (!aligned16(q)) bad.push_back(fmt("%s is not 16-byte aligned", name));
+  };
+  need(partial, "partial");
+  need(stream_io, "stream_io");
+  need(out, "out");
+  need(w_pre_ffn_norm, "w_pre_ffn_norm");
+  if (!gate) bad.push_back("gate is NULL");
+  if (!bad.empty()) return set_err(nullptr, MUSEMOE_EINVAL, join(bad));
+  BoundaryParams bp{};
+  bp.u_bf16 = partial;
+  bp.stream = stream_io;
+  bp.out = out;
+  bp.w_ffn_norm = nullptr;  // post_attn_norm is weightless
+  bp.w_next_norm = w_pre_ffn_norm;
+  bp.gate = gate;
+  bp.rows = rows;
+  bp.H = hidden;
+  bp.eps = eps;
+  cudaError_t e = launch_boundary(bp, reinterpret_cast<cudaStream_t>(stream), false);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "launch of the attention boundary");
+  return MUSEMOE_OK;
+}
+
 musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
   int32_t word = 0;

@@ -20,7 +20,10 @@ It is a plain, slow, step-by-step restatement of what the pages fix:
 * MXFP4 expert tensor shapes -- page "vllm.models.muse_spark.amd.mono.decoder",
   MonoDims.expert_shapes;
 * FFN boundary (post_ffn_norm, gated add into the fp32 stream in place, next
-  pre-norm to bf16) -- providers page, BoundaryProvider docstring.
+  pre-norm to bf16) -- providers page, BoundaryProvider docstring;
+* attention boundary before the block (weightless post_attn_norm, gated add,
+  pre_ffn_norm to bf16) -- providers page, AttentionBoundaryProvider
+  docstring, and decoder page (post_attn_norm has no weight).
 
 Every value is float64 unless a rounding is named. The rounding points are
 the storage dtypes the pages show: fp32 router logits and routing scores
@@ -421,6 +424,25 @@ def boundary(u: np.ndarray, stream, w_ffn_norm_bf16, gate: float,
     add = rms_norm(u, bf16_to_f64(w_ffn_norm_bf16), eps)
     s_new = round_f32(np.asarray(stream, dtype=np.float64) + float(np.float32(gate)) * add)
     out, c = round_bf16_near(rms_norm(s_new, bf16_to_f64(w_next_norm_bf16), eps), near)
+    if ties is not None:
+        ties["out"] = ties.get("out", 0) + c
+    return s_new, out
+
+
+def attention_boundary(partial_bf16: np.ndarray, stream, gate: float, w_pre_ffn_bf16,
+                       eps: float, near=None, ties=None):
+    """Attention boundary, the step before the block (providers page,
+    AttentionBoundaryProvider docstring): post_attn_norm of the o_proj output
+    ``partial`` (bf16), gated add into the fp32 stream in place, pre_ffn_norm
+    into bf16 out (the block's input x). post_attn_norm has no weight (decoder
+    page: each layer's check rejects a post_attn_norm with a weight). The
+    all-reduce of ``partial`` over ranks is outside this one-GPU path:
+    ``partial`` is the summed output. Reading, as for the FFN boundary: the
+    gated add is stream + gate * post_attn_norm(partial) with one scalar gate.
+    Returns (new stream as fp32 values, out as bf16 values)."""
+    add = rms_norm(bf16_to_f64(partial_bf16), 1.0, eps)
+    s_new = round_f32(np.asarray(stream, dtype=np.float64) + float(np.float32(gate)) * add)
+    out, c = round_bf16_near(rms_norm(s_new, bf16_to_f64(w_pre_ffn_bf16), eps), near)
     if ties is not None:
         ties["out"] = ties.get("out", 0) + c
     return s_new, out

@@ -39,6 +39,7 @@ T_X, T_ROUTER, T_BIAS, T_POOL, T_PRE_NORM = 1, 2, 3, 4, 5
 T_W13, T_W13_SCALE, T_W13_G, T_W2, T_W2_SCALE, T_W2_G = 6, 7, 8, 9, 10, 11
 T_POST_NORM, T_UNPOOL, T_FFN_NORM, T_NEXT_NORM, T_GATE, T_STREAM, T_HOT = (
     12, 13, 14, 15, 16, 17, 18)
+T_PARTIAL, T_PRE_FFN_NORM, T_ATTN_GATE = 19, 20, 21
 
 
 def build(force: bool = False) -> str:
@@ -180,6 +181,20 @@ def activations(cfg: Config, rows: int | None = None):
     x = normal_bf16(cfg.seed, T_X, (b, cfg.hidden))
     stream = normal_f32(cfg.seed, T_STREAM, (b, cfg.hidden))
     return x, stream
+
+
+def attention_boundary_inputs(cfg: Config, rows: int | None = None, hidden: int | None = None):
+    """Inputs of the attention boundary before the block: the o_proj output
+    partial (bf16 N(0,1), [b, H]), the residual stream (fp32 N(0,1)), the
+    pre_ffn_norm weight (bf16 1+N(0,0.05), [H]) and the gate (fp32 U(0.5,1.5))."""
+    b = cfg.rows if rows is None else rows
+    H = cfg.hidden if hidden is None else hidden
+    return {
+        "partial": normal_bf16(cfg.seed, T_PARTIAL, (b, H)),
+        "stream": normal_f32(cfg.seed, T_STREAM, (b, H)),
+        "w_pre_ffn_norm": normal_bf16(cfg.seed, T_PRE_FFN_NORM, (H,), 1.0, 0.05),
+        "gate": uniform_f32(cfg.seed, T_ATTN_GATE, (1,), 0.5, 1.5),
+    }
 
 
 def expert_tensors(cfg: Config, layer: int, e0: int = 0, ne: int | None = None):

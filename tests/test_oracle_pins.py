@@ -421,6 +421,56 @@ def test_boundary_linearity_and_zero_gate():
     np.testing.assert_array_equal(out, O.round_bf16(want))
 
 
+def test_attention_boundary_hand_worked():
+    # partial [1, -1, 1, -1] has RMS 1 (eps 0): the weightless norm leaves it;
+    # stream 0.5 + 2 * partial = [2.5, -1.5, 2.5, -1.5], RMS sqrt(4.25);
+    # 2.5 / sqrt(4.25) = 1.21268 -> bf16 1.2109375 (27/128 above 1, the next
+    # step is 28/128 = 1.21875); -1.5 / sqrt(4.25) = -0.72761 -> bf16
+    # -0.7265625 (186/256; 187/256 = 0.73047 is farther)
+    partial = np.array([[0x3F80, 0xBF80, 0x3F80, 0xBF80]], dtype=np.uint16)
+    stream = np.full((1, 4), 0.5, dtype=np.float32)
+    w = np.full(4, 0x3F80, dtype=np.uint16)
+    s_new, out = O.attention_boundary(partial, stream, 2.0, w, 0.0)
+    np.testing.assert_array_equal(s_new, [[2.5, -1.5, 2.5, -1.5]])
+    np.testing.assert_array_equal(out, [[1.2109375, -0.7265625, 1.2109375, -0.7265625]])
+
+
+def test_attention_boundary_norm_is_weightless_and_scale_free():
+    rng = np.random.default_rng(23)
+    partial = _bf16(rng.standard_normal((3, 64)))
+    w = _bf16(1 + 0.05 * rng.standard_normal(64))
+    zero = np.zeros((3, 64), dtype=np.float32)
+    # gate 1 onto a zero stream: the stream becomes the normalized partial,
+    # mean square 1 per row (eps 0), whatever the pre_ffn_norm weight
+    s_new, _ = O.attention_boundary(partial, zero, 1.0, w, 0.0)
+    np.testing.assert_allclose(np.mean(s_new * s_new, axis=1), 1.0, rtol=1e-6)
+    # x4 is exact in bf16 and the norm removes it
+    p4 = O.f64_to_bf16_bits(4.0 * O.bf16_to_f64(partial))
+    stream = rng.standard_normal((3, 64)).astype(np.float32)
+    a = O.attention_boundary(partial, stream, 0.6, w, 0.0)
+    b = O.attention_boundary(p4, stream, 0.6, w, 0.0)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_attention_boundary_zero_gate_and_unit_weight_ffn_form():
+    rng = np.random.default_rng(29)
+    partial = _bf16(rng.standard_normal((2, 48)))
+    stream = rng.standard_normal((2, 48)).astype(np.float32)
+    w = _bf16(1 + 0.05 * rng.standard_normal(48))
+    s0, out0 = O.attention_boundary(partial, stream, 0.0, w, 1e-6)
+    np.testing.assert_array_equal(s0, stream.astype(np.float64))
+    want = torch.nn.functional.rms_norm(torch.from_numpy(stream.astype(np.float64)), (48,),
+                                        torch.from_numpy(O.bf16_to_f64(w)), eps=1e-6).numpy()
+    np.testing.assert_array_equal(out0, O.round_bf16(want))
+    # the FFN boundary with a unit post-norm weight and the bf16 input as u
+    ones = np.full(48, 0x3F80, dtype=np.uint16)
+    sa, oa = O.attention_boundary(partial, stream, 0.8, w, 1e-6)
+    sf, of = O.boundary(O.bf16_to_f64(partial), stream, ones, 0.8, w, 1e-6)
+    np.testing.assert_array_equal(sa, sf)
+    np.testing.assert_array_equal(oa, of)
+
+
 # ---------------------------------------------------------------- near-tie rounding rule
 
 def test_round_bf16_near_takes_only_values_inside_the_band():
