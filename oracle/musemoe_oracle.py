@@ -24,6 +24,8 @@ It is a plain, slow, step-by-step restatement of what the pages fix:
 * attention boundary before the block (weightless post_attn_norm, gated add,
   pre_ffn_norm to bf16) -- providers page, AttentionBoundaryProvider
   docstring, and decoder page (post_attn_norm has no weight).
+* online rounding of BF16 expert weights to MXFP4 -- page
+  "vllm.models.muse_spark.amd.muse_moe_runner", _quantize_experts_to_mxfp4.
 
 Every value is float64 unless a rounding is named. The rounding points are
 the storage dtypes the pages show: fp32 router logits and routing scores
@@ -129,6 +131,45 @@ def unpack_fp4(packed: np.ndarray) -> np.ndarray:
 
 def e2m1_decode(codes: np.ndarray) -> np.ndarray:
     return E2M1[np.asarray(codes, dtype=np.uint8) & 0x0F]
+
+
+def quantize_mxfp4(w_bf16: np.ndarray):
+    """Round bf16 weights [..., cols] to packed OCP MXFP4: the online rounding
+    of BF16 experts on load (page "vllm.models.muse_spark.amd.muse_moe_runner",
+    _quantize_experts_to_mxfp4, applied to every decoder layer but the first
+    and the last per _online_mxfp4_applies).
+
+    Reading (the page names OCP MXFP4 and a library routine but prints no
+    formula): per block of 32 consecutive elements along cols, the shared
+    scale is 2^(floor(log2(amax)) - 2), 2 being the largest e2m1 exponent, so
+    that amax / scale lies in [4, 8); its exponent is clamped to [-126, 127]
+    (UE8M0 codes 1..254, those the kernel layout accepts); an all-zero block
+    takes 2^0. Each element becomes the e2m1 magnitude nearest |v| / scale,
+    ties to the even code (mantissa bit 0), which saturates at 6; the sign
+    bit is kept (a negative value that rounds to 0 gives code 0x8).
+
+    Returns (codes uint8 [..., cols/2], element 2j in the low nibble of byte
+    j; scales uint8 [..., cols/32])."""
+    v = bf16_to_f64(w_bf16)
+    cols = v.shape[-1]
+    assert cols % 32 == 0
+    blk = v.reshape(v.shape[:-1] + (cols // 32, 32))
+    amax = np.abs(blk).max(axis=-1)
+    _, ex = np.frexp(amax)  # amax = m * 2^ex, m in [0.5, 1): floor(log2) = ex - 1
+    e = np.where(amax > 0, ex - 1 - 2, 0)
+    e = np.clip(e, -126, 127)
+    a = np.abs(blk) / np.ldexp(1.0, e)[..., None]  # exact: a power of two
+    mags = E2M1[:8]
+    d = np.abs(a[..., None] - mags)
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    # among equally near magnitudes (a tie: at most two) take the even code
+    even = cand & ((np.arange(8) & 1) == 0)
+    code = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1))
+    code = code.astype(np.uint8) | (np.signbit(blk).astype(np.uint8) << 3)
+    codes = code.reshape(v.shape)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
 
 
 def ue8m0_decode(s: np.ndarray) -> np.ndarray:

@@ -471,6 +471,66 @@ def test_attention_boundary_zero_gate_and_unit_weight_ffn_form():
     np.testing.assert_array_equal(oa, of)
 
 
+# ---------------------------------------------------------------- online MXFP4 rounding
+
+def _blocks(rows):
+    return O.f64_to_bf16_bits(np.asarray(rows, dtype=np.float64))
+
+
+def test_quantize_mxfp4_hand_worked():
+    # amax 6: floor(log2 6) = 2, scale 2^0 (UE8M0 127); 6 -> code 7, -6 -> 0xF
+    b = np.zeros((1, 32)); b[0, 0], b[0, 1] = 6.0, -6.0
+    packed, scale = O.quantize_mxfp4(_blocks(b))
+    assert scale.tolist() == [[127]] and packed[0, 0] == 0xF7 and not packed[0, 1:].any()
+    # amax 7 keeps scale 2^0; ties go to the even code, 7 saturates at 6:
+    # 0.25->0, 0.75->1.0 (code 2), 1.25->1.0, 1.75->2.0 (4), 2.5->2.0,
+    # 3.5->4.0 (6), 5.0->4.0, 7.0->6.0 (7); 0.3->0.5 (1), -2.9->-3.0 (0xD)
+    row = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 0.3, -2.9] + [0.0] * 22
+    packed, scale = O.quantize_mxfp4(_blocks([row]))
+    codes = O.unpack_fp4(packed)[0, :10].tolist()
+    assert scale.tolist() == [[127]]
+    assert codes == [0, 2, 2, 4, 4, 6, 6, 7, 1, 0xD]
+    # all ones: amax 1 -> scale 2^-2 (UE8M0 125), 1 / 2^-2 = 4 -> code 6
+    packed, scale = O.quantize_mxfp4(_blocks(np.ones((1, 32))))
+    assert scale.tolist() == [[125]] and (O.unpack_fp4(packed) == 6).all()
+    # a zero block takes 2^0; -0.0 keeps its sign bit
+    z = np.zeros((1, 32)); z[0, 3] = -0.0
+    packed, scale = O.quantize_mxfp4(_blocks(z))
+    assert scale.tolist() == [[127]] and O.unpack_fp4(packed)[0, 3] == 8
+    # a subnormal amax (2^-130): exponent -132 clamps to -126 (UE8M0 1), the
+    # element is 2^-4 of the scale and rounds to 0
+    t = np.zeros((1, 32)); t[0, 5] = 2.0 ** -130
+    packed, scale = O.quantize_mxfp4(_blocks(t))
+    assert scale.tolist() == [[1]] and not packed.any()
+
+
+def test_quantize_mxfp4_is_nearest_and_scale_in_range():
+    rng = np.random.default_rng(31)
+    w = _bf16(0.02 * rng.standard_normal((6, 256)))
+    packed, scale = O.quantize_mxfp4(w)
+    v = O.bf16_to_f64(w).reshape(6, 8, 32)
+    sc = O.ue8m0_decode(scale)[..., None]
+    a = np.abs(v) / sc
+    assert (a.max(axis=-1) >= 4).all() and (a.max(axis=-1) < 8).all()
+    q = np.abs(O.e2m1_decode(O.unpack_fp4(packed))).reshape(6, 8, 32)
+    grid = O.E2M1[:8]
+    nearest = np.abs(a[..., None] - grid).min(axis=-1)
+    np.testing.assert_array_equal(np.abs(a - q), nearest)  # no nearer grid value exists
+    assert (np.sign(O.e2m1_decode(O.unpack_fp4(packed))).reshape(6, 8, 32) * np.sign(v) >= 0).all()
+
+
+def test_quantize_mxfp4_round_trips_representable_blocks():
+    rng = np.random.default_rng(37)
+    codes = rng.integers(0, 16, size=(4, 128)).astype(np.uint8)
+    codes[:, ::32] = 7  # one element of magnitude 6 per block fixes the scale
+    exps = rng.integers(110, 140, size=(4, 4)).astype(np.uint8)
+    vals = O.e2m1_decode(codes) * np.repeat(O.ue8m0_decode(exps), 32, axis=1)
+    packed, scale = O.quantize_mxfp4(O.f64_to_bf16_bits(vals))
+    np.testing.assert_array_equal(scale, exps)
+    # codes round-trip bit for bit (-0.0 included: its sign bit is kept)
+    np.testing.assert_array_equal(O.unpack_fp4(packed), codes)
+
+
 # ---------------------------------------------------------------- near-tie rounding rule
 
 def test_round_bf16_near_takes_only_values_inside_the_band():
