@@ -402,6 +402,31 @@ def bench_ours(args):
                      "note": f"{ab_reps} back-to-back launches on the same 0.5 MB (L2-warm); "
                              "latency-bound"}
 
+    # online MXFP4 rounding of bf16 expert weights (load time, not part of
+    # the step): w13 of 32 experts, [32 * 2I, P] bf16 = 256 MB (> L2)
+    q_rows, q_cols = 32 * 2 * cfg.inter, cfg.pooled
+    q_w = to_dev(synth.bf16_expert_weights(cfg, (q_rows, q_cols)))
+    q_codes = torch.empty((q_rows, q_cols // 2), dtype=torch.uint8, device=dev)
+    q_scales = torch.empty((q_rows, q_cols // 32), dtype=torch.uint8, device=dev)
+    q_reps = 20
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            mm.musemoe_quantize_mxfp4(q_w, q_codes, q_scales, q_rows, q_cols, s)
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0.record(s)
+        for _ in range(q_reps):
+            mm.musemoe_quantize_mxfp4(q_w, q_codes, q_scales, q_rows, q_cols, s)
+        q1.record(s)
+    torch.cuda.synchronize()
+    q_us = q0.elapsed_time(q1) * 1e3 / q_reps
+    n_el = q_rows * q_cols
+    q_bytes = 2 * n_el + n_el // 2 + n_el // 32
+    quant_mxfp4 = {"us_per_launch": q_us, "algorithmic_bytes": q_bytes,
+                   "achieved_gbs": q_bytes / (q_us / 1e6) / 1e9,
+                   "frac": q_bytes / (q_us / 1e6) / 1e9 / hbm_peak,
+                   "note": f"w13 of 32 experts [{q_rows}, {q_cols}] bf16, {q_reps} launches"}
+    del q_w, q_codes, q_scales
+
     # end to end through the public API with host buffers
     e2e_steps = max(20, min(2000, args.steps // 10))
     xh, sh = sets[0]["x_host"], sets[0]["stream_host"]
@@ -465,7 +490,7 @@ def bench_ours(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
-        "next": {"attention_boundary": attn_boundary},
+        "next": {"attention_boundary": attn_boundary, "quantize_mxfp4": quant_mxfp4},
     }
     if world > 1:
         import torch.distributed as dist

@@ -263,6 +263,22 @@ musemoe_status musemoe_attention_boundary(const uint16_t *partial, float *stream
                                           const float *gate, int32_t rows, int32_t hidden,
                                           float eps, musemoe_stream_t stream);
 
+/* Online rounding of BF16 expert weights to MXFP4 (page
+ * "vllm.models.muse_spark.amd.muse_moe_runner", _quantize_experts_to_mxfp4,
+ * which rounds the experts of every decoder layer but the first and the
+ * last on load). w_bf16 [rows, cols] bf16 (finite values), cols a multiple
+ * of 32 -> codes [rows, cols/2] (two e2m1 codes per byte, element 2j in the
+ * low nibble) and scales [rows, cols/32] (UE8M0), the plain layout that
+ * musemoe_pack_experts takes as its source. Per block of 32 elements: scale
+ * 2^(floor(log2(amax)) - 2) with the exponent clamped to [-126, 127] (2^0
+ * for an all-zero block); each element the e2m1 value nearest v / scale,
+ * ties to the even code, saturating at +-6, sign kept. Device pointers:
+ * w_bf16 and codes 16-byte aligned; the caller owns them. No handle and no
+ * allocation; asynchronous on stream. EINVAL with the reason in
+ * musemoe_last_error(NULL) on bad arguments, ECUDA if the launch fails. */
+musemoe_status musemoe_quantize_mxfp4(const uint16_t *w_bf16, uint8_t *codes, uint8_t *scales,
+                                      int64_t rows, int32_t cols, musemoe_stream_t stream);
+
 /* Reads (synchronously) and clears the handle's device health word. Returns
  * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
  * ran out since the last poll (that forward's outputs are invalid),

@@ -23,7 +23,8 @@ __all__ = [
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
-    "musemoe_route_static", "musemoe_attention_boundary", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
+    "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
+    "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
 ]
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
@@ -65,7 +66,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
-    "musemoe_route_static", "musemoe_attention_boundary",
+    "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
 MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
@@ -110,6 +111,7 @@ def library() -> ctypes.CDLL:
                                              c_i32, c_vp, c_vp, c_vp]
         lib.musemoe_attention_boundary.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                                                    c_f32, c_vp]
+        lib.musemoe_quantize_mxfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int:  # ctypes default
@@ -229,6 +231,13 @@ def musemoe_attention_boundary(partial, stream_io, out, w_pre_ffn_norm, gate, ro
     _check(library().musemoe_attention_boundary(_addr(partial), _addr(stream_io), _addr(out),
                                                 _addr(w_pre_ffn_norm), _addr(gate), rows, hidden,
                                                 eps, _stream(stream)))
+
+
+def musemoe_quantize_mxfp4(w_bf16, codes, scales, rows: int, cols: int, stream=None) -> None:
+    """Online rounding of bf16 weights [rows, cols] to MXFP4 codes
+    [rows, cols/2] and UE8M0 scales [rows, cols/32] (see include/musemoe.h)."""
+    _check(library().musemoe_quantize_mxfp4(_addr(w_bf16), _addr(codes), _addr(scales), rows,
+                                            cols, _stream(stream)))
 
 
 def make_weights(tensors: dict) -> Weights:

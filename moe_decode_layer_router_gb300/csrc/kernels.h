@@ -137,6 +137,12 @@ struct BoundaryParams {
 constexpr int kBoundaryMaxH = 8192;  // the row held in registers
 cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
 
+// ---- online rounding of bf16 weights to MXFP4 ------------------------------
+// elements = rows * cols with cols a multiple of 32: codes [rows, cols/2],
+// scales [rows, cols/32]; w 16-byte aligned, codes 4-byte aligned.
+cudaError_t launch_quant_mxfp4(const uint16_t* w, uint8_t* codes, uint8_t* scales,
+                               long long elements, int sms, cudaStream_t s);
+
 // ---- weight re-layout ----------------------------------------------------
 // Kernel layout of a [rows, row_bytes] expert tensor cut into cb-byte chunks
 // (cb = 64 for codes, the scale bytes of one code chunk for scales): tiles of

@@ -730,6 +730,27 @@ musemoe_status musemoe_attention_boundary(const uint16_t* partial, float* stream
   return MUSEMOE_OK;
 }
 
+musemoe_status musemoe_quantize_mxfp4(const uint16_t* w_bf16, uint8_t* codes, uint8_t* scales,
+                                      int64_t rows, int32_t cols, musemoe_stream_t stream) {
+  std::vector<std::string> bad;
+  if (rows < 1) bad.push_back(fmt("rows %lld < 1", (long long)rows));
+  if (cols < 32 || cols % 32) bad.push_back(fmt("cols %d is not a positive multiple of 32", cols));
+  if (!w_bf16) bad.push_back("w_bf16 is NULL");
+  else if (!aligned16(w_bf16)) bad.push_back("w_bf16 is not 16-byte aligned");
+  if (!codes) bad.push_back("codes is NULL");
+  else if (!aligned16(codes)) bad.push_back("codes is not 16-byte aligned");
+  if (!scales) bad.push_back("scales is NULL");
+  if (!bad.empty()) return set_err(nullptr, MUSEMOE_EINVAL, join(bad));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = launch_quant_mxfp4(w_bf16, codes, scales, (long long)rows * cols, sms,
+                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "launch of the MXFP4 rounding");
+  return MUSEMOE_OK;
+}
+
 musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
   int32_t word = 0;

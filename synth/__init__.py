@@ -40,6 +40,7 @@ T_W13, T_W13_SCALE, T_W13_G, T_W2, T_W2_SCALE, T_W2_G = 6, 7, 8, 9, 10, 11
 T_POST_NORM, T_UNPOOL, T_FFN_NORM, T_NEXT_NORM, T_GATE, T_STREAM, T_HOT = (
     12, 13, 14, 15, 16, 17, 18)
 T_PARTIAL, T_PRE_FFN_NORM, T_ATTN_GATE = 19, 20, 21
+T_W_BF16 = 22  # bf16 expert weights (online MXFP4 rounding)
 
 
 def build(force: bool = False) -> str:
@@ -195,6 +196,12 @@ def attention_boundary_inputs(cfg: Config, rows: int | None = None, hidden: int 
         "w_pre_ffn_norm": normal_bf16(cfg.seed, T_PRE_FFN_NORM, (H,), 1.0, 0.05),
         "gate": uniform_f32(cfg.seed, T_ATTN_GATE, (1,), 0.5, 1.5),
     }
+
+
+def bf16_expert_weights(cfg: Config, shape, std: float = 0.02, start: int = 0):
+    """BF16 expert weights of the given shape (N(0, std)), as the BF16 edge
+    layers hold them before any rounding."""
+    return normal_bf16(cfg.seed, T_W_BF16, shape, 0.0, std, start=start)
 
 
 def expert_tensors(cfg: Config, layer: int, e0: int = 0, ne: int | None = None):

@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"\b(musemoe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(musemoe_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
