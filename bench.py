@@ -94,8 +94,7 @@ def algorithmic_bytes(cfg, ids_list):
     for ids in ids_list:
         active = len(np.unique(ids))
         per.append({
-            "router": E * H * 4 + b * H * 2 + b * E * 4,
-            "route": b * E * 4 + E * 4 + routes * 12,
+            "router": E * H * 4 + b * H * 2 + b * E * 4 + b * E * 4 + E * 4 + routes * 12,
             "pool": P * H * 2 + b * H * 2 + b * P * 4 + P * 2 + 2 * b * P * 2,
             "w13": active * w13_e + b * P * 2 + routes * I * 2,
             "w2": active * w2_e + routes * I * 2 + routes * P * 4,

@@ -159,7 +159,7 @@ size_t musemoe_workspace_bytes(const musemoe_dims *dims, int32_t quant);
 
 /* Kernels one musemoe_forward launches for this quant (for taps->events). */
 int32_t musemoe_num_kernels(int32_t quant);
-/* Name of kernel i of the forward ("router", "route", "pool", "w13", ...). */
+/* Name of kernel i of the forward ("router", "pool", "w13", ...). */
 const char *musemoe_kernel_name(int32_t quant, int32_t i);
 
 /* Re-lays the expert tensors from their plain layout into the kernel layout

@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "pipeline.cuh"
+#include "route_dev.cuh"
 
 namespace musemoe {
 
@@ -81,6 +82,64 @@ __device__ __forceinline__ uint32_t swz(int r, int u) { return r * 128 + ((u ^ (
 // accumulates its columns for every token, and the CTA adds its threads'
 // sums (warp shuffles, then the 8 warps in order).
 constexpr int kRouterCols = 8;  // float4 columns per thread: K <= 8192
+static_assert(kGThreads == kRouteThreads, "the route tail runs the route kernel's block code");
+
+// Route tail of a router CTA (forward chain): after its logits, the CTA that
+// stores the last expert of an 8-token block (atomic ticket, no waiting)
+// routes the block's rows, one warp per row; the block that finishes last
+// builds the permute (a single block does it at once, from the ids it keeps
+// in shared memory). The routing needs nothing else, so it completes with
+// the router's launch.
+template <int EPL>
+__device__ __noinline__ void router_route_tail(const FrontParams& p, int tb, int t0, int ntok,
+                                               const float* bias_s, uint8_t* smem) {
+  __shared__ float s_w[kGWarps][256];
+  __shared__ int top[kGWarps][256];
+  __shared__ int last_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const RouteParams& rp = p.route;
+  __syncthreads();  // orders the CTA's logits stores before thread 0's fence and ticket
+  if (tid == 0) {
+    __threadfence();
+    last_s = atomicAdd(p.route_ticket + tb, 1) == p.E - 1;
+    if (last_s) {
+      p.route_ticket[tb] = 0;  // for the next launch
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!last_s) return;
+  const int nblk = (rp.rows + 7) / 8;
+  const int rt = rp.rows * rp.k;
+  int16_t* ids_s = reinterpret_cast<int16_t*>(smem);  // the input rows' staging, done with
+  unsigned char* work = smem + (((size_t)rt * 2 + 15) & ~(size_t)15);
+  if (nblk == 1) {
+    // one token block: its rows' ids stay in shared memory for the permute
+    if (warp < ntok) route_row_warp<EPL>(rp, t0 + warp, lane, s_w[warp], top[warp], ids_s, bias_s);
+    __syncthreads();
+    if (rt <= kRouteThreads && rp.E <= kRouteThreads) permute_small(rp, ids_s);
+    else permute(rp, ids_s, work);
+    return;
+  }
+  if (warp < ntok) route_row_warp<EPL>(rp, t0 + warp, lane, s_w[warp], top[warp], nullptr, bias_s);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    last_s = atomicAdd(p.route_done, 1) == nblk - 1;
+    if (last_s) {
+      *p.route_done = 0;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!last_s) return;
+  for (int i = tid; i < rt; i += kGThreads) ids_s[i] = (int16_t)__ldcg(rp.ids + i);
+  __syncthreads();
+  if (rt <= kRouteThreads && rp.E <= kRouteThreads) permute_small(rp, ids_s);
+  else permute(rp, ids_s, work);
+}
+
+template <int EPL>
 __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8_t* smem) {
   __shared__ float red[kGWarps][8];
   __shared__ __align__(8) unsigned long long xbar;
@@ -95,7 +154,11 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
-  // the weight row does not depend on the previous kernel
+  // the weight row (and, for the route tail, the selection bias) does not
+  // depend on the previous kernel
+  __shared__ float bias_s[256];
+  if (p.route_tail)
+    for (int i = threadIdx.x; i < p.E; i += kGThreads) bias_s[i] = __ldg(p.route.expert_bias + i);
   const float4* wr = reinterpret_cast<const float4*>(p.w_router + (size_t)e * p.K);
   float4 wv[kRouterCols];
 #pragma unroll
@@ -156,6 +219,7 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
     while (!mbar_try_wait(smem_u32(&xbar), 0u))
       if (globaltimer() - tw0 > kWaitLimitNs) break;
   }
+  if (p.route_tail) router_route_tail<EPL>(p, task / p.E, t0, ntok, bias_s, smem);
 }
 
 // Pre-expert RMSNorm (page "vllm.models.muse_spark.nvidia.specialized_decode.
@@ -491,11 +555,13 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
       }
     }
     __syncthreads();
-    if (last) norm_rows(p, tbk * 8 * NT, min(p.rows, (tbk + 1) * 8 * NT));
     // The expert kernel after this one reads the routing before its own
-    // wait: dependents launch only once the route kernel has completed.
+    // wait: dependents launch only once the router (which routes in its
+    // tail) has completed, and before the norm, so that the expert kernel's
+    // weight copies overlap it.
     pdl_wait();
     pdl_launch_dependents();
+    if (last) norm_rows(p, tbk * 8 * NT, min(p.rows, (tbk + 1) * 8 * NT));
   }
 }
 
@@ -506,9 +572,10 @@ __global__ void __launch_bounds__(kGThreads)
   gemv_cta<NT, POOL>(&tw, p, smem);
 }
 
+template <int EPL>
 __global__ void __launch_bounds__(kGThreads) k_router(FrontParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  router_cta(p, blockIdx.x, smem);
+  router_cta<EPL>(p, blockIdx.x, smem);
 }
 
 // ---- host ------------------------------------------------------------------
@@ -583,12 +650,18 @@ cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl)
   }
 }
 
-cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl) {
-  if (p.router_ctas == 0) return cudaSuccess;
-  if (p.K / 4 > kRouterCols * kGThreads) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)8 * p.K * 2;  // the 8 tokens' input rows
+template <int EPL>
+static cudaError_t launch_router_t(const FrontParams& p, cudaStream_t s, bool pdl) {
+  size_t smem = (size_t)8 * p.K * 2;  // the 8 tokens' input rows
+  if (p.route_tail) {
+    // the route tail reuses it for the permute: ids, ranks, per-chunk histograms
+    const size_t rt = (size_t)p.route.rows * p.route.k, nch = (rt + 31) / 32;
+    const size_t need = ((rt * 2 + 15) & ~(size_t)15) + ((rt + 15) & ~(size_t)15) + nch * p.E * 2;
+    smem = std::max(smem, (need + 15) & ~(size_t)15);
+  }
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_router<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -601,7 +674,16 @@ cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_router, p);
+  return cudaLaunchKernelEx(&cfg, k_router<EPL>, p);
+}
+
+cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl) {
+  if (p.router_ctas == 0) return cudaSuccess;
+  if (p.K / 4 > kRouterCols * kGThreads) return cudaErrorInvalidValue;
+  if (p.E <= 32) return launch_router_t<1>(p, s, pdl);
+  if (p.E <= 64) return launch_router_t<2>(p, s, pdl);
+  if (p.E <= 128) return launch_router_t<4>(p, s, pdl);
+  return launch_router_t<8>(p, s, pdl);
 }
 
 }  // namespace musemoe

@@ -17,6 +17,27 @@ enum Counter : int { kNumGroups = 0, kTicket = 1, kNumCounters = 8 };
 // health bits
 enum Health : int { kHealthHRange = 1, kHealthActRange = 2, kHealthTimeout = 4 };
 
+// ---- route: routing rule + token->expert permute ---------------------------
+struct RouteParams {
+  const float* logits;      // [rows, E]
+  const float* expert_bias;
+  int32_t* ids;             // [rows, k]
+  float* weights;           // [rows, k]
+  int rows, E, k;
+  int score;  // 0 sigmoid, 1 softmax
+  int has_multiplier;
+  float multiplier;
+  int has_division_eps;
+  float division_eps;
+  float route_scale;
+  // permute (skipped when route_list == nullptr)
+  int32_t* route_list;  // [rows*k]
+  int32_t* groups;      // [max_groups, 4]: expert, first route slot, ntok, 0
+  int32_t* counters;
+  int32_t* health;
+  int token_group;  // routes per group (8 * NT of the expert kernels)
+  int central;      // 1: one CTA routes every row and permutes (rows <= 32)
+};
 // ---- router GEMV (fp32 FFMA) and pooler / unpooler GEMV ------------------
 // The router runs router_ctas = E * ceil(rows / 8) CTAs, one per (expert,
 // 8-token block), each over the whole reduction. The bf16 GEMV Y = X W^T
@@ -44,6 +65,12 @@ struct FrontParams {
   uint8_t* h_op;        // f16 [rows, M] (FP4) or e4m3 [rows, M] (FP8)
   float* h_scale;       // [rows] (FP8)
   int32_t* norm_ticket; // [token blocks], zero between launches
+  // router only (route_tail != 0): the last router CTA of each 8-token block
+  // routes the block's rows, and the last block to finish builds the permute
+  int route_tail;
+  RouteParams route;
+  int32_t* route_ticket;  // [8-token blocks], zero between launches
+  int32_t* route_done;    // [1], zero between launches
 };
 cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl);   // GEMV
 cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl);          // router
@@ -51,27 +78,6 @@ int front_gemv_ctas(int M, int rows, int nt);
 int front_ctas_per_sm(int K, int nt);
 int front_max_k();
 
-// ---- route: routing rule + token->expert permute ---------------------------
-struct RouteParams {
-  const float* logits;      // [rows, E]
-  const float* expert_bias;
-  int32_t* ids;             // [rows, k]
-  float* weights;           // [rows, k]
-  int rows, E, k;
-  int score;  // 0 sigmoid, 1 softmax
-  int has_multiplier;
-  float multiplier;
-  int has_division_eps;
-  float division_eps;
-  float route_scale;
-  // permute (skipped when route_list == nullptr)
-  int32_t* route_list;  // [rows*k]
-  int32_t* groups;      // [max_groups, 4]: expert, first route slot, ntok, 0
-  int32_t* counters;
-  int32_t* health;
-  int token_group;  // routes per group (8 * NT of the expert kernels)
-  int central;      // 1: one CTA routes every row and permutes (rows <= 32)
-};
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
 
 // ---- routed experts --------------------------------------------------------

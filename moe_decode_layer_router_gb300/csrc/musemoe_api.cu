@@ -65,6 +65,7 @@ struct musemoe_handle {
   float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
   int32_t* expert_tickets[2] = {nullptr, nullptr};
   int32_t* norm_ticket = nullptr;
+  int32_t *route_ticket = nullptr, *route_done = nullptr;
   int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
   int32_t* health = nullptr;
   uint16_t *h = nullptr, *moe_out = nullptr, *x_stage = nullptr, *out_stage = nullptr;
@@ -101,6 +102,8 @@ void plan(musemoe_handle* h, Layout& L) {
   L.add(&h->groups, (size_t)h->max_groups * 16);
   L.add(&h->counters, kNumCounters * 4);
   L.add(&h->norm_ticket, (R + 7) / 8 * 4);  // one per pooler token block
+  L.add(&h->route_ticket, (R + 7) / 8 * 4);  // one per router token block
+  L.add(&h->route_done, 4);
   L.add(&h->health, 16);
   L.add(&h->act, RT * I * 2);
   if (fp8) {
@@ -222,8 +225,10 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     return true;
   };
 
-  // 1. router GEMV
+  // 1. router GEMV; its tail routes each 8-token block and builds the
+  // permute (the last CTA of a block, then the last block: no waiting)
   const int ntf = nt_front(rows);
+  const int nte = nt_expert(rows);
   FrontParams fp{};
   fp.x = x;
   fp.rows = rows;
@@ -245,13 +250,10 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fp.h_op = h->h_op;
   fp.h_scale = h->h_scale;
   fp.norm_ticket = h->norm_ticket;
-  before();
-  if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
-
-  // 2. routing + permute: it needs only the logits, so it runs before the
-  // pooler, whose weight copies overlap it
-  const int nte = nt_expert(rows);
-  RouteParams rp{};
+  fp.route_tail = 1;
+  fp.route_ticket = h->route_ticket;
+  fp.route_done = h->route_done;
+  RouteParams& rp = fp.route;
   rp.logits = h->logits;
   rp.expert_bias = w->expert_bias;
   rp.ids = h->ids;
@@ -270,12 +272,12 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   rp.counters = h->counters;
   rp.health = h->health;
   rp.token_group = 8 * nte;
-  rp.central = rows <= 32;
+  rp.central = 0;
   before();
-  if (!after(launch_route(rp, s, pdl), "route")) return MUSEMOE_ECUDA;
+  if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
 
-  // 2b. pooler GEMV; the last CTA of each token block applies the
-  // pre-expert norm to the block's rows
+  // 2. pooler GEMV (its weight copies overlap the router); the last CTA of
+  // each token block applies the pre-expert norm to the block's rows
   before();
   if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
 
@@ -518,14 +520,14 @@ size_t musemoe_workspace_bytes(const musemoe_dims* dims, int32_t quant) {
   return L.off;
 }
 
-int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 9 : 8; }
+int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 8 : 7; }
 
 const char* musemoe_kernel_name(int32_t quant, int32_t i) {
-  static const char* fp4[] = {"router", "route", "pool", "w13", "w2", "finalize", "unpool", "boundary"};
-  static const char* fp8[] = {"router", "route", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
+  static const char* fp4[] = {"router", "pool", "w13", "w2", "finalize", "unpool", "boundary"};
+  static const char* fp8[] = {"router", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
                               "boundary"};
-  if (quant == kFP8) return (i >= 0 && i < 9) ? fp8[i] : "";
-  return (i >= 0 && i < 8) ? fp4[i] : "";
+  if (quant == kFP8) return (i >= 0 && i < 8) ? fp8[i] : "";
+  return (i >= 0 && i < 7) ? fp4[i] : "";
 }
 
 musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const uint8_t* w13_src,

@@ -80,10 +80,10 @@ def test_health_reports_fp16_operand_overflow_and_clears():
 
 
 def test_num_kernels_and_names():
-    assert mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4) == 8
-    assert mm.musemoe_num_kernels(mm.MUSEMOE_FP8_W8A8) == 9
-    names = [mm.musemoe_kernel_name(mm.MUSEMOE_FP8_W8A8, i) for i in range(9)]
-    assert names == ["router", "route", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
+    assert mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4) == 7
+    assert mm.musemoe_num_kernels(mm.MUSEMOE_FP8_W8A8) == 8
+    names = [mm.musemoe_kernel_name(mm.MUSEMOE_FP8_W8A8, i) for i in range(8)]
+    assert names == ["router", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
                      "boundary"]
 
 
