@@ -557,10 +557,13 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
     __syncthreads();
     // The expert kernel after this one reads the routing before its own
     // wait: dependents launch only once the router (which routes in its
-    // tail) has completed, and before the norm, so that the expert kernel's
-    // weight copies overlap it.
-    pdl_wait();
-    pdl_launch_dependents();
+    // tail) has completed. In the CTA that applies the norm only warp 0
+    // waits and signals (then normalizes its rows): the norm reads nothing
+    // the router writes, and the expert kernel's weight copies overlap it.
+    if (!last || warp == 0) {
+      pdl_wait();
+      pdl_launch_dependents();
+    }
     if (last) norm_rows(p, tbk * 8 * NT, min(p.rows, (tbk + 1) * 8 * NT));
   }
 }
