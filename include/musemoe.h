@@ -279,6 +279,17 @@ musemoe_status musemoe_attention_boundary(const uint16_t *partial, float *stream
 musemoe_status musemoe_quantize_mxfp4(const uint16_t *w_bf16, uint8_t *codes, uint8_t *scales,
                                       int64_t rows, int32_t cols, musemoe_stream_t stream);
 
+/* Health self-test: runs the library's two bounded waits once on the
+ * handle's device, each on something nothing ever completes (an mbarrier
+ * phase, as a stage whose weight copies never land; a flag, as a split
+ * tile's owner waiting for a partial that never comes). Each gives up after
+ * its limit (200 ms) and records the timeout in the health word exactly as a
+ * forward would, so the next musemoe_poll_health returns MUSEMOE_ETIMEOUT
+ * and the context stays usable. For checking the failure path of a
+ * deployment; synchronizes the stream; not concurrent with forwards on the
+ * same handle. */
+musemoe_status musemoe_health_selftest(musemoe_handle *handle, musemoe_stream_t stream);
+
 /* Reads (synchronously) and clears the handle's device health word. Returns
  * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
  * ran out since the last poll (that forward's outputs are invalid),

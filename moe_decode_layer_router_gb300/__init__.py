@@ -24,7 +24,7 @@ __all__ = [
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
-    "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
+    "musemoe_health_selftest", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
 ]
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
@@ -67,6 +67,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
+    "musemoe_health_selftest",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
 MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
@@ -112,6 +113,7 @@ def library() -> ctypes.CDLL:
         lib.musemoe_attention_boundary.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                                                    c_f32, c_vp]
         lib.musemoe_quantize_mxfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
+        lib.musemoe_health_selftest.argtypes = [c_vp, c_vp]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int:  # ctypes default
@@ -231,6 +233,12 @@ def musemoe_attention_boundary(partial, stream_io, out, w_pre_ffn_norm, gate, ro
     _check(library().musemoe_attention_boundary(_addr(partial), _addr(stream_io), _addr(out),
                                                 _addr(w_pre_ffn_norm), _addr(gate), rows, hidden,
                                                 eps, _stream(stream)))
+
+
+def musemoe_health_selftest(handle, stream=None) -> None:
+    """Runs the library's bounded waits on things nothing completes; the next
+    musemoe_poll_health returns MUSEMOE_ETIMEOUT (see include/musemoe.h)."""
+    _check(library().musemoe_health_selftest(handle, _stream(stream)), handle)
 
 
 def musemoe_quantize_mxfp4(w_bf16, codes, scales, rows: int, cols: int, stream=None) -> None:

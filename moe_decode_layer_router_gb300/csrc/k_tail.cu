@@ -3,8 +3,40 @@
 // weighting and sum over the k routes of each token.
 #include "common.cuh"
 #include "kernels.h"
+#include "pipeline.cuh"
 
 namespace musemoe {
+
+// ---- health self-test -----------------------------------------------------
+// The library's two bounded waits, each on something nothing completes: an
+// mbarrier phase (as a stage whose copies never land) and a flag (as a split
+// tile's owner waiting for a partial that never comes). Each gives up after
+// kWaitLimitNs and records the timeout in the health word, as a forward
+// would; no copy is in flight, so the CTA leaves cleanly.
+__global__ void k_wait_selftest(int32_t* health, const int32_t* never) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  if (!mbar_wait_or_abort(smem_u32(&bar), 0u, &abort_flag)) atomicOr(health, kHealthTimeout);
+  int v = 0;
+  const unsigned long long t0 = globaltimer();
+  do {
+    __nanosleep(256);
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(never) : "memory");
+  } while (v == 0 && globaltimer() - t0 <= kWaitLimitNs);
+  if (v == 0) atomicOr(health, kHealthTimeout);
+}
+
+cudaError_t launch_wait_selftest(int32_t* health, const int32_t* never, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(health, never);
+  return cudaGetLastError();
+}
 
 // ---- FP8: per-route dynamic quantization of the bf16 activation ------------
 __global__ void __launch_bounds__(256) k_act_quant(ActQuantParams p) {

@@ -143,6 +143,9 @@ struct BoundaryParams {
 constexpr int kBoundaryMaxH = 8192;  // the row held in registers
 cudaError_t launch_boundary(const BoundaryParams& p, cudaStream_t s, bool pdl);
 
+// ---- health self-test: the bounded waits time out into the health word -----
+cudaError_t launch_wait_selftest(int32_t* health, const int32_t* never, cudaStream_t s);
+
 // ---- online rounding of bf16 weights to MXFP4 ------------------------------
 // elements = rows * cols with cols a multiple of 32: codes [rows, cols/2],
 // scales [rows, cols/32]; w 16-byte aligned, codes 4-byte aligned.

@@ -66,6 +66,7 @@ struct musemoe_handle {
   int32_t* expert_tickets[2] = {nullptr, nullptr};
   int32_t* norm_ticket = nullptr;
   int32_t *route_ticket = nullptr, *route_done = nullptr;
+  int32_t* never_set = nullptr;  // zero for good: the health self-test's flag
   int32_t *ids = nullptr, *route_list = nullptr, *groups = nullptr, *counters = nullptr;
   int32_t* health = nullptr;
   uint16_t *h = nullptr, *moe_out = nullptr, *x_stage = nullptr, *out_stage = nullptr;
@@ -104,6 +105,7 @@ void plan(musemoe_handle* h, Layout& L) {
   L.add(&h->norm_ticket, (R + 7) / 8 * 4);  // one per pooler token block
   L.add(&h->route_ticket, (R + 7) / 8 * 4);  // one per router token block
   L.add(&h->route_done, 4);
+  L.add(&h->never_set, 4);
   L.add(&h->health, 16);
   L.add(&h->act, RT * I * 2);
   if (fp8) {
@@ -750,6 +752,18 @@ musemoe_status musemoe_quantize_mxfp4(const uint16_t* w_bf16, uint8_t* codes, ui
     e = launch_quant_mxfp4(w_bf16, codes, scales, (long long)rows * cols, sms,
                            reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_err(nullptr, e, "launch of the MXFP4 rounding");
+  return MUSEMOE_OK;
+}
+
+musemoe_status musemoe_health_selftest(musemoe_handle* h, musemoe_stream_t stream) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != h->device)
+    return set_err(h, MUSEMOE_EINVAL, fmt("current device %d is not the handle's device %d", dev, h->device));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_wait_selftest(h->health, h->never_set, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_err(h, e, "health self-test");
   return MUSEMOE_OK;
 }
 

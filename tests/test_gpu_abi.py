@@ -79,6 +79,23 @@ def test_health_reports_fp16_operand_overflow_and_clears():
         run.close()
 
 
+def test_bounded_waits_time_out_into_the_health_word_and_the_context_survives():
+    cfg = synth.CONFIGS["tiny"]
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    t, W = H.upload_layer(cfg, w)
+    run = H.Run(cfg)
+    try:
+        mm.musemoe_health_selftest(run.handle)
+        assert mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_ETIMEOUT
+        assert mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_OK  # cleared by the poll
+        # the context is usable: a forward afterwards still matches the oracle
+        H.compare(cfg, w, x, st, run.forward(W, x, st))  # asserts the parity bounds
+        assert mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_OK
+    finally:
+        run.close()
+
+
 def test_num_kernels_and_names():
     assert mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4) == 7
     assert mm.musemoe_num_kernels(mm.MUSEMOE_FP8_W8A8) == 8
