@@ -73,6 +73,10 @@ typedef enum {
   /* e4m3 codes + fp32 scale per output row; expert inputs quantized to e4m3
    * per row with a dynamic fp32 scale (amax / 448) */
   MUSEMOE_FP8_W8A8 = 2,
+  /* unquantized bf16 experts, the form the first and last decoder layers
+   * keep (page "vllm.models.muse_spark.amd.muse_moe_runner",
+   * MuseSparkUnquantizedFusedMoE and _online_mxfp4_applies); no scales */
+  MUSEMOE_BF16 = 3,
 } musemoe_quant;
 
 typedef enum { MUSEMOE_SIGMOID = 0, MUSEMOE_SOFTMAX = 1 } musemoe_score;
@@ -107,11 +111,11 @@ typedef struct {
   const float *expert_bias;   /* fp32 [E], selection only */
   const uint16_t *w_pool;     /* bf16 [P, H] */
   const uint16_t *w_pre_norm; /* bf16 [P] (effective weight) */
-  const uint8_t *w13;         /* kernel layout of [E, 2I, P/2] (FP4) / [E, 2I, P] (FP8) */
-  const void *w13_scale;      /* kernel layout: MX u8, NV e4m3; FP8 fp32 [E, 2I] */
+  const uint8_t *w13;         /* kernel layout of [E, 2I, P/2] (FP4) / [E, 2I, P] (FP8) / bf16 [E, 2I, P] */
+  const void *w13_scale;      /* kernel layout: MX u8, NV e4m3; FP8 fp32 [E, 2I]; BF16 unused */
   const float *w13_gscale;    /* NVFP4 only: fp32 [E] */
-  const uint8_t *w2;          /* kernel layout of [E, P, I/2] (FP4) / [E, P, I] (FP8) */
-  const void *w2_scale;       /* kernel layout: MX u8, NV e4m3; FP8 fp32 [E, P] */
+  const uint8_t *w2;          /* kernel layout of [E, P, I/2] (FP4) / [E, P, I] (FP8) / bf16 [E, P, I] */
+  const void *w2_scale;       /* kernel layout: MX u8, NV e4m3; FP8 fp32 [E, P]; BF16 unused */
   const float *w2_gscale;     /* NVFP4 only: fp32 [E] */
   const uint16_t *w_post_norm; /* bf16 [P] */
   const uint16_t *w_unpool;    /* bf16 [H, P] */
@@ -165,18 +169,21 @@ const char *musemoe_kernel_name(int32_t quant, int32_t i);
 /* Re-lays the expert tensors from their plain layout into the kernel layout
  * the forward reads (done once, e.g. after loading weights).
  * Plain layout: codes row-major [E, N, K/2] for MXFP4/NVFP4 (two e2m1 codes
- * per byte, element 2j in the low nibble of byte j) or [E, N, K] e4m3 for FP8;
- * scales [E, N, K/32] UE8M0 (MXFP4), [E, N, K/16] e4m3 (NVFP4), fp32 [E, N]
- * (FP8). w13: N = 2I (gate rows first), K = P; w2: N = P, K = I.
- * Kernel layout: every row is cut into 64-byte code chunks (128 FP4 or 64 FP8
- * elements); rows are taken in tiles of 64, each tile is stored K-slice by
+ * per byte, element 2j in the low nibble of byte j), [E, N, K] e4m3 for FP8 or
+ * [E, N, K] bf16 for BF16; scales [E, N, K/32] UE8M0 (MXFP4), [E, N, K/16]
+ * e4m3 (NVFP4), fp32 [E, N] (FP8), none for BF16 (the scale pointers may be
+ * NULL). w13: N = 2I (gate rows first), K = P; w2: N = P, K = I.
+ * Kernel layout: every row is cut into 64-byte code chunks (128 FP4, 64 FP8 or
+ * 32 BF16 elements); rows are taken in tiles of 64, each tile is stored K-slice by
  * K-slice (4 chunks; the last slice holds the remaining 1..4), each slice by
  * group of 8 rows, then chunk, then row: codes
  * [E][N/64][slice][8 groups][chunks of the slice][8 rows][64 B]; scales the
  * same with the 4 (MXFP4) or 8 (NVFP4) scale bytes of a row's chunk in place
  * of its 64 code bytes; FP8 scales keep their layout. For FP4 the 64 bytes of
  * a chunk are also reordered: byte 8j + 2q + b moves to 16q + 2j + b (q < 4,
- * j < 8, b < 2). Each src may be its dst (in place): the tensors then pass
+ * j < 8, b < 2); for BF16 its 4-byte words are transposed as a 4 x 4 block:
+ * byte 16j + 4q + b moves to 16q + 4j + b (q, j, b < 4). Each src may be its
+ * dst (in place): the tensors then pass
  * through a temporary device buffer of at most 64 MB, allocated and freed by
  * this call, which synchronizes the stream before it returns. The NVFP4
  * global scales need no re-layout. MXFP4 scales must be UE8M0 codes

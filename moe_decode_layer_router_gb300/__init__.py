@@ -18,7 +18,7 @@ from . import _build
 
 __all__ = [
     "MUSEMOE_OK", "MUSEMOE_EINVAL", "MUSEMOE_EUNSUPPORTED", "MUSEMOE_ECUDA", "MUSEMOE_ENOMEM",
-    "MUSEMOE_ERANGE", "MUSEMOE_ETIMEOUT", "MUSEMOE_MXFP4", "MUSEMOE_NVFP4", "MUSEMOE_FP8_W8A8", "MUSEMOE_SIGMOID",
+    "MUSEMOE_ERANGE", "MUSEMOE_ETIMEOUT", "MUSEMOE_MXFP4", "MUSEMOE_NVFP4", "MUSEMOE_FP8_W8A8", "MUSEMOE_BF16", "MUSEMOE_SIGMOID",
     "MUSEMOE_SOFTMAX", "Dims", "Config", "Weights", "Taps", "MuseMoEError", "library",
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
@@ -29,7 +29,7 @@ __all__ = [
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
  MUSEMOE_ETIMEOUT) = (0, 1, 2, 3, 4, 5, 6)
-MUSEMOE_MXFP4, MUSEMOE_NVFP4, MUSEMOE_FP8_W8A8 = 0, 1, 2
+MUSEMOE_MXFP4, MUSEMOE_NVFP4, MUSEMOE_FP8_W8A8, MUSEMOE_BF16 = 0, 1, 2, 3
 MUSEMOE_SIGMOID, MUSEMOE_SOFTMAX = 0, 1
 _STATUS = {0: "OK", 1: "EINVAL", 2: "EUNSUPPORTED", 3: "ECUDA", 4: "ENOMEM", 5: "ERANGE",
            6: "ETIMEOUT"}

@@ -65,12 +65,12 @@ struct XGeo {
 template <int Q, int ROLE, int NT>
 __host__ __device__ __forceinline__ XGeo x_geo(int K, int N) {
   XGeo g;
-  const int rowbytes = (Q == kFP8) ? K : K / 2;
+  const int rowbytes = (Q == kFP8) ? K : (Q == kBF16) ? 2 * K : K / 2;
   g.NC = rowbytes / 64;
   g.KS = (g.NC + kSliceChunks - 1) / kSliceChunks;
   g.tiles = (ROLE == 0) ? (N / 2) / 64 : N / 128;
   g.SB = (Q == kMXFP4) ? 4 : (Q == kNVFP4) ? 8 : 0;
-  g.cbB = (Q == kFP8) ? 64 : 256;
+  g.cbB = (Q == kFP8 || Q == kBF16) ? 64 : 256;  // activation bytes of one 64-byte code chunk
   g.RS = kSliceChunks * g.cbB + 32;
   g.scale_off = 2 * kXCodeBlock;
   g.b_off = g.scale_off + 2 * 8 * kSliceChunks * 8 * g.SB;
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
             su = __ldg(ws + (size_t)e * p.N + p.I + i) * bs;
           }
           const float a = round_bf16(silu(v[nt][h] * sg) * (v[nt][2 + h] * su));
-          if (Q == kFP8) {
+          if (Q == kFP8 || Q == kBF16) {
             reinterpret_cast<uint16_t*>(p.out)[(size_t)ro * p.I + i] = f32_to_bf16_bits(a);
           } else {
             reinterpret_cast<__half*>(p.out)[(size_t)ro * p.I + i] = __float2half_rn(a);
@@ -440,13 +440,22 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       // one token tile: B fragments from the stage's activation rows, the
       // next chunk's read while the current one runs (two register buffers).
       // FP4: k-step j of chunk c is 4 f16 at element 128 c + 16 j + 4 q;
-      // FP8: both k-steps of chunk c are 16 e4m3 at byte 64 c + 16 q.
-      const uint8_t* bp = stg + G.b_off + min(g, ntok - 1) * G.RS + q * (Q == kFP8 ? 16 : 8);
+      // FP8: both k-steps of chunk c are 16 e4m3 at byte 64 c + 16 q;
+      // BF16: k-step j of chunk c is the bf16 pairs at elements 32 c + 16 j
+      // + 2 q and + 8 (the natural mma order).
+      const uint8_t* bp =
+          stg + G.b_off + min(g, ntok - 1) * G.RS + q * (Q == kFP8 ? 16 : Q == kBF16 ? 4 : 8);
       uint2 b4[2][8];
       uint4 b8[2];
       auto ldb = [&](int buf, int c) {
         if constexpr (Q == kFP8) {
           b8[buf] = *reinterpret_cast<const uint4*>(bp + c * 64);
+        } else if constexpr (Q == kBF16) {
+          const uint8_t* cp = bp + c * 64;
+          b4[buf][0] = make_uint2(*reinterpret_cast<const uint32_t*>(cp),
+                                  *reinterpret_cast<const uint32_t*>(cp + 16));
+          b4[buf][1] = make_uint2(*reinterpret_cast<const uint32_t*>(cp + 32),
+                                  *reinterpret_cast<const uint32_t*>(cp + 48));
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) b4[buf][j] = *reinterpret_cast<const uint2*>(bp + c * 256 + j * 32);
@@ -489,6 +498,12 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
         if constexpr (Q == kFP8)
           chunk_mma<Q, NT>(acc, L, Hh, sl, sh, ntile_act, [&](int nt, int) {
             return *reinterpret_cast<const uint4*>(brow[nt] + (size_t)cg * 64 + q * 16);
+          });
+        else if constexpr (Q == kBF16)
+          chunk_mma<Q, NT>(acc, L, Hh, sl, sh, ntile_act, [&](int nt, int j) {
+            const uint8_t* e0 = brow[nt] + ((size_t)cg * 32 + 16 * j + 2 * q) * 2;
+            return make_uint2(*reinterpret_cast<const uint32_t*>(e0),
+                              *reinterpret_cast<const uint32_t*>(e0 + 16));
           });
         else
           chunk_mma<Q, NT>(acc, L, Hh, sl, sh, ntile_act, [&](int nt, int j) {
@@ -634,6 +649,8 @@ cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pd
     case 3: return launch_x_q<kNVFP4, 1>(p, nt, s, pdl);
     case 4: return launch_x_q<kFP8, 0>(p, nt, s, pdl);
     case 5: return launch_x_q<kFP8, 1>(p, nt, s, pdl);
+    case 6: return launch_x_q<kBF16, 0>(p, nt, s, pdl);
+    case 7: return launch_x_q<kBF16, 1>(p, nt, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -666,7 +683,9 @@ int expert_ctas_per_sm(int quant, int role, int nt, int K, int N) {
     case 2: return x_occ_q<kNVFP4, 0>(nt, K, N);
     case 3: return x_occ_q<kNVFP4, 1>(nt, K, N);
     case 4: return x_occ_q<kFP8, 0>(nt, K, N);
-    default: return x_occ_q<kFP8, 1>(nt, K, N);
+    case 5: return x_occ_q<kFP8, 1>(nt, K, N);
+    case 6: return x_occ_q<kBF16, 0>(nt, K, N);
+    default: return x_occ_q<kBF16, 1>(nt, K, N);
   }
 }
 

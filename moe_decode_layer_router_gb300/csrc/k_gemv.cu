@@ -266,7 +266,7 @@ __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) 
 #pragma unroll
       for (int c = 0; c < 4; ++c) am = fmaxf(am, fabsf(hb[c]));
       hdst[i] = make_uint2(hbits[0], hbits[1]);
-      if (p.quant != kFP8) {
+      if (p.quant == kMXFP4 || p.quant == kNVFP4) {  // the f16 operand (BF16 and FP8 have their own)
 #pragma unroll
         for (int c = 0; c < 4; ++c) bad |= !(fabsf(hb[c]) <= 65504.f);  // NaN too
         uint32_t opbits[2];

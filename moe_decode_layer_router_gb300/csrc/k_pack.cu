@@ -28,10 +28,13 @@ cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s
 
 // One output byte per thread step: output offset o of the kernel layout
 // [tiles][slice][8 groups][chunks of the slice][8 rows][cb] takes source
-// byte (row, byte) of the plain row-major [rows, row_bytes] tensor; FP4 code
-// chunks also reorder their bytes (output 16q + 2j + b <- chunk byte 8j + 2q + b).
+// byte (row, byte) of the plain row-major [rows, row_bytes] tensor. Code
+// chunks also reorder their bytes so that a thread's 16 bytes are its mma
+// fragments: FP4 (permute 1), output 16q + 2j + b <- chunk byte 8j + 2q + b;
+// BF16 (permute 2, 32 values per chunk), a 4 x 4 transpose of 4-byte words,
+// output 16q + 4j + b <- chunk byte 16j + 4q + b.
 __global__ void k_pack_tiles(const uint8_t* src, uint8_t* dst, size_t bytes, int row_bytes, int cb,
-                             int permute_fp4) {
+                             int permute) {
   const int NC = row_bytes / cb;
   const size_t tile_bytes = (size_t)64 * row_bytes;
   const size_t full = (size_t)64 * kSliceChunks * cb;  // a full slice of a tile
@@ -45,9 +48,12 @@ __global__ void k_pack_tiles(const uint8_t* src, uint8_t* dst, size_t bytes, int
     const int r2 = rem % (ncs * 8 * cb);
     const int c = r2 / (8 * cb), r = (r2 / cb) % 8;
     int b = r2 % cb;
-    if (permute_fp4) {
+    if (permute == 1) {
       const int qq = b >> 4, j = (b >> 1) & 7, bb = b & 1;
       b = 8 * j + 2 * qq + bb;
+    } else if (permute == 2) {
+      const int qq = b >> 4, j = (b >> 2) & 3, bb = b & 3;
+      b = 16 * j + 4 * qq + bb;
     }
     dst[o] = src[t * tile_bytes + (size_t)(gi * 8 + r) * row_bytes +
                  (size_t)(kSliceChunks * s + c) * cb + b];
@@ -55,7 +61,7 @@ __global__ void k_pack_tiles(const uint8_t* src, uint8_t* dst, size_t bytes, int
 }
 
 cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
-                              bool permute_fp4, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s) {
+                              int permute, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s) {
   const size_t tile_bytes = (size_t)64 * row_bytes;
   const size_t tiles = rows / 64;
   const bool in_place = (src == dst);
@@ -71,7 +77,7 @@ cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int
       from = tmp;
     }
     const unsigned grid = (unsigned)std::min<size_t>((bytes + 255) / 256, 16384);
-    k_pack_tiles<<<grid, 256, 0, s>>>(from, dst + off, bytes, row_bytes, cb, permute_fp4 ? 1 : 0);
+    k_pack_tiles<<<grid, 256, 0, s>>>(from, dst + off, bytes, row_bytes, cb, permute);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -7,7 +7,7 @@
 
 namespace musemoe {
 
-enum Quant : int { kMXFP4 = 0, kNVFP4 = 1, kFP8 = 2 };
+enum Quant : int { kMXFP4 = 0, kNVFP4 = 1, kFP8 = 2, kBF16 = 3 };
 
 // The calling thread's error text that musemoe_last_error(NULL) returns.
 void set_thread_error(const std::string& m);
@@ -89,7 +89,7 @@ struct ExpertParams {
   const uint8_t* w;        // codes, kernel layout (launch_pack_tiles, cb = 64)
   const void* scale;       // MX/NV: kernel layout (cb = 4 / 8); FP8: fp32 [E, N]
   const float* gscale;     // NVFP4 [E]
-  const uint8_t* b;        // activation operand: f16 [*, K] or e4m3 [*, K]
+  const uint8_t* b;        // activation operand: f16 [*, K], e4m3 [*, K] or (BF16 experts) bf16 [*, K]
   const float* b_scale;    // FP8: per B row
   int b_by_token;          // 1: B row = route / k (w13 reads h); 0: B row = route
   const int32_t* route_list;
@@ -157,13 +157,14 @@ cudaError_t launch_quant_mxfp4(const uint16_t* w, uint8_t* codes, uint8_t* scale
 // (cb = 64 for codes, the scale bytes of one code chunk for scales): tiles of
 // 64 rows, each stored K-slice by K-slice (kSliceChunks chunks, the last
 // slice the remainder), each slice by 8-row group, chunk, row:
-// [rows / 64][slice][8][chunks of the slice][8][cb]. permute_fp4 also
-// reorders the bytes of each 64-byte code chunk for the FP4 mma fragments.
+// [rows / 64][slice][8][chunks of the slice][8][cb]. permute 1 (FP4) or 2
+// (BF16) also reorders the bytes of each 64-byte code chunk for the mma
+// fragments; 0 keeps them.
 // src may equal dst: the tiles then pass through `tmp` (at least one tile).
 // Sets *bad_dev to 1 if any of the n UE8M0 bytes is 0x00 or 0xFF.
 constexpr int kSliceChunks = 4;
 cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s);
 cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
-                              bool permute_fp4, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s);
+                              int permute, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s);
 
 }  // namespace musemoe

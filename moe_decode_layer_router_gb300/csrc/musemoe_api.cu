@@ -146,7 +146,8 @@ std::vector<std::string> refusals(const musemoe_dims* d, int32_t quant, const mu
     r.push_back(fmt("hidden %d above %d (a pooler row tile held in shared memory)", d->hidden, front_max_k()));
   if (d->pooled > front_max_k())
     r.push_back(fmt("pooled %d above %d (an unpooler row tile held in shared memory)", d->pooled, front_max_k()));
-  if (quant < 0 || quant > 2) r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1) or FP8_W8A8 (2)", quant));
+  if (quant < 0 || quant > 3)
+    r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1), FP8_W8A8 (2) or BF16 (3)", quant));
   if (c->score != 0 && c->score != 1) r.push_back(fmt("score %d is not sigmoid (0) or softmax (1)", c->score));
   if (!std::isfinite(c->route_scale)) r.push_back("route_scale is not finite");
   if (c->has_multiplier && !std::isfinite(c->multiplier)) r.push_back("multiplier is not finite");
@@ -185,9 +186,9 @@ std::string check_weights(const musemoe_handle* h, const musemoe_weights* w, boo
     need(w->w_pool, "w_pool");
     need(w->w_pre_norm, "w_pre_norm");
     need(w->w13, "w13");
-    need(w->w13_scale, "w13_scale");
+    if (h->quant != kBF16) need(w->w13_scale, "w13_scale");
     need(w->w2, "w2");
-    need(w->w2_scale, "w2_scale");
+    if (h->quant != kBF16) need(w->w2_scale, "w2_scale");
     if (h->quant == kNVFP4) {
       need(w->w13_gscale, "w13_gscale");
       need(w->w2_gscale, "w2_gscale");
@@ -296,7 +297,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.w = w->w13;
   ep.scale = w->w13_scale;
   ep.gscale = w->w13_gscale;
-  ep.b = h->h_op;
+  ep.b = h->quant == kBF16 ? reinterpret_cast<const uint8_t*>(h->h) : h->h_op;  // BF16: h itself
   ep.b_scale = h->h_scale;
   ep.b_by_token = 1;
   ep.route_list = h->route_list;
@@ -542,15 +543,20 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
   c.route_scale = 1.f;
   const std::vector<std::string> r = refusals(d, quant, &c);
   if (!r.empty()) return set_err(nullptr, MUSEMOE_EUNSUPPORTED, join(r));
+  const bool bf16 = quant == kBF16;  // no scales
   const void* ptrs[8] = {w13_src, w13_scale_src, w13_dst, w13_scale_dst,
                          w2_src,  w2_scale_src,  w2_dst,  w2_scale_dst};
-  for (const void* q : ptrs) {
+  for (int i = 0; i < 8; ++i) {
+    const void* q = ptrs[i];
+    if (bf16 && (i % 2)) continue;
     if (!q) return set_err(nullptr, MUSEMOE_EINVAL, "expert tensor pointers must not be NULL");
     if (!aligned16(q)) return set_err(nullptr, MUSEMOE_EINVAL, "expert tensors must be 16-byte aligned");
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t E = d->experts, P = d->pooled, I = d->inter;
   const bool fp8 = quant == kFP8;
+  // bytes per row of K values: FP4 K / 2, FP8 K, BF16 2 K
+  auto row_bytes = [&](size_t K) { return fp8 ? K : bf16 ? 2 * K : K / 2; };
   const int sper = quant == kMXFP4 ? 4 : 8;  // scale bytes per 64-byte code chunk
   struct M {
     const uint8_t* src;
@@ -583,10 +589,10 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
   // in-place re-layouts pass through a temporary buffer of whole row tiles
   size_t tmp_bytes = 0;
   for (const M& m : ms) {
-    const size_t rowbytes = fp8 ? m.K : m.K / 2;
+    const size_t rowbytes = row_bytes(m.K);
     const size_t total = m.rows * rowbytes, tile = 64 * rowbytes;
     if (m.src == m.dst) tmp_bytes = std::max(tmp_bytes, std::max(tile, std::min(total, kPackTmpBytes)));
-    if (!fp8 && m.ssrc == m.sdst) tmp_bytes = std::max(tmp_bytes, 64 * (rowbytes / 64) * sper);
+    if (!fp8 && !bf16 && m.ssrc == m.sdst) tmp_bytes = std::max(tmp_bytes, 64 * (rowbytes / 64) * sper);
   }
   uint8_t* tmp = nullptr;
   if (tmp_bytes) {
@@ -596,16 +602,18 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
                                                   cudaGetErrorString(e)));
   }
   for (const M& m : ms) {
-    const int rowbytes = (int)(fp8 ? m.K : m.K / 2);
-    if (e == cudaSuccess) e = launch_pack_tiles(m.src, m.dst, m.rows, rowbytes, 64, !fp8, tmp, tmp_bytes, s);
+    const int rowbytes = (int)row_bytes(m.K);
+    const int permute = fp8 ? 0 : bf16 ? 2 : 1;
+    if (e == cudaSuccess) e = launch_pack_tiles(m.src, m.dst, m.rows, rowbytes, 64, permute, tmp, tmp_bytes, s);
     if (e != cudaSuccess) break;
+    if (bf16) continue;  // no scales
     if (fp8) {  // per-row fp32 scales stay as they are
       if (m.ssrc != m.sdst)
         e = cudaMemcpyAsync(m.sdst, m.ssrc, m.rows * 4, cudaMemcpyDeviceToDevice, s);
     } else {
       const int srow = (int)(rowbytes / 64) * sper;
       e = launch_pack_tiles(reinterpret_cast<const uint8_t*>(m.ssrc), reinterpret_cast<uint8_t*>(m.sdst),
-                            m.rows, srow, sper, false, tmp, tmp_bytes, s);
+                            m.rows, srow, sper, 0, tmp, tmp_bytes, s);
     }
   }
   if (tmp) {

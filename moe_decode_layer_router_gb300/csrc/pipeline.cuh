@@ -82,8 +82,8 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
 }
 // The mma work of one 64-byte chunk of the fragment rows g (codes L, scales
 // sl) and g + 8 (codes H, scales sh) against the n-tiles' B fragments, which
-// `bfrag(nt, j)` returns: for FP4 the uint2 of k-step j (0..7), for FP8 the
-// uint4 of both k-steps (j unused).
+// `bfrag(nt, j)` returns: for FP4 the uint2 of k-step j (0..7), for BF16 the
+// uint2 of k-step j (0..1), for FP8 the uint4 of both k-steps (j unused).
 template <int Q, int NT, typename BFrag>
 __device__ __forceinline__ void chunk_mma(float (&acc)[NT][4], const uint4& L, const uint4& H,
                                           uint2 sl, uint2 sh, int ntile_act, BFrag&& bfrag) {
@@ -94,6 +94,16 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[NT][4], const uint4& L, c
       const uint4 bv = bfrag(nt, 0);
       mma_e4m3_16832(acc[nt], L.x, H.x, L.y, H.y, bv.x, bv.y);
       mma_e4m3_16832(acc[nt], L.z, H.z, L.w, H.w, bv.z, bv.w);
+    }
+  } else if constexpr (Q == kBF16) {
+    // bf16 codes as stored (the pack transposes a chunk's 4-byte words so
+    // that L / H are rows g / g + 8 at k 2q, 2q + 8 of k-step 0, then k-step 1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (nt >= ntile_act) break;
+      const uint2 b0 = bfrag(nt, 0), b1 = bfrag(nt, 1);
+      mma_bf16_16816(acc[nt], L.x, H.x, L.y, H.y, b0.x, b0.y);
+      mma_bf16_16816(acc[nt], L.z, H.z, L.w, H.w, b1.x, b1.y);
     }
   } else if constexpr (Q == kMXFP4) {
 #pragma unroll

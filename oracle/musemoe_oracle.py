@@ -369,6 +369,9 @@ def dequant_expert(quant: str, t: dict, e: int):
     MXFP4: e2m1 * 2^(s-127), one UE8M0 scale per 32 along K (decoder page,
     MonoDims.expert_shapes). NVFP4: e2m1 * e4m3 block scale per 16 along K *
     fp32 global scale of the expert. FP8: e4m3 * fp32 scale per output row.
+    BF16: the bf16 values (the unquantized experts of the first and last
+    decoder layers: muse_moe_runner page, MuseSparkUnquantizedFusedMoE and
+    _online_mxfp4_applies).
     """
     if quant == "mxfp4":
         w13 = _apply_block_scale(_fp4_values(t["w13"][e]), ue8m0_decode(t["w13_scale"][e]), 32)
@@ -381,6 +384,9 @@ def dequant_expert(quant: str, t: dict, e: int):
     elif quant == "fp8":
         w13 = e4m3_decode(t["w13"][e]) * t["w13_scale"][e].astype(np.float64)[:, None]
         w2 = e4m3_decode(t["w2"][e]) * t["w2_scale"][e].astype(np.float64)[:, None]
+    elif quant == "bf16":
+        w13 = bf16_to_f64(t["w13"][e])
+        w2 = bf16_to_f64(t["w2"][e])
     else:
         raise ValueError(quant)
     return w13, w2

@@ -31,7 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "_synth.so")
 _lib = None
 _lock = threading.Lock()
 
-MXFP4, NVFP4, FP8 = "mxfp4", "nvfp4", "fp8"
+MXFP4, NVFP4, FP8, BF16 = "mxfp4", "nvfp4", "fp8", "bf16"
 SIGMOID, SOFTMAX = "sigmoid", "softmax"
 
 # Tensor ids of the counter-based generator.
@@ -169,6 +169,11 @@ CONFIGS = {
                      division_eps=1e-6, hot_experts=16, seed=2, **_BIG),
     "large": Config("large", rows=256, quant=FP8, seed=3, **_BIG),
     "stack": Config("stack", rows=32, quant=MXFP4, seed=4, layers=60, **_BIG),
+    # BF16 experts (the first and last decoder layers keep them unquantized)
+    "edge_tiny": Config("edge_tiny", rows=4, hidden=512, pooled=256, inter=128, experts=16,
+                        top_k=2, quant=BF16, seed=5),
+    "edge": Config("edge", rows=8, quant=BF16, multiplier=0.5, seed=6,
+                   **{**_BIG, "experts": 32}),
 }
 
 
@@ -212,6 +217,7 @@ def expert_tensors(cfg: Config, layer: int, e0: int = 0, ne: int | None = None):
     and w2_scale [ne, P, I/32].
     NVFP4: the same codes, e4m3 block scales per 16 ([.., P/16], [.., I/16])
     and an fp32 global scale per expert and matrix (w13_gscale, w2_gscale).
+    BF16: bf16 N(0, 0.02) weights w13 [ne, 2I, P], w2 [ne, P, I], no scales.
     FP8: e4m3 codes w13 [ne, 2I, P], w2 [ne, P, I], fp32 scale per output
     channel (w13_scale [ne, 2I], w2_scale [ne, P]).
     """
@@ -234,6 +240,9 @@ def expert_tensors(cfg: Config, layer: int, e0: int = 0, ne: int | None = None):
                                         start=e0 * P * I // 16)
             out["w13_gscale"] = uniform_f32(s, T_W13_G, (ne,), 0.5, 2.0, start=e0)
             out["w2_gscale"] = uniform_f32(s, T_W2_G, (ne,), 0.5, 2.0, start=e0)
+    elif cfg.quant == BF16:
+        out["w13"] = normal_bf16(s, T_W13, (ne, 2 * I, P), 0.0, 0.02, start=e0 * 2 * I * P)
+        out["w2"] = normal_bf16(s, T_W2, (ne, P, I), 0.0, 0.02, start=e0 * P * I)
     elif cfg.quant == FP8:
         c13, s13 = fp8_rows(s, T_W13, ne * 2 * I, P, 0.05, row0=e0 * 2 * I)
         c2, s2 = fp8_rows(s, T_W2, ne * P, I, 0.05, row0=e0 * P)

@@ -23,7 +23,7 @@ WEIGHT_RTOL = 1e-5
 OUT_TOL = 2e-2
 
 QUANT = {synth.MXFP4: mm.MUSEMOE_MXFP4, synth.NVFP4: mm.MUSEMOE_NVFP4,
-         synth.FP8: mm.MUSEMOE_FP8_W8A8}
+         synth.FP8: mm.MUSEMOE_FP8_W8A8, synth.BF16: mm.MUSEMOE_BF16}
 
 
 def dims_of(cfg: synth.Config, max_rows: int | None = None) -> mm.Dims:
@@ -51,8 +51,9 @@ def upload_layer(cfg: synth.Config, w: dict, device="cuda"):
     """Device copies of one layer's tensors (expert codes packed in place into
     the kernel layout) and the Weights struct pointing at them."""
     t = {k: to_dev(v, device) for k, v in w.items()}
-    mm.musemoe_pack_experts(dims_of(cfg), QUANT[cfg.quant], t["w13"], t["w13_scale"], t["w13"],
-                            t["w13_scale"], t["w2"], t["w2_scale"], t["w2"], t["w2_scale"])
+    mm.musemoe_pack_experts(dims_of(cfg), QUANT[cfg.quant], t["w13"], t.get("w13_scale"),
+                            t["w13"], t.get("w13_scale"), t["w2"], t.get("w2_scale"), t["w2"],
+                            t.get("w2_scale"))
     torch.cuda.synchronize()
     return t, mm.make_weights(t)
 
@@ -99,7 +100,8 @@ class Run:
                 res[k] = O.bf16_to_f64(res[k + "_bits"])
         if "act" in res:
             bits = res["act"].view(np.uint16)
-            if cfg.quant == synth.FP8:
+            res["act_bf16"] = cfg.quant in (synth.FP8, synth.BF16)
+            if res["act_bf16"]:  # the bf16 activations themselves
                 res["act"] = O.bf16_to_f64(bits).reshape(b, cfg.top_k, cfg.inter)
             else:
                 res["act"] = bits.view(np.float16).astype(np.float64).reshape(b, cfg.top_k,
@@ -143,10 +145,11 @@ def oracle_as_gpu(cfg: synth.Config, ref: dict) -> dict:
     the comparison logic on the CPU)."""
     b, k = ref["ids"].shape
     act = ref["act"]
-    if cfg.quant != synth.FP8:
+    if cfg.quant not in (synth.FP8, synth.BF16):
         act = act.astype(np.float16).astype(np.float64)
     return dict(logits=ref["logits"], ids=ref["ids"].astype(np.int32), weights=ref["weights"],
-                h=ref["h"], act=act, y=ref["y"].reshape(b * k, -1).astype(np.float32),
+                h=ref["h"], act=act, act_bf16=cfg.quant in (synth.FP8, synth.BF16),
+                y=ref["y"].reshape(b * k, -1).astype(np.float32),
                 moe_out=ref["moe_out"], u=ref["u"], stream=ref["stream"], out=ref["out"])
 
 
@@ -173,16 +176,26 @@ def check_ids(gpu_ids: np.ndarray, routing: "O.Routing", k: int) -> int:
     return differ
 
 
-def kernel_layout(a: np.ndarray, chunk_bytes: int, permute_fp4: bool) -> np.ndarray:
+def kernel_layout(a: np.ndarray, chunk_bytes: int, permute_fp4: bool,
+                  permute_bf16: bool = False) -> np.ndarray:
     """Host restatement of the documented kernel layout of one plain expert
     tensor [E, N, row_bytes] (bytes): rows in tiles of 64, each tile K-slice
     by K-slice (4 chunks of chunk_bytes, the last slice the remainder), each
     slice [8 groups][chunks of the slice][8 rows][chunk_bytes]; FP4 code
-    chunks reordered byte 8j + 2q + b -> 16q + 2j + b."""
-    a = np.ascontiguousarray(a).view(np.uint8)
+    chunks reordered byte 8j + 2q + b -> 16q + 2j + b; BF16 code chunks
+    byte 16j + 4q + b -> 16q + 4j + b."""
+    a = np.ascontiguousarray(a)
+    a = a.view(np.uint8).reshape(a.shape[0], a.shape[1], -1)
     E, N, rb = a.shape
     nc = rb // chunk_bytes
     x = a.reshape(E, N // 64, 8, 8, nc, chunk_bytes)  # [E][tile][group][row][chunk][byte]
+    if permute_bf16:
+        src = np.empty(64, np.int64)
+        for qq in range(4):
+            for j in range(4):
+                for bb in range(4):
+                    src[16 * qq + 4 * j + bb] = 16 * j + 4 * qq + bb
+        x = x[..., src]
     if permute_fp4:
         src = np.empty(64, np.int64)
         for qq in range(4):
@@ -198,9 +211,11 @@ def kernel_layout(a: np.ndarray, chunk_bytes: int, permute_fp4: bool) -> np.ndar
 def near_of(g: dict) -> dict:
     """The GPU's bf16 values at the oracle's rounding points. For FP4 formats
     the act tap is the f16 copy of the bf16 activation, which equals it only
-    in the f16 normal range (|a| >= 2^-14); below that it is no hint (NaN)."""
+    in the f16 normal range (|a| >= 2^-14); below that it is no hint (NaN).
+    FP8 and BF16 tap the bf16 activation itself."""
     act = np.asarray(g["act"], dtype=np.float64)
-    act = np.where(np.abs(act) >= 2.0 ** -14, act, np.nan)
+    if not g.get("act_bf16", False):
+        act = np.where(np.abs(act) >= 2.0 ** -14, act, np.nan)
     return dict(h=g["h"], act=act, moe_out=g["moe_out"], out=g["out"])
 
 

@@ -42,7 +42,7 @@ def _compare_block(cfg, w, x, st, run=None, pre_norm=True, report=None):
     return g, rep
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "verify", "large"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "verify", "large", "edge_tiny", "edge"])
 def test_block_parity_full_size(name, record_property):
     cfg = synth.CONFIGS[name]
     w = synth.layer_tensors(cfg)
@@ -54,7 +54,7 @@ def test_block_parity_full_size(name, record_property):
     print(name, rep)
 
 
-@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8])
+@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8, synth.BF16])
 @pytest.mark.parametrize("score", [synth.SIGMOID, synth.SOFTMAX])
 def test_tiny_dims_every_quant_and_score(quant, score):
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, score=score, seed=11)
@@ -63,7 +63,7 @@ def test_tiny_dims_every_quant_and_score(quant, score):
     _compare_block(cfg, w, x, st)
 
 
-@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8])
+@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8, synth.BF16])
 def test_ragged_k_slices(quant):
     # P = 640, I = 384: w13 rows of 5 (FP4) / 10 (FP8) 64-byte chunks and w2
     # rows of 3 / 6 chunks, so the last K-slice of a tile is ragged and tiles
@@ -199,7 +199,7 @@ def test_forward_host_matches_device_forward():
 
 
 @pytest.mark.parametrize("dims", [(256, 128), (640, 384)])
-@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8])
+@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8, synth.BF16])
 def test_pack_matches_the_documented_layout(quant, dims):
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, pooled=dims[0], inter=dims[1])
     e = synth.expert_tensors(cfg, 0)
@@ -207,18 +207,24 @@ def test_pack_matches_the_documented_layout(quant, dims):
     dst = {k: torch.empty_like(v) for k, v in src.items()}
     d = H.dims_of(cfg)
     q = H.QUANT[quant]
-    mm.musemoe_pack_experts(d, q, src["w13"], src["w13_scale"], dst["w13"], dst["w13_scale"],
-                            src["w2"], src["w2_scale"], dst["w2"], dst["w2_scale"])
-    mm.musemoe_pack_experts(d, q, src["w13"], src["w13_scale"], src["w13"], src["w13_scale"],
-                            src["w2"], src["w2_scale"], src["w2"], src["w2_scale"])
+    mm.musemoe_pack_experts(d, q, src["w13"], src.get("w13_scale"), dst["w13"],
+                            dst.get("w13_scale"), src["w2"], src.get("w2_scale"), dst["w2"],
+                            dst.get("w2_scale"))
+    mm.musemoe_pack_experts(d, q, src["w13"], src.get("w13_scale"), src["w13"],
+                            src.get("w13_scale"), src["w2"], src.get("w2_scale"), src["w2"],
+                            src.get("w2_scale"))
     torch.cuda.synchronize()
     for k in ("w13", "w13_scale", "w2", "w2_scale"):
-        assert torch.equal(src[k], dst[k]), k   # in place == out of place
-    fp4 = quant != synth.FP8
+        if k in src:
+            assert torch.equal(src[k], dst[k]), k   # in place == out of place
+    fp4 = quant in (synth.MXFP4, synth.NVFP4)
     sc = 4 if quant == synth.MXFP4 else 8
     for k in ("w13", "w2"):
-        want = H.kernel_layout(e[k], 64, fp4)
-        np.testing.assert_array_equal(dst[k].cpu().numpy().reshape(want.shape), want)
+        want = H.kernel_layout(e[k], 64, fp4, permute_bf16=quant == synth.BF16)
+        got = dst[k].cpu().numpy().view(np.uint8).reshape(want.shape)
+        np.testing.assert_array_equal(got, want)
+        if quant == synth.BF16:
+            continue  # no scales
         if fp4:
             ws = H.kernel_layout(e[k + "_scale"], sc, False)
             np.testing.assert_array_equal(dst[k + "_scale"].cpu().numpy(), ws)

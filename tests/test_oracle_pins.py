@@ -1,6 +1,7 @@
 """Pins of the oracle against things other than itself: hand-worked closed
 forms, library routines for the number formats and norms, invariants of the
 routing rule, brute force on tiny experts. CPU only."""
+import dataclasses
 import json
 import math
 import os
@@ -11,6 +12,7 @@ import scipy.special
 import torch
 
 import oracle as O
+import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -469,6 +471,26 @@ def test_attention_boundary_zero_gate_and_unit_weight_ffn_form():
     sf, of = O.boundary(O.bf16_to_f64(partial), stream, ones, 0.8, w, 1e-6)
     np.testing.assert_array_equal(sa, sf)
     np.testing.assert_array_equal(oa, of)
+
+
+def test_bf16_experts_equal_their_exact_mxfp4_twins():
+    # MXFP4 values are exact in bf16: BF16 experts holding the dequantized
+    # MXFP4 weights give the same expert outputs through their own dequant
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], experts=4, seed=41)
+    t = synth.expert_tensors(cfg, 0)
+    tb = {}
+    for k in ("w13", "w2"):
+        vals = np.stack([O.dequant_expert("mxfp4", t, e)[0 if k == "w13" else 1] for e in range(4)])
+        tb[k] = O.f64_to_bf16_bits(vals)
+        np.testing.assert_array_equal(O.bf16_to_f64(tb[k]), vals)
+    rng = np.random.default_rng(43)
+    h = O.round_bf16(rng.standard_normal((3, cfg.pooled)))
+    ids = np.array([[0, 3], [2, 1], [3, 3]])
+    y4 = O.expert_outputs(h, ids, "mxfp4", t, cfg.inter)
+    yb = O.expert_outputs(h, ids, "bf16", tb, cfg.inter)
+    np.testing.assert_array_equal(y4, yb)
+    with pytest.raises(ValueError):
+        O.dequant_expert("int4", t, 0)
 
 
 # ---------------------------------------------------------------- online MXFP4 rounding
