@@ -26,6 +26,9 @@ It is a plain, slow, step-by-step restatement of what the pages fix:
   docstring, and decoder page (post_attn_norm has no weight).
 * online rounding of BF16 expert weights to MXFP4 -- page
   "vllm.models.muse_spark.amd.muse_moe_runner", _quantize_experts_to_mxfp4.
+* W4A4 expert inputs: dynamic MXFP4 activations (muse_moe_runner page, the
+  Quark w_mxfp4_a_mxfp4 scheme) and the NVFP4 expert input (providers page,
+  ExpertsInput: e2m1 codes with e4m3 block scales per 16).
 
 Every value is float64 unless a rounding is named. The rounding points are
 the storage dtypes the pages show: fp32 router logits and routing scores
@@ -343,6 +346,59 @@ def quantize_rows_e4m3(v: np.ndarray):
     return q, scale[..., 0]
 
 
+def quantize_act_nvfp4(v: np.ndarray):
+    """Dynamic NVFP4 quantization of bf16-valued activations [..., K] into the
+    expert input the stock layer hands the routed experts (providers page,
+    ExpertsInput: two e2m1 codes per byte, one e4m3 block scale per 16).
+
+    Reading (ExpertsInput carries codes and block scales and no global scale;
+    the page prints no quantizer): per block of 16 consecutive elements, the
+    scale is the e4m3 value nearest fp32(amax / 6) (ties to even, saturating
+    at 448), 6 being the largest e2m1 magnitude; each element becomes the
+    e2m1 magnitude nearest fp32(|v| / scale), ties to the even code,
+    saturating at 6, with the sign bit of v; a block whose scale is 0 gets
+    magnitude 0 everywhere (sign bits kept).
+
+    Returns (codes uint8 [..., K/2], element 2j in the low nibble of byte j;
+    scales e4m3 uint8 [..., K/16])."""
+    v = np.asarray(v, dtype=np.float64)
+    K = v.shape[-1]
+    assert K % 16 == 0
+    blk = v.reshape(v.shape[:-1] + (K // 16, 16))
+    amax = np.abs(blk).max(axis=-1)
+    s_code = e4m3_encode(round_f32(amax / 6.0))
+    sf = e4m3_decode(s_code)
+    safe = np.where(sf > 0, sf, 1.0)[..., None]
+    a = np.where(sf[..., None] > 0, round_f32(np.abs(blk) / safe), 0.0)
+    d = np.abs(a[..., None] - E2M1[:8])
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    even = cand & ((np.arange(8) & 1) == 0)
+    code = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1))
+    code = code.astype(np.uint8) | (np.signbit(blk).astype(np.uint8) << 3)
+    codes = code.reshape(v.shape)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return packed, s_code
+
+
+def fp4_activation(v: np.ndarray, fmt: str) -> np.ndarray:
+    """The values a W4A4 expert GEMM multiplies: bf16-valued activations
+    [..., K] rounded to MXFP4 (the OCP rule of quantize_mxfp4; muse_moe_runner
+    page, the Quark w_mxfp4_a_mxfp4 scheme with dynamic MXFP4 activations) or
+    to NVFP4 (quantize_act_nvfp4), then decoded exactly."""
+    v = np.asarray(v, dtype=np.float64)
+    K = v.shape[-1]
+    if fmt == "mxfp4":
+        packed, sc = quantize_mxfp4(f64_to_bf16_bits(v))
+        vals = E2M1[unpack_fp4(packed)]
+        return (vals.reshape(v.shape[:-1] + (K // 32, 32)) * ue8m0_decode(sc)[..., None]).reshape(v.shape)
+    if fmt == "nvfp4":
+        packed, sc = quantize_act_nvfp4(v)
+        vals = E2M1[unpack_fp4(packed)]
+        return (vals.reshape(v.shape[:-1] + (K // 16, 16)) * e4m3_decode(sc)[..., None]).reshape(v.shape)
+    raise ValueError(fmt)
+
+
 # --------------------------------------------------------------------------
 # Routed experts
 # --------------------------------------------------------------------------
@@ -371,8 +427,10 @@ def dequant_expert(quant: str, t: dict, e: int):
     fp32 global scale of the expert. FP8: e4m3 * fp32 scale per output row.
     BF16: the bf16 values (the unquantized experts of the first and last
     decoder layers: muse_moe_runner page, MuseSparkUnquantizedFusedMoE and
-    _online_mxfp4_applies).
+    _online_mxfp4_applies). The W4A4 forms ("mxfp4_a4", "nvfp4_a4") hold
+    their weights as MXFP4 / NVFP4.
     """
+    quant = {"mxfp4_a4": "mxfp4", "nvfp4_a4": "nvfp4"}.get(quant, quant)
     if quant == "mxfp4":
         w13 = _apply_block_scale(_fp4_values(t["w13"][e]), ue8m0_decode(t["w13_scale"][e]), 32)
         w2 = _apply_block_scale(_fp4_values(t["w2"][e]), ue8m0_decode(t["w2_scale"][e]), 32)
@@ -407,16 +465,21 @@ def expert_outputs(h: np.ndarray, ids: np.ndarray, quant: str, t: dict,
     up = gu[I:] (reading: the vLLM fused-w13 order, gate rows first);
     a = bf16(silu(gate) * up) (the MoE activations are bf16); y = W2_e a.
     FP8 W8A8 quantizes both expert inputs per row (quantize_rows_e4m3) and
-    multiplies the e4m3 values back by their scales. ``act_out`` ([b, k, I]),
+    multiplies the e4m3 values back by their scales. W4A4 ("mxfp4_a4",
+    "nvfp4_a4") rounds both expert inputs, h per token and a per route, to
+    the weights' FP4 format (fp4_activation). ``act_out`` ([b, k, I]),
     when given, receives the bf16 activations; ``near_act`` applies the
     near-tie rule of round_bf16_near to their rounding.
     """
     b, k = ids.shape
     P = h.shape[-1]
     y = np.zeros((b, k, P))
+    a4 = {"mxfp4_a4": "mxfp4", "nvfp4_a4": "nvfp4"}.get(quant)
     if quant == "fp8":
         qh, sh = quantize_rows_e4m3(h)
         h_in = e4m3_decode(qh) * sh[:, None]
+    elif a4 is not None:
+        h_in = fp4_activation(h, a4)
     else:
         h_in = h
     for e in np.unique(ids):
@@ -432,6 +495,8 @@ def expert_outputs(h: np.ndarray, ids: np.ndarray, quant: str, t: dict,
         if quant == "fp8":
             qa, sa = quantize_rows_e4m3(a)
             a = e4m3_decode(qa) * sa[:, None]
+        elif a4 is not None:
+            a = fp4_activation(a, a4)
         y[tok, slot] = a @ w2.T
     return y
 

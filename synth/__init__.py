@@ -32,6 +32,9 @@ _lib = None
 _lock = threading.Lock()
 
 MXFP4, NVFP4, FP8, BF16 = "mxfp4", "nvfp4", "fp8", "bf16"
+# W4A4: MXFP4 / NVFP4 weights, activations rounded to the same FP4 format
+MXFP4_A4, NVFP4_A4 = "mxfp4_a4", "nvfp4_a4"
+WEIGHT_FORMAT = {MXFP4_A4: MXFP4, NVFP4_A4: NVFP4}
 SIGMOID, SOFTMAX = "sigmoid", "softmax"
 
 # Tensor ids of the counter-based generator.
@@ -174,6 +177,14 @@ CONFIGS = {
                         top_k=2, quant=BF16, seed=5),
     "edge": Config("edge", rows=8, quant=BF16, multiplier=0.5, seed=6,
                    **{**_BIG, "experts": 32}),
+    # W4A4 (FP4 weights and FP4 activations)
+    "w4a4_tiny": Config("w4a4_tiny", rows=4, hidden=512, pooled=256, inter=128, experts=16,
+                        top_k=2, quant=MXFP4_A4, seed=7),
+    "w4a4_nv_tiny": Config("w4a4_nv_tiny", rows=5, hidden=512, pooled=256, inter=128,
+                           experts=16, top_k=3, quant=NVFP4_A4, score=SOFTMAX, seed=8),
+    "w4a4": Config("w4a4", rows=8, quant=MXFP4_A4, multiplier=0.5, seed=9, **_BIG),
+    "w4a4_nv": Config("w4a4_nv", rows=64, quant=NVFP4_A4, score=SOFTMAX, division_eps=1e-6,
+                      hot_experts=16, seed=10, **_BIG),
 }
 
 
@@ -217,6 +228,7 @@ def expert_tensors(cfg: Config, layer: int, e0: int = 0, ne: int | None = None):
     and w2_scale [ne, P, I/32].
     NVFP4: the same codes, e4m3 block scales per 16 ([.., P/16], [.., I/16])
     and an fp32 global scale per expert and matrix (w13_gscale, w2_gscale).
+    W4A4 (MXFP4_A4, NVFP4_A4): the weights of the FP4 format it names.
     BF16: bf16 N(0, 0.02) weights w13 [ne, 2I, P], w2 [ne, P, I], no scales.
     FP8: e4m3 codes w13 [ne, 2I, P], w2 [ne, P, I], fp32 scale per output
     channel (w13_scale [ne, 2I], w2_scale [ne, P]).
@@ -225,10 +237,11 @@ def expert_tensors(cfg: Config, layer: int, e0: int = 0, ne: int | None = None):
     E, P, I = cfg.experts, cfg.pooled, cfg.inter
     ne = E - e0 if ne is None else ne
     out = {}
-    if cfg.quant in (MXFP4, NVFP4):
+    wq = WEIGHT_FORMAT.get(cfg.quant, cfg.quant)
+    if wq in (MXFP4, NVFP4):
         out["w13"] = random_bytes(s, T_W13, (ne, 2 * I, P // 2), start=e0 * 2 * I * P // 2)
         out["w2"] = random_bytes(s, T_W2, (ne, P, I // 2), start=e0 * P * I // 2)
-        if cfg.quant == MXFP4:
+        if wq == MXFP4:
             out["w13_scale"] = int_u8(s, T_W13_SCALE, (ne, 2 * I, P // 32), -8, -4, 127,
                                       start=e0 * 2 * I * P // 32)
             out["w2_scale"] = int_u8(s, T_W2_SCALE, (ne, P, I // 32), -8, -4, 127,

@@ -571,3 +571,153 @@ def test_round_bf16_near_takes_only_values_inside_the_band():
     # without a hint it is plain round-to-nearest-even
     out3, n3 = O.round_bf16_near(row)
     assert n3 == 0 and np.array_equal(out3, O.round_bf16(row))
+
+
+# ---------------------------------------------------------------- W4A4 activations
+
+def _nv_expect(codes):
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
+
+
+def test_quantize_act_nvfp4_hand_worked():
+    # amax 6 -> scale e4m3(1.0) = 0x38; every e2m1 midpoint goes to the even code
+    a = [6, -3, 1.5, 0.5, 0, 2, -4, 1, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -6]
+    ca = [7, 13, 3, 1, 0, 4, 14, 2, 0, 2, 2, 4, 4, 6, 6, 15]
+    # amax 7 -> 7/6 = 1.1667 -> e4m3 1.125 (0x39); 7/1.125 = 6.22 saturates at 6;
+    # 1.125 -> 1 (code 2); -0.5625 -> 0.5 (code 9)
+    b = [7, 1.125, -0.5625] + [0] * 13
+    cb = [7, 2, 9] + [0] * 13
+    # all zero with one -0: scale 0, the sign bit kept
+    c = [0, -0.0] + [0] * 14
+    cc = [0, 8] + [0] * 14
+    # amax 2944 -> 490.7 saturates at 448 (0x7E); 2944/448 = 6.6 -> 6; 448 -> 1
+    d = [2944, 448] + [0] * 14
+    cd = [7, 2] + [0] * 14
+    # amax 2^-12 -> 2^-12/6 below half the smallest e4m3 subnormal: scale 0
+    e = [2.0 ** -12, -(2.0 ** -13)] + [0] * 14
+    ce = [0, 8] + [0] * 14
+    # amax 3 * 2^-8 -> exactly 2^-9, the smallest subnormal (0x01); 2^-10 -> 0.5
+    f = [3 * 2.0 ** -8, 2.0 ** -10] + [0] * 14
+    cf = [7, 1] + [0] * 14
+    rows = np.array([a + b + c + d + e + f], dtype=np.float64)
+    packed, sc = O.quantize_act_nvfp4(rows)
+    want = np.concatenate([_nv_expect(x) for x in (ca, cb, cc, cd, ce, cf)])
+    np.testing.assert_array_equal(packed[0], want)
+    np.testing.assert_array_equal(sc[0], np.array([0x38, 0x39, 0x00, 0x7E, 0x00, 0x01], np.uint8))
+    vals = O.fp4_activation(rows, "nvfp4")[0]
+    np.testing.assert_array_equal(vals[16:19], [6.75, 1.125, -0.5625])
+    assert vals[48] == 6 * 448.0 and vals[80] == 6 * 2.0 ** -9
+
+
+def _e4m3_table():
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().double().numpy()
+
+
+def test_quantize_act_nvfp4_brute_force():
+    # every scale is the nearest finite non-negative e4m3 value to fp32(amax/6)
+    # (ties to the even code, saturating), every code the nearest e2m1
+    # magnitude to fp32(|v| / scale) (ties to the even code), searched over all
+    tab = _e4m3_table()
+    pos = np.arange(127)  # finite codes 0x00..0x7E
+    rng = np.random.default_rng(53)
+    mags = 2.0 ** rng.integers(-14, 12, size=(48, 1))
+    v = O.round_bf16(rng.standard_normal((48, 16)) * mags)
+    packed, sc = O.quantize_act_nvfp4(v)
+    codes = O.unpack_fp4(packed)
+    for r in range(v.shape[0]):
+        t = np.float32(np.abs(v[r]).max()) / np.float32(6.0)
+        dist = np.abs(tab[pos] - float(t))
+        best = pos[dist == dist.min()]
+        s = best[0] if len(best) == 1 else best[best % 2 == 0][0]
+        if float(t) > 448.0:
+            s = 0x7E
+        assert sc[r, 0] == s, (r, sc[r, 0], s)
+        sf = tab[s]
+        for j in range(16):
+            q = 0.0 if sf == 0 else float(np.float32(abs(v[r, j])) / np.float32(sf))
+            d = np.abs(O.E2M1[:8] - q)
+            m = np.nonzero(d == d.min())[0]
+            mc = m[0] if len(m) == 1 else m[m % 2 == 0][0]
+            assert codes[r, j] == (mc | (8 if np.signbit(v[r, j]) else 0)), (r, j)
+
+
+def test_fp4_activation_round_trips_representable_blocks():
+    rng = np.random.default_rng(59)
+    mv = rng.choice(O.E2M1[1:8], size=(6, 32)) * rng.choice([-1.0, 1.0], size=(6, 32))
+    # MXFP4: a block whose amax is 6 * 2^e holds e2m1 multiples of 2^e exactly
+    ex = rng.integers(-6, 6, size=(6, 1))
+    mx = mv.copy()
+    mx[:, 0] = 6.0
+    mx = mx * 2.0 ** ex
+    np.testing.assert_array_equal(O.fp4_activation(mx, "mxfp4"), mx)
+    # NVFP4: amax = 6 * s with s an e4m3 value gives the scale s back
+    s = np.array([1.0, 0.5, 1.125, 2.0 ** -9, 448.0, 13.0])[:, None]
+    nv = mv[:, :16].copy()
+    nv[:, 3] = -6.0
+    nv = nv * s
+    np.testing.assert_array_equal(O.fp4_activation(nv, "nvfp4"), nv)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+def test_w4a4_expert_outputs_one_hot(fmt):
+    # one-hot experts: gate_i = h[i], up_i = h[I + i] and y[p] = a[p] (p < I), so
+    # y is the FP4 rounding of bf16(silu(hq[i]) * hq[I + i]) with hq the FP4
+    # rounding of h: both expert inputs rounded, at the format's block size
+    P, I = 64, 32
+    w13 = np.zeros((1, 2 * I, P), np.uint8)
+    for i in range(2 * I):
+        w13[0, i, i] = 2  # e2m1 1.0
+    w2 = np.zeros((1, P, I), np.uint8)
+    for p in range(I):
+        w2[0, p, p] = 2
+    pk = lambda c: (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    t = {"w13": pk(w13), "w2": pk(w2)}
+    if fmt == "mxfp4":
+        t["w13_scale"] = np.full((1, 2 * I, P // 32), 127, np.uint8)
+        t["w2_scale"] = np.full((1, P, I // 32), 127, np.uint8)
+    else:
+        t["w13_scale"] = np.full((1, 2 * I, P // 16), 0x38, np.uint8)
+        t["w2_scale"] = np.full((1, P, I // 16), 0x38, np.uint8)
+        t["w13_gscale"] = np.ones(1, np.float32)
+        t["w2_gscale"] = np.ones(1, np.float32)
+    rng = np.random.default_rng(61)
+    h = O.round_bf16(rng.standard_normal((2, P)) * np.array([[1.0], [0.03]]))
+    ids = np.zeros((2, 1), np.int64)
+    y = O.expert_outputs(h, ids, fmt + "_a4", t, I)[:, 0]
+
+    def fp4(v, block):  # brute force over the block's scale and the 8 magnitudes
+        out = np.empty_like(v)
+        tab = _e4m3_table()
+        for r in range(v.shape[0]):
+            for b0 in range(0, v.shape[1], block):
+                x = v[r, b0:b0 + block]
+                amax = np.abs(x).max()
+                if block == 32:
+                    sf = 2.0 ** (np.floor(np.log2(amax)) - 2) if amax > 0 else 1.0
+                    q = np.abs(x) / sf
+                else:
+                    t6 = float(np.float32(amax) / np.float32(6.0))
+                    fin = tab[:127]
+                    dd = np.abs(fin - t6)
+                    cands = np.nonzero(dd == dd.min())[0]
+                    sf = fin[cands[0] if len(cands) == 1 else cands[cands % 2 == 0][0]]
+                    q = (np.abs(x).astype(np.float32) / np.float32(sf)).astype(np.float64) \
+                        if sf > 0 else np.zeros_like(x)
+                d = np.abs(O.E2M1[:8][None, :] - q[:, None])
+                pick = []
+                for row in d:
+                    m = np.nonzero(row == row.min())[0]
+                    pick.append(m[0] if len(m) == 1 else m[m % 2 == 0][0])
+                out[r, b0:b0 + block] = np.sign(x) * O.E2M1[np.array(pick)] * sf
+        return out
+
+    blk = 32 if fmt == "mxfp4" else 16
+    hq = fp4(h, blk)
+    g, u = hq[:, :I], hq[:, I:]
+    a = torch.tensor(g / (1 + np.exp(-g)) * u).to(torch.bfloat16).double().numpy()
+    want = np.zeros((2, P))
+    want[:, :I] = fp4(a, blk)
+    np.testing.assert_array_equal(y, want)
+    # and neither input is left unrounded
+    assert not np.array_equal(hq, h) and not np.array_equal(want[:, :I], a)
