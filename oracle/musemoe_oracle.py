@@ -370,6 +370,9 @@ def quantize_act_nvfp4(v: np.ndarray):
     sf = e4m3_decode(s_code)
     safe = np.where(sf > 0, sf, 1.0)[..., None]
     a = np.where(sf[..., None] > 0, round_f32(np.abs(blk) / safe), 0.0)
+    # every quotient of 6 or more saturates to 6; bounding it keeps the
+    # distances below exact (at quotients near 1e35 they would all be equal)
+    a = np.minimum(a, 8.0)
     d = np.abs(a[..., None] - E2M1[:8])
     best = d.min(axis=-1, keepdims=True)
     cand = d == best

@@ -600,11 +600,15 @@ def test_quantize_act_nvfp4_hand_worked():
     # amax 3 * 2^-8 -> exactly 2^-9, the smallest subnormal (0x01); 2^-10 -> 0.5
     f = [3 * 2.0 ** -8, 2.0 ** -10] + [0] * 14
     cf = [7, 1] + [0] * 14
-    rows = np.array([a + b + c + d + e + f], dtype=np.float64)
+    # the largest finite bf16: scale 448, a quotient near 7.6e35 saturates to 6
+    g = [3.3895313892515355e38, -1.0] + [0] * 14
+    cg = [7, 8] + [0] * 14
+    rows = np.array([a + b + c + d + e + f + g], dtype=np.float64)
     packed, sc = O.quantize_act_nvfp4(rows)
-    want = np.concatenate([_nv_expect(x) for x in (ca, cb, cc, cd, ce, cf)])
+    want = np.concatenate([_nv_expect(x) for x in (ca, cb, cc, cd, ce, cf, cg)])
     np.testing.assert_array_equal(packed[0], want)
-    np.testing.assert_array_equal(sc[0], np.array([0x38, 0x39, 0x00, 0x7E, 0x00, 0x01], np.uint8))
+    np.testing.assert_array_equal(sc[0], np.array([0x38, 0x39, 0x00, 0x7E, 0x00, 0x01, 0x7E],
+                                                  np.uint8))
     vals = O.fp4_activation(rows, "nvfp4")[0]
     np.testing.assert_array_equal(vals[16:19], [6.75, 1.125, -0.5625])
     assert vals[48] == 6 * 448.0 and vals[80] == 6 * 2.0 ** -9
