@@ -204,27 +204,23 @@ def run_oracle(steps: int, budget_s: float, threads: int = 1) -> dict:
 
 # ------------------------------------------------------------ our arm
 
-def bench_bf16_experts(dev, hbm_peak: float) -> dict:
-    """The decode workload's shapes with BF16 experts (the unquantized form of
-    the first and last decoder layers): one weight set of 128 experts (1.6 GB;
-    the ~46 experts a step selects, about 560 MB, dwarf L2). Step time of a
-    graph of the forward, and the expert phase (w13 + w2 event times) against
-    its algorithmic bytes."""
-    import dataclasses
-
+def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20) -> dict:
+    """One weight set of ``cfg`` in the form ``quant_code``: the step time of a
+    graph of one forward (``steps`` replays after 10), the per-kernel event
+    times of ``reps`` debug forwards, and the selected experts."""
     import numpy as np
     import torch
 
     import moe_decode_layer_router_gb300 as mm
     import synth
 
-    cfg = dataclasses.replace(synth.CONFIGS["edge"], experts=128)
     dims = mm.Dims(max_rows=cfg.rows, hidden=cfg.hidden, pooled=cfg.pooled, inter=cfg.inter,
                    experts=cfg.experts, top_k=cfg.top_k)
-    conf = mm.Config(score=mm.MUSEMOE_SIGMOID, route_scale=cfg.route_scale, has_multiplier=1,
-                     multiplier=cfg.multiplier, has_division_eps=1,
-                     division_eps=cfg.division_eps, norm_eps=cfg.norm_eps, pre_expert_norm=1)
-    handle = mm.musemoe_create(dims, mm.MUSEMOE_BF16, conf)
+    conf = mm.Config(score=mm.MUSEMOE_SIGMOID if cfg.score == synth.SIGMOID else mm.MUSEMOE_SOFTMAX,
+                     route_scale=cfg.route_scale, has_multiplier=cfg.multiplier is not None,
+                     multiplier=cfg.multiplier or 1.0, has_division_eps=cfg.division_eps is not None,
+                     division_eps=cfg.division_eps or 0.0, norm_eps=cfg.norm_eps, pre_expert_norm=1)
+    handle = mm.musemoe_create(dims, quant_code, conf)
 
     def to_dev(a):
         if a.dtype == np.uint16:
@@ -232,8 +228,9 @@ def bench_bf16_experts(dev, hbm_peak: float) -> dict:
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     t = {k: to_dev(v) for k, v in synth.layer_tensors(cfg).items()}
-    mm.musemoe_pack_experts(dims, mm.MUSEMOE_BF16, t["w13"], None, t["w13"], None, t["w2"],
-                            None, t["w2"], None)
+    mm.musemoe_pack_experts(dims, quant_code, t["w13"], t.get("w13_scale"), t["w13"],
+                            t.get("w13_scale"), t["w2"], t.get("w2_scale"), t["w2"],
+                            t.get("w2_scale"))
     w = mm.make_weights(t)
     x, st = synth.activations(cfg)
     xd, sd = to_dev(x), to_dev(st)
@@ -245,7 +242,6 @@ def bench_bf16_experts(dev, hbm_peak: float) -> dict:
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         mm.musemoe_forward(handle, w, xd, sd, out, cfg.rows, s)
-    steps = 200
     with torch.cuda.stream(s):
         for _ in range(10):
             g.replay()
@@ -256,35 +252,73 @@ def bench_bf16_experts(dev, hbm_peak: float) -> dict:
         e1.record(s)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / steps
-    n = mm.musemoe_num_kernels(mm.MUSEMOE_BF16)
-    names = [mm.musemoe_kernel_name(mm.MUSEMOE_BF16, i) for i in range(n)]
+    n = mm.musemoe_num_kernels(quant_code)
+    names = [mm.musemoe_kernel_name(quant_code, i) for i in range(n)]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
     for e in ev:  # torch creates an event on its first record
         e.record(s)
     ids = torch.empty((cfg.rows, cfg.top_k), dtype=torch.int32, device=dev)
     dur = {nm: 0.0 for nm in names}
-    reps = 20
     with torch.cuda.stream(s):
         for _ in range(reps):
             mm.musemoe_forward_debug(handle, w, xd, sd, out, cfg.rows, s,
                                      mm.make_taps(events=ev, ids=ids))
             s.synchronize()
             for i, nm in enumerate(names):
-                dur[nm] += ev[2 * i].elapsed_time(ev[2 * i + 1]) / reps
+                dur[nm] += ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 / reps
     active = len(np.unique(ids.cpu().numpy()))
-    ebytes = active * (2 * cfg.inter * cfg.pooled + cfg.pooled * cfg.inter) * 2
-    e_us = (dur["w13"] + dur["w2"]) * 1e3
     health = mm.musemoe_poll_health(handle)
     mm.musemoe_destroy(handle)
-    del t
+    del t, g
+    torch.cuda.empty_cache()
+    return {"us_per_step": us, "kernel_us": dur, "active_experts": active,
+            "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range"}
+
+
+def bench_bf16_experts(dev, hbm_peak: float) -> dict:
+    """The decode workload's shapes with BF16 experts (the unquantized form of
+    the first and last decoder layers): one weight set of 128 experts (1.6 GB;
+    the ~46 experts a step selects, about 560 MB, dwarf L2). Step time of a
+    graph of the forward, and the expert phase (w13 + w2 event times) against
+    its algorithmic bytes."""
+    import dataclasses
+
+    import moe_decode_layer_router_gb300 as mm
+    import synth
+
+    cfg = dataclasses.replace(synth.CONFIGS["edge"], experts=128)
+    r = _bench_form(dev, cfg, mm.MUSEMOE_BF16)
+    us, dur = r["us_per_step"], r["kernel_us"]
+    ebytes = r["active_experts"] * (2 * cfg.inter * cfg.pooled + cfg.pooled * cfg.inter) * 2
+    e_us = dur["w13"] + dur["w2"]
     return {"workload": f"decode shapes (b={cfg.rows}, H={cfg.hidden}, P={cfg.pooled}, "
                         f"I={cfg.inter}, E={cfg.experts}, top-{cfg.top_k}) with BF16 experts",
             "rows_per_s": cfg.rows / (us / 1e6), "us_per_step": us,
-            "active_experts": active, "expert_bytes": ebytes,
+            "active_experts": r["active_experts"], "expert_bytes": ebytes,
             "expert_phase_us": e_us, "expert_phase_gbs": ebytes / (e_us / 1e6) / 1e9,
             "expert_phase_frac": ebytes / (e_us / 1e6) / 1e9 / hbm_peak,
-            "kernel_us": {k: v * 1e3 for k, v in dur.items()},
-            "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range"}
+            "kernel_us": dur, "health": r["health"]}
+
+
+def bench_w4a4(dev) -> dict:
+    """The decode workload (b=8, E=128, top-8) in the W4A4 forms next to its
+    W4A16 form, each timed the same way (one weight set, a graph of one
+    forward): what rounding both expert inputs to FP4 costs per step."""
+    import dataclasses
+
+    import moe_decode_layer_router_gb300 as mm
+    import synth
+
+    res = {"workload": "decode (b=8, H=5120, P=2048, I=1024, E=128, top-8), one weight set, "
+                       "graph of one forward"}
+    for name, quant, code in [("mxfp4_w4a16", synth.MXFP4, mm.MUSEMOE_MXFP4),
+                              ("mxfp4_w4a4", synth.MXFP4_A4, mm.MUSEMOE_MXFP4_A4),
+                              ("nvfp4_w4a4", synth.NVFP4_A4, mm.MUSEMOE_NVFP4_A4)]:
+        cfg = dataclasses.replace(synth.CONFIGS["decode"], quant=quant)
+        r = _bench_form(dev, cfg, code)
+        res[name] = {"us_per_step": r["us_per_step"], "rows_per_s": cfg.rows / (r["us_per_step"] / 1e6),
+                     "kernel_us": r["kernel_us"], "health": r["health"]}
+    return res
 
 
 def bench_ours(args):
@@ -532,6 +566,7 @@ def bench_ours(args):
     health = mm.musemoe_poll_health(handle)
     mm.musemoe_destroy(handle)
     bf16_experts = bench_bf16_experts(dev, hbm_peak)
+    w4a4 = bench_w4a4(dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -574,7 +609,7 @@ def bench_ours(args):
         "cpu_baseline": cpu,
         "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
         "next": {"attention_boundary": attn_boundary, "quantize_mxfp4": quant_mxfp4,
-                 "bf16_experts": bf16_experts},
+                 "bf16_experts": bf16_experts, "w4a4": w4a4},
     }
     if world > 1:
         import torch.distributed as dist

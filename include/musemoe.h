@@ -77,6 +77,16 @@ typedef enum {
    * keep (page "vllm.models.muse_spark.amd.muse_moe_runner",
    * MuseSparkUnquantizedFusedMoE and _online_mxfp4_applies); no scales */
   MUSEMOE_BF16 = 3,
+  /* W4A4: MXFP4 weights (as MUSEMOE_MXFP4) and both expert inputs, h per
+   * token and SiLU(gate)*up per route, rounded dynamically to MXFP4 (OCP
+   * rule: scale 2^(floor(log2 amax) - 2) per 32, nearest e2m1, ties to
+   * even); page "vllm.models.muse_spark.amd.muse_moe_runner", the Quark
+   * w_mxfp4_a_mxfp4 scheme. One extra launch (act_quant) per forward. */
+  MUSEMOE_MXFP4_A4 = 4,
+  /* W4A4: NVFP4 weights (as MUSEMOE_NVFP4) and both expert inputs rounded
+   * to NVFP4 (e4m3 scale nearest amax / 6 per 16, no global scale;
+   * providers page, ExpertsInput). */
+  MUSEMOE_NVFP4_A4 = 5,
 } musemoe_quant;
 
 typedef enum { MUSEMOE_SIGMOID = 0, MUSEMOE_SOFTMAX = 1 } musemoe_score;
@@ -286,6 +296,23 @@ musemoe_status musemoe_attention_boundary(const uint16_t *partial, float *stream
 musemoe_status musemoe_quantize_mxfp4(const uint16_t *w_bf16, uint8_t *codes, uint8_t *scales,
                                       int64_t rows, int32_t cols, musemoe_stream_t stream);
 
+/* The NVFP4 expert input (page
+ * "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
+ * ExpertsInput): bf16 activations [rows, cols] -> e2m1 codes [rows, cols/2]
+ * (element 2j in the low nibble of byte j) and e4m3 block scales
+ * [rows, cols/16]. Per 16 elements the scale is the e4m3 value nearest
+ * fp32(amax / 6) (ties to even, saturating at 448); each element takes the
+ * e2m1 magnitude nearest fp32(|v| / scale), ties to the even code,
+ * saturating at 6, sign kept; a block whose scale is 0 gets magnitude 0.
+ * The same rounding as the MUSEMOE_NVFP4_A4 forward. Device pointers:
+ * x_bf16 and codes 16-byte aligned; cols a multiple of 16; the caller owns
+ * them. No handle and no allocation; asynchronous on stream. EINVAL with the
+ * reason in musemoe_last_error(NULL) on bad arguments, ECUDA if the launch
+ * fails. (The MXFP4 expert input of MUSEMOE_MXFP4_A4 is
+ * musemoe_quantize_mxfp4 applied to the activations.) */
+musemoe_status musemoe_quantize_act_nvfp4(const uint16_t *x_bf16, uint8_t *codes, uint8_t *scales,
+                                          int64_t rows, int32_t cols, musemoe_stream_t stream);
+
 /* Health self-test: runs the library's two bounded waits once on the
  * handle's device, each on something nothing ever completes (an mbarrier
  * phase, as a stage whose weight copies never land; a flag, as a split
@@ -301,7 +328,8 @@ musemoe_status musemoe_health_selftest(musemoe_handle *handle, musemoe_stream_t 
  * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
  * ran out since the last poll (that forward's outputs are invalid),
  * MUSEMOE_ERANGE if a forward produced an expert operand (h or the
- * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504), MUSEMOE_OK
+ * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504; W4A4: an
+ * FP4-rounded input that fp16 does not hold exactly), MUSEMOE_OK
  * otherwise. */
 musemoe_status musemoe_poll_health(musemoe_handle *handle);
 

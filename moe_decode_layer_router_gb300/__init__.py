@@ -18,18 +18,20 @@ from . import _build
 
 __all__ = [
     "MUSEMOE_OK", "MUSEMOE_EINVAL", "MUSEMOE_EUNSUPPORTED", "MUSEMOE_ECUDA", "MUSEMOE_ENOMEM",
-    "MUSEMOE_ERANGE", "MUSEMOE_ETIMEOUT", "MUSEMOE_MXFP4", "MUSEMOE_NVFP4", "MUSEMOE_FP8_W8A8", "MUSEMOE_BF16", "MUSEMOE_SIGMOID",
+    "MUSEMOE_ERANGE", "MUSEMOE_ETIMEOUT", "MUSEMOE_MXFP4", "MUSEMOE_NVFP4", "MUSEMOE_FP8_W8A8", "MUSEMOE_BF16",
+    "MUSEMOE_MXFP4_A4", "MUSEMOE_NVFP4_A4", "MUSEMOE_SIGMOID",
     "MUSEMOE_SOFTMAX", "Dims", "Config", "Weights", "Taps", "MuseMoEError", "library",
     "musemoe_create", "musemoe_destroy", "musemoe_last_error", "musemoe_workspace_bytes",
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
-    "musemoe_health_selftest", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
+    "musemoe_quantize_act_nvfp4", "musemoe_health_selftest", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
 ]
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
  MUSEMOE_ETIMEOUT) = (0, 1, 2, 3, 4, 5, 6)
 MUSEMOE_MXFP4, MUSEMOE_NVFP4, MUSEMOE_FP8_W8A8, MUSEMOE_BF16 = 0, 1, 2, 3
+MUSEMOE_MXFP4_A4, MUSEMOE_NVFP4_A4 = 4, 5
 MUSEMOE_SIGMOID, MUSEMOE_SOFTMAX = 0, 1
 _STATUS = {0: "OK", 1: "EINVAL", 2: "EUNSUPPORTED", 3: "ECUDA", 4: "ENOMEM", 5: "ERANGE",
            6: "ETIMEOUT"}
@@ -67,7 +69,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
-    "musemoe_health_selftest",
+    "musemoe_quantize_act_nvfp4", "musemoe_health_selftest",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
 MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
@@ -113,6 +115,7 @@ def library() -> ctypes.CDLL:
         lib.musemoe_attention_boundary.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                                                    c_f32, c_vp]
         lib.musemoe_quantize_mxfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
+        lib.musemoe_quantize_act_nvfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
         lib.musemoe_health_selftest.argtypes = [c_vp, c_vp]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
@@ -246,6 +249,14 @@ def musemoe_quantize_mxfp4(w_bf16, codes, scales, rows: int, cols: int, stream=N
     [rows, cols/2] and UE8M0 scales [rows, cols/32] (see include/musemoe.h)."""
     _check(library().musemoe_quantize_mxfp4(_addr(w_bf16), _addr(codes), _addr(scales), rows,
                                             cols, _stream(stream)))
+
+
+def musemoe_quantize_act_nvfp4(x_bf16, codes, scales, rows: int, cols: int, stream=None) -> None:
+    """The NVFP4 expert input: bf16 activations [rows, cols] to e2m1 codes
+    [rows, cols/2] and e4m3 block scales [rows, cols/16] (see
+    include/musemoe.h)."""
+    _check(library().musemoe_quantize_act_nvfp4(_addr(x_bf16), _addr(codes), _addr(scales), rows,
+                                                cols, _stream(stream)))
 
 
 def make_weights(tensors: dict) -> Weights:

@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
             su = __ldg(ws + (size_t)e * p.N + p.I + i) * bs;
           }
           const float a = round_bf16(silu(v[nt][h] * sg) * (v[nt][2 + h] * su));
-          if (Q == kFP8 || Q == kBF16) {
+          if (Q == kFP8 || Q == kBF16 || p.act_bf16) {
             reinterpret_cast<uint16_t*>(p.out)[(size_t)ro * p.I + i] = f32_to_bf16_bits(a);
           } else {
             reinterpret_cast<__half*>(p.out)[(size_t)ro * p.I + i] = __float2half_rn(a);

@@ -13,24 +13,15 @@
 // Each lane rounds 8 consecutive elements (one 16-byte load); the 4 lanes of
 // a block take its amax with two shuffles on the bf16 magnitude bits, which
 // order like unsigned integers, so the scale needs no floating point.
-#include "common.cuh"
+//
+// Also here: the NVFP4 expert input of the W4A4 form (codes and e4m3 block
+// scales, the rule in act4.cuh).
+#include "act4.cuh"
 #include "kernels.h"
 
 namespace musemoe {
 
 constexpr int kQuantThreads = 256;
-
-__device__ __forceinline__ uint32_t e2m1_nearest(float a) {
-  // round to nearest on {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code
-  return a <= 0.25f ? 0u
-       : a < 0.75f  ? 1u
-       : a <= 1.25f ? 2u
-       : a < 1.75f  ? 3u
-       : a <= 2.5f  ? 4u
-       : a < 3.5f   ? 5u
-       : a <= 5.0f  ? 6u
-                    : 7u;
-}
 
 // The 8 elements of one lane: amax over its block's 4 lanes, scale, codes.
 __device__ __forceinline__ void quant8(const uint4& v, long long i, bool ok, int lane,
@@ -83,6 +74,53 @@ cudaError_t launch_quant_mxfp4(const uint16_t* w, uint8_t* codes, uint8_t* scale
   grid = grid < (long long)sms * 16 ? grid : (long long)sms * 16;
   if (grid < 1) grid = 1;
   k_quant_mxfp4<<<(unsigned)grid, kQuantThreads, 0, s>>>(w, codes, scales, n8);
+  return cudaGetLastError();
+}
+
+// The NVFP4 expert input (providers page, ExpertsInput): bf16 activations
+// [rows, cols] -> e2m1 codes [rows, cols/2] (element 2j in the low nibble of
+// byte j) and one e4m3 block scale per 16 elements [rows, cols/16]. Each
+// lane rounds 8 consecutive elements (one 16-byte load); the 2 lanes of a
+// block take its amax with one shuffle.
+__global__ void __launch_bounds__(kQuantThreads) k_quant_act_nvfp4(const uint16_t* x, uint8_t* codes,
+                                                                  uint8_t* scales, long long n8) {
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * kQuantThreads;
+  // n8 is even, so the 2 lanes of a block are both in range or both out
+  for (long long base = (long long)blockIdx.x * kQuantThreads + (threadIdx.x & ~31); base < n8;
+       base += stride) {
+    const long long i = base + lane;
+    const uint4 v = i < n8 ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[j] = bf16_bits_to_f32((j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xFFFFu));
+      m = fmaxf(m, fabsf(f[j]));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const uint32_t sc = nv_scale_code(m);
+    Fp4Scale s;
+    s.scale = e4m3_to_f32(sc);
+    s.inv = 0.f;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) packed |= fp4_code2(f[2 * j], f[2 * j + 1], s, 2) << (8 * j);
+    if (i < n8) {
+      reinterpret_cast<uint32_t*>(codes)[i] = packed;
+      if ((lane & 1) == 0) scales[i >> 1] = (uint8_t)sc;
+    }
+  }
+}
+
+cudaError_t launch_quant_act_nvfp4(const uint16_t* x, uint8_t* codes, uint8_t* scales,
+                                   long long elements, int sms, cudaStream_t s) {
+  const long long n8 = elements / 8;
+  long long grid = (n8 + kQuantThreads - 1) / kQuantThreads;
+  grid = grid < (long long)sms * 16 ? grid : (long long)sms * 16;
+  if (grid < 1) grid = 1;
+  k_quant_act_nvfp4<<<(unsigned)grid, kQuantThreads, 0, s>>>(x, codes, scales, n8);
   return cudaGetLastError();
 }
 

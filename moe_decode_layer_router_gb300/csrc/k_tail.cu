@@ -1,6 +1,7 @@
 // Tail of the expert phase: the FP8 per-route requantization of the bf16
 // activation between w13 and w2, and the per-route post-expert norm, router
 // weighting and sum over the k routes of each token.
+#include "act4.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "pipeline.cuh"
@@ -62,9 +63,58 @@ __global__ void __launch_bounds__(256) k_act_quant(ActQuantParams p) {
   if (lane == 0) p.scale[r] = s;
 }
 
+// ---- W4A4: per-route FP4 rounding of the bf16 activation ------------------
+// (page "vllm.models.muse_spark.amd.muse_moe_runner": the Quark
+// w_mxfp4_a_mxfp4 scheme rounds the expert inputs to MXFP4 dynamically;
+// providers page, ExpertsInput: the NVFP4 form). One warp per 256 elements
+// of a route (I is a multiple of 128, so a warp's span is whole blocks); a
+// lane rounds 8 consecutive elements (one 16-byte load), so a block is 4
+// (MXFP4) or 2 (NVFP4) neighbouring lanes. The rounded values are stored as
+// w2's f16 operand; one that f16 cannot hold exactly raises kHealthActRange.
+constexpr int kActSpan = 256;
+
+__global__ void __launch_bounds__(256) k_act_fp4(ActQuantParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int spans = (p.I + kActSpan - 1) / kActSpan;
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid >= p.routes * spans) return;  // the whole warp
+  const int r = wid / spans;
+  const int i = (wid - r * spans) * kActSpan + lane * 8;
+  const bool ok = i < p.I;
+  const uint4 v = ok ? __ldcg(reinterpret_cast<const uint4*>(p.act + (size_t)r * p.I + i))
+                     : make_uint4(0, 0, 0, 0);
+  const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+  float x[8];
+  float m = 0.f;
+  int bad = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    x[j] = bf16_bits_to_f32((j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xFFFFu));
+    m = fmaxf(m, fabsf(x[j]));
+    bad |= !(fabsf(x[j]) <= 3.0e38f);  // NaN or infinite
+  }
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  if (p.mode == 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  const Fp4Scale sc = fp4_block_scale(m, p.mode);
+  uint32_t o[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float r0, r1;
+    fp4_value2(fp4_code2(x[2 * c], x[2 * c + 1], sc, p.mode), sc, r0, r1);
+    const __half2 h2 = __floats2half2_rn(r0, r1);
+    bad |= (__low2float(h2) != r0) | (__high2float(h2) != r1);
+    o[c] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  if (ok) reinterpret_cast<uint4*>(p.q + ((size_t)r * p.I + i) * 2)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  if (bad) atomicOr(p.health, kHealthActRange);
+}
+
 cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.routes + 7) / 8);
+  cfg.gridDim = p.mode ? dim3((p.routes * ((p.I + kActSpan - 1) / kActSpan) + 7) / 8)
+                       : dim3((p.routes + 7) / 8);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -72,7 +122,7 @@ cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_act_quant, p);
+  return p.mode ? cudaLaunchKernelEx(&cfg, k_act_fp4, p) : cudaLaunchKernelEx(&cfg, k_act_quant, p);
 }
 
 // ---- tail: post-expert norm of each route, router weight, sum over k ------

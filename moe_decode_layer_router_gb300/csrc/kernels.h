@@ -60,6 +60,7 @@ struct FrontParams {
   // block applies the pre-expert RMSNorm to the block's rows of y
   const uint16_t* w_pre_norm;  // bf16 [M]
   int pre_norm, quant;
+  int act4;             // W4A4: h_op holds h rounded to MXFP4 (1) or NVFP4 (2)
   float norm_eps;
   uint16_t* h;          // bf16 [rows, M]
   uint8_t* h_op;        // f16 [rows, M] (FP4) or e4m3 [rows, M] (FP8)
@@ -96,6 +97,7 @@ struct ExpertParams {
   const int32_t* groups;
   const int32_t* counters;
   void* out;               // role 0: act f16/bf16 [rows*k, I]; role 1: y fp32 [rows*k, P]
+  int act_bf16;            // role 0, FP4 weights: store act as bf16 (W4A4 rounds it next)
   int32_t* health;
   float* part;             // partial sums of tiles split across CTAs (expert_part_bytes)
   int32_t* tickets;        // tile tickets (expert_tickets), zero between launches
@@ -108,11 +110,15 @@ size_t expert_part_bytes(int grid, int nt);
 size_t expert_tickets(int max_groups, int quant, int role, int K, int N);
 
 // FP8 only: per-route dynamic e4m3 quantization of the bf16 activation.
+// W4A4 (mode 1 MXFP4, 2 NVFP4): per-route FP4 rounding of the bf16
+// activation into w2's f16 operand (the rounded values, exact in f16).
 struct ActQuantParams {
   const uint16_t* act;  // bf16 [routes, I]
-  uint8_t* q;           // e4m3 [routes, I]
-  float* scale;         // [routes]
+  uint8_t* q;           // mode 0: e4m3 [routes, I]; modes 1, 2: f16 [routes, I]
+  float* scale;         // mode 0: [routes]
   int routes, I;
+  int mode;             // 0 FP8, 1 MXFP4, 2 NVFP4
+  int32_t* health;      // modes 1, 2: kHealthActRange when a value is not exact in f16
 };
 cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl);
 
@@ -151,6 +157,9 @@ cudaError_t launch_wait_selftest(int32_t* health, const int32_t* never, cudaStre
 // scales [rows, cols/32]; w 16-byte aligned, codes 4-byte aligned.
 cudaError_t launch_quant_mxfp4(const uint16_t* w, uint8_t* codes, uint8_t* scales,
                                long long elements, int sms, cudaStream_t s);
+// The NVFP4 expert input: bf16 [*, 16 m] -> e2m1 codes + e4m3 scales per 16.
+cudaError_t launch_quant_act_nvfp4(const uint16_t* x, uint8_t* codes, uint8_t* scales,
+                                   long long elements, int sms, cudaStream_t s);
 
 // ---- weight re-layout ----------------------------------------------------
 // Kernel layout of a [rows, row_bytes] expert tensor cut into cb-byte chunks

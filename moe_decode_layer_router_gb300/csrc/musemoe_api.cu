@@ -52,7 +52,8 @@ void musemoe::set_thread_error(const std::string& m) { g_thread_err = m; }
 
 struct musemoe_handle {
   musemoe_dims d{};
-  int quant = 0;
+  int quant = 0;  // the weight format (Quant)
+  int act4 = 0;   // W4A4: expert inputs rounded to MXFP4 (1) or NVFP4 (2)
   musemoe_config cfg{};
   int device = -1, sms = 0;
   int max_routes = 0, max_groups = 0;
@@ -75,6 +76,11 @@ struct musemoe_handle {
 };
 
 namespace {
+
+// public quant code -> the weights' format and the W4A4 activation rounding
+constexpr int kMXFP4_A4 = 4, kNVFP4_A4 = 5;
+int weight_format(int q) { return q == kMXFP4_A4 ? kMXFP4 : q == kNVFP4_A4 ? kNVFP4 : q; }
+int act4_of(int q) { return q == kMXFP4_A4 ? 1 : q == kNVFP4_A4 ? 2 : 0; }
 
 struct Layout {
   size_t off = 0;
@@ -111,6 +117,8 @@ void plan(musemoe_handle* h, Layout& L) {
   if (fp8) {
     L.add(&h->act_q, RT * I);
     L.add(&h->act_scale, RT * 4);
+  } else if (h->act4) {
+    L.add(&h->act_q, RT * I * 2);  // w2's f16 operand
   }
   L.add(&h->y, RT * P * 4);
   // Stream-K partial sums (shared by w13 and w2, which run one after the
@@ -146,8 +154,9 @@ std::vector<std::string> refusals(const musemoe_dims* d, int32_t quant, const mu
     r.push_back(fmt("hidden %d above %d (a pooler row tile held in shared memory)", d->hidden, front_max_k()));
   if (d->pooled > front_max_k())
     r.push_back(fmt("pooled %d above %d (an unpooler row tile held in shared memory)", d->pooled, front_max_k()));
-  if (quant < 0 || quant > 3)
-    r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1), FP8_W8A8 (2) or BF16 (3)", quant));
+  if (quant < 0 || quant > 5)
+    r.push_back(fmt("quant %d is not MXFP4 (0), NVFP4 (1), FP8_W8A8 (2), BF16 (3), "
+                    "MXFP4_A4 (4) or NVFP4_A4 (5)", quant));
   if (c->score != 0 && c->score != 1) r.push_back(fmt("score %d is not sigmoid (0) or softmax (1)", c->score));
   if (!std::isfinite(c->route_scale)) r.push_back("route_scale is not finite");
   if (c->has_multiplier && !std::isfinite(c->multiplier)) r.push_back("multiplier is not finite");
@@ -248,6 +257,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fp.w_pre_norm = w->w_pre_norm;
   fp.pre_norm = h->cfg.pre_expert_norm;
   fp.quant = h->quant;
+  fp.act4 = h->act4;
   fp.norm_eps = h->cfg.norm_eps;
   fp.h = h->h;
   fp.h_op = h->h_op;
@@ -304,6 +314,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.groups = h->groups;
   ep.counters = h->counters;
   ep.out = h->act;
+  ep.act_bf16 = h->act4 != 0;
   ep.health = h->health;
   ep.part = h->expert_part;
   ep.tickets = h->expert_tickets[0];
@@ -311,14 +322,16 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   before();
   if (!after(launch_expert(ep, nte, s, pdl), "w13")) return MUSEMOE_ECUDA;
 
-  // 3b. FP8: quantize the activation per route
-  if (h->quant == kFP8) {
+  // 3b. FP8 and W4A4: quantize the activation per route
+  if (h->quant == kFP8 || h->act4) {
     ActQuantParams aq{};
     aq.act = reinterpret_cast<const uint16_t*>(h->act);
     aq.q = h->act_q;
     aq.scale = h->act_scale;
     aq.routes = rows * d.top_k;
     aq.I = d.inter;
+    aq.mode = h->act4;
+    aq.health = h->health;
     before();
     if (!after(launch_act_quant(aq, s, pdl), "act_quant")) return MUSEMOE_ECUDA;
   }
@@ -330,7 +343,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.w = w->w2;
   ep.scale = w->w2_scale;
   ep.gscale = w->w2_gscale;
-  ep.b = h->quant == kFP8 ? h->act_q : h->act;
+  ep.b = (h->quant == kFP8 || h->act4) ? h->act_q : h->act;
   ep.b_scale = h->act_scale;
   ep.b_by_token = 0;
   ep.out = h->y;
@@ -456,7 +469,8 @@ musemoe_status musemoe_create(const musemoe_dims* dims, int32_t quant, const mus
   musemoe_handle* h = new (std::nothrow) musemoe_handle();
   if (!h) return set_err(nullptr, MUSEMOE_ENOMEM, "host allocation failed");
   h->d = *dims;
-  h->quant = quant;
+  h->quant = weight_format(quant);
+  h->act4 = act4_of(quant);
   h->cfg = *config;
   h->device = dev;
   h->sms = prop.multiProcessorCount;
@@ -466,7 +480,7 @@ musemoe_status musemoe_create(const musemoe_dims* dims, int32_t quant, const mus
     for (int i = 0; i < 4; ++i)
       h->expert_grid[role][i] =
           h->sms * std::min(kExpertCtasPerSm,
-                            expert_ctas_per_sm(quant, role, 1 << i,
+                            expert_ctas_per_sm(h->quant, role, 1 << i,
                                                   role == 0 ? dims->pooled : dims->inter,
                                                   role == 0 ? 2 * dims->inter : dims->pooled));
   Layout L;
@@ -514,7 +528,8 @@ size_t musemoe_workspace_bytes(const musemoe_dims* dims, int32_t quant) {
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   musemoe_handle h;
   h.d = *dims;
-  h.quant = quant;
+  h.quant = weight_format(quant);
+  h.act4 = act4_of(quant);
   h.sms = sms;
   h.max_routes = dims->max_rows * dims->top_k;
   h.max_groups = std::min(dims->experts, h.max_routes) + (h.max_routes + 7) / 8 + 1;
@@ -523,13 +538,13 @@ size_t musemoe_workspace_bytes(const musemoe_dims* dims, int32_t quant) {
   return L.off;
 }
 
-int32_t musemoe_num_kernels(int32_t quant) { return quant == kFP8 ? 8 : 7; }
+int32_t musemoe_num_kernels(int32_t quant) { return (quant == kFP8 || act4_of(quant)) ? 8 : 7; }
 
 const char* musemoe_kernel_name(int32_t quant, int32_t i) {
   static const char* fp4[] = {"router", "pool", "w13", "w2", "finalize", "unpool", "boundary"};
   static const char* fp8[] = {"router", "pool", "w13", "act_quant", "w2", "finalize", "unpool",
                               "boundary"};
-  if (quant == kFP8) return (i >= 0 && i < 8) ? fp8[i] : "";
+  if (quant == kFP8 || act4_of(quant)) return (i >= 0 && i < 8) ? fp8[i] : "";
   return (i >= 0 && i < 7) ? fp4[i] : "";
 }
 
@@ -543,6 +558,7 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
   c.route_scale = 1.f;
   const std::vector<std::string> r = refusals(d, quant, &c);
   if (!r.empty()) return set_err(nullptr, MUSEMOE_EUNSUPPORTED, join(r));
+  quant = weight_format(quant);      // W4A4 weights are MXFP4 / NVFP4
   const bool bf16 = quant == kBF16;  // no scales
   const void* ptrs[8] = {w13_src, w13_scale_src, w13_dst, w13_scale_dst,
                          w2_src,  w2_scale_src,  w2_dst,  w2_scale_dst};
@@ -763,6 +779,27 @@ musemoe_status musemoe_quantize_mxfp4(const uint16_t* w_bf16, uint8_t* codes, ui
   return MUSEMOE_OK;
 }
 
+musemoe_status musemoe_quantize_act_nvfp4(const uint16_t* x_bf16, uint8_t* codes, uint8_t* scales,
+                                          int64_t rows, int32_t cols, musemoe_stream_t stream) {
+  std::vector<std::string> bad;
+  if (rows < 1) bad.push_back(fmt("rows %lld < 1", (long long)rows));
+  if (cols < 16 || cols % 16) bad.push_back(fmt("cols %d is not a positive multiple of 16", cols));
+  if (!x_bf16) bad.push_back("x_bf16 is NULL");
+  else if (!aligned16(x_bf16)) bad.push_back("x_bf16 is not 16-byte aligned");
+  if (!codes) bad.push_back("codes is NULL");
+  else if (!aligned16(codes)) bad.push_back("codes is not 16-byte aligned");
+  if (!scales) bad.push_back("scales is NULL");
+  if (!bad.empty()) return set_err(nullptr, MUSEMOE_EINVAL, join(bad));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = launch_quant_act_nvfp4(x_bf16, codes, scales, (long long)rows * cols, sms,
+                               reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "launch of the NVFP4 expert input");
+  return MUSEMOE_OK;
+}
+
 musemoe_status musemoe_health_selftest(musemoe_handle* h, musemoe_stream_t stream) {
   if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
   int dev = -1;
@@ -785,8 +822,9 @@ musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (word) {
     std::string m;
     if (word & kHealthTimeout) m += "an expert kernel's bounded wait on its weight copies ran out; ";
-    if (word & kHealthHRange) m += "h beyond the fp16 operand range; ";
-    if (word & kHealthActRange) m += "SiLU(gate)*up beyond the fp16 operand range; ";
+    if (word & kHealthHRange) m += "h (or, W4A4, its FP4 rounding) beyond the fp16 operand range; ";
+    if (word & kHealthActRange)
+      m += "SiLU(gate)*up (or, W4A4, its FP4 rounding) beyond the fp16 operand range; ";
     return set_err(h, (word & kHealthTimeout) ? MUSEMOE_ETIMEOUT : MUSEMOE_ERANGE, m);
   }
   return MUSEMOE_OK;

@@ -23,7 +23,12 @@ WEIGHT_RTOL = 1e-5
 OUT_TOL = 2e-2
 
 QUANT = {synth.MXFP4: mm.MUSEMOE_MXFP4, synth.NVFP4: mm.MUSEMOE_NVFP4,
-         synth.FP8: mm.MUSEMOE_FP8_W8A8, synth.BF16: mm.MUSEMOE_BF16}
+         synth.FP8: mm.MUSEMOE_FP8_W8A8, synth.BF16: mm.MUSEMOE_BF16,
+         synth.MXFP4_A4: mm.MUSEMOE_MXFP4_A4, synth.NVFP4_A4: mm.MUSEMOE_NVFP4_A4}
+# forms whose act tap holds the bf16 activation itself (the others tap its
+# f16 copy, the w2 operand)
+ACT_BF16 = (synth.FP8, synth.BF16, synth.MXFP4_A4, synth.NVFP4_A4)
+W4A4 = (synth.MXFP4_A4, synth.NVFP4_A4)
 
 
 def dims_of(cfg: synth.Config, max_rows: int | None = None) -> mm.Dims:
@@ -100,7 +105,7 @@ class Run:
                 res[k] = O.bf16_to_f64(res[k + "_bits"])
         if "act" in res:
             bits = res["act"].view(np.uint16)
-            res["act_bf16"] = cfg.quant in (synth.FP8, synth.BF16)
+            res["act_bf16"] = cfg.quant in ACT_BF16
             if res["act_bf16"]:  # the bf16 activations themselves
                 res["act"] = O.bf16_to_f64(bits).reshape(b, cfg.top_k, cfg.inter)
             else:
@@ -145,10 +150,10 @@ def oracle_as_gpu(cfg: synth.Config, ref: dict) -> dict:
     the comparison logic on the CPU)."""
     b, k = ref["ids"].shape
     act = ref["act"]
-    if cfg.quant not in (synth.FP8, synth.BF16):
+    if cfg.quant not in ACT_BF16:
         act = act.astype(np.float16).astype(np.float64)
     return dict(logits=ref["logits"], ids=ref["ids"].astype(np.int32), weights=ref["weights"],
-                h=ref["h"], act=act, act_bf16=cfg.quant in (synth.FP8, synth.BF16),
+                h=ref["h"], act=act, act_bf16=cfg.quant in ACT_BF16,
                 y=ref["y"].reshape(b * k, -1).astype(np.float32),
                 moe_out=ref["moe_out"], u=ref["u"], stream=ref["stream"], out=ref["out"])
 
@@ -212,7 +217,7 @@ def near_of(g: dict) -> dict:
     """The GPU's bf16 values at the oracle's rounding points. For FP4 formats
     the act tap is the f16 copy of the bf16 activation, which equals it only
     in the f16 normal range (|a| >= 2^-14); below that it is no hint (NaN).
-    FP8 and BF16 tap the bf16 activation itself."""
+    FP8, BF16 and W4A4 tap the bf16 activation itself."""
     act = np.asarray(g["act"], dtype=np.float64)
     if not g.get("act_bf16", False):
         act = np.where(np.abs(act) >= 2.0 ** -14, act, np.nan)
@@ -256,8 +261,11 @@ def e2e_bound(cfg: synth.Config) -> float:
     activation per row with a dynamic scale, so a single near-tie rounding
     upstream moves whole rows of e4m3 codes by one step (up to 2^-4
     relative); its independent bound is 1e-1 and its strict check is the
-    stage-wise one."""
-    return OUT_TOL if cfg.quant != synth.FP8 else FP8_E2E_TOL
+    stage-wise one. W4A4 rounds the same two inputs per block of 32 / 16
+    with a dynamic scale: a near tie upstream moves an e2m1 code by one step
+    (up to 1/3 relative) or a block scale by a factor of 2; the same 1e-1
+    bound, the same stage-wise strict check."""
+    return FP8_E2E_TOL if cfg.quant in (synth.FP8,) + W4A4 else OUT_TOL
 
 
 FP8_E2E_TOL = 1e-1

@@ -42,7 +42,8 @@ def _compare_block(cfg, w, x, st, run=None, pre_norm=True, report=None):
     return g, rep
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "verify", "large", "edge_tiny", "edge"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "verify", "large", "edge_tiny", "edge",
+                                  "w4a4_tiny", "w4a4_nv_tiny", "w4a4", "w4a4_nv"])
 def test_block_parity_full_size(name, record_property):
     cfg = synth.CONFIGS[name]
     w = synth.layer_tensors(cfg)
@@ -54,7 +55,8 @@ def test_block_parity_full_size(name, record_property):
     print(name, rep)
 
 
-@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8, synth.BF16])
+@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8, synth.BF16, synth.MXFP4_A4,
+                                   synth.NVFP4_A4])
 @pytest.mark.parametrize("score", [synth.SIGMOID, synth.SOFTMAX])
 def test_tiny_dims_every_quant_and_score(quant, score):
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, score=score, seed=11)
@@ -63,7 +65,8 @@ def test_tiny_dims_every_quant_and_score(quant, score):
     _compare_block(cfg, w, x, st)
 
 
-@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8, synth.BF16])
+@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8, synth.BF16,
+                                   synth.MXFP4_A4, synth.NVFP4_A4])
 def test_ragged_k_slices(quant):
     # P = 640, I = 384: w13 rows of 5 (FP4) / 10 (FP8) 64-byte chunks and w2
     # rows of 3 / 6 chunks, so the last K-slice of a tile is ragged and tiles

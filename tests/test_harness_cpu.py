@@ -11,7 +11,8 @@ import synth
 from . import _harness as H
 
 
-@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8])
+@pytest.mark.parametrize("quant", [synth.MXFP4, synth.NVFP4, synth.FP8, synth.BF16,
+                                   synth.MXFP4_A4, synth.NVFP4_A4])
 def test_oracle_outputs_pass_the_comparison(quant):
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, seed=21)
     w = synth.layer_tensors(cfg)
@@ -31,6 +32,19 @@ def test_planted_mistakes_fail_the_comparison(tensor):
     flat = g[tensor].reshape(-1)
     i = int(np.argmax(np.abs(flat)))
     flat[i] = flat[i] * 1.5 + 0.25
+    with pytest.raises(AssertionError):
+        H.compare(cfg, w, x, st, g)
+
+
+@pytest.mark.parametrize("quant", [synth.MXFP4_A4, synth.NVFP4_A4])
+def test_w4a4_without_activation_rounding_fails_the_comparison(quant):
+    # a forward that skipped the FP4 rounding of the expert inputs (the W4A16
+    # result on the same weights) must not pass as W4A4
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant, seed=23)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    w4a16 = dataclasses.replace(cfg, quant=synth.WEIGHT_FORMAT[quant])
+    g = H.oracle_as_gpu(cfg, H.oracle_block(w4a16, x, st, w))
     with pytest.raises(AssertionError):
         H.compare(cfg, w, x, st, g)
 
