@@ -236,7 +236,7 @@ musemoe_status musemoe_forward_host(musemoe_handle *handle, const musemoe_weight
 /* No allocation: the router GEMV + routing rule of musemoe_route without a
  * handle, for callers that cannot allocate device memory (their memory
  * belongs to another allocator, such as a serving engine's pooled one, or a
- * new allocation is not allowed where they run). The paper has no
+ * new allocation is not allowed where they run). The source pages have no
  * counterpart: it is a calling convention of this library. Inputs and
  * outputs as musemoe_route (w_router fp32 [experts, hidden], expert_bias
  * fp32 [experts], x bf16 [rows, hidden] -> ids_out int32 [rows, top_k],
