@@ -105,7 +105,7 @@ def _spawn(fn, *args):
         return dict(result)
 
 
-@pytest.mark.parametrize("cfg_name", ["tiny"])
+@pytest.mark.parametrize("cfg_name", ["tiny", "edge_tiny", "w4a4_tiny", "w4a4_nv_tiny"])
 def test_expert_parallel_matches_single_process(cfg_name):
     sys.path.insert(0, ROOT)
     import oracle as O
