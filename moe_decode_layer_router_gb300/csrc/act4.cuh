@@ -19,6 +19,7 @@
 namespace musemoe {
 
 // round to nearest on {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code
+// (the weight rounding's form, one element at a time)
 __device__ __forceinline__ uint32_t e2m1_nearest(float a) {
   return a <= 0.25f ? 0u
        : a < 0.75f  ? 1u
@@ -28,11 +29,6 @@ __device__ __forceinline__ uint32_t e2m1_nearest(float a) {
        : a < 3.5f   ? 5u
        : a <= 5.0f  ? 6u
                     : 7u;
-}
-
-// the magnitude of e2m1 code c (0..7)
-__device__ __forceinline__ float e2m1_magnitude(uint32_t c) {
-  return c < 4u ? 0.5f * (float)c : c == 4u ? 2.f : c == 5u ? 3.f : c == 6u ? 4.f : 6.f;
 }
 
 // floor(log2(m)) of a finite positive fp32 (subnormals included)
@@ -79,18 +75,6 @@ __device__ __forceinline__ Fp4Scale fp4_block_scale(float amax, int mode) {
   return s;
 }
 
-// the e2m1 code (sign in bit 3) of v in a block with scale s
-__device__ __forceinline__ uint32_t fp4_code(float v, const Fp4Scale& s, int mode) {
-  const float a = mode == 1 ? fabsf(v) * s.inv : (s.scale > 0.f ? __fdiv_rn(fabsf(v), s.scale) : 0.f);
-  return e2m1_nearest(a) | ((__float_as_uint(v) >> 31) << 3);
-}
-
-// the value v rounds to (exact in fp32)
-__device__ __forceinline__ float fp4_value(uint32_t code, const Fp4Scale& s) {
-  const float m = e2m1_magnitude(code & 7u) * s.scale;
-  return (code & 8u) ? -m : m;
-}
-
 // Two non-negative fp32 -> two e2m1 magnitude codes, `lo` in the low nibble:
 // the hardware conversion rounds to nearest, ties to the even code, and
 // saturates at 6, the rule above.
@@ -103,8 +87,9 @@ __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
 }
 
 // The codes of v0, v1 in a block with scale s as one byte (v0 in the low
-// nibble, sign in bit 3 of each nibble): fp4_code twice, with the magnitudes
-// from the hardware conversion and the sign bits set explicitly.
+// nibble, sign in bit 3 of each nibble): the magnitudes of |v| / s (an exact
+// product for MXFP4, an IEEE fp32 quotient for NVFP4) from the hardware
+// conversion, the sign bits of v set explicitly.
 __device__ __forceinline__ uint32_t fp4_code2(float v0, float v1, const Fp4Scale& s, int mode) {
   float a0 = 0.f, a1 = 0.f;
   if (mode == 1) {
