@@ -38,8 +38,8 @@ WEIGHT_SETS = 4
 # DRAM traffic of one launch of the dominant kernel, from the ncu capture
 # summarized in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "8842eab7ef2f239833afa72f1a1a5438ce2b36cb",
-               "bytes_per_launch": 102625536 + 2877440}
+NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "d6eb909b9b0a568a16b601c47c6cdf3f7a9358c4",
+               "bytes_per_launch": 102626816 + 2461952}
 
 
 def _args():
@@ -204,10 +204,13 @@ def run_oracle(steps: int, budget_s: float, threads: int = 1) -> dict:
 
 # ------------------------------------------------------------ our arm
 
-def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20) -> dict:
+def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20,
+                flush: bool = False) -> dict:
     """One weight set of ``cfg`` in the form ``quant_code``: the step time of a
     graph of one forward (``steps`` replays after 10), the per-kernel event
-    times of ``reps`` debug forwards, and the selected experts."""
+    times of ``reps`` debug forwards, and the selected experts. ``flush``
+    (for weights that fit in L2): every replay and debug forward is timed
+    alone after a 256 MB write that evicts L2."""
     import numpy as np
     import torch
 
@@ -242,16 +245,29 @@ def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20) -> 
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         mm.musemoe_forward(handle, w, xd, sd, out, cfg.rows, s)
+    scrub = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev) if flush else None
     with torch.cuda.stream(s):
         for _ in range(10):
             g.replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(steps):
-            g.replay()
-        e1.record(s)
+        if flush:
+            us = 0.0
+            for _ in range(steps):
+                scrub.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+                e1.synchronize()
+                us += e0.elapsed_time(e1) * 1e3 / steps
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                g.replay()
+            e1.record(s)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / steps
+    if not flush:
+        us = e0.elapsed_time(e1) * 1e3 / steps
     n = mm.musemoe_num_kernels(quant_code)
     names = [mm.musemoe_kernel_name(quant_code, i) for i in range(n)]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
@@ -261,6 +277,8 @@ def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20) -> 
     dur = {nm: 0.0 for nm in names}
     with torch.cuda.stream(s):
         for _ in range(reps):
+            if flush:
+                scrub.zero_()
             mm.musemoe_forward_debug(handle, w, xd, sd, out, cfg.rows, s,
                                      mm.make_taps(events=ev, ids=ids))
             s.synchronize()
@@ -269,7 +287,7 @@ def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20) -> 
     active = len(np.unique(ids.cpu().numpy()))
     health = mm.musemoe_poll_health(handle)
     mm.musemoe_destroy(handle)
-    del t, g
+    del t, g, scrub
     torch.cuda.empty_cache()
     return {"us_per_step": us, "kernel_us": dur, "active_experts": active,
             "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range"}
@@ -296,6 +314,30 @@ def bench_bf16_experts(dev, hbm_peak: float) -> dict:
             "rows_per_s": cfg.rows / (us / 1e6), "us_per_step": us,
             "active_experts": r["active_experts"], "expert_bytes": ebytes,
             "expert_phase_us": e_us, "expert_phase_gbs": ebytes / (e_us / 1e6) / 1e9,
+            "expert_phase_frac": ebytes / (e_us / 1e6) / 1e9 / hbm_peak,
+            "kernel_us": dur, "health": r["health"]}
+
+
+def bench_verify(dev, hbm_peak: float) -> dict:
+    """The verify workload (b=64, NVFP4, softmax, 16 hot experts): its
+    selected experts' weights fit in L2, so every forward is timed alone
+    after an L2-evicting write; the expert phase against its algorithmic
+    bytes (codes, e4m3 block scales, global scales)."""
+    import moe_decode_layer_router_gb300 as mm
+    import synth
+
+    cfg = synth.CONFIGS["verify"]
+    r = _bench_form(dev, cfg, mm.MUSEMOE_NVFP4, steps=50, reps=10, flush=True)
+    us, dur = r["us_per_step"], r["kernel_us"]
+    A, P, I = r["active_experts"], cfg.pooled, cfg.inter
+    ebytes = A * (2 * I * P // 2 + 2 * I * P // 16 + P * I // 2 + P * I // 16 + 8)
+    e_us = dur["w13"] + dur["w2"]
+    return {"workload": f"verify (b={cfg.rows}, H={cfg.hidden}, P={P}, I={I}, E={cfg.experts}, "
+                        f"top-{cfg.top_k}, NVFP4, softmax, {cfg.hot_experts} hot experts), "
+                        "L2 evicted before each forward",
+            "rows_per_s": cfg.rows / (us / 1e6), "us_per_step": us, "active_experts": A,
+            "expert_bytes": ebytes, "expert_phase_us": e_us,
+            "expert_phase_gbs": ebytes / (e_us / 1e6) / 1e9,
             "expert_phase_frac": ebytes / (e_us / 1e6) / 1e9 / hbm_peak,
             "kernel_us": dur, "health": r["health"]}
 
@@ -567,6 +609,7 @@ def bench_ours(args):
     mm.musemoe_destroy(handle)
     bf16_experts = bench_bf16_experts(dev, hbm_peak)
     w4a4 = bench_w4a4(dev)
+    verify_b64 = bench_verify(dev, hbm_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -609,7 +652,8 @@ def bench_ours(args):
         "cpu_baseline": cpu,
         "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
         "next": {"attention_boundary": attn_boundary, "quantize_mxfp4": quant_mxfp4,
-                 "bf16_experts": bf16_experts, "w4a4": w4a4},
+                 "bf16_experts": bf16_experts, "w4a4": w4a4,
+                 "verify_b64": verify_b64},
     }
     if world > 1:
         import torch.distributed as dist

@@ -25,9 +25,9 @@
 // memory stages with 1-D bulk copies (cp.async.bulk), completion counted on
 // one mbarrier per stage: the unit's codes and block scales are two
 // contiguous blocks each in the kernel layout ([E][N/64][slice][8 groups]
-// [chunks][8 rows][64 B]); with one token tile the group's activation rows
-// of the slice come along (padded rows, conflict-free fragment reads), with
-// wider tiles the warps read them from L1/L2. The 8 compute warps release a
+// [chunks][8 rows][64 B]); the group's activation rows of the slice (up to
+// 8 per token tile) come along (padded rows, conflict-free fragment reads).
+// The 8 compute warps release a
 // stage through a second mbarrier. Every wait is bounded: past the limit the
 // CTA raises a health bit and leaves.
 //
@@ -74,7 +74,7 @@ __host__ __device__ __forceinline__ XGeo x_geo(int K, int N) {
   g.RS = kSliceChunks * g.cbB + 32;
   g.scale_off = 2 * kXCodeBlock;
   g.b_off = g.scale_off + 2 * 8 * kSliceChunks * 8 * g.SB;
-  g.stage_bytes = (g.b_off + (NT == 1 ? 8 * g.RS : 0) + 127) & ~127;
+  g.stage_bytes = (g.b_off + 8 * NT * g.RS + 127) & ~127;
   return g;
 }
 
@@ -88,7 +88,7 @@ __device__ __forceinline__ long long x_start(int c, long long U, int G) { return
 // widest token tiles.
 template <int Q, int NT>
 constexpr int x_min_blocks() {
-  return (NT >= 8 || (NT >= 4 && Q != kMXFP4)) ? 1 : 2;
+  return NT >= 4 ? 1 : 2;
 }
 
 template <int Q, int ROLE, int NT>
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
                           nc * 64 * G.SB, bar, pol_first);
         }
       };
-      // the activation rows of a unit (one token tile) into stage st
+      // the activation rows of a unit (its group's tokens) into stage st
       auto issue_b = [&](int st, int grp, const int4& g4, int slice, int nc) {
         const uint32_t dst = stage0 + st * G.stage_bytes;
         const uint32_t bar = smem_u32(&full_b[st]);
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
         if (n == n_early && !waited) {
           pdl_wait();
           waited = true;
-          if (NT == 1) issue_early_b();
+          issue_early_b();
         }
         if (use > 0 && !mbar_wait_or_abort(smem_u32(&empty_b[st]), (uint32_t)(use - 1) & 1u,
                                            &abort_flag)) {
@@ -299,16 +299,16 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
         if (use > 0) asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         const int nc = min(kSliceChunks, G.NC - slice * kSliceChunks);
         uint32_t bytes = 2u * nc * (4096 + 64 * G.SB);
-        if (NT == 1) bytes += (uint32_t)(gd.z * nc * G.cbB);
+        bytes += (uint32_t)(gd.z * nc * G.cbB);
         mbar_expect_tx(smem_u32(&full_b[st]), bytes);
         issue_w(st, gd.x, tile, slice, nc);
-        if (n >= n_early && NT == 1) issue_b(st, grp, gd, slice, nc);
+        if (n >= n_early) issue_b(st, grp, gd, slice, nc);
       }
       if (!waited && n == n_early) {
         // every unit was early (count <= S)
         pdl_wait();
         waited = true;
-        if (NT == 1) issue_early_b();
+        issue_early_b();
       }
       // the copies still in flight must land before the CTA leaves
       const int issued = n;
@@ -330,7 +330,6 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-  const uint8_t* brow[NT];
   int ntok = 0, rbase = 0, e = 0, ntile_act = 0;
   bool fresh = true;  // the next unit starts a tile (or this CTA's range)
   // the warp's two fragment row groups in the stage: (code block, group)
@@ -402,12 +401,6 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
       rbase = gd.y;
       ntok = gd.z;
       ntile_act = (ntok + 7) >> 3;
-      // lanes past the group's last token read that token's row (their
-      // results are never stored): every fragment read is valid
-      if constexpr (NT > 1) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) brow[nt] = b_row(route_of(grp, rbase, min(nt * 8 + g, ntok - 1)));
-      }
       fresh = false;
     }
     const int c0 = slice * kSliceChunks;
@@ -488,26 +481,35 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
         }
       }
     } else {
+      // several token tiles: the B fragments of tile nt from the stage's
+      // activation rows 8 nt + g, at the offsets of the one-tile case; lanes
+      // past the group's last token read that token's row (their results
+      // are never stored), so every fragment read is of a row this unit
+      // copied
+      const uint8_t* bpn[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        bpn[nt] = stg + G.b_off + min(nt * 8 + g, ntok - 1) * G.RS +
+                  q * (Q == kFP8 ? 16 : Q == kBF16 ? 4 : 8);
 #pragma unroll
       for (int c = 0; c < kSliceChunks; ++c) {
         if (c >= nc) break;
-        const int cg = c0 + c;
         uint4 L, Hh;
         uint2 sl, sh;
         load_a(c, L, Hh, sl, sh);
         if constexpr (Q == kFP8)
           chunk_mma<Q, NT>(acc, L, Hh, sl, sh, ntile_act, [&](int nt, int) {
-            return *reinterpret_cast<const uint4*>(brow[nt] + (size_t)cg * 64 + q * 16);
+            return *reinterpret_cast<const uint4*>(bpn[nt] + c * 64);
           });
         else if constexpr (Q == kBF16)
           chunk_mma<Q, NT>(acc, L, Hh, sl, sh, ntile_act, [&](int nt, int j) {
-            const uint8_t* e0 = brow[nt] + ((size_t)cg * 32 + 16 * j + 2 * q) * 2;
+            const uint8_t* e0 = bpn[nt] + c * 64 + 32 * j;
             return make_uint2(*reinterpret_cast<const uint32_t*>(e0),
                               *reinterpret_cast<const uint32_t*>(e0 + 16));
           });
         else
           chunk_mma<Q, NT>(acc, L, Hh, sl, sh, ntile_act, [&](int nt, int j) {
-            return *reinterpret_cast<const uint2*>(brow[nt] + ((size_t)cg * 128 + 16 * j + 4 * q) * 2);
+            return *reinterpret_cast<const uint2*>(bpn[nt] + c * 256 + j * 32);
           });
       }
     }
