@@ -12,7 +12,8 @@
  *   pooler GEMM H -> P and the pre-expert RMSNorm -> bf16 h
  *     (page "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
  *     MoEProvider docstring);
- *   routed experts on MXFP4 / NVFP4 / FP8 weights: fused w13 (gate rows
+ *   routed experts on MXFP4 / NVFP4 / FP8 / BF16 weights (and the W4A4
+ *     forms, FP4 activations): fused w13 (gate rows
  *     first), SiLU(gate) * up -> bf16, w2; one UNWEIGHTED output per route
  *     (muse_moe_runner page, MuseSparkAiterExperts: unit router weights);
  *   per-route post-expert RMSNorm, then the router weight, summed over the
