@@ -44,6 +44,26 @@ def test_workspace_bytes_and_names_need_no_gpu(lib):
     assert mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4) == 7
 
 
+@pytest.mark.parametrize("quant,n", [(0, 7), (1, 7), (2, 8), (3, 7), (4, 8), (5, 8)])
+def test_every_form_names_its_launches(lib, quant, n):
+    # FP8 and the W4A4 forms launch act_quant between w13 and w2
+    names = [mm.musemoe_kernel_name(quant, i) for i in range(mm.musemoe_num_kernels(quant))]
+    assert len(names) == n
+    want = ["router", "pool", "w13"] + (["act_quant"] if n == 8 else []) + \
+        ["w2", "finalize", "unpool", "boundary"]
+    assert names == want
+    assert mm.musemoe_kernel_name(quant, n) == ""
+
+
+def test_w4a4_workspace_holds_the_rounded_activation(lib):
+    # the W4A4 forms add w2's f16 operand [rows * k, I] to their weight format's workspace
+    d = mm.Dims(max_rows=8, hidden=5120, pooled=2048, inter=1024, experts=128, top_k=8)
+    extra = 8 * 8 * 1024 * 2
+    for w4, a4 in [(mm.MUSEMOE_MXFP4, mm.MUSEMOE_MXFP4_A4), (mm.MUSEMOE_NVFP4, mm.MUSEMOE_NVFP4_A4)]:
+        assert mm.musemoe_workspace_bytes(d, a4) >= mm.musemoe_workspace_bytes(d, w4) + extra
+    assert mm.musemoe_workspace_bytes(d, 6) == 0  # no such form
+
+
 def test_create_rejects_bad_arguments_before_touching_a_device(lib):
     d = mm.Dims(max_rows=0, hidden=100, pooled=256, inter=128, experts=16, top_k=2)
     c = mm.Config(score=0, route_scale=2.5, norm_eps=1e-6, pre_expert_norm=1)
