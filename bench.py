@@ -607,9 +607,13 @@ def bench_ours(args):
 
     health = mm.musemoe_poll_health(handle)
     mm.musemoe_destroy(handle)
-    bf16_experts = bench_bf16_experts(dev, hbm_peak)
-    w4a4 = bench_w4a4(dev)
-    verify_b64 = bench_verify(dev, hbm_peak)
+    # the other forms and the verify workload: single-GPU lines, measured
+    # once (the scaling runs skip them)
+    bf16_experts = w4a4 = verify_b64 = None
+    if world == 1:
+        bf16_experts = bench_bf16_experts(dev, hbm_peak)
+        w4a4 = bench_w4a4(dev)
+        verify_b64 = bench_verify(dev, hbm_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
