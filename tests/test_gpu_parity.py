@@ -126,6 +126,19 @@ def test_large_rows_multiple_token_groups():
     _compare_block(cfg, w, x, st)
 
 
+@pytest.mark.parametrize("quant,rows", [(synth.NVFP4, 256), (synth.FP8, 64), (synth.BF16, 64),
+                                        (synth.BF16, 256), (synth.MXFP4_A4, 64)])
+def test_wide_token_tiles_every_form(quant, rows):
+    # rows above 32 run the expert kernels with four (up to 64 rows) or eight
+    # token tiles per warp; hot experts fill groups of 32 / 64 tokens, whose
+    # activation rows ride in the stages beside the weights
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=rows, top_k=2, hot_experts=2,
+                              hot_bias=5.0, quant=quant, seed=13)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st)
+
+
 def test_route_entry_point_matches_oracle():
     cfg = synth.CONFIGS["decode"]
     d = synth.dense_tensors(cfg, 0)
