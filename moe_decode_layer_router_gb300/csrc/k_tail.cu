@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) k_act_fp4(ActQuantParams p) {
   for (int j = 0; j < 8; ++j) {
     x[j] = bf16_bits_to_f32((j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xFFFFu));
     m = fmaxf(m, fabsf(x[j]));
-    bad |= !(fabsf(x[j]) <= 3.0e38f);  // NaN or infinite
+    bad |= !(fabsf(x[j]) <= 3.40282347e38f);  // NaN or infinite (above FLT_MAX)
   }
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   if (p.mode == 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
