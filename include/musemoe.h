@@ -241,9 +241,11 @@ musemoe_status musemoe_forward_host(musemoe_handle *handle, const musemoe_weight
  * counterpart: it is a calling convention of this library. Inputs and
  * outputs as musemoe_route (w_router fp32 [experts, hidden], expert_bias
  * fp32 [experts], x bf16 [rows, hidden] -> ids_out int32 [rows, top_k],
- * weights_out fp32 [rows, top_k]); hidden a multiple of 64, experts 1..256,
- * rows 1..MUSEMOE_STATIC_MAX_ROWS (larger gives EINVAL with the reason in
- * musemoe_last_error(NULL)).
+ * weights_out fp32 [rows, top_k]); hidden a multiple of 64 up to 8192
+ * (larger gives EUNSUPPORTED), experts 1..256, rows
+ * 1..MUSEMOE_STATIC_MAX_ROWS (larger gives EINVAL with the reason in
+ * musemoe_last_error(NULL)). A non-NULL stream must belong to the current
+ * device (else EINVAL): the scratch used is the current device's.
  * The scratch (the fp32 logits) is one fixed device array of
  * MUSEMOE_STATIC_SCRATCH_BYTES inside the library, held on every device
  * that loads the library until the process exits; the call makes no
@@ -320,14 +322,17 @@ musemoe_status musemoe_quantize_act_nvfp4(const uint16_t *x_bf16, uint8_t *codes
  * tile's owner waiting for a partial that never comes). Each gives up after
  * its limit (200 ms) and records the timeout in the health word exactly as a
  * forward would, so the next musemoe_poll_health returns MUSEMOE_ETIMEOUT
- * and the context stays usable. For checking the failure path of a
+ * and the context stays usable. It also leaves the expert kernels' split-tile
+ * tickets raised, as contributors arriving after their owner gave up would. For checking the failure path of a
  * deployment; synchronizes the stream; not concurrent with forwards on the
  * same handle. */
 musemoe_status musemoe_health_selftest(musemoe_handle *handle, musemoe_stream_t stream);
 
 /* Reads (synchronously) and clears the handle's device health word. Returns
  * MUSEMOE_ETIMEOUT if an expert kernel's bounded wait for its weight copies
- * ran out since the last poll (that forward's outputs are invalid),
+ * ran out since the last poll (that forward's outputs are invalid; the poll
+ * then zeroes every inter-CTA ticket of the handle, so the next forward
+ * starts clean),
  * MUSEMOE_ERANGE if a forward produced an expert operand (h or the
  * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504; W4A4: an
  * FP4-rounded input that fp16 does not hold exactly), MUSEMOE_OK

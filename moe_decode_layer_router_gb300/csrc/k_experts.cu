@@ -17,9 +17,11 @@
 // Work units = (token group, tile, K-slice of 4 64-byte chunks), numbered in
 // that order; CTA c runs units [U c / G, U (c + 1) / G) of the U units, so
 // every CTA streams the same number of weight bytes. A tile whose slices
-// span several CTAs leaves one fp32 partial per CTA and warp; the warp that
-// arrives last at the tile's ticket (atomic count, nobody waits) adds the
-// partials in CTA order, so results do not depend on scheduling.
+// span several CTAs leaves one fp32 partial per CTA and warp; the CTA that
+// holds the tile's last unit owns it: each of its warps waits (bounded) until
+// the tile's other CTAs have signalled their partials through the tile's
+// ticket, then adds the partials in CTA order, so results do not depend on
+// scheduling.
 //
 // Data movement: a producer lane streams each unit into a ring of shared
 // memory stages with 1-D bulk copies (cp.async.bulk), completion counted on

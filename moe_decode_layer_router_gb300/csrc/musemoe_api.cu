@@ -65,6 +65,8 @@ struct musemoe_handle {
   float *h_raw = nullptr, *u = nullptr;
   float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
   int32_t* expert_tickets[2] = {nullptr, nullptr};
+  size_t expert_ticket_bytes[2] = {0, 0};
+  size_t block_ticket_bytes = 0;  // norm_ticket and route_ticket, each
   int32_t* norm_ticket = nullptr;
   int32_t *route_ticket = nullptr, *route_done = nullptr;
   int32_t* never_set = nullptr;  // zero for good: the health self-test's flag
@@ -108,8 +110,9 @@ void plan(musemoe_handle* h, Layout& L) {
   L.add(&h->route_list, RT * 4);
   L.add(&h->groups, (size_t)h->max_groups * 16);
   L.add(&h->counters, kNumCounters * 4);
-  L.add(&h->norm_ticket, (R + 7) / 8 * 4);  // one per pooler token block
-  L.add(&h->route_ticket, (R + 7) / 8 * 4);  // one per router token block
+  h->block_ticket_bytes = (R + 7) / 8 * 4;
+  L.add(&h->norm_ticket, h->block_ticket_bytes);   // one per pooler token block
+  L.add(&h->route_ticket, h->block_ticket_bytes);  // one per router token block
   L.add(&h->route_done, 4);
   L.add(&h->never_set, 4);
   L.add(&h->health, 16);
@@ -126,9 +129,10 @@ void plan(musemoe_handle* h, Layout& L) {
   // most kExpertCtasPerSm CTAs per SM
   const int nt_max = nt_expert(d.max_rows);
   L.add(&h->expert_part, expert_part_bytes(kExpertCtasPerSm * h->sms, nt_max));
-  L.add(&h->expert_tickets[0],
-        expert_tickets(h->max_groups, h->quant, 0, d.pooled, 2 * d.inter) * 4);
-  L.add(&h->expert_tickets[1], expert_tickets(h->max_groups, h->quant, 1, d.inter, d.pooled) * 4);
+  h->expert_ticket_bytes[0] = expert_tickets(h->max_groups, h->quant, 0, d.pooled, 2 * d.inter) * 4;
+  h->expert_ticket_bytes[1] = expert_tickets(h->max_groups, h->quant, 1, d.inter, d.pooled) * 4;
+  L.add(&h->expert_tickets[0], h->expert_ticket_bytes[0]);
+  L.add(&h->expert_tickets[1], h->expert_ticket_bytes[1]);
   L.add(&h->moe_out, R * P * 2);
   L.add(&h->x_stage, R * H * 2);
   L.add(&h->stream_stage, R * H * 4);
@@ -806,7 +810,13 @@ musemoe_status musemoe_health_selftest(musemoe_handle* h, musemoe_stream_t strea
   if (cudaGetDevice(&dev) == cudaSuccess && dev != h->device)
     return set_err(h, MUSEMOE_EINVAL, fmt("current device %d is not the handle's device %d", dev, h->device));
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_wait_selftest(h->health, h->never_set, s);
+  // the split-tile tickets as contributors arriving after their owner gave
+  // up would leave them (raised), for the poll that reports the timeout to
+  // clear
+  cudaError_t e = cudaSuccess;
+  for (int r = 0; r < 2 && e == cudaSuccess; ++r)
+    e = cudaMemsetAsync(h->expert_tickets[r], 0x01, h->expert_ticket_bytes[r], s);
+  if (e == cudaSuccess) e = launch_wait_selftest(h->health, h->never_set, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_err(h, e, "health self-test");
   return MUSEMOE_OK;
@@ -819,6 +829,18 @@ musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (e == cudaSuccess) e = cudaMemset(h->health, 0, 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_err(h, e, "health read");
+  if (word & kHealthTimeout) {
+    // A CTA that gave up left its tile tickets in an unknown state (a late
+    // contributor may still have added to one): the next forward must start
+    // from zeroed tickets. The device is idle here (synchronized above).
+    for (int r = 0; r < 2 && e == cudaSuccess; ++r)
+      e = cudaMemset(h->expert_tickets[r], 0, h->expert_ticket_bytes[r]);
+    if (e == cudaSuccess) e = cudaMemset(h->norm_ticket, 0, h->block_ticket_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->route_ticket, 0, h->block_ticket_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->route_done, 0, 4);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_err(h, e, "ticket reset");
+  }
   if (word) {
     std::string m;
     if (word & kHealthTimeout) m += "an expert kernel's bounded wait on its weight copies ran out; ";

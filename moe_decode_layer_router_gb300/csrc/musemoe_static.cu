@@ -18,6 +18,7 @@ namespace {
 constexpr size_t kLogitsBytes = 64 * 1024;  // rows * E * 4 <= 64 * 256 * 4
 static_assert(kLogitsBytes <= MUSEMOE_STATIC_SCRATCH_BYTES, "scratch too small");
 constexpr int kMaxDevices = 64;
+constexpr int kStaticMaxHidden = 8192;  // the router GEMV's row held in registers
 
 // The scratch. In host code this name is only a stand-in for the device
 // array: its device address comes from cudaGetSymbolAddress.
@@ -52,6 +53,10 @@ extern "C" musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, 
     return fail(MUSEMOE_EINVAL, "top_k " + std::to_string(top_k) + " outside 1..experts");
   if (hidden < 64 || hidden % 64)
     return fail(MUSEMOE_EUNSUPPORTED, "hidden " + std::to_string(hidden) + " is not a multiple of 64");
+  if (hidden > kStaticMaxHidden)
+    return fail(MUSEMOE_EUNSUPPORTED, "hidden " + std::to_string(hidden) + " above " +
+                                          std::to_string(kStaticMaxHidden) +
+                                          " (a router thread holds at most 32 weights of a row)");
   if (config->score != 0 && config->score != 1)
     return fail(MUSEMOE_EINVAL, "score is not sigmoid (0) or softmax (1)");
   const void* ptrs[] = {w_router, expert_bias, x, ids_out, weights_out};
@@ -62,6 +67,18 @@ extern "C" musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(MUSEMOE_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(MUSEMOE_EUNSUPPORTED, "device index out of range");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (st) {
+    // the kernels run on the stream's device but write the scratch of the
+    // current device: the two must be the same
+    int sdev = -1;
+    e = cudaStreamGetDevice(st, &sdev);
+    if (e != cudaSuccess)
+      return fail(MUSEMOE_EINVAL, std::string("cudaStreamGetDevice: ") + cudaGetErrorString(e));
+    if (sdev != dev)
+      return fail(MUSEMOE_EINVAL, "stream belongs to device " + std::to_string(sdev) +
+                                      ", not the current device " + std::to_string(dev));
+  }
   void* base = nullptr;
   {
     // first call on this device: look up the array's device address (with
@@ -77,7 +94,6 @@ extern "C" musemoe_status musemoe_route_static(int32_t hidden, int32_t experts, 
     base = g_scratch_dev[dev];
   }
   float* logits = static_cast<float*>(base);  // [rows, experts]
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   FrontParams fp{};
   fp.x = x;
   fp.rows = rows;

@@ -53,7 +53,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
 }
 
 // One warp routes row t: scores from the fp32 logits, selection keys, the
-// bitonic top-k, then the weights from the UNBIASED scores of the selected
+// top-k as k rounds of a warp argmax, then the weights from the UNBIASED scores of the selected
 // ids. `s_w` (E floats) and `top` (k ints) are the warp's shared scratch.
 template <int EPL>
 __device__ void route_row_warp(const RouteParams& p, int t, int lane, float* s_w, int* top,

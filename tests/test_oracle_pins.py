@@ -725,3 +725,66 @@ def test_w4a4_expert_outputs_one_hot(fmt):
     np.testing.assert_array_equal(y, want)
     # and neither input is left unrounded
     assert not np.array_equal(hq, h) and not np.array_equal(want[:, :I], a)
+
+
+def _e4m3_nearest_brute(v):
+    """e4m3 value nearest each element of v (fp64), searched over every finite
+    code; ties to the even code; beyond the largest finite value, 448."""
+    tab = _e4m3_table()
+    fin = tab[:127]  # 0x00..0x7E: the non-negative finite values
+    out = np.empty_like(v)
+    for i, x in np.ndenumerate(v):
+        a = abs(x)
+        if a >= 448.0:
+            m = 448.0
+        else:
+            d = np.abs(fin - a)
+            c = np.nonzero(d == d.min())[0]
+            m = fin[c[0] if len(c) == 1 else c[c % 2 == 0][0]]
+        out[i] = math.copysign(m, x)
+    return out
+
+
+def test_fp8_expert_outputs_permuted_one_hot():
+    # permuted one-hot FP8 experts with a distinct fp32 scale per output row:
+    # gu[i] = s13[i] * hq[pi(i)], y[p] = s2[p] * aq[p] (p < I), where hq / aq
+    # are h per token and a per route requantized to e4m3 with their own
+    # dynamic scale fp32(amax / 448) (the W8A8 reading of both expert inputs).
+    # A scale applied per column (transposed), or an activation that skips its
+    # requantization, fails against this brute force.
+    P, I = 64, 16
+    rng = np.random.default_rng(67)
+    pi = rng.permutation(P)[:2 * I]
+    w13 = np.zeros((1, 2 * I, P), np.uint8)
+    w13[0, np.arange(2 * I), pi] = 0x38  # e4m3 1.0
+    w2 = np.zeros((1, P, I), np.uint8)
+    w2[0, np.arange(I), np.arange(I)] = 0x38
+    s13 = (0.5 + np.arange(2 * I) / 37.0).astype(np.float32)
+    s2 = (0.75 + np.arange(P) / 53.0).astype(np.float32)
+    t = {"w13": w13, "w13_scale": s13[None], "w2": w2, "w2_scale": s2[None]}
+    h = O.round_bf16(rng.standard_normal((3, P)) * np.array([[1.0], [0.02], [40.0]]))
+    ids = np.zeros((3, 1), np.int64)
+    y = O.expert_outputs(h, ids, "fp8", t, I)[:, 0]
+
+    def requant(v):
+        out = np.empty_like(v)
+        for r in range(v.shape[0]):
+            s = float(np.float32(np.abs(v[r]).max() / 448.0))
+            q = (v[r].astype(np.float32) / np.float32(s)).astype(np.float64)
+            out[r] = _e4m3_nearest_brute(q) * s
+        return out
+
+    hq = requant(h)
+    gu = hq[:, pi] * s13.astype(np.float64)
+    g, u = gu[:, :I], gu[:, I:]
+    a = torch.tensor(g / (1 + np.exp(-g)) * u).to(torch.bfloat16).double().numpy()
+    aq = requant(a)
+    want = np.zeros((3, P))
+    want[:, :I] = aq * s2[:I].astype(np.float64)
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=0)
+    # the planted mistakes differ from it
+    skip_a = np.zeros((3, P))
+    skip_a[:, :I] = a * s2[:I].astype(np.float64)
+    assert np.abs(skip_a - want).max() > 1e-3 * np.abs(want).max()
+    assert not np.allclose(hq[:, pi] * s13[::-1].astype(np.float64), gu)  # scales on other rows
+    assert not np.array_equal(hq, h) and not np.array_equal(aq, a)

@@ -57,6 +57,46 @@ def test_route_static_matches_route_on_two_calls(name):
         run.close()
 
 
+def test_route_static_allocates_nothing():
+    # every buffer exists before the measurement and the first call (which
+    # loads the library's code and scratch onto the device) is outside it:
+    # the device's free memory must not move across the calls that follow
+    cfg = synth.CONFIGS["verify"]
+    d = synth.dense_tensors(cfg, 0)
+    x, _ = synth.activations(cfg)
+    wr, wb, xd = H.to_dev(d["w_router"]), H.to_dev(d["expert_bias"]), H.to_dev(x)
+    b, k = x.shape[0], cfg.top_k
+    ids = torch.empty((b, k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((b, k), dtype=torch.float32, device="cuda")
+    conf = H.config_of(cfg)
+
+    def call():
+        mm.musemoe_route_static(cfg.hidden, cfg.experts, cfg.top_k, conf, wr, wb, xd, b, ids, wts)
+
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+
+
+def test_route_static_refuses_a_hidden_beyond_the_router_row():
+    cfg = synth.CONFIGS["decode"]
+    H_ = 8192 + 64
+    x = torch.zeros((1, H_), dtype=torch.int16, device="cuda")
+    w = torch.zeros((cfg.experts, H_), dtype=torch.float32, device="cuda")
+    bias = torch.zeros((cfg.experts,), dtype=torch.float32, device="cuda")
+    ids = torch.zeros((1, cfg.top_k), dtype=torch.int32, device="cuda")
+    wts = torch.zeros((1, cfg.top_k), dtype=torch.float32, device="cuda")
+    with pytest.raises(mm.MuseMoEError) as ei:
+        mm.musemoe_route_static(H_, cfg.experts, cfg.top_k, H.config_of(cfg), w, bias, x, 1,
+                                ids, wts)
+    assert ei.value.status == mm.MUSEMOE_EUNSUPPORTED and "8192" in str(ei.value)
+
+
 def test_route_static_rejects_rows_beyond_its_scratch():
     cfg = synth.CONFIGS["decode"]
     n = mm.MUSEMOE_STATIC_MAX_ROWS + 1
