@@ -92,6 +92,15 @@ typedef enum {
 
 typedef enum { MUSEMOE_SIGMOID = 0, MUSEMOE_SOFTMAX = 1 } musemoe_score;
 
+/* Which kernels run the routed experts (musemoe_set_expert_path). */
+typedef enum {
+  /* the tensor-core (tcgen05) kernels above 32 rows, where a hot expert's
+   * token group is a dense contraction; the warp-level kernels below */
+  MUSEMOE_PATH_AUTO = 0,
+  MUSEMOE_PATH_MMA = 1,     /* always the warp-level (mma.sync) kernels */
+  MUSEMOE_PATH_TCGEN05 = 2, /* always the tensor-core kernels (not BF16) */
+} musemoe_expert_path;
+
 /* Block sizes. hidden H, pooled P, inter I (per expert), experts E. */
 typedef struct {
   int32_t max_rows; /* largest `rows` any call of this handle will pass */
@@ -323,9 +332,9 @@ musemoe_status musemoe_quantize_act_nvfp4(const uint16_t *x_bf16, uint8_t *codes
  * its limit (200 ms) and records the timeout in the health word exactly as a
  * forward would, so the next musemoe_poll_health returns MUSEMOE_ETIMEOUT
  * and the context stays usable. It also leaves the expert kernels' split-tile
- * tickets raised, as contributors arriving after their owner gave up would. For checking the failure path of a
- * deployment; synchronizes the stream; not concurrent with forwards on the
- * same handle. */
+ * tickets raised, as contributors arriving after their owner gave up
+ * would. For checking the failure path of a deployment; synchronizes the
+ * stream; not concurrent with forwards on the same handle. */
 musemoe_status musemoe_health_selftest(musemoe_handle *handle, musemoe_stream_t stream);
 
 /* Reads (synchronously) and clears the handle's device health word. Returns
@@ -335,9 +344,21 @@ musemoe_status musemoe_health_selftest(musemoe_handle *handle, musemoe_stream_t 
  * starts clean),
  * MUSEMOE_ERANGE if a forward produced an expert operand (h or the
  * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504; W4A4: an
- * FP4-rounded input that fp16 does not hold exactly), MUSEMOE_OK
- * otherwise. */
+ * FP4-rounded input that fp16 does not hold exactly) or, on the tensor-core
+ * expert kernels, met an MXFP4 block scale outside 2^-23..2^13 (its products
+ * with e2m1 are exact f16 operands only inside), MUSEMOE_OK otherwise. */
 musemoe_status musemoe_poll_health(musemoe_handle *handle);
+
+/* Selects the routed-expert kernels of the handle's later forwards
+ * (musemoe_expert_path; AUTO after create). Both paths compute the same
+ * block (page "vllm.models.muse_spark.nvidia.specialized_decode.runtime.
+ * providers", RoutedExpertsOps: the routed experts of the MoE provider) with
+ * the same operands and fp32 accumulation; they differ in summation order.
+ * The tensor-core path (tcgen05.mma: kind::f8f6f4 for FP8, kind::f16 on
+ * dequantized FP4) serves MXFP4, NVFP4, FP8 and the W4A4 forms; TCGEN05 on a
+ * BF16 handle is EUNSUPPORTED. EINVAL for an unknown path. Host only; not
+ * concurrent with a forward on the handle. */
+musemoe_status musemoe_set_expert_path(musemoe_handle *handle, int32_t path);
 
 #ifdef __cplusplus
 }

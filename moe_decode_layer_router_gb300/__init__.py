@@ -25,7 +25,9 @@ __all__ = [
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
-    "musemoe_quantize_act_nvfp4", "musemoe_health_selftest", "EXPORTED_SYMBOLS", "WEIGHT_FIELDS",
+    "musemoe_quantize_act_nvfp4", "musemoe_health_selftest", "musemoe_set_expert_path",
+    "MUSEMOE_PATH_AUTO", "MUSEMOE_PATH_MMA", "MUSEMOE_PATH_TCGEN05", "EXPORTED_SYMBOLS",
+    "WEIGHT_FIELDS",
 ]
 
 (MUSEMOE_OK, MUSEMOE_EINVAL, MUSEMOE_EUNSUPPORTED, MUSEMOE_ECUDA, MUSEMOE_ENOMEM, MUSEMOE_ERANGE,
@@ -33,6 +35,7 @@ __all__ = [
 MUSEMOE_MXFP4, MUSEMOE_NVFP4, MUSEMOE_FP8_W8A8, MUSEMOE_BF16 = 0, 1, 2, 3
 MUSEMOE_MXFP4_A4, MUSEMOE_NVFP4_A4 = 4, 5
 MUSEMOE_SIGMOID, MUSEMOE_SOFTMAX = 0, 1
+MUSEMOE_PATH_AUTO, MUSEMOE_PATH_MMA, MUSEMOE_PATH_TCGEN05 = 0, 1, 2
 _STATUS = {0: "OK", 1: "EINVAL", 2: "EUNSUPPORTED", 3: "ECUDA", 4: "ENOMEM", 5: "ERANGE",
            6: "ETIMEOUT"}
 
@@ -69,7 +72,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_num_kernels", "musemoe_kernel_name", "musemoe_pack_experts", "musemoe_route",
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
-    "musemoe_quantize_act_nvfp4", "musemoe_health_selftest",
+    "musemoe_quantize_act_nvfp4", "musemoe_health_selftest", "musemoe_set_expert_path",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
 MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
@@ -117,6 +120,7 @@ def library() -> ctypes.CDLL:
         lib.musemoe_quantize_mxfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
         lib.musemoe_quantize_act_nvfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
         lib.musemoe_health_selftest.argtypes = [c_vp, c_vp]
+        lib.musemoe_set_expert_path.argtypes = [c_vp, c_i32]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int:  # ctypes default
@@ -242,6 +246,12 @@ def musemoe_health_selftest(handle, stream=None) -> None:
     """Runs the library's bounded waits on things nothing completes; the next
     musemoe_poll_health returns MUSEMOE_ETIMEOUT (see include/musemoe.h)."""
     _check(library().musemoe_health_selftest(handle, _stream(stream)), handle)
+
+
+def musemoe_set_expert_path(handle, path: int) -> None:
+    """Selects the routed-expert kernels of the handle's later forwards:
+    MUSEMOE_PATH_AUTO, _MMA (warp-level) or _TCGEN05 (tensor cores)."""
+    _check(library().musemoe_set_expert_path(handle, path), handle)
 
 
 def musemoe_quantize_mxfp4(w_bf16, codes, scales, rows: int, cols: int, stream=None) -> None:

@@ -412,8 +412,10 @@ __global__ void __launch_bounds__(kXThreads, x_min_blocks<Q, NT>()) k_expert(Exp
     // scales of chunk c of the stage
     auto load_a = [&](int c, uint4& L, uint4& Hh, uint2& sl, uint2& sh) {
       const int lo = gi_lo * nc + c, hi = gi_hi * nc + c;
-      L = *reinterpret_cast<const uint4*>(stg + blk_lo * kXCodeBlock + lo * 512 + g * 64 + q * 16);
-      Hh = *reinterpret_cast<const uint4*>(stg + blk_hi * kXCodeBlock + hi * 512 + g * 64 + q * 16);
+      // FP8 blocks are stored 64-byte swizzled (unit q of row g at q ^ ((g >> 1) & 3))
+      const int qs = (Q == kFP8) ? (q ^ ((g >> 1) & 3)) : q;
+      L = *reinterpret_cast<const uint4*>(stg + blk_lo * kXCodeBlock + lo * 512 + g * 64 + qs * 16);
+      Hh = *reinterpret_cast<const uint4*>(stg + blk_hi * kXCodeBlock + hi * 512 + g * 64 + qs * 16);
       sl = make_uint2(0, 0);
       sh = make_uint2(0, 0);
       const uint8_t* sc = stg + G.scale_off;

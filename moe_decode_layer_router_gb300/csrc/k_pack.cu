@@ -32,7 +32,11 @@ cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s
 // chunks also reorder their bytes so that a thread's 16 bytes are its mma
 // fragments: FP4 (permute 1), output 16q + 2j + b <- chunk byte 8j + 2q + b;
 // BF16 (permute 2, 32 values per chunk), a 4 x 4 transpose of 4-byte words,
-// output 16q + 4j + b <- chunk byte 16j + 4q + b.
+// output 16q + 4j + b <- chunk byte 16j + 4q + b. FP8 (permute 3): the
+// 64-byte swizzle of the tensor cores' shared-memory operands within each
+// [8 rows][64 B] block, 16-byte unit u of row r stored at unit
+// u ^ ((r >> 1) & 3), so that a bulk copy of a block is a canonical
+// 64-byte-swizzled K-major operand.
 __global__ void k_pack_tiles(const uint8_t* src, uint8_t* dst, size_t bytes, int row_bytes, int cb,
                              int permute) {
   const int NC = row_bytes / cb;
@@ -54,6 +58,8 @@ __global__ void k_pack_tiles(const uint8_t* src, uint8_t* dst, size_t bytes, int
     } else if (permute == 2) {
       const int qq = b >> 4, j = (b >> 2) & 3, bb = b & 3;
       b = 16 * j + 4 * qq + bb;
+    } else if (permute == 3) {
+      b = (((b >> 4) ^ ((r >> 1) & 3)) << 4) | (b & 15);
     }
     dst[o] = src[t * tile_bytes + (size_t)(gi * 8 + r) * row_bytes +
                  (size_t)(kSliceChunks * s + c) * cb + b];

@@ -15,7 +15,7 @@ void set_thread_error(const std::string& m);
 // counters[] slots in the workspace
 enum Counter : int { kNumGroups = 0, kTicket = 1, kNumCounters = 8 };
 // health bits
-enum Health : int { kHealthHRange = 1, kHealthActRange = 2, kHealthTimeout = 4 };
+enum Health : int { kHealthHRange = 1, kHealthActRange = 2, kHealthTimeout = 4, kHealthWRange = 8 };
 
 // ---- route: routing rule + token->expert permute ---------------------------
 struct RouteParams {
@@ -105,6 +105,12 @@ struct ExpertParams {
   int stages;  // set by the launcher
 };
 cudaError_t launch_expert(const ExpertParams& p, int nt, cudaStream_t s, bool pdl);
+// The same work on the fifth-generation tensor cores (tcgen05; MXFP4, NVFP4
+// and FP8 weights): token groups of up to expert_tc_group_tokens() routes,
+// p.grid CTAs (one per SM), partial sums in expert_tc_part_bytes(p.grid).
+cudaError_t launch_expert_tc(const ExpertParams& p, cudaStream_t s, bool pdl);
+size_t expert_tc_part_bytes(int grid);
+int expert_tc_group_tokens();
 int expert_ctas_per_sm(int quant, int role, int nt, int K, int N);
 size_t expert_part_bytes(int grid, int nt);
 size_t expert_tickets(int max_groups, int quant, int role, int K, int N);
@@ -168,7 +174,9 @@ cudaError_t launch_quant_act_nvfp4(const uint16_t* x, uint8_t* codes, uint8_t* s
 // slice the remainder), each slice by 8-row group, chunk, row:
 // [rows / 64][slice][8][chunks of the slice][8][cb]. permute 1 (FP4) or 2
 // (BF16) also reorders the bytes of each 64-byte code chunk for the mma
-// fragments; 0 keeps them.
+// fragments; 3 (FP8) swizzles the 16-byte units of each [8][64 B] block
+// (unit u of row r at u ^ ((r >> 1) & 3), the tensor cores' 64-byte
+// swizzle); 0 keeps them.
 // src may equal dst: the tiles then pass through `tmp` (at least one tile).
 // Sets *bad_dev to 1 if any of the n UE8M0 bytes is 0x00 or 0xFF.
 constexpr int kSliceChunks = 4;

@@ -40,6 +40,10 @@ int nt_front(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
 // groups (its weights stream twice), cheaper than wider, mostly empty tiles.
 int nt_expert(int rows) { return rows <= 32 ? 1 : rows <= 64 ? 4 : 8; }
 int nt_index(int nt) { return nt == 1 ? 0 : nt == 2 ? 1 : nt == 4 ? 2 : 3; }
+// Above this many rows an expert's token group is a dense contraction
+// (dozens of tokens per hot expert): the tensor-core (tcgen05) expert kernels
+// take MXFP4, NVFP4, FP8 and the W4A4 forms there.
+constexpr int kTcMinRows = 33;
 
 // Router CTAs: one per (expert, block of 8 tokens).
 int router_ctas(int E, int rows) { return E * ((rows + 7) / 8); }
@@ -53,6 +57,7 @@ void musemoe::set_thread_error(const std::string& m) { g_thread_err = m; }
 struct musemoe_handle {
   musemoe_dims d{};
   int quant = 0;  // the weight format (Quant)
+  int expert_path = 0;  // MUSEMOE_PATH_AUTO / _MMA / _TCGEN05
   int act4 = 0;   // W4A4: expert inputs rounded to MXFP4 (1) or NVFP4 (2)
   musemoe_config cfg{};
   int device = -1, sms = 0;
@@ -128,7 +133,8 @@ void plan(musemoe_handle* h, Layout& L) {
   // other) for the widest token tile, and one ticket array per matrix; at
   // most kExpertCtasPerSm CTAs per SM
   const int nt_max = nt_expert(d.max_rows);
-  L.add(&h->expert_part, expert_part_bytes(kExpertCtasPerSm * h->sms, nt_max));
+  L.add(&h->expert_part, std::max(expert_part_bytes(kExpertCtasPerSm * h->sms, nt_max),
+                                  expert_tc_part_bytes(h->sms)));
   h->expert_ticket_bytes[0] = expert_tickets(h->max_groups, h->quant, 0, d.pooled, 2 * d.inter) * 4;
   h->expert_ticket_bytes[1] = expert_tickets(h->max_groups, h->quant, 1, d.inter, d.pooled) * 4;
   L.add(&h->expert_tickets[0], h->expert_ticket_bytes[0]);
@@ -215,6 +221,12 @@ std::string check_weights(const musemoe_handle* h, const musemoe_weights* w, boo
   return join(bad);
 }
 
+// Whether a forward of `rows` runs its experts on the tensor-core kernels.
+bool use_tc(const musemoe_handle* h, int rows) {
+  if (h->quant == kBF16 || h->expert_path == MUSEMOE_PATH_MMA) return false;
+  return h->expert_path == MUSEMOE_PATH_TCGEN05 || rows >= kTcMinRows;
+}
+
 musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const uint16_t* x,
                             float* stream, uint16_t* out, int rows, cudaStream_t s,
                             const musemoe_taps* taps) {
@@ -245,6 +257,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   // permute (the last CTA of a block, then the last block: no waiting)
   const int ntf = nt_front(rows);
   const int nte = nt_expert(rows);
+  const bool tc = use_tc(h, rows);
   FrontParams fp{};
   fp.x = x;
   fp.rows = rows;
@@ -288,7 +301,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   rp.groups = h->groups;
   rp.counters = h->counters;
   rp.health = h->health;
-  rp.token_group = 8 * nte;
+  rp.token_group = tc ? expert_tc_group_tokens() : 8 * nte;
   rp.central = 0;
   before();
   if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
@@ -322,9 +335,10 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.health = h->health;
   ep.part = h->expert_part;
   ep.tickets = h->expert_tickets[0];
-  ep.grid = h->expert_grid[0][nt_index(nte)];
+  ep.grid = tc ? h->sms : h->expert_grid[0][nt_index(nte)];
   before();
-  if (!after(launch_expert(ep, nte, s, pdl), "w13")) return MUSEMOE_ECUDA;
+  if (!after(tc ? launch_expert_tc(ep, s, pdl) : launch_expert(ep, nte, s, pdl), "w13"))
+    return MUSEMOE_ECUDA;
 
   // 3b. FP8 and W4A4: quantize the activation per route
   if (h->quant == kFP8 || h->act4) {
@@ -352,9 +366,10 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.b_by_token = 0;
   ep.out = h->y;
   ep.tickets = h->expert_tickets[1];
-  ep.grid = h->expert_grid[1][nt_index(nte)];
+  ep.grid = tc ? h->sms : h->expert_grid[1][nt_index(nte)];
   before();
-  if (!after(launch_expert(ep, nte, s, pdl), "w2")) return MUSEMOE_ECUDA;
+  if (!after(tc ? launch_expert_tc(ep, s, pdl) : launch_expert(ep, nte, s, pdl), "w2"))
+    return MUSEMOE_ECUDA;
 
   // 5. post-expert norm, weight, reduce
   FinalizeParams fz{};
@@ -623,7 +638,7 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
   }
   for (const M& m : ms) {
     const int rowbytes = (int)row_bytes(m.K);
-    const int permute = fp8 ? 0 : bf16 ? 2 : 1;
+    const int permute = fp8 ? 3 : bf16 ? 2 : 1;
     if (e == cudaSuccess) e = launch_pack_tiles(m.src, m.dst, m.rows, rowbytes, 64, permute, tmp, tmp_bytes, s);
     if (e != cudaSuccess) break;
     if (bf16) continue;  // no scales
@@ -822,6 +837,16 @@ musemoe_status musemoe_health_selftest(musemoe_handle* h, musemoe_stream_t strea
   return MUSEMOE_OK;
 }
 
+musemoe_status musemoe_set_expert_path(musemoe_handle* h, int32_t path) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  if (path != MUSEMOE_PATH_AUTO && path != MUSEMOE_PATH_MMA && path != MUSEMOE_PATH_TCGEN05)
+    return set_err(h, MUSEMOE_EINVAL, fmt("expert path %d is not AUTO (0), MMA (1) or TCGEN05 (2)", path));
+  if (path == MUSEMOE_PATH_TCGEN05 && h->quant == kBF16)
+    return set_err(h, MUSEMOE_EUNSUPPORTED, "BF16 experts have no tensor-core (tcgen05) expert kernel");
+  h->expert_path = path;
+  return MUSEMOE_OK;
+}
+
 musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
   int32_t word = 0;
@@ -847,6 +872,9 @@ musemoe_status musemoe_poll_health(musemoe_handle* h) {
     if (word & kHealthHRange) m += "h (or, W4A4, its FP4 rounding) beyond the fp16 operand range; ";
     if (word & kHealthActRange)
       m += "SiLU(gate)*up (or, W4A4, its FP4 rounding) beyond the fp16 operand range; ";
+    if (word & kHealthWRange)
+      m += "an MXFP4 block scale outside 2^-23..2^13, beyond the fp16 operand range of the "
+           "tensor-core expert kernels; ";
     return set_err(h, (word & kHealthTimeout) ? MUSEMOE_ETIMEOUT : MUSEMOE_ERANGE, m);
   }
   return MUSEMOE_OK;

@@ -182,18 +182,27 @@ def check_ids(gpu_ids: np.ndarray, routing: "O.Routing", k: int) -> int:
 
 
 def kernel_layout(a: np.ndarray, chunk_bytes: int, permute_fp4: bool,
-                  permute_bf16: bool = False) -> np.ndarray:
+                  permute_bf16: bool = False, swizzle_fp8: bool = False) -> np.ndarray:
     """Host restatement of the documented kernel layout of one plain expert
     tensor [E, N, row_bytes] (bytes): rows in tiles of 64, each tile K-slice
     by K-slice (4 chunks of chunk_bytes, the last slice the remainder), each
     slice [8 groups][chunks of the slice][8 rows][chunk_bytes]; FP4 code
     chunks reordered byte 8j + 2q + b -> 16q + 2j + b; BF16 code chunks
-    byte 16j + 4q + b -> 16q + 4j + b."""
+    byte 16j + 4q + b -> 16q + 4j + b; FP8 code chunks 64-byte swizzled,
+    16-byte unit u of row r (within its 8-row group) stored at unit
+    u ^ ((r >> 1) & 3)."""
     a = np.ascontiguousarray(a)
     a = a.view(np.uint8).reshape(a.shape[0], a.shape[1], -1)
     E, N, rb = a.shape
     nc = rb // chunk_bytes
     x = a.reshape(E, N // 64, 8, 8, nc, chunk_bytes)  # [E][tile][group][row][chunk][byte]
+    if swizzle_fp8:
+        y = np.empty_like(x)
+        for r in range(8):
+            for u in range(4):
+                us = u ^ ((r >> 1) & 3)
+                y[:, :, :, r, :, 16 * us:16 * us + 16] = x[:, :, :, r, :, 16 * u:16 * u + 16]
+        x = y
     if permute_bf16:
         src = np.empty(64, np.int64)
         for qq in range(4):

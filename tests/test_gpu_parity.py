@@ -236,7 +236,8 @@ def test_pack_matches_the_documented_layout(quant, dims):
     fp4 = quant in (synth.MXFP4, synth.NVFP4)
     sc = 4 if quant == synth.MXFP4 else 8
     for k in ("w13", "w2"):
-        want = H.kernel_layout(e[k], 64, fp4, permute_bf16=quant == synth.BF16)
+        want = H.kernel_layout(e[k], 64, fp4, permute_bf16=quant == synth.BF16,
+                               swizzle_fp8=quant == synth.FP8)
         got = dst[k].cpu().numpy().view(np.uint8).reshape(want.shape)
         np.testing.assert_array_equal(got, want)
         if quant == synth.BF16:

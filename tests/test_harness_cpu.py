@@ -77,3 +77,16 @@ def test_kernel_layout_ragged_last_slice():
     # and chunk 2 of row 9 in the full slice 0: (1*4 + 2)*8*4 + 1*4
     off = (1 * 4 + 2) * 8 * 4 + 1 * 4
     assert np.array_equal(k.reshape(-1)[off:off + 4], plain[0, 9, 8:12])
+
+def test_kernel_layout_fp8_swizzle():
+    rng = np.random.default_rng(2)
+    plain = rng.integers(0, 256, size=(1, 64, 128), dtype=np.uint8)  # 2 chunks of 64 B
+    k = H.kernel_layout(plain, 64, False, swizzle_fp8=True)
+    # row 13 = group 1, row 5: unit u of chunk 1 sits at unit u ^ ((5 >> 1) & 3) = u ^ 2
+    blk = k.reshape(-1)[(1 * 2 + 1) * 512 + 5 * 64:(1 * 2 + 1) * 512 + 6 * 64]
+    for u in range(4):
+        us = u ^ 2
+        assert np.array_equal(blk[16 * us:16 * us + 16], plain[0, 13, 64 + 16 * u:64 + 16 * u + 16])
+    # row 1 of group 0: (1 >> 1) & 3 = 0, units in place
+    blk0 = k.reshape(-1)[64:128]
+    assert np.array_equal(blk0, plain[0, 1, :64])
