@@ -181,9 +181,11 @@ const char *musemoe_last_error(const musemoe_handle *handle);
 /* Device workspace bytes musemoe_create allocates for these dims. */
 size_t musemoe_workspace_bytes(const musemoe_dims *dims, int32_t quant);
 
-/* Kernels one musemoe_forward launches for this quant (for taps->events). */
+/* Stages one musemoe_forward runs for this quant (for taps->events): one
+ * kernel each, except that above 32 rows the "pool" stage is two launches
+ * (the dense tensor-core GEMM, then the pre-expert norm), timed together. */
 int32_t musemoe_num_kernels(int32_t quant);
-/* Name of kernel i of the forward ("router", "pool", "w13", ...). */
+/* Name of stage i of the forward ("router", "pool", "w13", ...). */
 const char *musemoe_kernel_name(int32_t quant, int32_t i);
 
 /* Re-lays the expert tensors from their plain layout into the kernel layout

@@ -16,7 +16,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmusemoe.so")
 
 SOURCES = ["musemoe_api.cu", "musemoe_static.cu", "k_gemv.cu", "k_route.cu", "k_experts.cu",
-           "k_tail.cu", "k_pack.cu", "k_boundary.cu", "k_quant.cu", "k_experts_tc.cu"]
+           "k_tail.cu", "k_pack.cu", "k_boundary.cu", "k_quant.cu", "k_experts_tc.cu",
+           "k_dense_tc.cu"]
 HEADERS = ["common.cuh", "kernels.h", "pipeline.cuh", "tc.cuh", "act4.cuh", "route_dev.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -82,7 +82,8 @@ __device__ __forceinline__ uint32_t swz(int r, int u) { return r * 128 + ((u ^ (
 // of the expert's fp32 weight row (at most kRouterCols). Then each thread
 // accumulates its columns for every token, and the CTA adds its threads'
 // sums (warp shuffles, then the 8 warps in order).
-constexpr int kRouterCols = 8;  // float4 columns per thread: K <= 8192
+constexpr int kRouterCols = 8;   // float4 columns per thread: K <= 8192
+constexpr int kRouterCols4 = 5;  // with four experts per CTA: K <= 5120
 static_assert(kGThreads == kRouteThreads, "the route tail runs the route kernel's block code");
 
 // Route tail of a router CTA (forward chain): after its logits, the CTA that
@@ -93,7 +94,7 @@ static_assert(kGThreads == kRouteThreads, "the route tail runs the route kernel'
 // the router's launch.
 template <int EPL>
 __device__ __noinline__ void router_route_tail(const FrontParams& p, int tb, int t0, int ntok,
-                                               const float* bias_s, uint8_t* smem) {
+                                               const float* bias_s, uint8_t* smem, int ctas_per_block) {
   __shared__ float s_w[kGWarps][256];
   __shared__ int top[kGWarps][256];
   __shared__ int last_s;
@@ -102,7 +103,7 @@ __device__ __noinline__ void router_route_tail(const FrontParams& p, int tb, int
   __syncthreads();  // orders the CTA's logits stores before thread 0's fence and ticket
   if (tid == 0) {
     __threadfence();
-    last_s = atomicAdd(p.route_ticket + tb, 1) == p.E - 1;
+    last_s = atomicAdd(p.route_ticket + tb, 1) == ctas_per_block - 1;
     if (last_s) {
       p.route_ticket[tb] = 0;  // for the next launch
       __threadfence();
@@ -140,13 +141,17 @@ __device__ __noinline__ void router_route_tail(const FrontParams& p, int tb, int
   else permute(rp, ids_s, work);
 }
 
-template <int EPL>
+// EG experts per CTA (EG > 1 for more than 8 rows: the 8 tokens' rows in
+// shared memory serve EG weight rows, EG times fewer input-row copies), at
+// most NCOL float4 weight columns per thread and expert.
+template <int EPL, int EG, int NCOL>
 __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8_t* smem) {
-  __shared__ float red[kGWarps][8];
+  __shared__ float red[kGWarps][8 * EG];
   __shared__ __align__(8) unsigned long long xbar;
   __shared__ int abort_flag;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int e = task % p.E, t0 = (task / p.E) * 8;
+  const int ng = p.E / EG;  // CTAs per token block
+  const int e0 = (task % ng) * EG, t0 = (task / ng) * 8;
   const int ntok = min(8, p.rows - t0);
   const int K4 = p.K / 4;
   if (threadIdx.x == 0) {
@@ -160,12 +165,15 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
   __shared__ float bias_s[256];
   if (p.route_tail)
     for (int i = threadIdx.x; i < p.E; i += kGThreads) bias_s[i] = __ldg(p.route.expert_bias + i);
-  const float4* wr = reinterpret_cast<const float4*>(p.w_router + (size_t)e * p.K);
-  float4 wv[kRouterCols];
+  float4 wv[EG][NCOL];
 #pragma unroll
-  for (int u = 0; u < kRouterCols; ++u) {
-    const int c = threadIdx.x + u * kGThreads;
-    wv[u] = c < K4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g = 0; g < EG; ++g) {
+    const float4* wr = reinterpret_cast<const float4*>(p.w_router + (size_t)(e0 + g) * p.K);
+#pragma unroll
+    for (int u = 0; u < NCOL; ++u) {
+      const int c = threadIdx.x + u * kGThreads;
+      wv[g][u] = c < K4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   pdl_wait();  // x may be the previous kernel's output
   // dependents launch only now: the pooler two launches on reads x without
@@ -176,26 +184,33 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
     for (int t = 0; t < ntok; ++t)
       bulk_g2s(smem_u32(smem) + t * p.K * 2, p.x + (size_t)(t0 + t) * p.K, p.K * 2, smem_u32(&xbar));
   }
-  float acc[8];
+  float acc[EG][8];
 #pragma unroll
-  for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+  for (int g = 0; g < EG; ++g)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[g][t] = 0.f;
   const bool ok = mbar_wait_or_abort(smem_u32(&xbar), 0u, &abort_flag);
   if (ok) {
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem);
 #pragma unroll
-    for (int u = 0; u < kRouterCols; ++u) {
+    for (int u = 0; u < NCOL; ++u) {
       const int c = threadIdx.x + u * kGThreads;
       if (c >= K4) break;
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         if (t >= ntok) break;
         const uint2 xv = *reinterpret_cast<const uint2*>(xs + t * p.K + 4 * c);
-        float a = acc[t];
-        a = fmaf(wv[u].x, bf16_bits_to_f32(xv.x & 0xFFFFu), a);
-        a = fmaf(wv[u].y, bf16_bits_to_f32(xv.x >> 16), a);
-        a = fmaf(wv[u].z, bf16_bits_to_f32(xv.y & 0xFFFFu), a);
-        a = fmaf(wv[u].w, bf16_bits_to_f32(xv.y >> 16), a);
-        acc[t] = a;
+        const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
+        const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
+#pragma unroll
+        for (int g = 0; g < EG; ++g) {
+          float a = acc[g][t];
+          a = fmaf(wv[g][u].x, x0, a);
+          a = fmaf(wv[g][u].y, x1, a);
+          a = fmaf(wv[g][u].z, x2, a);
+          a = fmaf(wv[g][u].w, x3, a);
+          acc[g][t] = a;
+        }
       }
     }
   } else if (!abort_flag) {
@@ -203,16 +218,21 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
     if (p.health) atomicOr(p.health, kHealthTimeout);
   }
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const float v = warp_sum(acc[t]);
-    if (lane == 0) red[warp][t] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x < ntok) {
-    float v = 0.f;
+  for (int g = 0; g < EG; ++g)
 #pragma unroll
-    for (int w = 0; w < kGWarps; ++w) v += red[w][threadIdx.x];
-    p.logits[(size_t)(t0 + threadIdx.x) * p.E + e] = v;
+    for (int t = 0; t < 8; ++t) {
+      const float v = warp_sum(acc[g][t]);
+      if (lane == 0) red[warp][g * 8 + t] = v;
+    }
+  __syncthreads();
+  if (threadIdx.x < 8 * EG) {
+    const int g = threadIdx.x >> 3, t = threadIdx.x & 7;
+    if (t < ntok) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGWarps; ++w) v += red[w][threadIdx.x];
+      p.logits[(size_t)(t0 + t) * p.E + e0 + g] = v;
+    }
   }
   // the copies must have landed before the CTA leaves (after a timeout)
   if (threadIdx.x == 0 && !ok) {
@@ -220,7 +240,7 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
     while (!mbar_try_wait(smem_u32(&xbar), 0u))
       if (globaltimer() - tw0 > kWaitLimitNs) break;
   }
-  if (p.route_tail) router_route_tail<EPL>(p, task / p.E, t0, ntok, bias_s, smem);
+  if (p.route_tail) router_route_tail<EPL>(p, task / ng, t0, ntok, bias_s, smem, ng);
 }
 
 // Pre-expert RMSNorm (page "vllm.models.muse_spark.nvidia.specialized_decode.
@@ -679,10 +699,21 @@ __global__ void __launch_bounds__(kGThreads)
   gemv_cta<NT, POOL>(&tw, p, smem);
 }
 
-template <int EPL>
+// The pre-expert norm of eight rows per CTA (the pooler ran as a dense
+// tensor-core GEMM): the expert kernel launched next reads the routing
+// before its own wait, so this kernel lets it launch only after its own wait
+// (the pooler, and the router before it, have completed).
+__global__ void __launch_bounds__(kGThreads) k_pool_norm(FrontParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t0 = blockIdx.x * kGWarps;
+  norm_rows(p, t0, min(p.rows, t0 + kGWarps));
+}
+
+template <int EPL, int EG, int NCOL>
 __global__ void __launch_bounds__(kGThreads) k_router(FrontParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  router_cta<EPL>(p, blockIdx.x, smem);
+  router_cta<EPL, EG, NCOL>(p, blockIdx.x, smem);
 }
 
 // ---- host ------------------------------------------------------------------
@@ -747,6 +778,20 @@ int front_ctas_per_sm(int K, int nt) {
 }
 int front_max_k() { return kGMaxK; }
 
+cudaError_t launch_pool_norm(const FrontParams& p, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.rows + kGWarps - 1) / kGWarps);
+  cfg.blockDim = dim3(kGThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_pool_norm, p);
+}
+
 cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl) {
   if (p.gemv_ctas == 0) return cudaSuccess;
   switch (nt) {
@@ -757,7 +802,7 @@ cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl)
   }
 }
 
-template <int EPL>
+template <int EPL, int EG, int NCOL>
 static cudaError_t launch_router_t(const FrontParams& p, cudaStream_t s, bool pdl) {
   size_t smem = (size_t)8 * p.K * 2;  // the 8 tokens' input rows
   if (p.route_tail) {
@@ -767,12 +812,12 @@ static cudaError_t launch_router_t(const FrontParams& p, cudaStream_t s, bool pd
     smem = std::max(smem, (need + 15) & ~(size_t)15);
   }
   if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_router<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_router<EPL, EG, NCOL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.router_ctas);
+  cfg.gridDim = dim3(p.router_ctas / EG);
   cfg.blockDim = dim3(kGThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -781,16 +826,25 @@ static cudaError_t launch_router_t(const FrontParams& p, cudaStream_t s, bool pd
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_router<EPL>, p);
+  return cudaLaunchKernelEx(&cfg, k_router<EPL, EG, NCOL>, p);
+}
+
+template <int EG, int NCOL>
+static cudaError_t launch_router_g(const FrontParams& p, cudaStream_t s, bool pdl) {
+  if (p.E <= 32) return launch_router_t<1, EG, NCOL>(p, s, pdl);
+  if (p.E <= 64) return launch_router_t<2, EG, NCOL>(p, s, pdl);
+  if (p.E <= 128) return launch_router_t<4, EG, NCOL>(p, s, pdl);
+  return launch_router_t<8, EG, NCOL>(p, s, pdl);
 }
 
 cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl) {
   if (p.router_ctas == 0) return cudaSuccess;
   if (p.K / 4 > kRouterCols * kGThreads) return cudaErrorInvalidValue;
-  if (p.E <= 32) return launch_router_t<1>(p, s, pdl);
-  if (p.E <= 64) return launch_router_t<2>(p, s, pdl);
-  if (p.E <= 128) return launch_router_t<4>(p, s, pdl);
-  return launch_router_t<8>(p, s, pdl);
+  // more than 8 rows: four experts per CTA where their weight columns fit the
+  // registers (K <= 5 * 4 * 256) and the experts divide evenly
+  if (p.rows > 8 && p.E % 4 == 0 && p.K / 4 <= kRouterCols4 * kGThreads)
+    return launch_router_g<4, kRouterCols4>(p, s, pdl);
+  return launch_router_g<1, kRouterCols>(p, s, pdl);
 }
 
 }  // namespace musemoe

@@ -39,8 +39,9 @@ struct RouteParams {
   int central;      // 1: one CTA routes every row and permutes (rows <= 32)
 };
 // ---- router GEMV (fp32 FFMA) and pooler / unpooler GEMV ------------------
-// The router runs router_ctas = E * ceil(rows / 8) CTAs, one per (expert,
-// 8-token block), each over the whole reduction. The bf16 GEMV Y = X W^T
+// The router runs router_ctas = E * ceil(rows / 8) (expert, 8-token block)
+// tasks, each over the whole reduction: one task per CTA, or above 8 rows
+// four experts' tasks per CTA. The bf16 GEMV Y = X W^T
 // (W [M, K] row-major, K a multiple of 64 and at most front_max_k()) runs on
 // front_gemv_ctas(M, rows, nt) CTAs, one per 16-row tile and token block.
 struct FrontParams {
@@ -74,6 +75,28 @@ struct FrontParams {
   int32_t* route_done;    // [1], zero between launches
 };
 cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl);   // GEMV
+// The pooler's pre-expert norm as its own launch (after launch_dense_tc):
+// rows of p.y -> p.h / p.h_op / p.h_scale, eight rows per CTA. Waits for its
+// predecessor before it lets its dependents launch.
+cudaError_t launch_pool_norm(const FrontParams& p, cudaStream_t s, bool pdl);
+
+// ---- dense bf16 GEMM on the tensor cores (pooler / unpooler, larger buckets)
+// y[rows, M] = x[rows, K] w[M, K]^T, fp32; K a multiple of 64; grid CTAs (one
+// per SM); partial sums in dense_tc_part_bytes(grid), tickets
+// dense_tc_tickets(rows, M) int32 (zero between launches).
+struct DenseParams {
+  const uint16_t* x;  // bf16 [rows, K]
+  const uint16_t* w;  // bf16 [M, K]
+  float* y;           // fp32 [rows, M]
+  int rows, M, K;
+  float* part;
+  int32_t* tickets;
+  int32_t* health;
+  int grid;
+};
+cudaError_t launch_dense_tc(const DenseParams& p, cudaStream_t s, bool pdl);
+size_t dense_tc_part_bytes(int grid);
+size_t dense_tc_tickets(int rows, int M);
 cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl);          // router
 int front_gemv_ctas(int M, int rows, int nt);
 int front_ctas_per_sm(int K, int nt);

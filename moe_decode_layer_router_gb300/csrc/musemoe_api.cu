@@ -70,6 +70,8 @@ struct musemoe_handle {
   float *h_raw = nullptr, *u = nullptr;
   float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
   int32_t* expert_tickets[2] = {nullptr, nullptr};
+  float* dense_part = nullptr;                     // dense tensor-core GEMMs (rows above 32)
+  int32_t* dense_tickets[2] = {nullptr, nullptr};  // pooler, unpooler
   size_t expert_ticket_bytes[2] = {0, 0};
   size_t block_ticket_bytes = 0;  // norm_ticket and route_ticket, each
   int32_t* norm_ticket = nullptr;
@@ -139,6 +141,11 @@ void plan(musemoe_handle* h, Layout& L) {
   h->expert_ticket_bytes[1] = expert_tickets(h->max_groups, h->quant, 1, d.inter, d.pooled) * 4;
   L.add(&h->expert_tickets[0], h->expert_ticket_bytes[0]);
   L.add(&h->expert_tickets[1], h->expert_ticket_bytes[1]);
+  if (d.max_rows >= kTcMinRows) {
+    L.add(&h->dense_part, dense_tc_part_bytes(h->sms));
+    L.add(&h->dense_tickets[0], dense_tc_tickets(d.max_rows, d.pooled) * 4);
+    L.add(&h->dense_tickets[1], dense_tc_tickets(d.max_rows, d.hidden) * 4);
+  }
   L.add(&h->moe_out, R * P * 2);
   L.add(&h->x_stage, R * H * 2);
   L.add(&h->stream_stage, R * H * 4);
@@ -219,6 +226,12 @@ std::string check_weights(const musemoe_handle* h, const musemoe_weights* w, boo
     need(w->gate, "gate");
   }
   return join(bad);
+}
+
+// Whether a forward of `rows` runs the pooler and unpooler as dense
+// tensor-core GEMMs (the same rows as the expert kernels' dense buckets).
+bool use_dense_tc(const musemoe_handle* h, int rows) {
+  return h->dense_part != nullptr && rows >= kTcMinRows;
 }
 
 // Whether a forward of `rows` runs its experts on the tensor-core kernels.
@@ -307,9 +320,31 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
 
   // 2. pooler GEMV (its weight copies overlap the router); the last CTA of
-  // each token block applies the pre-expert norm to the block's rows
-  before();
-  if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
+  // each token block applies the pre-expert norm to the block's rows. Above
+  // 32 rows: a dense tensor-core GEMM, then the norm as its own launch
+  const bool dense = use_dense_tc(h, rows);
+  if (dense) {
+    DenseParams dp{};
+    dp.x = x;
+    dp.w = w->w_pool;
+    dp.y = h->h_raw;
+    dp.rows = rows;
+    dp.M = d.pooled;
+    dp.K = d.hidden;
+    dp.part = h->dense_part;
+    dp.tickets = h->dense_tickets[0];
+    dp.health = h->health;
+    dp.grid = h->sms;
+    // one "pool" stage of the taps' events: the GEMM and the norm launch
+    before();
+    cudaError_t r = launch_dense_tc(dp, s, pdl);
+    if (r == cudaSuccess) r = cudaGetLastError();
+    if (r == cudaSuccess) r = launch_pool_norm(fp, s, pdl);
+    if (!after(r, "pool")) return MUSEMOE_ECUDA;
+  } else {
+    before();
+    if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
+  }
 
   // 3. w13 + SiLU * up
   ExpertParams ep{};
@@ -395,8 +430,24 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   up.M = d.hidden;
   up.K = d.pooled;
   up.gemv_ctas = front_gemv_ctas(d.hidden, rows, ntf);
-  before();
-  if (!after(launch_front(up, ntf, s, pdl), "unpool")) return MUSEMOE_ECUDA;
+  if (dense) {
+    DenseParams dp{};
+    dp.x = h->moe_out;
+    dp.w = w->w_unpool;
+    dp.y = h->u;
+    dp.rows = rows;
+    dp.M = d.hidden;
+    dp.K = d.pooled;
+    dp.part = h->dense_part;
+    dp.tickets = h->dense_tickets[1];
+    dp.health = h->health;
+    dp.grid = h->sms;
+    before();
+    if (!after(launch_dense_tc(dp, s, pdl), "unpool")) return MUSEMOE_ECUDA;
+  } else {
+    before();
+    if (!after(launch_front(up, ntf, s, pdl), "unpool")) return MUSEMOE_ECUDA;
+  }
 
   // 7. FFN boundary
   BoundaryParams bp{};

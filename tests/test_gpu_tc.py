@@ -122,3 +122,17 @@ def test_tc_path_refused_for_bf16_experts():
         assert ei.value.status == mm.MUSEMOE_EINVAL
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("quant,rows", [(synth.MXFP4, 33), (synth.NVFP4, 64), (synth.FP8, 100),
+                                        (synth.BF16, 48), (synth.MXFP4_A4, 300)])
+def test_dense_tc_front_every_form(quant, rows):
+    # above 32 rows the pooler and unpooler run as dense tensor-core GEMMs (two
+    # token blocks at 300 rows), the pre-expert norm as its own launch; shapes
+    # whose reduction spans many 64-element blocks and tiles split across CTAs
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=rows, hidden=1024, pooled=640,
+                              inter=256, quant=quant, seed=36)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    g = _run_path(cfg, w, x, st, mm.MUSEMOE_PATH_AUTO)
+    H.compare(cfg, w, x, st, g)
