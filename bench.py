@@ -175,8 +175,10 @@ sys.path.insert(0, {root!r})
 import numpy as np
 import synth, oracle as O
 cfg = synth.CONFIGS[{workload!r}]
-w = synth.layer_tensors(cfg)
+w = synth.layer_tensors(cfg, {layer})
 x, st = synth.activations(cfg)
+rows = {rows} or cfg.rows
+x, st = x[:rows].copy(), st[:rows].copy()
 p = synth.routing_params(cfg)
 times = []
 deadline = time.perf_counter() + {budget}
@@ -186,20 +188,34 @@ for i in range({steps}):
     times.append(time.perf_counter() - t0)
     if time.perf_counter() > deadline:
         break
-print(json.dumps({{"times": times, "rows": cfg.rows}}))
+print(json.dumps({{"times": times, "rows": rows}}))
 """
 
 
-def run_oracle(steps: int, budget_s: float, threads: int = 1) -> dict:
-    """Times the oracle on full decode steps (8 rows each) in a child
-    process pinned to `threads` BLAS/OpenMP threads."""
+def run_oracle(steps: int, budget_s: float, threads: int = 1, workload: str = WORKLOAD,
+               rows: int = 0, layer: int = 0) -> dict:
+    """Times the oracle on `steps` blocks of `workload` (its first `rows`
+    rows, all if 0; layer `layer` of a stack) in a child process pinned to
+    `threads` BLAS/OpenMP threads."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = str(threads)
-    code = ORACLE_SNIPPET.format(root=ROOT, workload=WORKLOAD, steps=steps, budget=budget_s)
+    code = ORACLE_SNIPPET.format(root=ROOT, workload=workload, steps=steps, budget=budget_s,
+                                 rows=rows, layer=layer)
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                          check=True)
     return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def _pct(v, q):
+    """q-th percentile of the list v (linear interpolation)."""
+    import numpy as np
+    return float(np.percentile(np.asarray(v, dtype=np.float64), q))
+
+
+def _stats(us):
+    return {"p10_us": _pct(us, 10), "p50_us": _pct(us, 50), "p90_us": _pct(us, 90),
+            "mean_us": float(sum(us) / len(us)), "replays": len(us)}
 
 
 # ------------------------------------------------------------ our arm
@@ -246,11 +262,11 @@ def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20,
     with torch.cuda.graph(g, stream=s):
         mm.musemoe_forward(handle, w, xd, sd, out, cfg.rows, s)
     scrub = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev) if flush else None
+    per = []
     with torch.cuda.stream(s):
         for _ in range(10):
             g.replay()
         if flush:
-            us = 0.0
             for _ in range(steps):
                 scrub.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -258,7 +274,8 @@ def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20,
                 g.replay()
                 e1.record(s)
                 e1.synchronize()
-                us += e0.elapsed_time(e1) * 1e3 / steps
+                per.append(e0.elapsed_time(e1) * 1e3)
+            us = sum(per) / len(per)
         else:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s)
@@ -290,6 +307,7 @@ def _bench_form(dev, cfg, quant_code: int, steps: int = 200, reps: int = 20,
     del t, g, scrub
     torch.cuda.empty_cache()
     return {"us_per_step": us, "kernel_us": dur, "active_experts": active,
+            "replay_stats": _stats(per) if per else None,
             "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range"}
 
 
@@ -318,28 +336,189 @@ def bench_bf16_experts(dev, hbm_peak: float) -> dict:
             "kernel_us": dur, "health": r["health"]}
 
 
-def bench_verify(dev, hbm_peak: float) -> dict:
-    """The verify workload (b=64, NVFP4, softmax, 16 hot experts): its
-    selected experts' weights fit in L2, so every forward is timed alone
-    after an L2-evicting write; the expert phase against its algorithmic
-    bytes (codes, e4m3 block scales, global scales)."""
+def expert_bytes_per_expert(cfg) -> int:
+    """Codes and scales of one expert's w13 and w2 in the workload's form."""
+    import synth
+    P, I = cfg.pooled, cfg.inter
+    q = synth.WEIGHT_FORMAT.get(cfg.quant, cfg.quant)
+    if q == synth.MXFP4:
+        return 2 * I * P // 2 + 2 * I * P // 32 + P * I // 2 + P * I // 32
+    if q == synth.NVFP4:
+        return 2 * I * P // 2 + 2 * I * P // 16 + P * I // 2 + P * I // 16 + 8
+    if q == synth.FP8:
+        return 2 * I * P + 2 * I * 4 + P * I + P * 4
+    return (2 * I * P + P * I) * 2  # BF16
+
+
+def block_bytes(cfg, active: float) -> float:
+    """Algorithmic bytes of one forward: the dense weights once, the selected
+    experts' codes and scales once, the activations (x, stream in and out,
+    out) once."""
+    H, P, E = cfg.hidden, cfg.pooled, cfg.experts
+    dense = E * H * 4 + E * 4 + 2 * P * H * 2 + (P + 3 * H) * 2
+    return dense + active * expert_bytes_per_expert(cfg) + 12 * cfg.rows * H
+
+
+def block_flops(cfg) -> float:
+    """2 x multiply-adds of one forward (router, pooler, routed experts, unpooler)."""
+    b, H, P, I, E, k = cfg.rows, cfg.hidden, cfg.pooled, cfg.inter, cfg.experts, cfg.top_k
+    return 2.0 * (b * E * H + b * P * H + b * k * (2 * I * P + P * I) + b * H * P)
+
+
+def bench_bucket(dev, name: str, quant_code: int, hbm_peak: float, cpu_rows: int,
+                 cpu_budget: float) -> dict:
+    """One single-layer bucket (a graph of one forward, L2 evicted before each
+    replay, 200 replays timed one by one): rows/s at the median, p10/p90, the
+    expert phase (w13 + w2 event times) and the whole block against their
+    algorithmic bytes, and the oracle on a bounded sample of the same
+    workload on one host core."""
     import moe_decode_layer_router_gb300 as mm
     import synth
 
-    cfg = synth.CONFIGS["verify"]
-    r = _bench_form(dev, cfg, mm.MUSEMOE_NVFP4, steps=50, reps=10, flush=True)
-    us, dur = r["us_per_step"], r["kernel_us"]
-    A, P, I = r["active_experts"], cfg.pooled, cfg.inter
-    ebytes = A * (2 * I * P // 2 + 2 * I * P // 16 + P * I // 2 + P * I // 16 + 8)
+    cfg = synth.CONFIGS[name]
+    r = _bench_form(dev, cfg, quant_code, steps=200, reps=10, flush=True)
+    st, dur = r["replay_stats"], r["kernel_us"]
+    us = st["p50_us"]
+    A = r["active_experts"]
+    ebytes = A * expert_bytes_per_expert(cfg)
     e_us = dur["w13"] + dur["w2"]
-    return {"workload": f"verify (b={cfg.rows}, H={cfg.hidden}, P={P}, I={I}, E={cfg.experts}, "
-                        f"top-{cfg.top_k}, NVFP4, softmax, {cfg.hot_experts} hot experts), "
-                        "L2 evicted before each forward",
+    bbytes = block_bytes(cfg, A)
+    eflops = 2.0 * cfg.rows * cfg.top_k * 3 * cfg.inter * cfg.pooled
+    ora = run_oracle(steps=3, budget_s=cpu_budget, threads=1, workload=name, rows=cpu_rows)
+    ot = sum(ora["times"]) / len(ora["times"])
+    return {"workload": f"{name} (b={cfg.rows}, H={cfg.hidden}, P={cfg.pooled}, I={cfg.inter}, "
+                        f"E={cfg.experts}, top-{cfg.top_k}, {cfg.quant}, "
+                        f"{'softmax' if cfg.score == synth.SOFTMAX else 'sigmoid'}"
+                        + (f", {cfg.hot_experts} hot experts" if cfg.hot_experts else "") + ")",
+            "timing": "graph of one forward, L2 evicted before each replay", "replays": st,
             "rows_per_s": cfg.rows / (us / 1e6), "us_per_step": us, "active_experts": A,
-            "expert_bytes": ebytes, "expert_phase_us": e_us,
-            "expert_phase_gbs": ebytes / (e_us / 1e6) / 1e9,
-            "expert_phase_frac": ebytes / (e_us / 1e6) / 1e9 / hbm_peak,
-            "kernel_us": dur, "health": r["health"]}
+            "roofline": {"bound": "hbm", "kernel": "w13+w2 (expert phase)", "unit": "GB/s",
+                         "algorithmic_bytes": ebytes,
+                         "achieved": ebytes / (e_us / 1e6) / 1e9, "peak": hbm_peak,
+                         "frac": ebytes / (e_us / 1e6) / 1e9 / hbm_peak},
+            "expert_phase_us": e_us,
+            "expert_tflops": eflops / (e_us / 1e6) / 1e12,
+            "block": {"algorithmic_bytes": bbytes, "achieved_gbs": bbytes / (us / 1e6) / 1e9,
+                      "frac": bbytes / (us / 1e6) / 1e9 / hbm_peak,
+                      "tflops": block_flops(cfg) / (us / 1e6) / 1e12},
+            "kernel_us": dur, "health": r["health"],
+            "cpu_baseline": {"value": ora["rows"] / ot, "unit": "rows/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"{len(ora['times'])} blocks of the first {ora['rows']} "
+                                       f"rows ({sum(ora['times']):.1f} s, numpy float64, "
+                                       "1 BLAS thread)"}}
+
+
+def bench_stack(dev, hbm_peak: float) -> dict:
+    """The 60-layer stack (b=32, MXFP4, independent weights per layer, 28 GB,
+    far beyond L2): one CUDA graph of the 60 chained forwards (each layer's
+    output is the next one's input, the stream carried in place), replayed and
+    timed; per layer rows/s, the expert phase of three layers from their
+    per-kernel event times, and the oracle on one layer on one host core."""
+    import numpy as np
+    import torch
+
+    import moe_decode_layer_router_gb300 as mm
+    import synth
+
+    cfg = synth.CONFIGS["stack"]
+    dims = mm.Dims(max_rows=cfg.rows, hidden=cfg.hidden, pooled=cfg.pooled, inter=cfg.inter,
+                   experts=cfg.experts, top_k=cfg.top_k)
+    conf = mm.Config(score=mm.MUSEMOE_SIGMOID, route_scale=cfg.route_scale,
+                     has_multiplier=int(cfg.multiplier is not None),
+                     multiplier=cfg.multiplier or 1.0,
+                     has_division_eps=int(cfg.division_eps is not None),
+                     division_eps=cfg.division_eps or 0.0, norm_eps=cfg.norm_eps,
+                     pre_expert_norm=1)
+    handle = mm.musemoe_create(dims, mm.MUSEMOE_MXFP4, conf)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    layers = []
+    for layer in range(cfg.layers):
+        t = {k: to_dev(v) for k, v in synth.layer_tensors(cfg, layer).items()}
+        mm.musemoe_pack_experts(dims, mm.MUSEMOE_MXFP4, t["w13"], t["w13_scale"], t["w13"],
+                                t["w13_scale"], t["w2"], t["w2_scale"], t["w2"], t["w2_scale"])
+        layers.append({"t": t, "w": mm.make_weights(t)})
+    x, st = synth.activations(cfg)
+    bufs = [to_dev(x), torch.empty_like(to_dev(x))]
+    sd = to_dev(st)
+    s = torch.cuda.Stream()
+
+    def chain():
+        for l_, L in enumerate(layers):
+            mm.musemoe_forward(handle, L["w"], bufs[l_ % 2], sd, bufs[(l_ + 1) % 2], cfg.rows, s)
+
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    per = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+        for _ in range(20):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            e1.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e3)
+    torch.cuda.synchronize()
+    st_ = _stats(per)
+    us_layer = st_["p50_us"] / cfg.layers
+    # expert phase of three layers (each kernel timed alone)
+    n = mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4)
+    names = [mm.musemoe_kernel_name(mm.MUSEMOE_MXFP4, i) for i in range(n)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    for e in ev:
+        e.record(s)
+    ids = torch.empty((cfg.rows, cfg.top_k), dtype=torch.int32, device=dev)
+    ebytes, e_us, kern = 0.0, 0.0, {nm: 0.0 for nm in names}
+    probe = [0, cfg.layers // 2, cfg.layers - 1]
+    with torch.cuda.stream(s):
+        for l_ in probe:
+            mm.musemoe_forward_debug(handle, layers[l_]["w"], bufs[0], sd, bufs[1], cfg.rows, s,
+                                     mm.make_taps(events=ev, ids=ids))
+            s.synchronize()
+            d = {nm: ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i, nm in enumerate(names)}
+            for nm in names:
+                kern[nm] += d[nm] / len(probe)
+            e_us += d["w13"] + d["w2"]
+            ebytes += len(np.unique(ids.cpu().numpy())) * expert_bytes_per_expert(cfg)
+    health = mm.musemoe_poll_health(handle)
+    mm.musemoe_destroy(handle)
+    del layers, g
+    torch.cuda.empty_cache()
+    active = ebytes / len(probe) / expert_bytes_per_expert(cfg)
+    bbytes = block_bytes(cfg, active)
+    ora = run_oracle(steps=2, budget_s=20.0, threads=1, workload="stack", rows=0, layer=0)
+    ot = sum(ora["times"]) / len(ora["times"])
+    return {"workload": f"stack ({cfg.layers} chained layers, b={cfg.rows}, H={cfg.hidden}, "
+                        f"P={cfg.pooled}, I={cfg.inter}, E={cfg.experts}, top-{cfg.top_k}, "
+                        "MXFP4, independent weights per layer)",
+            "timing": "one graph of the 60 chained forwards (28 GB of weights, beyond L2)",
+            "replays": st_, "us_per_stack": st_["p50_us"], "us_per_layer": us_layer,
+            "rows_layers_per_s": cfg.rows * cfg.layers / (st_["p50_us"] / 1e6),
+            "active_experts": active,
+            "roofline": {"bound": "hbm", "kernel": "w13+w2 (expert phase, 3 layers)",
+                         "unit": "GB/s", "algorithmic_bytes": ebytes / len(probe),
+                         "achieved": ebytes / (e_us / 1e6) / 1e9, "peak": hbm_peak,
+                         "frac": ebytes / (e_us / 1e6) / 1e9 / hbm_peak},
+            "block": {"algorithmic_bytes_per_layer": bbytes,
+                      "achieved_gbs": bbytes / (us_layer / 1e6) / 1e9,
+                      "frac": bbytes / (us_layer / 1e6) / 1e9 / hbm_peak},
+            "kernel_us": kern, "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
+            "cpu_baseline": {"value": ora["rows"] / ot, "unit": "rows*layers/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"{len(ora['times'])} blocks of layer 0 on "
+                                       f"{ora['rows']} rows ({sum(ora['times']):.1f} s, numpy "
+                                       "float64, 1 BLAS thread)"}}
 
 
 def bench_w4a4(dev) -> dict:
@@ -483,6 +662,18 @@ def bench_ours(args):
     clocks = sampler.stop() if sampler else None
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # the step's spread: 200 replays of the graph (WEIGHT_SETS steps each)
+    # timed one by one, per step
+    rep_us = []
+    if not args.eager:
+        with torch.cuda.stream(s):
+            for _ in range(200):
+                r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                r0.record(s)
+                group()
+                r1.record(s)
+                r1.synchronize()
+                rep_us.append(r0.elapsed_time(r1) * 1e3 / WEIGHT_SETS)
     kernels = mm.musemoe_num_kernels(quant)
     ms_step = ms / args.steps
     value = whole_job_rate(world, cfg.rows, args.steps, ms / 1e3)
@@ -609,11 +800,14 @@ def bench_ours(args):
     mm.musemoe_destroy(handle)
     # the other forms and the verify workload: single-GPU lines, measured
     # once (the scaling runs skip them)
-    bf16_experts = w4a4 = verify_b64 = None
+    bf16_experts = w4a4 = None
+    buckets = None
     if world == 1:
         bf16_experts = bench_bf16_experts(dev, hbm_peak)
         w4a4 = bench_w4a4(dev)
-        verify_b64 = bench_verify(dev, hbm_peak)
+        buckets = {"verify": bench_bucket(dev, "verify", mm.MUSEMOE_NVFP4, hbm_peak, 16, 15.0),
+                   "large": bench_bucket(dev, "large", mm.MUSEMOE_FP8_W8A8, hbm_peak, 16, 15.0),
+                   "stack": bench_stack(dev, hbm_peak)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -637,6 +831,9 @@ def bench_ours(args):
                          f"{set_bytes / 1e6:.0f} MB",
                    "cuda_graph": (f"{WEIGHT_SETS} forwards per graph" if not args.eager
                                   else False)},
+        "step_spread": (dict(_stats(rep_us), note=f"per step: 200 replays of the "
+                             f"{WEIGHT_SETS}-forward graph, each timed alone")
+                        if rep_us else None),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic,
@@ -655,9 +852,9 @@ def bench_ours(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "health": "ok" if health == mm.MUSEMOE_OK else "fp16 range",
+        "buckets": buckets,
         "next": {"attention_boundary": attn_boundary, "quantize_mxfp4": quant_mxfp4,
-                 "bf16_experts": bf16_experts, "w4a4": w4a4,
-                 "verify_b64": verify_b64},
+                 "bf16_experts": bf16_experts, "w4a4": w4a4},
     }
     if world > 1:
         import torch.distributed as dist

@@ -237,6 +237,36 @@ musemoe_status musemoe_forward_debug(musemoe_handle *handle, const musemoe_weigh
                                      int32_t rows, musemoe_stream_t stream_,
                                      const musemoe_taps *taps);
 
+/* Expert parallelism, the rank's half of the block (page
+ * "vllm.models.muse_spark.amd.mono.decoder", deployment_refusals and
+ * MonoDims: expert parallel ranks each hold experts [r E/g, (r+1) E/g); page
+ * "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
+ * MoEProvider: the tail's EP combine). Runs the replicated front (router,
+ * routing rule, pooler + pre-expert norm) on all rows, the routed experts
+ * for the routes whose expert lies in [expert_first, expert_first +
+ * expert_count) only, and the post-expert norm and router weight of those
+ * routes, and writes their sum per row to moe_partial, fp32 [rows, pooled]
+ * (no bf16 rounding: the ranks' partials are summed first, by the caller's
+ * all-reduce). w->w_router and w->expert_bias hold all experts; w13, w2 and
+ * their scales (NVFP4: global scales) hold the rank's expert_count experts,
+ * packed by musemoe_pack_experts with dims->experts = expert_count. Device
+ * pointers, 16-byte aligned; asynchronous; allocates nothing. EINVAL for an
+ * empty or out-of-range expert range or missing tensors. */
+musemoe_status musemoe_forward_ep_partial(musemoe_handle *handle, const musemoe_weights *w,
+                                         const uint16_t *x, float *moe_partial, int32_t rows,
+                                         int32_t expert_first, int32_t expert_count,
+                                         musemoe_stream_t stream_);
+
+/* The replicated back of an expert-parallel block: moe_out = bf16(moe_sum)
+ * (moe_sum fp32 [rows, pooled], the all-reduced sum of every rank's
+ * moe_partial), then the unpooler and the FFN boundary into stream_io (fp32,
+ * in place) and out (bf16), as musemoe_forward ends. Uses w->w_unpool,
+ * w_ffn_norm, w_next_norm and gate. With one rank holding every expert,
+ * partial + combine equals musemoe_forward bit for bit. */
+musemoe_status musemoe_forward_ep_combine(musemoe_handle *handle, const musemoe_weights *w,
+                                         const float *moe_sum, float *stream_io, uint16_t *out,
+                                         int32_t rows, musemoe_stream_t stream_);
+
 /* musemoe_forward on HOST buffers (pinned memory recommended): copies x and
  * stream to the workspace, runs the block, copies stream and out back and
  * synchronizes the stream. Not graph-capturable. */

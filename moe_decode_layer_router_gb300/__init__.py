@@ -26,7 +26,7 @@ __all__ = [
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
     "musemoe_quantize_act_nvfp4", "musemoe_health_selftest", "musemoe_set_expert_path",
-    "MUSEMOE_PATH_AUTO", "MUSEMOE_PATH_MMA", "MUSEMOE_PATH_TCGEN05", "EXPORTED_SYMBOLS",
+    "musemoe_forward_ep_partial", "musemoe_forward_ep_combine", "MUSEMOE_PATH_AUTO", "MUSEMOE_PATH_MMA", "MUSEMOE_PATH_TCGEN05", "EXPORTED_SYMBOLS",
     "WEIGHT_FIELDS",
 ]
 
@@ -73,6 +73,7 @@ EXPORTED_SYMBOLS = [
     "musemoe_forward", "musemoe_forward_debug", "musemoe_forward_host", "musemoe_poll_health",
     "musemoe_route_static", "musemoe_attention_boundary", "musemoe_quantize_mxfp4",
     "musemoe_quantize_act_nvfp4", "musemoe_health_selftest", "musemoe_set_expert_path",
+    "musemoe_forward_ep_partial", "musemoe_forward_ep_combine",
 ]
 MUSEMOE_STATIC_MAX_ROWS = 64
 MUSEMOE_STATIC_SCRATCH_BYTES = 64 * 1024
@@ -121,6 +122,10 @@ def library() -> ctypes.CDLL:
         lib.musemoe_quantize_act_nvfp4.argtypes = [c_vp, c_vp, c_vp, ctypes.c_int64, c_i32, c_vp]
         lib.musemoe_health_selftest.argtypes = [c_vp, c_vp]
         lib.musemoe_set_expert_path.argtypes = [c_vp, c_i32]
+        lib.musemoe_forward_ep_partial.argtypes = [c_vp, P(Weights), c_vp, c_vp, c_i32, c_i32,
+                                                   c_i32, c_vp]
+        lib.musemoe_forward_ep_combine.argtypes = [c_vp, P(Weights), c_vp, c_vp, c_vp, c_i32,
+                                                   c_vp]
         for name in EXPORTED_SYMBOLS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int:  # ctypes default
@@ -246,6 +251,25 @@ def musemoe_health_selftest(handle, stream=None) -> None:
     """Runs the library's bounded waits on things nothing completes; the next
     musemoe_poll_health returns MUSEMOE_ETIMEOUT (see include/musemoe.h)."""
     _check(library().musemoe_health_selftest(handle, _stream(stream)), handle)
+
+
+def musemoe_forward_ep_partial(handle, weights: Weights, x, moe_partial, rows: int,
+                               expert_first: int, expert_count: int, stream=None) -> None:
+    """The rank's partial moe_out (fp32) of an expert-parallel block: its
+    experts [expert_first, expert_first + expert_count) only (see
+    include/musemoe.h)."""
+    _check(library().musemoe_forward_ep_partial(handle, ctypes.byref(weights), _addr(x),
+                                                _addr(moe_partial), rows, expert_first,
+                                                expert_count, _stream(stream)), handle)
+
+
+def musemoe_forward_ep_combine(handle, weights: Weights, moe_sum, stream_io, out, rows: int,
+                               stream=None) -> None:
+    """bf16(moe_sum), the unpooler and the FFN boundary: the back of an
+    expert-parallel block after the all-reduce (see include/musemoe.h)."""
+    _check(library().musemoe_forward_ep_combine(handle, ctypes.byref(weights), _addr(moe_sum),
+                                                _addr(stream_io), _addr(out), rows,
+                                                _stream(stream)), handle)
 
 
 def musemoe_set_expert_path(handle, path: int) -> None:

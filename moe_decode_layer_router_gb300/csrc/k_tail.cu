@@ -1,6 +1,8 @@
 // Tail of the expert phase: the FP8 per-route requantization of the bf16
 // activation between w13 and w2, and the per-route post-expert norm, router
 // weighting and sum over the k routes of each token.
+#include <algorithm>
+
 #include "act4.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -141,12 +143,22 @@ __global__ void __launch_bounds__(kFinalizeThreads) k_finalize(FinalizeParams p)
   extern __shared__ __align__(16) float4 fsm4[];
   __shared__ float part[kFinalizeUnroll * 2][kFinalizeThreads / 32];
   __shared__ float rstd[256], wt[256];
+  __shared__ int loc[256];  // the route contributes (always, unless expert parallel)
   const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int NW = kFinalizeThreads / 32;
   const int P4 = p.P / 4;
   const bool stash = p.stash != 0;
   const float4* y4 = reinterpret_cast<const float4*>(p.y) + (size_t)t * p.k * P4;
-  for (int j = threadIdx.x; j < p.k; j += kFinalizeThreads) wt[j] = __ldcg(p.weights + (size_t)t * p.k + j);
+  for (int j = threadIdx.x; j < p.k; j += kFinalizeThreads) {
+    wt[j] = __ldcg(p.weights + (size_t)t * p.k + j);
+    int l = 1;
+    if (p.part) {  // expert parallel: another rank holds this route's expert
+      const int e = __ldcg(p.ids + (size_t)t * p.k + j);
+      l = (e >= p.ep_first && e < p.ep_first + p.ep_count);
+    }
+    loc[j] = l;
+  }
+  __syncthreads();
   // sums of squares, kFinalizeUnroll routes per round, all their loads in flight
   for (int j0 = 0; j0 < p.k; j0 += kFinalizeUnroll) {
     float ss[kFinalizeUnroll];
@@ -157,8 +169,8 @@ __global__ void __launch_bounds__(kFinalizeThreads) k_finalize(FinalizeParams p)
       float4 v[kFinalizeUnroll];
 #pragma unroll
       for (int u = 0; u < kFinalizeUnroll; ++u)
-        v[u] = (j0 + u < p.k && i < P4) ? __ldcg(y4 + (size_t)(j0 + u) * P4 + i)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = (j0 + u < p.k && i < P4 && loc[j0 + u]) ? __ldcg(y4 + (size_t)(j0 + u) * P4 + i)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < kFinalizeUnroll; ++u) {
         ss[u] += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
@@ -185,6 +197,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) k_finalize(FinalizeParams p)
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
     for (int j = 0; j < p.k; ++j) {
+      if (!loc[j]) continue;  // (expert parallel) its y row was never written
       const float4 v = stash ? fsm4[(size_t)j * P4 + i] : __ldcg(y4 + (size_t)j * P4 + i);
       const float r = rstd[j], c = wt[j];
       a0 = fmaf(c, (v.x * r) * w0, a0);
@@ -192,11 +205,33 @@ __global__ void __launch_bounds__(kFinalizeThreads) k_finalize(FinalizeParams p)
       a2 = fmaf(c, (v.z * r) * w2, a2);
       a3 = fmaf(c, (v.w * r) * w3, a3);
     }
+    if (p.part) {
+      reinterpret_cast<float4*>(p.part + (size_t)t * p.P)[i] = make_float4(a0, a1, a2, a3);
+      continue;
+    }
     uint2 o;
     o.x = (uint32_t)f32_to_bf16_bits(a0) | ((uint32_t)f32_to_bf16_bits(a1) << 16);
     o.y = (uint32_t)f32_to_bf16_bits(a2) | ((uint32_t)f32_to_bf16_bits(a3) << 16);
     reinterpret_cast<uint2*>(p.moe_out + (size_t)t * p.P)[i] = o;
   }
+}
+
+// fp32 -> bf16, four per thread (the summed expert-parallel moe_out)
+__global__ void __launch_bounds__(256) k_round_bf16(const float4* src, uint2* dst, long long n4) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = __ldcg(src + i);
+    dst[i] = make_uint2((uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16),
+                        (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16));
+  }
+}
+
+cudaError_t launch_round_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s) {
+  const long long n4 = n / 4;
+  const unsigned grid = (unsigned)std::min<long long>((n4 + 255) / 256, 1024);
+  k_round_bf16<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
+                                    reinterpret_cast<uint2*>(dst), n4);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl) {

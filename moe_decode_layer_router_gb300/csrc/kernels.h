@@ -37,6 +37,10 @@ struct RouteParams {
   int32_t* health;
   int token_group;  // routes per group (8 * NT of the expert kernels)
   int central;      // 1: one CTA routes every row and permutes (rows <= 32)
+  // expert parallelism: token groups only for the experts [ep_first,
+  // ep_first + ep_count), whose group expert index is local (e - ep_first);
+  // ep_count 0 = every expert
+  int ep_first, ep_count;
 };
 // ---- router GEMV (fp32 FFMA) and pooler / unpooler GEMV ------------------
 // The router runs router_ctas = E * ceil(rows / 8) (expert, 8-token block)
@@ -160,8 +164,17 @@ struct FinalizeParams {
   int rows, k, P;
   float eps;
   int stash;  // set by launch_finalize: route rows kept in shared memory
+  // expert parallelism (part != nullptr): only the routes whose expert id is
+  // in [ep_first, ep_first + ep_count) contribute, and the fp32 sum goes to
+  // part [rows, P] (no bf16 rounding: the ranks' parts are summed first)
+  const int32_t* ids;  // [rows, k]
+  float* part;
+  int ep_first, ep_count;
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s, bool pdl);
+// fp32 [n] -> bf16 [n] (round to nearest even), n a multiple of 4; no
+// programmatic dependency on the previous kernel.
+cudaError_t launch_round_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s);
 
 // ---- FFN boundary ------------------------------------------------------------
 struct BoundaryParams {

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <new>
 #include <string>
 #include <vector>
@@ -240,9 +241,21 @@ bool use_tc(const musemoe_handle* h, int rows) {
   return h->expert_path == MUSEMOE_PATH_TCGEN05 || rows >= kTcMinRows;
 }
 
+// Expert parallelism: the forward runs this rank's experts [first, first +
+// count) only and stops after the finalize, which writes the fp32 partial.
+struct EpArgs {
+  int first, count;
+  float* part;
+};
+
+musemoe_status launch_back(musemoe_handle* h, const musemoe_weights* w, float* stream,
+                           uint16_t* out, int rows, cudaStream_t s, bool pdl,
+                           const std::function<void()>& before,
+                           const std::function<bool(cudaError_t, const char*)>& after);
+
 musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const uint16_t* x,
                             float* stream, uint16_t* out, int rows, cudaStream_t s,
-                            const musemoe_taps* taps) {
+                            const musemoe_taps* taps, const EpArgs* epa = nullptr) {
   const musemoe_dims& d = h->d;
   musemoe_event_t* ev = taps ? taps->events : nullptr;
   const bool pdl = (ev == nullptr);
@@ -316,6 +329,8 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   rp.health = h->health;
   rp.token_group = tc ? expert_tc_group_tokens() : 8 * nte;
   rp.central = 0;
+  rp.ep_first = epa ? epa->first : 0;
+  rp.ep_count = epa ? epa->count : 0;
   before();
   if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
 
@@ -416,9 +431,54 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fz.k = d.top_k;
   fz.P = d.pooled;
   fz.eps = h->cfg.norm_eps;
+  if (epa) {
+    fz.ids = h->ids;
+    fz.part = epa->part;
+    fz.ep_first = epa->first;
+    fz.ep_count = epa->count;
+  }
   before();
   if (!after(launch_finalize(fz, s, pdl), "finalize")) return MUSEMOE_ECUDA;
+  if (epa) return MUSEMOE_OK;  // the partial moe_out is the rank's output
+  const musemoe_status bs = launch_back(h, w, stream, out, rows, s, pdl, before, after);
+  if (bs != MUSEMOE_OK) return bs;
 
+  if (taps) {
+    struct Cp {
+      void* dst;
+      const void* src;
+      size_t bytes;
+    } cps[] = {
+        {taps->logits, h->logits, (size_t)rows * d.experts * 4},
+        {taps->ids, h->ids, (size_t)rows * d.top_k * 4},
+        {taps->weights, h->weights, (size_t)rows * d.top_k * 4},
+        {taps->h, h->h, (size_t)rows * d.pooled * 2},
+        {taps->act, h->act, (size_t)rows * d.top_k * d.inter * 2},
+        {taps->y, h->y, (size_t)rows * d.top_k * d.pooled * 4},
+        {taps->moe_out, h->moe_out, (size_t)rows * d.pooled * 2},
+        {taps->u, h->u, (size_t)rows * d.hidden * 4},
+    };
+    for (const Cp& c : cps)
+      if (c.dst) {
+        const cudaError_t r = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, s);
+        if (r != cudaSuccess) return cuda_err(h, r, "tap copy");
+      }
+  }
+  (void)e;
+  if (bad_event) {
+    cudaGetLastError();  // clear the failed record
+    return set_err(h, MUSEMOE_EINVAL, "taps->events holds an event that could not be recorded");
+  }
+  return MUSEMOE_OK;
+}
+
+musemoe_status launch_back(musemoe_handle* h, const musemoe_weights* w, float* stream,
+                           uint16_t* out, int rows, cudaStream_t s, bool pdl,
+                           const std::function<void()>& before,
+                           const std::function<bool(cudaError_t, const char*)>& after) {
+  const musemoe_dims& d = h->d;
+  const int ntf = nt_front(rows);
+  const bool dense = use_dense_tc(h, rows);
   // 6. unpooler GEMV
   FrontParams up{};
   up.x = h->moe_out;
@@ -463,32 +523,6 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   before();
   if (!after(launch_boundary(bp, s, pdl), "boundary")) return MUSEMOE_ECUDA;
 
-  if (taps) {
-    struct Cp {
-      void* dst;
-      const void* src;
-      size_t bytes;
-    } cps[] = {
-        {taps->logits, h->logits, (size_t)rows * d.experts * 4},
-        {taps->ids, h->ids, (size_t)rows * d.top_k * 4},
-        {taps->weights, h->weights, (size_t)rows * d.top_k * 4},
-        {taps->h, h->h, (size_t)rows * d.pooled * 2},
-        {taps->act, h->act, (size_t)rows * d.top_k * d.inter * 2},
-        {taps->y, h->y, (size_t)rows * d.top_k * d.pooled * 4},
-        {taps->moe_out, h->moe_out, (size_t)rows * d.pooled * 2},
-        {taps->u, h->u, (size_t)rows * d.hidden * 4},
-    };
-    for (const Cp& c : cps)
-      if (c.dst) {
-        const cudaError_t r = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, s);
-        if (r != cudaSuccess) return cuda_err(h, r, "tap copy");
-      }
-  }
-  (void)e;
-  if (bad_event) {
-    cudaGetLastError();  // clear the failed record
-    return set_err(h, MUSEMOE_EINVAL, "taps->events holds an event that could not be recorded");
-  }
   return MUSEMOE_OK;
 }
 
@@ -767,6 +801,95 @@ musemoe_status musemoe_forward_debug(musemoe_handle* h, const musemoe_weights* w
   musemoe_status st = check_call(h, w, x, stream, out, rows, false);
   if (st != MUSEMOE_OK) return st;
   return launch_chain(h, w, x, stream, out, rows, reinterpret_cast<cudaStream_t>(s), taps);
+}
+
+musemoe_status musemoe_forward_ep_partial(musemoe_handle* h, const musemoe_weights* w,
+                                         const uint16_t* x, float* moe_partial, int32_t rows,
+                                         int32_t expert_first, int32_t expert_count,
+                                         musemoe_stream_t stream) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  if (rows < 1 || rows > h->d.max_rows)
+    return set_err(h, MUSEMOE_EINVAL, fmt("rows %d outside 1..max_rows (%d)", rows, h->d.max_rows));
+  std::vector<std::string> bad;
+  if (expert_count < 1 || expert_first < 0 || expert_first + expert_count > h->d.experts)
+    bad.push_back(fmt("expert range [%d, %d) is not a non-empty range of the %d experts",
+                      expert_first, expert_first + expert_count, h->d.experts));
+  auto need = [&](const void* q, const char* name) {
+    if (!q) bad.push_back(fmt("%s is NULL", name));
+    else if (!aligned16(q)) bad.push_back(fmt("%s is not 16-byte aligned", name));
+  };
+  need(x, "x");
+  need(moe_partial, "moe_partial");
+  if (!w) {
+    bad.push_back("weights is NULL");
+  } else {
+    need(w->w_router, "w_router");
+    need(w->expert_bias, "expert_bias");
+    need(w->w_pool, "w_pool");
+    need(w->w_pre_norm, "w_pre_norm");
+    need(w->w13, "w13");
+    need(w->w2, "w2");
+    if (h->quant != kBF16) {
+      need(w->w13_scale, "w13_scale");
+      need(w->w2_scale, "w2_scale");
+    }
+    if (h->quant == kNVFP4) {
+      need(w->w13_gscale, "w13_gscale");
+      need(w->w2_gscale, "w2_gscale");
+    }
+    need(w->w_post_norm, "w_post_norm");
+  }
+  if (!bad.empty()) return set_err(h, MUSEMOE_EINVAL, join(bad));
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != h->device)
+    return set_err(h, MUSEMOE_EINVAL, fmt("current device %d is not the handle's device %d", dev, h->device));
+  const EpArgs ep{expert_first, expert_count, moe_partial};
+  return launch_chain(h, w, x, nullptr, nullptr, rows, reinterpret_cast<cudaStream_t>(stream),
+                      nullptr, &ep);
+}
+
+musemoe_status musemoe_forward_ep_combine(musemoe_handle* h, const musemoe_weights* w,
+                                         const float* moe_sum, float* stream_io, uint16_t* out,
+                                         int32_t rows, musemoe_stream_t stream) {
+  if (!h) return set_err(nullptr, MUSEMOE_EINVAL, "handle is NULL");
+  if (rows < 1 || rows > h->d.max_rows)
+    return set_err(h, MUSEMOE_EINVAL, fmt("rows %d outside 1..max_rows (%d)", rows, h->d.max_rows));
+  std::vector<std::string> bad;
+  auto need = [&](const void* q, const char* name) {
+    if (!q) bad.push_back(fmt("%s is NULL", name));
+    else if (!aligned16(q)) bad.push_back(fmt("%s is not 16-byte aligned", name));
+  };
+  need(moe_sum, "moe_sum");
+  need(stream_io, "stream_io");
+  need(out, "out");
+  if (!w) {
+    bad.push_back("weights is NULL");
+  } else {
+    need(w->w_unpool, "w_unpool");
+    need(w->w_ffn_norm, "w_ffn_norm");
+    need(w->w_next_norm, "w_next_norm");
+    need(w->gate, "gate");
+  }
+  if (!bad.empty()) return set_err(h, MUSEMOE_EINVAL, join(bad));
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != h->device)
+    return set_err(h, MUSEMOE_EINVAL, fmt("current device %d is not the handle's device %d", dev, h->device));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // moe_out = bf16(sum of the ranks' partials): the rounding the single-GPU
+  // finalize applies to the same fp32 sum; launched without programmatic
+  // dependency on the caller's previous kernel (the all-reduce)
+  cudaError_t e = launch_round_bf16(moe_sum, h->moe_out, (long long)rows * h->d.pooled, s);
+  if (e != cudaSuccess) return cuda_err(h, e, "launch of the moe_out rounding");
+  auto before = []() {};
+  auto after = [&](cudaError_t r, const char* name) -> bool {
+    if (r == cudaSuccess) r = cudaGetLastError();
+    if (r != cudaSuccess) {
+      h->err = fmt("launch of %s failed: %s", name, cudaGetErrorString(r));
+      return false;
+    }
+    return true;
+  };
+  return launch_back(h, w, stream_io, out, rows, s, true, before, after);
 }
 
 musemoe_status musemoe_forward_host(musemoe_handle* h, const musemoe_weights* w,

@@ -172,10 +172,13 @@ static __device__ void permute(const RouteParams& p, int16_t* ids_s, unsigned ch
   }
   __syncthreads();
   // offsets of experts, and of their token groups
+  const int ep_lo = p.ep_count > 0 ? p.ep_first : 0;
+  const int ep_hi = p.ep_count > 0 ? p.ep_first + p.ep_count : E;
   {
     const int e = tid;
     const int c = e < E ? cnt_s[e] : 0;
-    const int ng = (c + p.token_group - 1) / p.token_group;
+    // token groups of this rank's experts only
+    const int ng = (e >= ep_lo && e < ep_hi) ? (c + p.token_group - 1) / p.token_group : 0;
     int tot;
     const int off = block_exclusive_scan(c, scan_scratch, &tot);
     if (e < E) off_s[e] = off;
@@ -191,9 +194,10 @@ static __device__ void permute(const RouteParams& p, int16_t* ids_s, unsigned ch
     p.route_list[off_s[e] + hist[(r >> 5) * E + e] + rank_s[r]] = r;
   }
   for (int e = tid; e < E; e += kRouteThreads) {
+    if (e < ep_lo || e >= ep_hi) continue;
     const int c = cnt_s[e];
     for (int gi = 0, s = 0; s < c; ++gi, s += p.token_group) {
-      int4 gd = make_int4(e, off_s[e] + s, min(p.token_group, c - s), 0);
+      int4 gd = make_int4(e - ep_lo, off_s[e] + s, min(p.token_group, c - s), 0);
       reinterpret_cast<int4*>(p.groups)[goff_s[e] + gi] = gd;
     }
   }
@@ -220,11 +224,15 @@ static __device__ void permute_small(const RouteParams& p, const int16_t* ids_s)
     first += (e2 < tid);
   }
   if (tid < rt) p.route_list[rank] = tid;
-  const int ng = tid < E ? (cnt + p.token_group - 1) / p.token_group : 0;
+  const int ep_lo = p.ep_count > 0 ? p.ep_first : 0;
+  const int ep_hi = p.ep_count > 0 ? p.ep_first + p.ep_count : E;
+  const bool local = tid < E && tid >= ep_lo && tid < ep_hi;  // token groups of this rank's experts
+  const int ng = local ? (cnt + p.token_group - 1) / p.token_group : 0;
   int gtot;
   const int goff = block_exclusive_scan(ng, scan_scratch, &gtot);
-  for (int gi = 0, s = 0; s < cnt && tid < E; ++gi, s += p.token_group)
-    reinterpret_cast<int4*>(p.groups)[goff + gi] = make_int4(tid, first + s, min(p.token_group, cnt - s), 0);
+  for (int gi = 0, s = 0; s < cnt && local; ++gi, s += p.token_group)
+    reinterpret_cast<int4*>(p.groups)[goff + gi] =
+        make_int4(tid - ep_lo, first + s, min(p.token_group, cnt - s), 0);
   if (tid == 0) {
     p.counters[kNumGroups] = gtot;
     p.counters[kTicket] = 0;

@@ -273,7 +273,10 @@ def e2e_bound(cfg: synth.Config) -> float:
     stage-wise one. W4A4 rounds the same two inputs per block of 32 / 16
     with a dynamic scale: a near tie upstream moves an e2m1 code by one step
     (up to 1/3 relative) or a block scale by a factor of 2; the same 1e-1
-    bound, the same stage-wise strict check."""
+    bound, the same stage-wise strict check. Measured on the oracle itself
+    (test_harness_cpu.test_requantized_forms_drift_beyond_the_w4a16_bound):
+    one bf16 step in one input element per row moves its own stream / out by
+    about 5 % of RMS for FP8 and 11-20 % for W4A4, 1.6 % for W4A16."""
     return FP8_E2E_TOL if cfg.quant in (synth.FP8,) + W4A4 else OUT_TOL
 
 

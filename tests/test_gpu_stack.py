@@ -3,11 +3,12 @@ boundaries, b=32 rows, H=5120, P=2048, I=1024, E=128, top-8, MXFP4 experts,
 independent weights per layer (seed 4 + layer), the stream carried and each
 layer's bf16 output fed to the next.
 
-The GPU runs the whole chain on all 32 rows. Rows never interact, so the
-oracle follows a sample of rows through all 60 layers in four chains:
-* stage-wise: at each layer the oracle starts from the GPU's layer input and
-  continues through the GPU's near-tie decisions (ids, bf16 roundings); every
-  stage must match on the same inputs;
+The GPU runs the whole chain on all 32 rows. Every row is checked
+stage-wise at every layer: the oracle starts from the GPU's layer input and
+continues through the GPU's near-tie decisions (ids, bf16 roundings); every
+stage must match on the same inputs (these 60 checks are independent of one
+another and run in spawned worker processes). Rows never interact, so the
+oracle follows a sample of rows through all 60 layers in three chains:
 * tracked: the oracle carries its own x and stream through all 60 layers and
   takes the GPU's value only where a decision is a near tie (the expert
   selection within 1e-6, a bf16 rounding within the near-tie band); the
@@ -23,6 +24,8 @@ so two correct computations of the stack drift apart by several percent of
 RMS over 60 layers (the perturbed chain measures this for the oracle
 itself). The independent chain's drift from the GPU must stay within a small
 multiple of the oracle's own drift under that one-step change."""
+import multiprocessing as mp
+import os
 import time
 
 import numpy as np
@@ -35,6 +38,7 @@ import synth
 from moe_decode_layer_router_gb300 import _build
 
 from . import _harness as H
+from . import _stack_check
 
 pytestmark = pytest.mark.gpu
 
@@ -56,13 +60,21 @@ def test_stack_of_60_layers():
     x0, st0 = synth.activations(cfg)
     run = H.Run(cfg)
     rows = SAMPLE_ROWS
-    xs, ss = x0[rows].copy(), st0[rows].astype(np.float64)       # stage-wise chain
-    xt, st_ = x0[rows].copy(), st0[rows].astype(np.float64)      # tracked chain
-    xi, si = x0[rows].copy(), st0[rows].astype(np.float64)       # independent chain
-    xp, sp = x0[rows].copy(), st0[rows].astype(np.float64)       # perturbed chain
-    xp[:, 0] += 1                                                # one bf16 step
-    max_stage = {}
-    near_total = {}
+    all_rows = []  # every row's stage-wise errors, per layer
+    sample = []    # the sample rows' GPU decisions per layer, for the chains
+    # one BLAS thread per worker (the workers share the host's cores)
+    saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                            "MKL_NUM_THREADS")}
+    os.environ.update({v: "1" for v in saved})
+    try:
+        pool = mp.get_context("spawn").Pool(max(2, min(16, (os.cpu_count() or 2) - 1)))
+    finally:
+        for v, old in saved.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    pending = []
     try:
         xd = H.to_dev(x0)
         sd = H.to_dev(st0)
@@ -78,61 +90,52 @@ def test_stack_of_60_layers():
                 act=torch.empty((b * cfg.top_k, cfg.inter), dtype=torch.int16, device="cuda"),
                 moe_out=torch.empty((b, cfg.pooled), dtype=torch.int16, device="cuda"),
                 u=torch.empty((b, cfg.hidden), dtype=torch.float32, device="cuda"))
+            x_in = xd.cpu().numpy().view(np.uint16).copy()
+            s_in = sd.cpu().numpy().astype(np.float64)
             mm.musemoe_forward_debug(run.handle, W, xd, sd, out, b, None, mm.make_taps(**taps))
             torch.cuda.synchronize()
             g = {k: v.cpu().numpy() for k, v in taps.items()}
-            gids = g["ids"][rows]
-            gh = O.bf16_to_f64(g["h"].view(np.uint16)[rows])
-            gact = g["act"].view(np.float16).astype(np.float64).reshape(b, cfg.top_k, -1)[rows]
-            gmo = O.bf16_to_f64(g["moe_out"].view(np.uint16)[rows])
-            gout = O.bf16_to_f64(out.cpu().numpy().view(np.uint16)[rows])
-            gstream = sd.cpu().numpy().astype(np.float64)[rows]
-            near = dict(h=gh, act=np.where(np.abs(gact) >= 2.0 ** -14, gact, np.nan),
-                        moe_out=gmo, out=gout)
-            # stage-wise: the oracle continues through the GPU's near-tie decisions
-            ref = H.oracle_block(cfg, xs, ss, w, force_ids=gids, near=near)
-            H.check_ids(gids, O.route(O.router_logits(xs, w["w_router"]), w["expert_bias"],
-                                      cfg.top_k, cfg.route_scale, cfg.multiplier, cfg.score,
-                                      cfg.division_eps), cfg.top_k)
-            np.testing.assert_allclose(g["weights"][rows], ref["weights"], rtol=H.WEIGHT_RTOL)
-            errs = {"h": H.rel_err(gh, ref["h"]), "moe_out": H.rel_err(gmo, ref["moe_out"]),
-                    "u": H.rel_err(g["u"][rows], ref["u"]),
-                    "stream": H.rel_err(gstream, ref["stream"]),
-                    "out": H.rel_err(gout, ref["out"])}
-            for k, v in errs.items():
-                max_stage[k] = max(max_stage.get(k, 0.0), v)
-                assert v <= H.STAGE_TOL[k], (layer, k, v)
-            for k, v in ref["near_ties"].items():
-                near_total[k] = near_total.get(k, 0) + v
-            # the stage-wise chain moves on with the GPU's own layer output
-            xs, ss = O.f64_to_bf16_bits(gout), gstream
-            # tracked chain: own state, the GPU's decisions at near ties only
-            H.check_ids(gids, O.route(O.router_logits(xt, w["w_router"]), w["expert_bias"],
-                                      cfg.top_k, cfg.route_scale, cfg.multiplier, cfg.score,
-                                      cfg.division_eps), cfg.top_k)
-            trk = H.oracle_block(cfg, xt, st_, w, force_ids=gids, near=near)
-            xt, st_ = trk["out_bits"], trk["stream"]
-            # independent chain: own roundings, the GPU's expert selection
-            ind = H.oracle_block(cfg, xi, si, w, force_ids=gids)
-            # perturbed chain: own roundings, the independent chain's selection
-            per = H.oracle_block(cfg, xp, sp, w, force_ids=ind["ids"])
-            xi, si = ind["out_bits"], ind["stream"]
-            xp, sp = per["out_bits"], per["stream"]
+            ga = {"ids": g["ids"], "weights": g["weights"],
+                  "h": O.bf16_to_f64(g["h"].view(np.uint16)),
+                  "act": g["act"].view(np.float16).astype(np.float64).reshape(b, cfg.top_k, -1),
+                  "moe_out": O.bf16_to_f64(g["moe_out"].view(np.uint16)), "u": g["u"],
+                  "out": O.bf16_to_f64(out.cpu().numpy().view(np.uint16)),
+                  "stream": sd.cpu().numpy().astype(np.float64)}
+            # every row, stage-wise, in a worker process
+            pending.append(pool.apply_async(_stack_check.check_layer, ((layer, x_in, s_in, ga),)))
+            sample.append({k: ga[k][rows] for k in ("ids", "h", "act", "moe_out", "out")})
             xd = out
             del t, W
         g_stream = sd.cpu().numpy()[rows].astype(np.float64)
         g_out = O.bf16_to_f64(xd.cpu().numpy().view(np.uint16)[rows])
-        tracked = {"stream": H.rel_err(g_stream, st_),
-                   "out": H.rel_err(g_out, O.bf16_to_f64(xt))}
-        independent = {"stream": H.rel_err(g_stream, si),
-                       "out": H.rel_err(g_out, O.bf16_to_f64(xi))}
-        perturbed = {"stream": H.rel_err(sp, si),
-                     "out": H.rel_err(O.bf16_to_f64(xp), O.bf16_to_f64(xi))}
+        x_s, s_s = x0[rows].copy(), st0[rows].astype(np.float64)
+        chains = [pool.apply_async(_stack_check.run_chains, ((kind, x_s, s_s, sample),))
+                  for kind in ("tracked", "independent")]
+        max_stage, near_total = {}, {}
+        for res in pending:
+            r = res.get()
+            assert not r["bad"], (r["layer"], r["bad"])
+            for k, v in r["errs"].items():
+                max_stage[k] = max(max_stage.get(k, 0.0), v)
+            for k, v in r["near_ties"].items():
+                near_total[k] = near_total.get(k, 0) + v
+        fin = {}
+        for c in chains:
+            fin.update(c.get())
     finally:
+        pool.terminate()
         run.close()
-    print("stack: max stage errors", max_stage, "near ties", near_total, "tracked", tracked,
-          "independent", independent, "oracle drift under one bf16 step", perturbed,
-          f"({time.time() - t0:.0f} s)")
+    st_, xt = fin["tracked"]
+    si, xi = fin["independent"]
+    sp, xp = fin["perturbed"]
+    tracked = {"stream": H.rel_err(g_stream, st_), "out": H.rel_err(g_out, O.bf16_to_f64(xt))}
+    independent = {"stream": H.rel_err(g_stream, si), "out": H.rel_err(g_out, O.bf16_to_f64(xi))}
+    perturbed = {"stream": H.rel_err(sp, si),
+                 "out": H.rel_err(O.bf16_to_f64(xp), O.bf16_to_f64(xi))}
+    print("stack: every row stage-wise over", len(pending), "layers, max errors", max_stage,
+          "near ties", near_total, "tracked", tracked, "independent", independent,
+          "oracle drift under one bf16 step", perturbed, f"({time.time() - t0:.0f} s)")
+    assert len(pending) == cfg.layers
     assert max(tracked.values()) <= H.OUT_TOL, tracked
     for k in ("stream", "out"):
         assert independent[k] <= DRIFT_FACTOR * max(perturbed[k], H.OUT_TOL), (

@@ -90,3 +90,36 @@ def test_kernel_layout_fp8_swizzle():
     # row 1 of group 0: (1 >> 1) & 3 = 0, units in place
     blk0 = k.reshape(-1)[64:128]
     assert np.array_equal(blk0, plain[0, 1, :64])
+
+
+def _self_drift(cfg, seed):
+    """The oracle against itself: max |change| / RMS of stream and out when one
+    element of every input row moves by one bf16 step (the routing kept)."""
+    import oracle as O
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    p = synth.routing_params(cfg)
+    a = O.block(x, st, w, quant=cfg.quant, norm_eps=cfg.norm_eps, **p)
+    rng = np.random.default_rng(100 + seed)
+    xp = x.copy()
+    xp[np.arange(x.shape[0]), rng.integers(0, x.shape[1], size=x.shape[0])] += 1
+    b = O.block(xp, st, w, quant=cfg.quant, norm_eps=cfg.norm_eps, force_ids=a["ids"], **p)
+    return max(H.rel_err(b[k], a[k]) for k in ("stream", "out"))
+
+
+def test_requantized_forms_drift_beyond_the_w4a16_bound():
+    # Why FP8 W8A8 and W4A4 are held to FP8_E2E_TOL independently (and
+    # strictly stage-wise): their per-row / per-block dynamic requantization
+    # turns a one-step change of one input element per row into a change of
+    # the oracle's OWN outputs well beyond the 2e-2 block bound, so no
+    # computation that rounds at the pages' points can meet 2e-2 against an
+    # independent oracle run; the W4A16 form stays inside it. The bound is
+    # within a small multiple of the oracle's own drift (decode shapes, 16
+    # experts, 16 rows).
+    base = dataclasses.replace(synth.CONFIGS["decode"], rows=16, experts=16, seed=41)
+    d = {q: _self_drift(dataclasses.replace(base, quant=q), 0)
+         for q in (synth.MXFP4, synth.FP8, synth.MXFP4_A4, synth.NVFP4_A4)}
+    assert d[synth.MXFP4] <= H.OUT_TOL, d
+    for q in (synth.FP8, synth.MXFP4_A4, synth.NVFP4_A4):
+        assert d[q] > H.OUT_TOL, (q, d)
+    assert H.FP8_E2E_TOL <= 2.5 * d[synth.FP8], d

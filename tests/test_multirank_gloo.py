@@ -133,3 +133,73 @@ def test_bench_timing_takes_slowest_rank():
         m, rate = res[r]
         assert m == 15.0
         assert rate == pytest.approx(WORLD * 8 * 100 / 0.015)
+
+
+def _ep_rank_library(rank: int, world: int, port: int, cfg_name: str, result):
+    """A rank of the expert-parallel block through the library on cuda:0: its
+    experts' partial moe_out (musemoe_forward_ep_partial), the all-reduce over
+    gloo (host tensors), then musemoe_forward_ep_combine. The ranks' kernels
+    never wait on one another: they meet only in the host all-reduce."""
+    _init(rank, world, port)
+    try:
+        import dataclasses
+
+        import moe_decode_layer_router_gb300 as mm
+        import synth
+        from tests import _harness as H
+        torch.cuda.set_device(0)
+        mm.library()
+        cfg = synth.CONFIGS[cfg_name]
+        w = synth.layer_tensors(cfg)
+        x, st = synth.activations(cfg)
+        E = cfg.experts
+        lo, hi = rank * E // world, (rank + 1) * E // world
+        keys = ("w13", "w13_scale", "w13_gscale", "w2", "w2_scale", "w2_gscale")
+        t = {k: H.to_dev(v) for k, v in w.items() if k not in keys}
+        for k in keys:
+            if k in w:
+                t[k] = H.to_dev(np.ascontiguousarray(w[k][lo:hi]))
+        mm.musemoe_pack_experts(H.dims_of(dataclasses.replace(cfg, experts=hi - lo)),
+                                H.QUANT[cfg.quant], t["w13"], t.get("w13_scale"), t["w13"],
+                                t.get("w13_scale"), t["w2"], t.get("w2_scale"), t["w2"],
+                                t.get("w2_scale"))
+        W = mm.make_weights(t)
+        run = H.Run(cfg)
+        try:
+            part = torch.empty((cfg.rows, cfg.pooled), dtype=torch.float32, device="cuda")
+            mm.musemoe_forward_ep_partial(run.handle, W, H.to_dev(x), part, cfg.rows, lo, hi - lo)
+            torch.cuda.synchronize()
+            host = part.cpu()
+            dist.all_reduce(host, op=dist.ReduceOp.SUM)
+            sd = H.to_dev(st)
+            out = torch.empty((cfg.rows, cfg.hidden), dtype=torch.int16, device="cuda")
+            mm.musemoe_forward_ep_combine(run.handle, W, host.cuda(), sd, out, cfg.rows)
+            torch.cuda.synchronize()
+            ok = mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_OK
+        finally:
+            run.close()
+        result[rank] = dict(stream=sd.cpu().numpy().astype(np.float64),
+                            out=out.cpu().numpy().view(np.uint16).copy(), ok=ok)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg_name", ["tiny", "decode"])
+def test_expert_parallel_library_on_two_ranks(cfg_name):
+    sys.path.insert(0, ROOT)
+    import oracle as O
+    import synth
+    from tests import _harness as H
+    cfg = synth.CONFIGS[cfg_name]
+    res = _spawn(_ep_rank_library, cfg_name)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    ref = O.block(x, st, w, quant=cfg.quant, norm_eps=cfg.norm_eps,
+                  **synth.routing_params(cfg))
+    # both ranks hold the same all-reduced block output, within the block's bounds
+    np.testing.assert_array_equal(res[0]["out"], res[1]["out"])
+    np.testing.assert_array_equal(res[0]["stream"], res[1]["stream"])
+    assert res[0]["ok"] and res[1]["ok"]
+    assert H.rel_err(res[0]["stream"], ref["stream"]) <= H.OUT_TOL
+    assert H.rel_err(O.bf16_to_f64(res[0]["out"]), ref["out"]) <= H.OUT_TOL
