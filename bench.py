@@ -12,8 +12,8 @@ runs 4 steps, chained on the device as consecutive layers' blocks would be.
 
 N > 1 (under torchrun) runs N independent replicas, one per GPU (the block
 has no cross-GPU step): value = rows of all ranks / max over ranks of the
-timed region. --impl reference times the oracle (numpy, float64) on the host
-cores on a bounded sample of the same workload.
+timed region. --impl reference times the oracle (plain C, float64, one host
+core) on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -172,8 +172,8 @@ class ClockSampler:
 ORACLE_SNIPPET = r"""
 import json, os, sys, time
 sys.path.insert(0, {root!r})
-import numpy as np
-import synth, oracle as O
+import synth
+from oracle import c_oracle as C
 cfg = synth.CONFIGS[{workload!r}]
 w = synth.layer_tensors(cfg, {layer})
 x, st = synth.activations(cfg)
@@ -184,7 +184,7 @@ times = []
 deadline = time.perf_counter() + {budget}
 for i in range({steps}):
     t0 = time.perf_counter()
-    O.block(x, st, w, quant=cfg.quant, norm_eps=cfg.norm_eps, **p)
+    C.block(x, st, w, quant=cfg.quant, norm_eps=cfg.norm_eps, omp={omp}, **p)
     times.append(time.perf_counter() - t0)
     if time.perf_counter() > deadline:
         break
@@ -194,14 +194,17 @@ print(json.dumps({{"times": times, "rows": rows}}))
 
 def run_oracle(steps: int, budget_s: float, threads: int = 1, workload: str = WORKLOAD,
                rows: int = 0, layer: int = 0) -> dict:
-    """Times the oracle on `steps` blocks of `workload` (its first `rows`
-    rows, all if 0; layer `layer` of a stack) in a child process pinned to
-    `threads` BLAS/OpenMP threads."""
+    """Times the C oracle (plain C, float64, no BLAS) on `steps` blocks of
+    `workload` (its first `rows` rows, all if 0; layer `layer` of a stack) in
+    a child process: the single-threaded build for threads == 1, else the
+    OpenMP build of the same source on `threads` threads."""
+    from oracle import c_oracle
+    c_oracle.build()
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = str(threads)
     code = ORACLE_SNIPPET.format(root=ROOT, workload=workload, steps=steps, budget=budget_s,
-                                 rows=rows, layer=layer)
+                                 rows=rows, layer=layer, omp=threads > 1)
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                          check=True)
     return json.loads(out.stdout.strip().splitlines()[-1])
@@ -405,8 +408,8 @@ def bench_bucket(dev, name: str, quant_code: int, hbm_peak: float, cpu_rows: int
             "cpu_baseline": {"value": ora["rows"] / ot, "unit": "rows/s", "cores": 1,
                              "kind": "oracle",
                              "sample": f"{len(ora['times'])} blocks of the first {ora['rows']} "
-                                       f"rows ({sum(ora['times']):.1f} s, numpy float64, "
-                                       "1 BLAS thread)"}}
+                                       f"rows ({sum(ora['times']):.1f} s, plain C float64, "
+                                       "one thread)"}}
 
 
 def bench_stack(dev, hbm_peak: float) -> dict:
@@ -497,7 +500,7 @@ def bench_stack(dev, hbm_peak: float) -> dict:
     torch.cuda.empty_cache()
     active = ebytes / len(probe) / expert_bytes_per_expert(cfg)
     bbytes = block_bytes(cfg, active)
-    ora = run_oracle(steps=2, budget_s=20.0, threads=1, workload="stack", rows=0, layer=0)
+    ora = run_oracle(steps=2, budget_s=20.0, threads=1, workload="stack", rows=8, layer=0)
     ot = sum(ora["times"]) / len(ora["times"])
     return {"workload": f"stack ({cfg.layers} chained layers, b={cfg.rows}, H={cfg.hidden}, "
                         f"P={cfg.pooled}, I={cfg.inter}, E={cfg.experts}, top-{cfg.top_k}, "
@@ -517,8 +520,8 @@ def bench_stack(dev, hbm_peak: float) -> dict:
             "cpu_baseline": {"value": ora["rows"] / ot, "unit": "rows*layers/s", "cores": 1,
                              "kind": "oracle",
                              "sample": f"{len(ora['times'])} blocks of layer 0 on "
-                                       f"{ora['rows']} rows ({sum(ora['times']):.1f} s, numpy "
-                                       "float64, 1 BLAS thread)"}}
+                                       f"{ora['rows']} rows ({sum(ora['times']):.1f} s, plain "
+                                       "C float64, one thread)"}}
 
 
 def bench_w4a4(dev) -> dict:
@@ -811,12 +814,19 @@ def bench_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = run_oracle(steps=6, budget_s=20.0, threads=1)
+        r = run_oracle(steps=4, budget_s=20.0, threads=1)
         tot = sum(r["times"])
+        ncores = os.cpu_count() or 1
+        rm = run_oracle(steps=6, budget_s=10.0, threads=ncores)
+        tm = sum(rm["times"])
         cpu = {"value": r["rows"] * len(r["times"]) / tot, "unit": "rows/s", "cores": 1,
                "kind": "oracle",
                "sample": f"{len(r['times'])} full decode steps of {r['rows']} rows "
-                         f"({tot:.1f} s, numpy float64, 1 BLAS thread)"}
+                         f"({tot:.1f} s, plain C float64, one thread)",
+               "openmp_all_cores": {"value": rm["rows"] * len(rm["times"]) / tm,
+                                    "unit": "rows/s", "cores": ncores,
+                                    "sample": f"{len(rm['times'])} steps, the OpenMP build of "
+                                              f"the same C source on {ncores} threads"}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
@@ -871,15 +881,17 @@ def bench_reference(args):
         return
     warm = max(3, args.warmup) if args.warmup < 3 else args.warmup
     # bound the whole run to a few minutes: one oracle step is a full 8-row
-    # decode step (seconds on one core)
+    # decode step (about five seconds on one core)
     w_run = run_oracle(steps=min(warm, 3), budget_s=60.0, threads=1)
     per = sum(w_run["times"]) / len(w_run["times"])
     k = max(1, min(args.steps, int(120.0 / max(per, 1e-3))))
     r = run_oracle(steps=k, budget_s=150.0, threads=1)
     tot = sum(r["times"])
     value = r["rows"] * len(r["times"]) / tot
-    sample = (f"{len(r['times'])} full decode steps of {r['rows']} rows (capped from "
-              f"{args.steps} to fit a few minutes; numpy float64, 1 BLAS thread)")
+    capped = (f"capped from {args.steps} to fit a few minutes; "
+              if len(r["times"]) < args.steps else "")
+    sample = (f"{len(r['times'])} full decode steps of {r['rows']} rows ({capped}"
+              f"plain C float64, one thread)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
         "n_gpus": world, "steps": len(r["times"]), "warmup": warm,
