@@ -51,6 +51,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step's kernels directly instead of replaying a CUDA graph")
+    ap.add_argument("--bucket", choices=["verify", "large"], default=None,
+                    help="time one single-layer bucket alone (--steps graph replays, --warmup "
+                         "debug forwards) and print its object: a bounded run for profiling")
     return ap.parse_args()
 
 
@@ -208,6 +211,16 @@ def run_oracle(steps: int, budget_s: float, threads: int = 1, workload: str = WO
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                          check=True)
     return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def _hbm_peak():
+    """The measured HBM copy bandwidth (GB/s) and its source; the profiling
+    recipe's fallback when no measurement is on disk."""
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(pk_path)) if os.path.exists(pk_path) else {}
+    if peaks.get("hbm_gbs"):
+        return float(peaks["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
 
 
 def _pct(v, q):
@@ -369,7 +382,7 @@ def block_flops(cfg) -> float:
 
 
 def bench_bucket(dev, name: str, quant_code: int, hbm_peak: float, cpu_rows: int,
-                 cpu_budget: float) -> dict:
+                 cpu_budget: float, replays: int = 200, reps: int = 10) -> dict:
     """One single-layer bucket (a graph of one forward, L2 evicted before each
     replay, 200 replays timed one by one): rows/s at the median, p10/p90, the
     expert phase (w13 + w2 event times) and the whole block against their
@@ -379,7 +392,7 @@ def bench_bucket(dev, name: str, quant_code: int, hbm_peak: float, cpu_rows: int
     import synth
 
     cfg = synth.CONFIGS[name]
-    r = _bench_form(dev, cfg, quant_code, steps=200, reps=10, flush=True)
+    r = _bench_form(dev, cfg, quant_code, steps=replays, reps=reps, flush=True)
     st, dur = r["replay_stats"], r["kernel_us"]
     us = st["p50_us"]
     A = r["active_experts"]
@@ -387,8 +400,13 @@ def bench_bucket(dev, name: str, quant_code: int, hbm_peak: float, cpu_rows: int
     e_us = dur["w13"] + dur["w2"]
     bbytes = block_bytes(cfg, A)
     eflops = 2.0 * cfg.rows * cfg.top_k * 3 * cfg.inter * cfg.pooled
-    ora = run_oracle(steps=3, budget_s=cpu_budget, threads=1, workload=name, rows=cpu_rows)
-    ot = sum(ora["times"]) / len(ora["times"])
+    cpu = None
+    if cpu_rows:
+        ora = run_oracle(steps=3, budget_s=cpu_budget, threads=1, workload=name, rows=cpu_rows)
+        ot = sum(ora["times"]) / len(ora["times"])
+        cpu = {"value": ora["rows"] / ot, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(ora['times'])} blocks of the first {ora['rows']} rows "
+                         f"({sum(ora['times']):.1f} s, plain C float64, one thread)"}
     return {"workload": f"{name} (b={cfg.rows}, H={cfg.hidden}, P={cfg.pooled}, I={cfg.inter}, "
                         f"E={cfg.experts}, top-{cfg.top_k}, {cfg.quant}, "
                         f"{'softmax' if cfg.score == synth.SOFTMAX else 'sigmoid'}"
@@ -404,12 +422,7 @@ def bench_bucket(dev, name: str, quant_code: int, hbm_peak: float, cpu_rows: int
             "block": {"algorithmic_bytes": bbytes, "achieved_gbs": bbytes / (us / 1e6) / 1e9,
                       "frac": bbytes / (us / 1e6) / 1e9 / hbm_peak,
                       "tflops": block_flops(cfg) / (us / 1e6) / 1e12},
-            "kernel_us": dur, "health": r["health"],
-            "cpu_baseline": {"value": ora["rows"] / ot, "unit": "rows/s", "cores": 1,
-                             "kind": "oracle",
-                             "sample": f"{len(ora['times'])} blocks of the first {ora['rows']} "
-                                       f"rows ({sum(ora['times']):.1f} s, plain C float64, "
-                                       "one thread)"}}
+            "kernel_us": dur, "health": r["health"], "cpu_baseline": cpu}
 
 
 def bench_stack(dev, hbm_peak: float) -> dict:
@@ -563,6 +576,14 @@ def bench_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     _build.build()
     synth.build()
+    if args.bucket:
+        code = {"verify": mm.MUSEMOE_NVFP4, "large": mm.MUSEMOE_FP8_W8A8}[args.bucket]
+        peak, _ = _hbm_peak()
+        b = bench_bucket(dev, args.bucket, code, peak, 0 if args.no_cpu_baseline else 16, 15.0,
+                         replays=max(1, args.steps), reps=max(3, args.warmup))
+        if rank == 0:
+            print(json.dumps({"bucket": args.bucket, **b}))
+        return
     cfg = synth.CONFIGS[WORKLOAD]
     quant = mm.MUSEMOE_MXFP4
     dims = mm.Dims(max_rows=cfg.rows, hidden=cfg.hidden, pooled=cfg.pooled, inter=cfg.inter,
@@ -709,13 +730,7 @@ def bench_ours(args):
     kernel_bytes = {nm: sum(m[nm] for m in model) / len(model) for nm in names}
     share = {nm: kernel_ms[nm] / sum(kernel_ms.values()) for nm in names}
     dom = max(names, key=lambda nm: kernel_ms[nm])
-    peaks = {}
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        peaks = json.load(open(pk_path))
-    hbm_peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if hbm_peak else "fallback"
-    hbm_peak = hbm_peak or 6800.0
+    hbm_peak, peak_src = _hbm_peak()
     achieved = kernel_bytes[dom] / (kernel_ms[dom] / 1e3) / 1e9
     src = open(os.path.join(ROOT, "moe_decode_layer_router_gb300", "csrc", "k_experts.cu"),
                "rb").read()

@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
     constexpr int LT = C::loaders * 32;
     constexpr int RSTEP = LT / 16;
     constexpr int RPT = kTN / RSTEP;  // rows per thread
+    constexpr int kLag = 1;           // copy groups left in flight when a piece is released
     const int uu = lt & 15, r0 = lt >> 4;
     const size_t rowB = (size_t)p.K * kel;
     uint32_t roff[RPT];
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
     SKWalk wk;
     wk.begin();
     int gcur = -1;
-    int piece = 0;
+    int piece = 0, released = 0;  // pieces issued / released to the MMA side
     bool ok = true;
     for (int n = 0; n < count && ok; ++n) {
       wk.next(R);
@@ -381,12 +382,24 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
       const int pieces = C::fp4 ? nc : 1;
       for (int c = 0; c < pieces; ++c, ++piece) {
         const int bs = piece % C::n_b, use = piece / C::n_b;
-        unsigned long long* const fb = C::fp4 ? &cfull[bs] : &full_b[bs];
         unsigned long long* const eb = C::fp4 ? &cempty[bs] : &empty_b[bs];
-        if (use > 0 && !__all_sync(0xffffffffu, wait(eb, (uint32_t)(use - 1) & 1u))) {
-          if (lane == 0) fail();
-          ok = false;
-          break;
+        if (use > 0) {
+          const uint32_t ph = (uint32_t)(use - 1) & 1u;
+          if (!__all_sync(0xffffffffu, mbar_test(smem_u32(eb), ph))) {
+            // the slot is still in use: release the pending pieces before
+            // blocking on it, so that no finished piece waits behind it
+            if (piece > released) {
+              asm volatile("cp.async.wait_all;\n" ::: "memory");
+              tc::fence_proxy_async_smem();
+              for (; released < piece; ++released)
+                mbar_arrive(smem_u32(C::fp4 ? &cfull[released % C::n_b] : &full_b[released % C::n_b]));
+            }
+            if (!__all_sync(0xffffffffu, wait(eb, ph))) {
+              if (lane == 0) fail();
+              ok = false;
+              break;
+            }
+          }
         }
         if (lt == 0) TL(3, tlc, 1);
         const uint32_t dst = b0s + bs * kTBSlot;
@@ -413,14 +426,26 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
                              "l"(src + roff[m]));
           }
         }
-        // the slot's barrier receives this thread's arrival once its copies
-        // have landed; the thread runs on to the next piece
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(fb))
-                     : "memory");
+        // one copy group per piece; the pieces issued kLag pieces earlier
+        // or before have landed once all but the newest kLag groups have:
+        // the thread makes its rows visible to the tensor core (async proxy)
+        // and arrives on those pieces' slots, so the MMA side needs no
+        // proxy fence
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        if (piece - kLag >= released) {
+          asm volatile("cp.async.wait_group %0;\n" ::"n"(kLag) : "memory");
+          tc::fence_proxy_async_smem();
+          for (; released <= piece - kLag; ++released)
+            mbar_arrive(smem_u32(C::fp4 ? &cfull[released % C::n_b] : &full_b[released % C::n_b]));
+        }
         if (lt == 0) TL(3, tlc, 2);
       }
     }
-    asm volatile("cp.async.wait_all;\n" ::: "memory");  // nothing in flight at exit
+    // the pieces still in flight: land, publish, arrive (nothing in flight at exit)
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    tc::fence_proxy_async_smem();
+    for (; released < piece; ++released)
+      mbar_arrive(smem_u32(C::fp4 ? &cfull[released % C::n_b] : &full_b[released % C::n_b]));
   } else if (warp == C::w_mma) {
     // ---------------- MMA issue (one lane) ----------------
     if (lane == 0) {
@@ -460,9 +485,6 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
             break;
           }
           TL(1, tlc, 3);
-          // the B rows came through cp.async (generic proxy); the MMA reads
-          // them through the async proxy
-          tc::fence_proxy_async_smem();
           tc::fence_after_sync();
           // descriptors of the unit's first k-step; k-step (c, h) starts
           // c * 512 + h * 32 bytes further (the start-address field counts 16 B)
@@ -487,7 +509,6 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
               break;
             }
             TL(1, tlc, 3);
-            tc::fence_proxy_async_smem();
             tc::fence_after_sync();
             const uint32_t a_t = tmem + kTAOff + as * kTAcc;
             // k-step j: A columns 8j.., B bytes (j / 4) * 8192 + (j % 4) * 32
@@ -628,13 +649,28 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         gcur = wk.grp;
         gd = group_of(gcur);
       }
+      const int e = gd.x, ntok = gd.z;
+      // the tile's weight-row scales, loaded ahead of the accumulator wait
+      // so that their latency hides behind it: w13 gate / up row scales
+      // (sg, su), w2 the row's scale (sg); NVFP4 the expert's global scale
+      float sg = 1.f, su = 1.f;
+      if (Q == kNVFP4) sg = su = __ldg(p.gscale + e);
+      if (Q == kFP8) {
+        const float* ws = reinterpret_cast<const float*>(p.scale);
+        if (ROLE == 0) {
+          const int i = wk.tile * 64 + (row >> 4) * 8 + (row & 7);
+          sg = __ldg(ws + (size_t)e * p.N + i);
+          su = __ldg(ws + (size_t)e * p.N + p.I + i);
+        } else {
+          sg = __ldg(ws + (size_t)e * p.N + wk.tile * 128 + row);
+        }
+      }
       if (!__all_sync(0xffffffffu, wait(&accfull[acc], (uint32_t)(acc_use >> 1) & 1u))) {
         if (lane == 0) fail();
         break;
       }
       if (tid == 0) TL(4, tlc, 1);
       tc::fence_after_sync();
-      const int e = gd.x, ntok = gd.z;
       const int ncol = (ntok + 15) >> 4;  // 16-column chunks holding tokens
       const int tb = wk.u - wk.slice;     // the tile's first unit
       const bool tile_end = (wk.slice == KS - 1);
@@ -667,10 +703,18 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         good = __shfl_sync(0xffffffffu, got, 0) != 0;
         if (!good && lane == 0) fail();
       }
+      bool released = false;
       for (int cc = 0; cc < ncol && good; ++cc) {
         float v[16];
         tc::ld_32x32b_x16(tsrc + cc * 16, v);
         tc::wait_ld();
+        if (cc == ncol - 1) {
+          // the accumulator is in registers: the MMA lane may reuse it
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&accempty[acc]));
+          released = true;
+        }
         if (mode == 1) {
           float4* dst = part + slot_of(blockIdx.x) + (cc * kTM + row) * 4;
 #pragma unroll
@@ -679,25 +723,41 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           continue;
         }
         if (mode == 2) {
+          // the other CTAs' partials, summed in CTA order; two contributors'
+          // loads are in flight together
           float s[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) s[i] = 0.f;
-          for (int c = c_first; c < c_last; ++c) {
-            const float4* src = part + slot_of(c) + (cc * kTM + row) * 4;
+          int c = c_first;
+          for (; c < c_last; c += 2) {
+            const bool two = c + 1 < c_last;
+            const float4* s0 = part + slot_of(c) + (cc * kTM + row) * 4;
+            const float4* s1 = part + slot_of(two ? c + 1 : c) + (cc * kTM + row) * 4;
+            float4 x0[4], x1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x0[i] = __ldcg(s0 + i);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x1[i] = two ? __ldcg(s1 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 x = __ldcg(src + i);
-              s[4 * i] += x.x;
-              s[4 * i + 1] += x.y;
-              s[4 * i + 2] += x.z;
-              s[4 * i + 3] += x.w;
+              s[4 * i] += x0[i].x;
+              s[4 * i + 1] += x0[i].y;
+              s[4 * i + 2] += x0[i].z;
+              s[4 * i + 3] += x0[i].w;
+            }
+            if (two) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                s[4 * i] += x1[i].x;
+                s[4 * i + 1] += x1[i].y;
+                s[4 * i + 2] += x1[i].z;
+                s[4 * i + 3] += x1[i].w;
+              }
             }
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = s[i] + v[i];
         }
-        float gsc = 1.f;
-        if (Q == kNVFP4) gsc = __ldg(p.gscale + e);
         if (ROLE == 0) {
           // lanes l (gate) and l ^ 8 (up) hold the same i: the gate lane
           // finishes columns 0..7 of the chunk, the up lane 8..15
@@ -710,12 +770,6 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
             const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
             g8[t] = is_gate ? v[t] : recv;
             u8[t] = is_gate ? recv : v[8 + t];
-          }
-          float sg = gsc, su = gsc;
-          const float* ws = reinterpret_cast<const float*>(p.scale);
-          if (Q == kFP8) {
-            sg = __ldg(ws + (size_t)e * p.N + i);
-            su = __ldg(ws + (size_t)e * p.N + p.I + i);
           }
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
@@ -738,8 +792,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           }
         } else {
           const int pr = wk.tile * 128 + row;
-          float sc = gsc;
-          if (Q == kFP8) sc = __ldg(reinterpret_cast<const float*>(p.scale) + (size_t)e * p.N + pr);
+          const float sc = sg;
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             const int nn = cc * 16 + t;
@@ -755,9 +808,11 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         __syncwarp();  // orders the lanes' partial stores before lane 0's release
         if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;\n" ::"l"(flag) : "memory");
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&accempty[acc]));
+      if (!released) {
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&accempty[acc]));
+      }
       if (tid == 0) TL(4, tlc, 2 + mode);
       acc ^= 1;
       ++acc_use;

@@ -46,6 +46,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
       : "memory");
   return ok != 0;
 }
+// Whether the mbarrier phase has completed (never blocks).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the mbarrier phase to complete, at most `limit_ns`.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase,
                                           unsigned long long limit_ns) {
