@@ -7,9 +7,9 @@
 // One CTA per SM (persistent), Stream-K over units = (token group, tile of
 // 128 weight rows, K-slice of 4 64-byte chunks). The MMA is
 // D[128 weight rows x N tokens] += A[128 x K] * B[N x K]^T with N the group's
-// tokens rounded up to 16, fp32 accumulation in tensor memory (two
-// accumulators of 64 columns, so the epilogue of one tile overlaps the MMAs
-// of the next; FP4 adds four 64-column A slots).
+// tokens rounded up to 16, fp32 accumulation in tensor memory (four
+// accumulators of 64 columns, so the epilogue of a tile overlaps the MMAs of
+// the next ones; FP4 adds four 64-column A slots).
 //
 // w13 (role 0): a tile is 64 gate rows and the matching 64 up rows,
 // interleaved by 8-row groups in A (group 2j gate rows i0 + 8j.., group
@@ -53,45 +53,81 @@ constexpr int kTN = 64;          // tokens per group at most (MMA N, padded to 1
 constexpr int kTAcc = 64;        // tensor-memory columns of one accumulator
 constexpr int kTEpi = 4;         // epilogue warps
 constexpr int kTDq = 8;          // dequantizing warps (FP4)
-constexpr int kTMeta = 8;        // token groups cached in shared memory
+constexpr int kTMeta = 4;        // token groups cached in shared memory
 constexpr int kTBSlot = 16384;   // one B piece (64 tokens x 256 B)
-constexpr int kTAOff = 2 * 64;   // tensor-memory column of the first A slot (FP4)
+constexpr int kTAOff = 4 * 64;   // tensor-memory column of the first A slot (FP4), after 4 accumulators
 constexpr int kTCodeBlock = 8 * kSliceChunks * 512;  // codes of one 64-row block's slice
-constexpr int kTSmemMax = 227 * 1024;
+constexpr int kTSmemMax = 227 * 1024;  // dynamic + static shared memory of a CTA
+constexpr int kTReserve = 3 * 1024;    // alignment slack (1024) + static shared memory (< 2048)
+
+// forms of the kernel beyond the weight formats: W4A4 on the FP4 tensor cores
+constexpr int kA4MX = 4, kA4NV = 5;
 
 template <int Q>
 struct TcCfg {
-  static constexpr bool fp4 = (Q == kMXFP4 || Q == kNVFP4);
+  static constexpr bool fp4 = (Q == kMXFP4 || Q == kNVFP4);  // FP4 weights dequantized to f16
+  static constexpr bool a4 = (Q == kA4MX || Q == kA4NV);     // W4A4, block-scaled FP4 MMA
+  static constexpr int apc = Q == kA4NV ? 2 : 1;  // W4A4: scale atoms per 64-byte code chunk
+  static constexpr int sf_bytes = a4 ? kSliceChunks * apc * 512 : 0;  // an operand's atoms per slice
   static constexpr int loaders = fp4 ? 2 : 4;  // B loader warps
-  static constexpr int warps = kTEpi + (fp4 ? kTDq : 0) + 2 + loaders;
+  static constexpr int sfw = a4 ? 1 : 0;       // W4A4: the scale-atom copy warp
+  static constexpr int warps = kTEpi + (fp4 ? kTDq : 0) + 2 + loaders + sfw;
   static constexpr int w_dq0 = kTEpi;                       // first dequant warp
   static constexpr int w_prod = kTEpi + (fp4 ? kTDq : 0);   // producer warp
   static constexpr int w_mma = w_prod + 1;
   static constexpr int w_load0 = w_prod + 2;
+  static constexpr int w_sf = w_load0 + loaders;
   static constexpr int threads = warps * 32;
   static constexpr int SB = (Q == kMXFP4) ? 4 : (Q == kNVFP4) ? 8 : 0;  // scale bytes / row / chunk
   static constexpr int scale_block = 8 * kSliceChunks * 8 * SB;        // scales of one block's slice
-  static constexpr int stage_bytes = 2 * kTCodeBlock + 2 * scale_block;
-  static constexpr int n_b = 4;             // B slots (FP8: one per stage; FP4: one per chunk slot)
-  static constexpr int n_a = fp4 ? 4 : 0;   // A slots (tensor memory, 64 columns each)
-  static constexpr int tmem_cols = fp4 ? 512 : 128;
+  // a weight stage: the unit's codes, their scales (FP4) or scale atoms (W4A4)
+  static constexpr int stage_bytes = 2 * kTCodeBlock + 2 * scale_block + sf_bytes;
+  // a B slot: the tokens' rows of a piece (+ W4A4: their scale atoms)
+  static constexpr int bslot = kTBSlot + sf_bytes;
+  // weight stages: FP4 next to four chunk slots; FP8 / W4A4 one B slot per
+  // stage; kTReserve is left for the 1024-byte alignment and the static
+  // shared memory (barriers, token-group cache)
+  static constexpr int stages =
+      fp4 ? ((kTSmemMax - kTReserve - 4 * bslot) / stage_bytes > 4
+                 ? 4
+                 : (kTSmemMax - kTReserve - 4 * bslot) / stage_bytes)
+          : ((kTSmemMax - kTReserve) / (stage_bytes + bslot) > 4
+                 ? 4
+                 : (kTSmemMax - kTReserve) / (stage_bytes + bslot));
+  static constexpr int n_b = fp4 ? 4 : stages;  // B slots (FP8 / W4A4: a unit's B rows ride in its stage)
+  static constexpr int n_a = fp4 ? 4 : 0;       // A slots (tensor memory, 64 columns each)
+  // accumulators (64 columns each): four, so that the epilogue may lag three
+  // tiles (FP4: next to four 64-column A slots, the whole tensor memory)
+  static constexpr int n_acc = 4;
+  static constexpr int tmem_cols = (fp4 || a4) ? 512 : 256;
+  // W4A4: the scale atoms of stage st in tensor memory, A then B, 4 columns each
+  static constexpr int sf_cols = a4 ? 2 * kSliceChunks * apc * 4 : 0;
 };
 
 template <int Q>
 __host__ __device__ constexpr int tc_stages() {
-  // weight stages in what the B and A slots leave of the shared memory
-  return (kTSmemMax - 3 * 1024 - TcCfg<Q>::n_b * kTBSlot) / TcCfg<Q>::stage_bytes > 4
-             ? 4
-             : (kTSmemMax - 3 * 1024 - TcCfg<Q>::n_b * kTBSlot) / TcCfg<Q>::stage_bytes;
+  return TcCfg<Q>::stages;
 }
 template <int Q>
 __host__ __device__ constexpr int tc_smem_bytes() {
-  return 1024 + tc_stages<Q>() * TcCfg<Q>::stage_bytes + TcCfg<Q>::n_b * kTBSlot;
+  return 1024 + tc_stages<Q>() * TcCfg<Q>::stage_bytes + TcCfg<Q>::n_b * TcCfg<Q>::bslot;
 }
-static_assert(tc_stages<kMXFP4>() >= 2 && tc_stages<kNVFP4>() >= 2 && tc_stages<kFP8>() >= 2,
+static_assert(tc_stages<kMXFP4>() >= 2 && tc_stages<kNVFP4>() >= 2 && tc_stages<kFP8>() >= 2 &&
+                  tc_stages<kA4MX>() >= 2 && tc_stages<kA4NV>() >= 2,
               "at least two weight stages");
-static_assert(tc_stages<kFP8>() == TcCfg<kFP8>::n_b, "FP8: a unit's B rows ride in its stage");
-static_assert(tc_smem_bytes<kNVFP4>() <= kTSmemMax && tc_smem_bytes<kFP8>() <= kTSmemMax, "smem");
+static_assert(tc_stages<kFP8>() == 4, "FP8: four stages");
+static_assert(tc_smem_bytes<kMXFP4>() + kTReserve - 1024 <= kTSmemMax &&
+                  tc_smem_bytes<kNVFP4>() + kTReserve - 1024 <= kTSmemMax &&
+                  tc_smem_bytes<kFP8>() + kTReserve - 1024 <= kTSmemMax &&
+                  tc_smem_bytes<kA4MX>() + kTReserve - 1024 <= kTSmemMax &&
+                  tc_smem_bytes<kA4NV>() + kTReserve - 1024 <= kTSmemMax,
+              "dynamic + static shared memory within a CTA's maximum");
+static_assert(TcCfg<kNVFP4>::n_acc * kTAcc + TcCfg<kNVFP4>::n_a * 64 <= 512 && kTAOff == 4 * kTAcc,
+              "FP4 tensor memory: accumulators, then the A slots");
+static_assert(TcCfg<kFP8>::n_acc * kTAcc <= TcCfg<kFP8>::tmem_cols, "FP8 tensor memory");
+static_assert(TcCfg<kA4NV>::n_acc * kTAcc + tc_stages<kA4NV>() * TcCfg<kA4NV>::sf_cols <= 512 &&
+                  TcCfg<kA4MX>::n_acc * kTAcc + tc_stages<kA4MX>() * TcCfg<kA4MX>::sf_cols <= 512,
+              "W4A4 tensor memory: accumulators and scale atoms");
 
 // CTA c runs units [U c / G, U (c + 1) / G); the CTA holding unit u:
 __device__ __forceinline__ int tc_cta_of(long long u, long long U, int G) {
@@ -203,13 +239,17 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
   // memory, loaders): cfull[cs] counts both, cempty[cs] is the MMA's commit.
   __shared__ __align__(8) unsigned long long full_b[4], empty_b[4];
   __shared__ __align__(8) unsigned long long cfull[4], cempty[4];
-  __shared__ __align__(8) unsigned long long accfull[2], accempty[2], drain_b;
+  __shared__ __align__(8) unsigned long long accfull[4], accempty[4], drain_b;
+  __shared__ __align__(8) unsigned long long sffull[4];  // W4A4: a stage's scale atoms in tensor memory
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ int4 meta_g[kTMeta];
   __shared__ int meta_r[kTMeta][kTN];
+  static_assert(sizeof(meta_g) + sizeof(meta_r) + 16 * 8 + 64 <= kTReserve - 1024,
+                "static shared memory within the reserve");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kNA = C::n_a > 0 ? C::n_a : 1;  // A slots (FP4; 1 keeps the other forms' dead code defined)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sbase = smem_raw + (base - smem_u32(smem_raw));
   constexpr int S = tc_stages<Q>();
@@ -239,12 +279,13 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
     meta_g[i] = __ldcg(reinterpret_cast<const int4*>(p.groups) + g_first + i);
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) {
+      mbar_init(smem_u32(&sffull[i]), 1);
       mbar_init(smem_u32(&full_b[i]), C::fp4 ? 1 : 1 + C::loaders * 32);
       mbar_init(smem_u32(&empty_b[i]), C::fp4 ? kTDq : 1);
       mbar_init(smem_u32(&cfull[i]), kTDq + C::loaders * 32);
       mbar_init(smem_u32(&cempty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::n_acc; ++i) {
       mbar_init(smem_u32(&accfull[i]), 1);
       mbar_init(smem_u32(&accempty[i]), kTEpi);
     }
@@ -284,7 +325,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
   if (warp == C::w_prod) {
     // ---------------- producer: the weight codes and scales ----------------
     if (lane == 0) {
-      int tlc = 0;
+      [[maybe_unused]] int tlc = 0;
       TL(0, tlc, 0);
       const int NRT = p.N / 64;
       const size_t tile_codes = (size_t)NC * 4096, tile_scales = (size_t)NC * 64 * C::SB;
@@ -309,13 +350,13 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         TL(0, tlc, 1);
         const int nc = min(kSliceChunks, NC - wk.slice * kSliceChunks);
         const uint32_t bar = smem_u32(&full_b[st]);
-        mbar_expect_tx(bar, 2u * nc * (4096 + 64 * C::SB));
+        mbar_expect_tx(bar, 2u * nc * (4096 + 64 * C::SB) + (C::a4 ? (uint32_t)(nc * C::apc * 512) : 0u));
         const uint32_t dst = st0 + st * C::stage_bytes;
         for (int blk = 0; blk < 2; ++blk) {
           const int rt = (ROLE == 0) ? (blk == 0 ? wk.tile : p.I / 64 + wk.tile) : 2 * wk.tile + blk;
           const size_t ti = (size_t)e * NRT + rt;
           const uint8_t* src = p.w + ti * tile_codes + (size_t)wk.slice * kSliceChunks * 4096;
-          if (Q == kFP8 && ROLE == 0) {
+          if (!C::fp4 && ROLE == 0) {
             // 8-row groups interleaved: group g of the gate block -> A group
             // 2g, of the up block -> 2g + 1
             for (int g8 = 0; g8 < 8; ++g8)
@@ -328,6 +369,13 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
                           sb + ti * tile_scales + (size_t)wk.slice * kSliceChunks * 64 * C::SB,
                           nc * 64 * C::SB, bar, pol);
         }
+        if (C::a4) {
+          // W4A4: the slice's weight scale atoms ([tiles][slice][atom][512] per expert)
+          const size_t tile_atoms = (size_t)NC * C::apc * 512;
+          bulk_g2s_hint(dst + 2 * kTCodeBlock,
+                        sb + ((size_t)e * tiles + wk.tile) * tile_atoms + (size_t)wk.slice * C::sf_bytes,
+                        nc * C::apc * 512, bar, pol);
+        }
         issued = n + 1;
         TL(0, tlc, 2);
       }
@@ -336,6 +384,44 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         const int last = st + ((issued - 1 - st) / S) * S;
         const unsigned long long t0 = globaltimer();
         while (!mbar_try_wait(smem_u32(&full_b[st]), (uint32_t)(last / S) & 1u))
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+      }
+    }
+  } else if (C::a4 && warp == C::w_sf) {
+    // ---------------- W4A4: scale atoms -> tensor memory ----------------
+    // Once a unit's stage has landed (which also means that the MMAs of the
+    // stage's previous unit, the last readers of its tensor-memory columns,
+    // have completed), one lane copies the unit's A and B scale atoms into
+    // the stage's columns and commits the copies to sffull[stage].
+    if (lane == 0) {
+      SKWalk wk;
+      wk.begin();
+      int issued = 0;
+      for (int n = 0; n < count; ++n) {
+        wk.next(R);
+        const int st = n % S;
+        if (!wait(&full_b[st], (uint32_t)(n / S) & 1u)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const int nc = min(kSliceChunks, NC - wk.slice * kSliceChunks);
+        const uint32_t sfa_t = tmem + C::n_acc * kTAcc + st * C::sf_cols;
+        const uint32_t sfb_t = sfa_t + C::sf_cols / 2;
+        const uint32_t sa = st0 + st * C::stage_bytes + 2 * kTCodeBlock;
+        const uint32_t sbb = b0s + st * C::bslot + kTBSlot;
+        for (int a = 0; a < nc * C::apc; ++a) {
+          tc::cp_scale_atom(sfa_t + 4 * a, sa + 512 * a);
+          tc::cp_scale_atom(sfb_t + 4 * a, sbb + 512 * a);
+        }
+        tc::commit(smem_u32(&sffull[st]));
+        issued = n + 1;
+      }
+      // the copies must land before the tensor memory is freed
+      for (int st = 0; st < S && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / S) * S;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&sffull[st]), (uint32_t)(last / S) & 1u))
           if (globaltimer() - t0 > kWaitLimitNs) break;
       }
     }
@@ -351,10 +437,12 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
     constexpr int RPT = kTN / RSTEP;  // rows per thread
     constexpr int kLag = 1;           // copy groups left in flight when a piece is released
     const int uu = lt & 15, r0 = lt >> 4;
-    const size_t rowB = (size_t)p.K * kel;
+    const size_t rowB = C::a4 ? (size_t)p.K / 2 : (size_t)p.K * kel;
+    const int sf_row = p.K / (Q == kA4NV ? 16 : 32);  // W4A4: scale bytes of a B row
     uint32_t roff[RPT];
+    uint32_t rsf[C::a4 ? RPT : 1];
     int nrow = 0;
-    int tlc = 0;
+    [[maybe_unused]] int tlc = 0;
     if (lt == 0) TL(3, tlc, 0);
     SKWalk wk;
     wk.begin();
@@ -373,7 +461,9 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           roff[m] = 0;
           if (tn < gd.z) {
             const int ro = route_of(gcur, gd.y, tn);
-            roff[m] = (uint32_t)((size_t)(p.b_by_token ? ro / p.k : ro) * rowB);
+            const int brow = p.b_by_token ? ro / p.k : ro;
+            roff[m] = (uint32_t)((size_t)brow * rowB);
+            if constexpr (C::a4) rsf[m] = (uint32_t)brow * (uint32_t)sf_row;
             nrow = m + 1;
           }
         }
@@ -402,7 +492,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           }
         }
         if (lt == 0) TL(3, tlc, 1);
-        const uint32_t dst = b0s + bs * kTBSlot;
+        const uint32_t dst = b0s + bs * C::bslot;
         if constexpr (C::fp4) {
           // f16 chunk slice * 4 + c of each row: 256 B = 16 units, 128-byte swizzle
           const uint8_t* src = p.b + (size_t)(wk.slice * kSliceChunks + c) * 256 + uu * 16;
@@ -424,6 +514,22 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
                                  dst + cc * 512 + tc::sw64_off(r0 + RSTEP * m, u4, nc * 512)),
                              "l"(src + roff[m]));
+          }
+          if constexpr (C::a4) {
+            // the rows' scale atoms: atom uu of the slice holds blocks 4 uu .. 4 uu + 3,
+            // token n's four bytes at (n % 32) * 16 + (n / 32) * 4
+            if (uu < nc * C::apc) {
+              const uint8_t* ssrc = p.b_sf + (size_t)(wk.slice * kSliceChunks * C::apc + uu) * 4;
+              const uint32_t sdst = dst + kTBSlot + uu * 512;
+#pragma unroll
+              for (int m = 0; m < RPT; ++m)
+                if (m < nrow) {
+                  const int tn = r0 + RSTEP * m;
+                  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(
+                                   sdst + (tn & 31) * 16 + (tn >> 5) * 4),
+                               "l"(ssrc + rsf[m]));
+                }
+            }
           }
         }
         // one copy group per piece; the pieces issued kLag pieces earlier
@@ -449,12 +555,12 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
   } else if (warp == C::w_mma) {
     // ---------------- MMA issue (one lane) ----------------
     if (lane == 0) {
-      int tlc = 0;
+      [[maybe_unused]] int tlc = 0;
       TL(1, tlc, 0);
       SKWalk wk;
       wk.begin();
       int gcur = -1;
-      uint32_t idesc = 0;
+      uint32_t idesc = 0, idesc_hi = 0;  // W4A4 MXFP4: the second step of an atom (scale-ID 2)
       int piece = 0, achunk = 0, acc = 0, acc_use = 0;
       bool fresh = true, ok = true;
       for (int n = 0; n < count && ok; ++n) {
@@ -463,12 +569,17 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           gcur = wk.grp;
           const int nt = group_of(gcur).z;
           const int npad = (nt + 15) & ~15;
-          idesc = (Q == kFP8) ? tc::instr_desc(tc::kE4M3, tc::kE4M3, kTM, npad)
-                              : tc::instr_desc(tc::kF16, tc::kF16, kTM, npad);
+          if constexpr (C::a4) {
+            idesc = tc::instr_desc_fp4(kTM, npad, Q == kA4MX ? 1u : 0u, 0u);
+            idesc_hi = tc::instr_desc_fp4(kTM, npad, 1u, 2u);
+          } else {
+            idesc = (Q == kFP8) ? tc::instr_desc(tc::kE4M3, tc::kE4M3, kTM, npad)
+                                : tc::instr_desc(tc::kF16, tc::kF16, kTM, npad);
+          }
         }
         if (fresh) {
           // the accumulator must have been drained by the epilogue
-          if (acc_use > 1 && !wait(&accempty[acc], (uint32_t)((acc_use >> 1) - 1) & 1u)) {
+          if (acc_use >= C::n_acc && !wait(&accempty[acc], (uint32_t)(acc_use / C::n_acc - 1) & 1u)) {
             fail();
             break;
           }
@@ -477,7 +588,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         }
         const uint32_t d_tmem = tmem + acc * kTAcc;
         const int nc = min(kSliceChunks, NC - wk.slice * kSliceChunks);
-        if constexpr (Q == kFP8) {
+        if constexpr (!C::fp4) {
           const int st = n % S;
           const int bs = st;  // the unit's B rows ride in its stage
           if (!wait(&full_b[st], (uint32_t)(n / S) & 1u)) {
@@ -489,21 +600,49 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           // descriptors of the unit's first k-step; k-step (c, h) starts
           // c * 512 + h * 32 bytes further (the start-address field counts 16 B)
           const uint64_t da0 = tc::smem_desc(st0 + st * C::stage_bytes, 16, nc * 512, tc::kSw64);
-          const uint64_t db0 = tc::smem_desc(b0s + bs * kTBSlot, 16, nc * 512, tc::kSw64);
+          const uint64_t db0 = tc::smem_desc(b0s + bs * C::bslot, 16, nc * 512, tc::kSw64);
+          if constexpr (C::a4) {
+            // the unit's scale atoms, copied into this stage's tensor-memory
+            // columns (A then B) by the scale warp
+            if (!wait(&sffull[st], (uint32_t)(n / S) & 1u)) {
+              fail();
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t sfa_t = tmem + C::n_acc * kTAcc + st * C::sf_cols;
+            const uint32_t sfb_t = sfa_t + C::sf_cols / 2;
 #pragma unroll
-          for (int c = 0; c < kSliceChunks; ++c)
+            for (int c = 0; c < kSliceChunks; ++c)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              if (c < nc)
-                tc::mma_f8f6f4(d_tmem, da0 + (uint64_t)(c * 32 + h * 2), db0 + (uint64_t)(c * 32 + h * 2),
-                               idesc, (fresh && c == 0 && h == 0) ? 0u : 1u);
+              for (int h = 0; h < 2; ++h)
+                if (c < nc) {
+                  const uint32_t acc_in = (fresh && c == 0 && h == 0) ? 0u : 1u;
+                  if constexpr (Q == kA4NV) {
+                    const int atom = 2 * c + h;  // four blocks of 16 per 64-element step
+                    tc::mma_nvf4(d_tmem, da0 + (uint64_t)(c * 32 + h * 2), db0 + (uint64_t)(c * 32 + h * 2),
+                                 idesc, sfa_t + 4 * atom, sfb_t + 4 * atom, acc_in);
+                  } else {
+                    // the chunk's atom holds both steps: scale-ID 0, then 2
+                    tc::mma_mxf4(d_tmem, da0 + (uint64_t)(c * 32 + h * 2), db0 + (uint64_t)(c * 32 + h * 2),
+                                 h ? idesc_hi : idesc, sfa_t + 4 * c, sfb_t + 4 * c, acc_in);
+                  }
+                }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kSliceChunks; ++c)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if (c < nc)
+                  tc::mma_f8f6f4(d_tmem, da0 + (uint64_t)(c * 32 + h * 2), db0 + (uint64_t)(c * 32 + h * 2),
+                                 idesc, (fresh && c == 0 && h == 0) ? 0u : 1u);
+          }
           tc::commit(smem_u32(&empty_b[st]));
           TL(1, tlc, 4);
           ++piece;
         } else {
           for (int c = 0; c < nc; ++c, ++piece, ++achunk) {
-            const int as = achunk % C::n_a, bs = as;  // A and B of a chunk share its slot
-            if (!wait(&cfull[as], (uint32_t)(achunk / C::n_a) & 1u)) {
+            const int as = achunk % kNA, bs = as;  // A and B of a chunk share its slot
+            if (!wait(&cfull[as], (uint32_t)(achunk / kNA) & 1u)) {
               fail();
               ok = false;
               break;
@@ -513,7 +652,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
             const uint32_t a_t = tmem + kTAOff + as * kTAcc;
             // k-step j: A columns 8j.., B bytes (j / 4) * 8192 + (j % 4) * 32
             // (the descriptor's start-address field counts 16 B)
-            const uint64_t db0 = tc::smem_desc(b0s + bs * kTBSlot, 16, 1024, tc::kSw128);
+            const uint64_t db0 = tc::smem_desc(b0s + bs * C::bslot, 16, 1024, tc::kSw128);
             const uint32_t acc0 = (fresh && c == 0) ? 0u : 1u;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -527,7 +666,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         fresh = false;
         if (wk.closes(R)) {
           tc::commit(smem_u32(&accfull[acc]));
-          acc ^= 1;
+          acc = acc + 1 == C::n_acc ? 0 : acc + 1;
           ++acc_use;
           fresh = true;
         }
@@ -553,7 +692,8 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
     const int sr = r & 7;
     SKWalk wk;
     wk.begin();
-    int achunk = 0, tlc = 0;
+    int achunk = 0;
+    [[maybe_unused]] int tlc = 0;
     bool ok = true;
     const bool tl0 = (dw == 0 && lane == 0);
     if (tl0) TL(2, tlc, 0);
@@ -568,7 +708,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
       const int nc = min(kSliceChunks, NC - wk.slice * kSliceChunks);
       const uint8_t* stg = sbase + st * C::stage_bytes;
       for (int c = 0; c < nc; ++c, ++achunk) {
-        const int as = achunk % C::n_a, use = achunk / C::n_a;
+        const int as = achunk % kNA, use = achunk / kNA;
         if (use > 0 && !__all_sync(0xffffffffu, wait(&cempty[as], (uint32_t)(use - 1) & 1u))) {
           if (lane == 0) fail();
           ok = false;
@@ -634,7 +774,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
     pdl_wait();  // the activation scales, and the outputs' previous readers
     const int row = warp * 32 + lane;  // tensor-memory lane = A row
     const uint32_t t_row = (uint32_t)(warp * 32) << 16;
-    int tlc = 0;
+    [[maybe_unused]] int tlc = 0;
     if (tid == 0) TL(4, tlc, 0);
     SKWalk wk;
     wk.begin();
@@ -654,7 +794,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
       // so that their latency hides behind it: w13 gate / up row scales
       // (sg, su), w2 the row's scale (sg); NVFP4 the expert's global scale
       float sg = 1.f, su = 1.f;
-      if (Q == kNVFP4) sg = su = __ldg(p.gscale + e);
+      if (Q == kNVFP4 || Q == kA4NV) sg = su = __ldg(p.gscale + e);
       if (Q == kFP8) {
         const float* ws = reinterpret_cast<const float*>(p.scale);
         if (ROLE == 0) {
@@ -665,7 +805,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
           sg = __ldg(ws + (size_t)e * p.N + wk.tile * 128 + row);
         }
       }
-      if (!__all_sync(0xffffffffu, wait(&accfull[acc], (uint32_t)(acc_use >> 1) & 1u))) {
+      if (!__all_sync(0xffffffffu, wait(&accfull[acc], (uint32_t)(acc_use / C::n_acc) & 1u))) {
         if (lane == 0) fail();
         break;
       }
@@ -771,16 +911,26 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
             g8[t] = is_gate ? v[t] : recv;
             u8[t] = is_gate ? recv : v[8 + t];
           }
+          // the chunk's routes (and FP8 activation scales), all loads in
+          // flight together ahead of the stores
+          int ro8[8];
+          float bs8[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             const int nn = cc * 16 + (is_gate ? 0 : 8) + t;
-            if (nn >= ntok) break;
-            const int ro = route_of(gcur, gd.y, nn);
+            ro8[t] = nn < ntok ? route_of(gcur, gd.y, nn) : -1;
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            bs8[t] = (Q == kFP8 && ro8[t] >= 0) ? __ldcg(p.b_scale + ro8[t] / p.k) : 1.f;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int ro = ro8[t];
+            if (ro < 0) break;
             float gs = sg, us = su;
             if (Q == kFP8) {
-              const float bs = __ldcg(p.b_scale + ro / p.k);
-              gs *= bs;
-              us *= bs;
+              gs *= bs8[t];
+              us *= bs8[t];
             }
             const float a = round_bf16(silu(g8[t] * gs) * (u8[t] * us));
             if (Q == kFP8 || p.act_bf16) {
@@ -793,13 +943,18 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         } else {
           const int pr = wk.tile * 128 + row;
           const float sc = sg;
+          int ro16[16];
+          float bs16[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) ro16[t] = cc * 16 + t < ntok ? route_of(gcur, gd.y, cc * 16 + t) : -1;
+#pragma unroll
+          for (int t = 0; t < 16; ++t) bs16[t] = (Q == kFP8 && ro16[t] >= 0) ? __ldcg(p.b_scale + ro16[t]) : 1.f;
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            const int nn = cc * 16 + t;
-            if (nn >= ntok) break;
-            const int ro = route_of(gcur, gd.y, nn);
+            const int ro = ro16[t];
+            if (ro < 0) break;
             float s = sc;
-            if (Q == kFP8) s *= __ldcg(p.b_scale + ro);
+            if (Q == kFP8) s *= bs16[t];
             reinterpret_cast<float*>(p.out)[(size_t)ro * p.P + pr] = v[t] * s;
           }
         }
@@ -814,7 +969,7 @@ __global__ void __launch_bounds__(TcCfg<Q>::threads, 1) k_expert_tc(ExpertParams
         if (lane == 0) mbar_arrive(smem_u32(&accempty[acc]));
       }
       if (tid == 0) TL(4, tlc, 2 + mode);
-      acc ^= 1;
+      acc = acc + 1 == C::n_acc ? 0 : acc + 1;
       ++acc_use;
       if (!good) break;
     }
@@ -848,6 +1003,16 @@ static cudaError_t launch_tc_t(const ExpertParams& p, cudaStream_t s, bool pdl) 
 }
 
 cudaError_t launch_expert_tc(const ExpertParams& p, cudaStream_t s, bool pdl) {
+  if (p.act4) {
+    if (p.quant != (p.act4 == 2 ? kNVFP4 : kMXFP4) || !p.b_sf) return cudaErrorInvalidValue;
+    switch ((p.act4 == 2 ? 2 : 0) + p.role) {
+      case 0: return launch_tc_t<kA4MX, 0>(p, s, pdl);
+      case 1: return launch_tc_t<kA4MX, 1>(p, s, pdl);
+      case 2: return launch_tc_t<kA4NV, 0>(p, s, pdl);
+      case 3: return launch_tc_t<kA4NV, 1>(p, s, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.quant * 2 + p.role) {
     case 0: return launch_tc_t<kMXFP4, 0>(p, s, pdl);
     case 1: return launch_tc_t<kMXFP4, 1>(p, s, pdl);

@@ -251,22 +251,27 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
 // registers (its loads and its norm weights' issued together); a longer one
 // is read from L2 once per pass.
 constexpr int kNV = 16;
-// The W4A4 form of norm_rows: h as there, and the f16 operand holds h
-// rounded to FP4 (act4.cuh). A lane holds float4s lane, lane + 32, ..., so an
-// FP4 block is 8 (MXFP4) or 4 (NVFP4) neighbouring lanes; M is a multiple of
-// 128, so every step is warp-uniform. Two passes over the row (it stays in
-// L2), four float4s per lane in flight. Out of line and with its arguments by
-// value, so the other forms keep their registers.
+// The W4A4 form of norm_rows: h as there, and h rounded to FP4 (act4.cuh)
+// as the experts' operand: e2m1 codes [rows, M / 2] (the lower element of a
+// pair in the low nibble) and one scale byte per block [rows, M / blk]
+// (UE8M0 for MXFP4, e4m3 for NVFP4). A lane holds float4s lane, lane + 32,
+// ..., so an FP4 block is 8 (MXFP4) or 4 (NVFP4) neighbouring lanes, the
+// first of which stores the block's scale; M is a multiple of 128, so every
+// step is warp-uniform. Two passes over the row (it stays in L2), four
+// float4s per lane in flight. Out of line and with its arguments by value,
+// so the other forms keep their registers.
 struct Act4Row {
   const float* y;
   const uint16_t* w;
   uint16_t* h;
   uint8_t* h_op;
+  uint8_t* h_sf;
   int M, pre_norm, act4;
   float eps;
 };
 
-// one float4 of a row: bf16 h, its FP4 rounding as the f16 operand
+// one float4 of a row: bf16 h, the codes of its FP4 rounding and, from the
+// block's first lane, the block scale; flags a value that is not finite
 __device__ __forceinline__ int act4_put(const Act4Row& r, int t, int i, const float4& x,
                                         const uint2& wb, float rstd) {
   const float xv[4] = {x.x, x.y, x.z, x.w};
@@ -288,23 +293,19 @@ __device__ __forceinline__ int act4_put(const Act4Row& r, int t, int i, const fl
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     am = fmaxf(am, fabsf(hb[c]));
-    bad |= !(fabsf(hb[c]) <= 65504.f);  // NaN too
+    bad |= !(fabsf(hb[c]) <= 3.40282347e38f);  // NaN or infinite
   }
   reinterpret_cast<uint2*>(r.h + (size_t)t * r.M)[i] = make_uint2(hbits[0], hbits[1]);
   am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
   am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
   if (r.act4 == 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
   const Fp4Scale sc = fp4_block_scale(am, r.act4);
-  uint32_t ob[2];
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    float r0, r1;
-    fp4_value2(fp4_code2(hb[2 * c], hb[2 * c + 1], sc, r.act4), sc, r0, r1);
-    const __half2 h2 = __floats2half2_rn(r0, r1);
-    bad |= (__low2float(h2) != r0) | (__high2float(h2) != r1);
-    ob[c] = *reinterpret_cast<const uint32_t*>(&h2);
-  }
-  reinterpret_cast<uint2*>(r.h_op + (size_t)t * r.M * 2)[i] = make_uint2(ob[0], ob[1]);
+  const uint32_t codes = fp4_code2(hb[0], hb[1], sc, r.act4) | (fp4_code2(hb[2], hb[3], sc, r.act4) << 8);
+  reinterpret_cast<uint16_t*>(r.h_op + (size_t)t * (r.M / 2))[i] = (uint16_t)codes;
+  const int per = r.act4 == 1 ? 8 : 4;  // float4s per block
+  if (i % per == 0)
+    r.h_sf[(size_t)t * (r.M / (4 * per)) + i / per] =
+        (uint8_t)(r.act4 == 1 ? (uint32_t)(mx_scale_exp(am) + 127) : nv_scale_code(am));
   return bad;
 }
 
@@ -351,7 +352,7 @@ __device__ __noinline__ void norm_rows_act4(Act4Row r, int32_t* health, int t0, 
 
 __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) {
   if (p.act4) {
-    norm_rows_act4(Act4Row{p.y, p.w_pre_norm, p.h, p.h_op, p.M, p.pre_norm, p.act4, p.norm_eps},
+    norm_rows_act4(Act4Row{p.y, p.w_pre_norm, p.h, p.h_op, p.h_sf, p.M, p.pre_norm, p.act4, p.norm_eps},
                    p.health, t0, t1);
     return;
   }

@@ -90,4 +90,56 @@ cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int
   return cudaSuccess;
 }
 
+// ---- W4A4: block scales -> the tensor cores' scale atoms --------------------
+// One output byte per thread step of one expert: output offset o of
+// [tiles][slice][atoms of the slice][512] is the scale of A-tile row m =
+// (b / 16) % 32 + 32 * ((b % 16) / 4) and block j = b % 4 of the atom (b = o %
+// 512); the atom's four blocks are blocks 4 * (atom index along K) .. + 3 of
+// the row.
+__global__ void k_pack_sf_atoms(const uint8_t* src, uint8_t* dst, int N, int I, int nblk, int role,
+                                int apc, size_t bytes) {
+  const int NC = nblk * (apc == 1 ? 32 : 16) / 128;  // 128-element chunks of a row
+  const size_t tile_bytes = (size_t)NC * apc * 512;
+  const size_t slice_bytes = (size_t)kSliceChunks * apc * 512;
+  for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < bytes;
+       o += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(o / tile_bytes);
+    const size_t ot = o % tile_bytes;
+    const int sl = (int)(ot / slice_bytes);
+    const int a = (int)((ot % slice_bytes) / 512), b = (int)(ot % 512);
+    const int m = b / 16 + 32 * ((b % 16) / 4), j = b % 4;
+    int row;
+    if (role == 0) {
+      const int ga = m >> 3;  // 8-row group of the tile: even gate, odd up
+      row = ((ga & 1) ? I : 0) + t * 64 + (ga >> 1) * 8 + (m & 7);
+    } else {
+      row = t * 128 + m;
+    }
+    const int blk = 4 * (sl * kSliceChunks * apc + a) + j;
+    dst[o] = src[(size_t)row * nblk + blk];
+  }
+}
+
+cudaError_t launch_pack_sf_atoms(const uint8_t* src, uint8_t* dst, int E, int N, int I, int K,
+                                 int role, int nv, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s) {
+  const int nblk = K / (nv ? 16 : 32), apc = nv ? 2 : 1;
+  const size_t per = (size_t)N * nblk;  // one expert's scale bytes
+  if (K % 128 || (role == 0 ? (N != 2 * I || I % 64) : N % 128)) return cudaErrorInvalidValue;
+  const bool in_place = (src == dst);
+  if (in_place && (!tmp || tmp_bytes < per)) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)std::min<size_t>((per + 255) / 256, 4096);
+  for (int e = 0; e < E; ++e) {
+    const uint8_t* from = src + (size_t)e * per;
+    if (in_place) {
+      cudaError_t err = cudaMemcpyAsync(tmp, from, per, cudaMemcpyDeviceToDevice, s);
+      if (err != cudaSuccess) return err;
+      from = tmp;
+    }
+    k_pack_sf_atoms<<<grid, 256, 0, s>>>(from, dst + (size_t)e * per, N, I, nblk, role, apc, per);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace musemoe

@@ -71,8 +71,11 @@ __global__ void __launch_bounds__(256) k_act_quant(ActQuantParams p) {
 // providers page, ExpertsInput: the NVFP4 form). One warp per 256 elements
 // of a route (I is a multiple of 128, so a warp's span is whole blocks); a
 // lane rounds 8 consecutive elements (one 16-byte load), so a block is 4
-// (MXFP4) or 2 (NVFP4) neighbouring lanes. The rounded values are stored as
-// w2's f16 operand; one that f16 cannot hold exactly raises kHealthActRange.
+// (MXFP4) or 2 (NVFP4) neighbouring lanes, the first of which stores the
+// block's scale. Output: w2's operand, e2m1 codes [routes, I / 2] (the lower
+// element of a pair in the low nibble) and one scale byte per block
+// [routes, I / blk] (UE8M0 / e4m3); a value that is not finite raises
+// kHealthActRange.
 constexpr int kActSpan = 256;
 
 __global__ void __launch_bounds__(256) k_act_fp4(ActQuantParams p) {
@@ -100,16 +103,16 @@ __global__ void __launch_bounds__(256) k_act_fp4(ActQuantParams p) {
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   if (p.mode == 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   const Fp4Scale sc = fp4_block_scale(m, p.mode);
-  uint32_t o[4];
+  uint32_t codes = 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float r0, r1;
-    fp4_value2(fp4_code2(x[2 * c], x[2 * c + 1], sc, p.mode), sc, r0, r1);
-    const __half2 h2 = __floats2half2_rn(r0, r1);
-    bad |= (__low2float(h2) != r0) | (__high2float(h2) != r1);
-    o[c] = *reinterpret_cast<const uint32_t*>(&h2);
+  for (int c = 0; c < 4; ++c) codes |= fp4_code2(x[2 * c], x[2 * c + 1], sc, p.mode) << (8 * c);
+  if (ok) {
+    reinterpret_cast<uint32_t*>(p.q + (size_t)r * (p.I / 2))[i / 8] = codes;
+    const int per = p.mode == 1 ? 32 : 16;  // elements per block
+    if (i % per == 0)
+      p.sf[(size_t)r * (p.I / per) + i / per] =
+          (uint8_t)(p.mode == 1 ? (uint32_t)(mx_scale_exp(m) + 127) : nv_scale_code(m));
   }
-  if (ok) reinterpret_cast<uint4*>(p.q + ((size_t)r * p.I + i) * 2)[0] = make_uint4(o[0], o[1], o[2], o[3]);
   if (bad) atomicOr(p.health, kHealthActRange);
 }
 

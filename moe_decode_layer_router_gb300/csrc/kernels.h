@@ -65,11 +65,12 @@ struct FrontParams {
   // block applies the pre-expert RMSNorm to the block's rows of y
   const uint16_t* w_pre_norm;  // bf16 [M]
   int pre_norm, quant;
-  int act4;             // W4A4: h_op holds h rounded to MXFP4 (1) or NVFP4 (2)
+  int act4;             // W4A4: h_op / h_sf hold h rounded to MXFP4 (1) or NVFP4 (2)
   float norm_eps;
   uint16_t* h;          // bf16 [rows, M]
-  uint8_t* h_op;        // f16 [rows, M] (FP4) or e4m3 [rows, M] (FP8)
+  uint8_t* h_op;        // f16 [rows, M] (FP4), e4m3 [rows, M] (FP8), W4A4: e2m1 codes [rows, M / 2]
   float* h_scale;       // [rows] (FP8)
+  uint8_t* h_sf;        // W4A4: block scales [rows, M / 32] (UE8M0) or [rows, M / 16] (e4m3)
   int32_t* norm_ticket; // [token blocks], zero between launches
   // router only (route_tail != 0): the last router CTA of each 8-token block
   // routes the block's rows, and the last block to finish builds the permute
@@ -117,8 +118,13 @@ struct ExpertParams {
   const uint8_t* w;        // codes, kernel layout (launch_pack_tiles, cb = 64)
   const void* scale;       // MX/NV: kernel layout (cb = 4 / 8); FP8: fp32 [E, N]
   const float* gscale;     // NVFP4 [E]
-  const uint8_t* b;        // activation operand: f16 [*, K], e4m3 [*, K] or (BF16 experts) bf16 [*, K]
+  const uint8_t* b;        // activation operand: f16 [*, K], e4m3 [*, K] or (BF16 experts) bf16 [*, K];
+                           // W4A4: e2m1 codes [*, K / 2] (two per byte, the lower element in the low nibble)
   const float* b_scale;    // FP8: per B row
+  int act4;                // W4A4 on the FP4 tensor cores: 1 MXFP4, 2 NVFP4 (launch_expert_tc only;
+                           // w and scale then in the layouts of launch_pack_tiles permute 3 and
+                           // launch_pack_sf_atoms)
+  const uint8_t* b_sf;     // W4A4: block scales of the B rows [*, K / 32] (UE8M0) or [*, K / 16] (e4m3)
   int b_by_token;          // 1: B row = route / k (w13 reads h); 0: B row = route
   const int32_t* route_list;
   const int32_t* groups;
@@ -144,14 +150,15 @@ size_t expert_tickets(int max_groups, int quant, int role, int K, int N);
 
 // FP8 only: per-route dynamic e4m3 quantization of the bf16 activation.
 // W4A4 (mode 1 MXFP4, 2 NVFP4): per-route FP4 rounding of the bf16
-// activation into w2's f16 operand (the rounded values, exact in f16).
+// activation into w2's operand: e2m1 codes and block scales.
 struct ActQuantParams {
   const uint16_t* act;  // bf16 [routes, I]
-  uint8_t* q;           // mode 0: e4m3 [routes, I]; modes 1, 2: f16 [routes, I]
+  uint8_t* q;           // mode 0: e4m3 [routes, I]; modes 1, 2: e2m1 codes [routes, I / 2]
   float* scale;         // mode 0: [routes]
+  uint8_t* sf;          // modes 1, 2: block scales [routes, I / 32] (UE8M0) or [routes, I / 16] (e4m3)
   int routes, I;
   int mode;             // 0 FP8, 1 MXFP4, 2 NVFP4
-  int32_t* health;      // modes 1, 2: kHealthActRange when a value is not exact in f16
+  int32_t* health;      // modes 1, 2: kHealthActRange for a value that is not finite
 };
 cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl);
 
@@ -219,5 +226,16 @@ constexpr int kSliceChunks = 4;
 cudaError_t check_ue8m0(const uint8_t* p, size_t n, int* bad_dev, cudaStream_t s);
 cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, size_t rows, int row_bytes, int cb,
                               int permute, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s);
+// Block scales of one FP4 expert matrix (plain [E, N, K / blk] bytes, blk 32
+// MXFP4 or 16 NVFP4) -> the tensor cores' scale atoms for W4A4: per expert,
+// A tile of 128 rows (w13, role 0: gate rows t*64.. and up rows I + t*64..
+// interleaved by 8-row groups, row m of the tile in group m / 8; w2: rows
+// t*128..), K-slice of kSliceChunks 128-element chunks, atom of 4 blocks
+// (MXFP4: one chunk; NVFP4: half a chunk), 512 bytes with the scale of tile
+// row m and block j at byte (m % 32) * 16 + (m / 32) * 4 + j:
+// [E][tiles][slice][atoms of the slice][512]. src may equal dst (each
+// expert's scales then pass through `tmp`, at least N * K / blk bytes).
+cudaError_t launch_pack_sf_atoms(const uint8_t* src, uint8_t* dst, int E, int N, int I, int K,
+                                 int role, int nv, uint8_t* tmp, size_t tmp_bytes, cudaStream_t s);
 
 }  // namespace musemoe

@@ -82,6 +82,7 @@ struct musemoe_handle {
   int32_t* health = nullptr;
   uint16_t *h = nullptr, *moe_out = nullptr, *x_stage = nullptr, *out_stage = nullptr;
   uint8_t *h_op = nullptr, *act = nullptr, *act_q = nullptr;
+  uint8_t *h_sf = nullptr, *act_sf = nullptr;  // W4A4: block scales of h_op / act_q
   std::string err;
 };
 
@@ -113,7 +114,12 @@ void plan(musemoe_handle* h, Layout& L) {
   L.add(&h->ids, RT * 4);
   L.add(&h->weights, RT * 4);
   L.add(&h->h, R * P * 2);
-  L.add(&h->h_op, R * P * (fp8 ? 1 : 2));
+  if (h->act4) {
+    L.add(&h->h_op, R * P / 2);   // W4A4: h's e2m1 codes
+    L.add(&h->h_sf, R * P / 16);  // and its block scales (one per 16 at most)
+  } else {
+    L.add(&h->h_op, R * P * (fp8 ? 1 : 2));
+  }
   L.add(&h->h_scale, R * 4);
   L.add(&h->route_list, RT * 4);
   L.add(&h->groups, (size_t)h->max_groups * 16);
@@ -129,7 +135,8 @@ void plan(musemoe_handle* h, Layout& L) {
     L.add(&h->act_q, RT * I);
     L.add(&h->act_scale, RT * 4);
   } else if (h->act4) {
-    L.add(&h->act_q, RT * I * 2);  // w2's f16 operand
+    L.add(&h->act_q, RT * I / 2);    // w2's e2m1 codes
+    L.add(&h->act_sf, RT * I / 16);  // and block scales
   }
   L.add(&h->y, RT * P * 4);
   // Stream-K partial sums (shared by w13 and w2, which run one after the
@@ -237,6 +244,7 @@ bool use_dense_tc(const musemoe_handle* h, int rows) {
 
 // Whether a forward of `rows` runs its experts on the tensor-core kernels.
 bool use_tc(const musemoe_handle* h, int rows) {
+  if (h->act4) return true;  // W4A4: the FP4 tensor cores at every size
   if (h->quant == kBF16 || h->expert_path == MUSEMOE_PATH_MMA) return false;
   return h->expert_path == MUSEMOE_PATH_TCGEN05 || rows >= kTcMinRows;
 }
@@ -304,6 +312,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fp.norm_eps = h->cfg.norm_eps;
   fp.h = h->h;
   fp.h_op = h->h_op;
+  fp.h_sf = h->h_sf;
   fp.h_scale = h->h_scale;
   fp.norm_ticket = h->norm_ticket;
   fp.route_tail = 1;
@@ -376,6 +385,8 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.gscale = w->w13_gscale;
   ep.b = h->quant == kBF16 ? reinterpret_cast<const uint8_t*>(h->h) : h->h_op;  // BF16: h itself
   ep.b_scale = h->h_scale;
+  ep.act4 = h->act4;
+  ep.b_sf = h->h_sf;
   ep.b_by_token = 1;
   ep.route_list = h->route_list;
   ep.groups = h->groups;
@@ -396,6 +407,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     aq.act = reinterpret_cast<const uint16_t*>(h->act);
     aq.q = h->act_q;
     aq.scale = h->act_scale;
+    aq.sf = h->act_sf;
     aq.routes = rows * d.top_k;
     aq.I = d.inter;
     aq.mode = h->act4;
@@ -413,6 +425,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   ep.gscale = w->w2_gscale;
   ep.b = (h->quant == kFP8 || h->act4) ? h->act_q : h->act;
   ep.b_scale = h->act_scale;
+  ep.b_sf = h->act_sf;
   ep.b_by_token = 0;
   ep.out = h->y;
   ep.tickets = h->expert_tickets[1];
@@ -662,6 +675,7 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
   c.route_scale = 1.f;
   const std::vector<std::string> r = refusals(d, quant, &c);
   if (!r.empty()) return set_err(nullptr, MUSEMOE_EUNSUPPORTED, join(r));
+  const int a4 = act4_of(quant);     // W4A4: the FP4 tensor cores' layouts
   quant = weight_format(quant);      // W4A4 weights are MXFP4 / NVFP4
   const bool bf16 = quant == kBF16;  // no scales
   const void* ptrs[8] = {w13_src, w13_scale_src, w13_dst, w13_scale_dst,
@@ -713,6 +727,9 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
     const size_t total = m.rows * rowbytes, tile = 64 * rowbytes;
     if (m.src == m.dst) tmp_bytes = std::max(tmp_bytes, std::max(tile, std::min(total, kPackTmpBytes)));
     if (!fp8 && !bf16 && m.ssrc == m.sdst) tmp_bytes = std::max(tmp_bytes, 64 * (rowbytes / 64) * sper);
+    // W4A4 scale atoms mix the gate and up halves of an expert: one expert's
+    // scales pass through the temporary
+    if (a4 && m.ssrc == m.sdst) tmp_bytes = std::max(tmp_bytes, m.rows / E * (m.K / (a4 == 2 ? 16 : 32)));
   }
   uint8_t* tmp = nullptr;
   if (tmp_bytes) {
@@ -721,12 +738,20 @@ musemoe_status musemoe_pack_experts(const musemoe_dims* d, int32_t quant, const 
       return set_err(nullptr, MUSEMOE_ENOMEM, fmt("pack: temporary of %zu bytes: %s", tmp_bytes,
                                                   cudaGetErrorString(e)));
   }
-  for (const M& m : ms) {
+  for (int mi = 0; mi < 2; ++mi) {
+    const M& m = ms[mi];
     const int rowbytes = (int)row_bytes(m.K);
-    const int permute = fp8 ? 3 : bf16 ? 2 : 1;
+    // codes: FP8 and W4A4 in natural order with the 64-byte swizzle (the
+    // tensor cores read them as they land), the other forms in mma fragment order
+    const int permute = (fp8 || a4) ? 3 : bf16 ? 2 : 1;
     if (e == cudaSuccess) e = launch_pack_tiles(m.src, m.dst, m.rows, rowbytes, 64, permute, tmp, tmp_bytes, s);
     if (e != cudaSuccess) break;
     if (bf16) continue;  // no scales
+    if (a4) {
+      e = launch_pack_sf_atoms(reinterpret_cast<const uint8_t*>(m.ssrc), reinterpret_cast<uint8_t*>(m.sdst),
+                               (int)E, (int)(m.rows / E), (int)I, (int)m.K, mi, a4 == 2, tmp, tmp_bytes, s);
+      continue;
+    }
     if (fp8) {  // per-row fp32 scales stay as they are
       if (m.ssrc != m.sdst)
         e = cudaMemcpyAsync(m.sdst, m.ssrc, m.rows * 4, cudaMemcpyDeviceToDevice, s);
@@ -1017,6 +1042,9 @@ musemoe_status musemoe_set_expert_path(musemoe_handle* h, int32_t path) {
     return set_err(h, MUSEMOE_EINVAL, fmt("expert path %d is not AUTO (0), MMA (1) or TCGEN05 (2)", path));
   if (path == MUSEMOE_PATH_TCGEN05 && h->quant == kBF16)
     return set_err(h, MUSEMOE_EUNSUPPORTED, "BF16 experts have no tensor-core (tcgen05) expert kernel");
+  if (path == MUSEMOE_PATH_MMA && h->act4)
+    return set_err(h, MUSEMOE_EUNSUPPORTED,
+                   "the W4A4 forms run on the FP4 tensor cores only (their weights are packed for them)");
   h->expert_path = path;
   return MUSEMOE_OK;
 }

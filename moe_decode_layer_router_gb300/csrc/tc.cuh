@@ -99,6 +99,50 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled FP4 MMA (kind::mxf4nvf4): A and B e2m1, two per byte, each
+// 64-element K step scaled per block by scale factors in tensor memory
+// (`sfa`, `sfb`: the column of the step's scale atom, see cp_scale_atom).
+// scale_vec::4X: blocks of 16 with e4m3 scales (NVFP4), the atom's four
+// bytes the step's four blocks; scale_vec::2X: blocks of 32 with UE8M0
+// scales (MXFP4), an atom holding two steps, selected by the descriptor's
+// scale-IDs 0 (bytes 0, 1) and 2 (bytes 2, 3).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of the block-scaled FP4 MMA, both operands E2M1 (1)
+// and K-major: B scale-ID (bits 4..5), A / B formats (7..9, 10..12), N >> 3
+// (17..22), scale type (23: e4m3 0, UE8M0 1), M >> 4 (24..28), A scale-ID
+// (29..30).
+__host__ __device__ __forceinline__ uint32_t instr_desc_fp4(int M, int N, uint32_t ue8m0,
+                                                            uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (ue8m0 << 23) |
+         ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
+}
+// One scale atom, shared memory -> tensor memory: 32 rows of 16 bytes (row l
+// holds the four scale bytes of matrix rows l, l + 32, l + 64, l + 96), copied
+// into four columns from `taddr` of lanes l of every lane quarter. Issued by
+// the MMA thread; the MMAs it issues afterwards see the copy.
+__device__ __forceinline__ void cp_scale_atom(uint32_t taddr, uint32_t smem_addr) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n" ::"r"(taddr),
+               "l"(smem_desc(smem_addr, 128, 128, kSwNone))
+               : "memory");
+}
+
 // The mbarrier at `bar` (shared) receives one arrival once every MMA this
 // thread issued before has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {

@@ -55,12 +55,16 @@ def test_every_form_names_its_launches(lib, quant, n):
     assert mm.musemoe_kernel_name(quant, n) == ""
 
 
-def test_w4a4_workspace_holds_the_rounded_activation(lib):
-    # the W4A4 forms add w2's f16 operand [rows * k, I] to their weight format's workspace
-    d = mm.Dims(max_rows=8, hidden=5120, pooled=2048, inter=1024, experts=128, top_k=8)
-    extra = 8 * 8 * 1024 * 2
+def test_w4a4_workspace_holds_the_rounded_inputs(lib):
+    # the W4A4 forms hold both FP4 expert inputs as e2m1 codes and block
+    # scales: h [rows, P / 2 + P / 16] in place of the weight format's f16 h
+    # operand [rows, P], and w2's input [rows * k, I / 2 + I / 16] on top
+    R, P, I, k = 8, 2048, 1024, 8
+    d = mm.Dims(max_rows=R, hidden=5120, pooled=P, inter=I, experts=128, top_k=k)
+    want = (R * P // 2 + R * P // 16) - R * P * 2 + R * k * (I // 2 + I // 16)
     for w4, a4 in [(mm.MUSEMOE_MXFP4, mm.MUSEMOE_MXFP4_A4), (mm.MUSEMOE_NVFP4, mm.MUSEMOE_NVFP4_A4)]:
-        assert mm.musemoe_workspace_bytes(d, a4) >= mm.musemoe_workspace_bytes(d, w4) + extra
+        got = mm.musemoe_workspace_bytes(d, a4) - mm.musemoe_workspace_bytes(d, w4)
+        assert abs(got - want) <= 4 * 256, (got, want)  # each buffer rounds up to 256 bytes
     assert mm.musemoe_workspace_bytes(d, 6) == 0  # no such form
 
 

@@ -82,7 +82,7 @@ def test_tc_ragged_rows_of_a_larger_handle(rows):
     H.compare(cfg, w, x[:rows].copy(), st[:rows].copy(), g)
 
 
-@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8, synth.MXFP4_A4])
+@pytest.mark.parametrize("quant", [synth.NVFP4, synth.FP8])
 def test_mma_path_still_serves_wide_tiles(quant):
     # the warp-level kernels forced at 64 rows (four token tiles per warp)
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=64, top_k=2, hot_experts=2,
@@ -108,6 +108,22 @@ def test_both_paths_match_the_oracle_at_full_size(name):
     ra = H.compare(cfg, w, x, st, a)
     rb = H.compare(cfg, w, x, st, b)
     print(name, "tcgen05", ra, "mma", rb)
+
+
+@pytest.mark.parametrize("quant", [synth.MXFP4_A4, synth.NVFP4_A4])
+def test_w4a4_runs_on_the_fp4_tensor_cores_only(quant):
+    # the W4A4 weights are packed for the block-scaled FP4 MMA: the
+    # warp-level path is refused, AUTO and TCGEN05 accepted
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], quant=quant)
+    run = H.Run(cfg)
+    try:
+        with pytest.raises(mm.MuseMoEError) as ei:
+            mm.musemoe_set_expert_path(run.handle, mm.MUSEMOE_PATH_MMA)
+        assert ei.value.status == mm.MUSEMOE_EUNSUPPORTED
+        mm.musemoe_set_expert_path(run.handle, mm.MUSEMOE_PATH_TCGEN05)
+        mm.musemoe_set_expert_path(run.handle, mm.MUSEMOE_PATH_AUTO)
+    finally:
+        run.close()
 
 
 def test_tc_path_refused_for_bf16_experts():
