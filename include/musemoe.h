@@ -82,11 +82,14 @@ typedef enum {
    * token and SiLU(gate)*up per route, rounded dynamically to MXFP4 (OCP
    * rule: scale 2^(floor(log2 amax) - 2) per 32, nearest e2m1, ties to
    * even); page "vllm.models.muse_spark.amd.muse_moe_runner", the Quark
-   * w_mxfp4_a_mxfp4 scheme. One extra launch (act_quant) per forward. */
+   * w_mxfp4_a_mxfp4 scheme. One extra launch (act_quant) per forward. The
+   * W4A4 forms multiply e2m1 by e2m1 on the block-scaled FP4 tensor cores
+   * (tcgen05.mma kind::mxf4nvf4) at every batch size; musemoe_pack_experts
+   * lays their weights out for that kernel only. */
   MUSEMOE_MXFP4_A4 = 4,
   /* W4A4: NVFP4 weights (as MUSEMOE_NVFP4) and both expert inputs rounded
    * to NVFP4 (e4m3 scale nearest amax / 6 per 16, no global scale;
-   * providers page, ExpertsInput). */
+   * providers page, ExpertsInput); the FP4 tensor cores as above. */
   MUSEMOE_NVFP4_A4 = 5,
 } musemoe_quant;
 
@@ -95,9 +98,10 @@ typedef enum { MUSEMOE_SIGMOID = 0, MUSEMOE_SOFTMAX = 1 } musemoe_score;
 /* Which kernels run the routed experts (musemoe_set_expert_path). */
 typedef enum {
   /* the tensor-core (tcgen05) kernels above 32 rows, where a hot expert's
-   * token group is a dense contraction; the warp-level kernels below */
+   * token group is a dense contraction; the warp-level kernels below (the
+   * W4A4 forms: the FP4 tensor cores at every size) */
   MUSEMOE_PATH_AUTO = 0,
-  MUSEMOE_PATH_MMA = 1,     /* always the warp-level (mma.sync) kernels */
+  MUSEMOE_PATH_MMA = 1,     /* always the warp-level (mma.sync) kernels (not W4A4) */
   MUSEMOE_PATH_TCGEN05 = 2, /* always the tensor-core kernels (not BF16) */
 } musemoe_expert_path;
 
@@ -204,7 +208,17 @@ const char *musemoe_kernel_name(int32_t quant, int32_t i);
  * of its 64 code bytes; FP8 scales keep their layout. For FP4 the 64 bytes of
  * a chunk are also reordered: byte 8j + 2q + b moves to 16q + 2j + b (q < 4,
  * j < 8, b < 2); for BF16 its 4-byte words are transposed as a 4 x 4 block:
- * byte 16j + 4q + b moves to 16q + 4j + b (q, j, b < 4). Each src may be its
+ * byte 16j + 4q + b moves to 16q + 4j + b (q, j, b < 4). FP8 and the W4A4
+ * forms keep the bytes of a chunk in order but swizzle its 16-byte units
+ * within each [8 rows][64 B] block (unit u of row r stored at unit
+ * u ^ ((r >> 1) & 3), the tensor cores' 64-byte swizzle). W4A4 scales are
+ * laid out as the tensor cores' scale atoms instead: per expert, tile of 128
+ * rows (w13: gate rows 64t.. and up rows I + 64t.. interleaved by groups of
+ * 8 rows, row m of the tile in group m / 8, even groups gate; w2: rows
+ * 128t..), K-slice of 4 chunks and atom of 4 scale blocks (MXFP4: one chunk,
+ * NVFP4: half a chunk), 512 bytes holding the scale of tile row m and block
+ * j at byte (m % 32) * 16 + (m / 32) * 4 + j:
+ * [E][tiles][slice][atoms of the slice][512 B]. Each src may be its
  * dst (in place): the tensors then pass
  * through a temporary device buffer of at most 64 MB, allocated and freed by
  * this call, which synchronizes the stream before it returns. The NVFP4
@@ -375,8 +389,8 @@ musemoe_status musemoe_health_selftest(musemoe_handle *handle, musemoe_stream_t 
  * then zeroes every inter-CTA ticket of the handle, so the next forward
  * starts clean),
  * MUSEMOE_ERANGE if a forward produced an expert operand (h or the
- * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504; W4A4: an
- * FP4-rounded input that fp16 does not hold exactly) or, on the tensor-core
+ * SiLU(gate)*up activation) beyond the fp16 range (|v| > 65504; W4A4: a
+ * value that is not finite) or, on the tensor-core
  * expert kernels, met an MXFP4 block scale outside 2^-23..2^13 (its products
  * with e2m1 are exact f16 operands only inside), MUSEMOE_OK otherwise. */
 musemoe_status musemoe_poll_health(musemoe_handle *handle);
@@ -387,8 +401,9 @@ musemoe_status musemoe_poll_health(musemoe_handle *handle);
  * providers", RoutedExpertsOps: the routed experts of the MoE provider) with
  * the same operands and fp32 accumulation; they differ in summation order.
  * The tensor-core path (tcgen05.mma: kind::f8f6f4 for FP8, kind::f16 on
- * dequantized FP4) serves MXFP4, NVFP4, FP8 and the W4A4 forms; TCGEN05 on a
- * BF16 handle is EUNSUPPORTED. EINVAL for an unknown path. Host only; not
+ * dequantized FP4, kind::mxf4nvf4 block-scaled for the W4A4 forms) serves
+ * MXFP4, NVFP4, FP8 and W4A4; TCGEN05 on a BF16 handle and MMA on a W4A4
+ * handle are EUNSUPPORTED. EINVAL for an unknown path. Host only; not
  * concurrent with a forward on the handle. */
 musemoe_status musemoe_set_expert_path(musemoe_handle *handle, int32_t path);
 

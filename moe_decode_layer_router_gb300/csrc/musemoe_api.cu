@@ -1071,9 +1071,9 @@ musemoe_status musemoe_poll_health(musemoe_handle* h) {
   if (word) {
     std::string m;
     if (word & kHealthTimeout) m += "an expert kernel's bounded wait on its weight copies ran out; ";
-    if (word & kHealthHRange) m += "h (or, W4A4, its FP4 rounding) beyond the fp16 operand range; ";
+    if (word & kHealthHRange) m += "h beyond the fp16 operand range (W4A4: not finite); ";
     if (word & kHealthActRange)
-      m += "SiLU(gate)*up (or, W4A4, its FP4 rounding) beyond the fp16 operand range; ";
+      m += "SiLU(gate)*up beyond the fp16 operand range (W4A4: not finite); ";
     if (word & kHealthWRange)
       m += "an MXFP4 block scale outside 2^-23..2^13, beyond the fp16 operand range of the "
            "tensor-core expert kernels; ";
