@@ -51,7 +51,7 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step's kernels directly instead of replaying a CUDA graph")
-    ap.add_argument("--bucket", choices=["verify", "large"], default=None,
+    ap.add_argument("--bucket", choices=["decode", "verify", "large", "w4a4", "w4a4_nv"], default=None,
                     help="time one single-layer bucket alone (--steps graph replays, --warmup "
                          "debug forwards) and print its object: a bounded run for profiling")
     return ap.parse_args()
@@ -577,7 +577,8 @@ def bench_ours(args):
     _build.build()
     synth.build()
     if args.bucket:
-        code = {"verify": mm.MUSEMOE_NVFP4, "large": mm.MUSEMOE_FP8_W8A8}[args.bucket]
+        code = {"decode": mm.MUSEMOE_MXFP4, "verify": mm.MUSEMOE_NVFP4, "large": mm.MUSEMOE_FP8_W8A8,
+                "w4a4": mm.MUSEMOE_MXFP4_A4, "w4a4_nv": mm.MUSEMOE_NVFP4_A4}[args.bucket]
         peak, _ = _hbm_peak()
         b = bench_bucket(dev, args.bucket, code, peak, 0 if args.no_cpu_baseline else 16, 15.0,
                          replays=max(1, args.steps), reps=max(3, args.warmup))

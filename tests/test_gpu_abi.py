@@ -96,6 +96,30 @@ def test_bounded_waits_time_out_into_the_health_word_and_the_context_survives():
         run.close()
 
 
+def test_timeout_poll_resets_the_split_tile_tickets():
+    # the self-test raises the expert kernels' tickets as contributors that
+    # arrived after their owner gave up would leave them; the poll that
+    # reports the timeout must zero them. K = 2048 makes four K-slices per
+    # tile and 48 rows fewer units per CTA than that, so on the tensor-core
+    # path most tiles are split across CTAs: a ticket left raised would let
+    # an owner add partials that were never written
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=48, pooled=2048, inter=512, top_k=2,
+                              seed=61)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    t, W = H.upload_layer(cfg, w)
+    run = H.Run(cfg)
+    try:
+        mm.musemoe_set_expert_path(run.handle, mm.MUSEMOE_PATH_TCGEN05)
+        H.compare(cfg, w, x, st, run.forward(W, x, st))
+        mm.musemoe_health_selftest(run.handle)
+        assert mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_ETIMEOUT
+        H.compare(cfg, w, x, st, run.forward(W, x, st))
+        assert mm.musemoe_poll_health(run.handle) == mm.MUSEMOE_OK
+    finally:
+        run.close()
+
+
 def test_num_kernels_and_names():
     assert mm.musemoe_num_kernels(mm.MUSEMOE_MXFP4) == 7
     assert mm.musemoe_num_kernels(mm.MUSEMOE_FP8_W8A8) == 8
