@@ -36,10 +36,13 @@ WORKLOAD = "decode"
 WEIGHT_SETS = 4
 
 # DRAM traffic of one launch of the dominant kernel, from the ncu capture
-# summarized in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
-# valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "d6eb909b9b0a568a16b601c47c6cdf3f7a9358c4",
-               "bytes_per_launch": 102626816 + 2461952}
+# summarized in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum) of
+# the decode bucket's w13 (48 active experts), with that launch's
+# algorithmic bytes: the bench scales it to its own launches by the ratio
+# (the traffic grows with the selected experts' bytes). Valid only for the
+# kernel source it was taken on.
+NCU_TRAFFIC = {"kernel": "w13", "source_sha1": "9d4e2eb8f37c324d628e9e521305f8430d3c94e0",
+               "bytes_per_launch": 107081728 + 2624256, "algorithmic_bytes": 107118592}
 
 
 def _args():
@@ -738,7 +741,8 @@ def bench_ours(args):
     traffic = None
     if (NCU_TRAFFIC["kernel"] == dom and NCU_TRAFFIC["source_sha1"] ==
             hashlib.sha1(src).hexdigest()):
-        traffic = NCU_TRAFFIC["bytes_per_launch"]
+        traffic = (NCU_TRAFFIC["bytes_per_launch"] / NCU_TRAFFIC["algorithmic_bytes"] *
+                   kernel_bytes[dom])
     step_bytes = sum(sum(m[nm] for nm in names) for m in model) / len(model)
     expert_bytes = sum(m["expert_bytes"] for m in model) / len(model)
     expert_ms = kernel_ms["w13"] + kernel_ms["w2"]
