@@ -26,7 +26,6 @@
 #include <algorithm>
 #include <mutex>
 
-#include "act4.cuh"
 #include "pipeline.cuh"
 #include "route_dev.cuh"
 
@@ -251,111 +250,9 @@ __device__ __forceinline__ void router_cta(const FrontParams& p, int task, uint8
 // registers (its loads and its norm weights' issued together); a longer one
 // is read from L2 once per pass.
 constexpr int kNV = 16;
-// The W4A4 form of norm_rows: h as there, and h rounded to FP4 (act4.cuh)
-// as the experts' operand: e2m1 codes [rows, M / 2] (the lower element of a
-// pair in the low nibble) and one scale byte per block [rows, M / blk]
-// (UE8M0 for MXFP4, e4m3 for NVFP4). A lane holds float4s lane, lane + 32,
-// ..., so an FP4 block is 8 (MXFP4) or 4 (NVFP4) neighbouring lanes, the
-// first of which stores the block's scale; M is a multiple of 128, so every
-// step is warp-uniform. Two passes over the row (it stays in L2), four
-// float4s per lane in flight. Out of line and with its arguments by value,
-// so the other forms keep their registers.
-struct Act4Row {
-  const float* y;
-  const uint16_t* w;
-  uint16_t* h;
-  uint8_t* h_op;
-  uint8_t* h_sf;
-  int M, pre_norm, act4;
-  float eps;
-};
-
-// one float4 of a row: bf16 h, the codes of its FP4 rounding and, from the
-// block's first lane, the block scale; flags a value that is not finite
-__device__ __forceinline__ int act4_put(const Act4Row& r, int t, int i, const float4& x,
-                                        const uint2& wb, float rstd) {
-  const float xv[4] = {x.x, x.y, x.z, x.w};
-  const float wv[4] = {bf16_bits_to_f32(wb.x & 0xFFFFu), bf16_bits_to_f32(wb.x >> 16),
-                       bf16_bits_to_f32(wb.y & 0xFFFFu), bf16_bits_to_f32(wb.y >> 16)};
-  float hb[4];
-  uint32_t hbits[2];
-  float am = 0.f;
-  int bad = 0;
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const float v0 = r.pre_norm ? (xv[2 * c] * rstd) * wv[2 * c] : xv[2 * c];
-    const float v1 = r.pre_norm ? (xv[2 * c + 1] * rstd) * wv[2 * c + 1] : xv[2 * c + 1];
-    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
-    hbits[c] = *reinterpret_cast<const uint32_t*>(&b2);
-    hb[2 * c] = __uint_as_float(hbits[c] << 16);
-    hb[2 * c + 1] = __uint_as_float(hbits[c] & 0xFFFF0000u);
-  }
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    am = fmaxf(am, fabsf(hb[c]));
-    bad |= !(fabsf(hb[c]) <= 3.40282347e38f);  // NaN or infinite
-  }
-  reinterpret_cast<uint2*>(r.h + (size_t)t * r.M)[i] = make_uint2(hbits[0], hbits[1]);
-  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-  if (r.act4 == 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
-  const Fp4Scale sc = fp4_block_scale(am, r.act4);
-  const uint32_t codes = fp4_code2(hb[0], hb[1], sc, r.act4) | (fp4_code2(hb[2], hb[3], sc, r.act4) << 8);
-  reinterpret_cast<uint16_t*>(r.h_op + (size_t)t * (r.M / 2))[i] = (uint16_t)codes;
-  const int per = r.act4 == 1 ? 8 : 4;  // float4s per block
-  if (i % per == 0)
-    r.h_sf[(size_t)t * (r.M / (4 * per)) + i / per] =
-        (uint8_t)(r.act4 == 1 ? (uint32_t)(mx_scale_exp(am) + 127) : nv_scale_code(am));
-  return bad;
-}
-
-__device__ __noinline__ void norm_rows_act4(Act4Row r, int32_t* health, int t0, int t1) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n4 = r.M / 4;
-  const uint2* wsrc = reinterpret_cast<const uint2*>(r.w);
-  constexpr int kB = 4;  // float4s per lane per round, all loads of a round in flight
-  int bad = 0;
-  for (int t = t0 + warp; t < t1; t += kGWarps) {
-    const float4* src = reinterpret_cast<const float4*>(r.y + (size_t)t * r.M);
-    float ss = 0.f;
-#pragma unroll 1
-    for (int base = 0; base < n4; base += kB * 32) {
-      float4 v[kB];
-#pragma unroll
-      for (int j = 0; j < kB; ++j) {
-        const int i = base + j * 32 + lane;
-        v[j] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int j = 0; j < kB; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-    }
-    ss = warp_sum(ss);
-    const float rstd = r.pre_norm ? 1.0f / sqrtf(ss / (float)r.M + r.eps) : 1.0f;
-    // a rolled loop: the rounding's code stays small enough to stay cached
-#pragma unroll 1
-    for (int base = 0; base < n4; base += kB * 32) {
-      float4 v[kB];
-      uint2 wb[kB];
-#pragma unroll
-      for (int j = 0; j < kB; ++j) {
-        const int i = base + j * 32 + lane;
-        v[j] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        wb[j] = (i < n4 && r.pre_norm) ? __ldg(wsrc + i) : make_uint2(0u, 0u);
-      }
-#pragma unroll
-      for (int j = 0; j < kB; ++j)
-        if (base + j * 32 < n4) bad |= act4_put(r, t, base + j * 32 + lane, v[j], wb[j], rstd);
-    }
-  }
-  if (bad) atomicOr(health, kHealthHRange);
-}
-
+// W4A4 writes h only: the forward rounds it to FP4 next (k_act_fp4, many
+// warps per row) and a value that is not finite raises kHealthHRange here.
 __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) {
-  if (p.act4) {
-    norm_rows_act4(Act4Row{p.y, p.w_pre_norm, p.h, p.h_op, p.h_sf, p.M, p.pre_norm, p.act4, p.norm_eps},
-                   p.health, t0, t1);
-    return;
-  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n4 = p.M / 4;
   const uint2* wsrc = reinterpret_cast<const uint2*>(p.w_pre_norm);
@@ -391,7 +288,10 @@ __device__ __forceinline__ void norm_rows(const FrontParams& p, int t0, int t1) 
 #pragma unroll
       for (int c = 0; c < 4; ++c) am = fmaxf(am, fabsf(hb[c]));
       hdst[i] = make_uint2(hbits[0], hbits[1]);
-      if (p.quant == kMXFP4 || p.quant == kNVFP4) {  // the f16 operand (BF16 and FP8 have their own)
+      if (p.act4) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) bad |= !(fabsf(hb[c]) <= 3.40282347e38f);  // NaN or infinite
+      } else if (p.quant == kMXFP4 || p.quant == kNVFP4) {  // the f16 operand (BF16 and FP8 have their own)
 #pragma unroll
         for (int c = 0; c < 4; ++c) bad |= !(fabsf(hb[c]) <= 65504.f);  // NaN too
         uint32_t opbits[2];

@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(256) k_act_quant(ActQuantParams p) {
 // kHealthActRange.
 constexpr int kActSpan = 256;
 
+template <int MODE>  // 1 MXFP4, 2 NVFP4
 __global__ void __launch_bounds__(256) k_act_fp4(ActQuantParams p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -101,17 +102,17 @@ __global__ void __launch_bounds__(256) k_act_fp4(ActQuantParams p) {
     bad |= !(fabsf(x[j]) <= 3.40282347e38f);  // NaN or infinite (above FLT_MAX)
   }
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-  if (p.mode == 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-  const Fp4Scale sc = fp4_block_scale(m, p.mode);
+  if (MODE == 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  const Fp4Scale sc = fp4_block_scale(m, MODE);
   uint32_t codes = 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) codes |= fp4_code2(x[2 * c], x[2 * c + 1], sc, p.mode) << (8 * c);
+  for (int c = 0; c < 4; ++c) codes |= fp4_code2(x[2 * c], x[2 * c + 1], sc, MODE) << (8 * c);
   if (ok) {
-    reinterpret_cast<uint32_t*>(p.q + (size_t)r * (p.I / 2))[i / 8] = codes;
-    const int per = p.mode == 1 ? 32 : 16;  // elements per block
-    if (i % per == 0)
-      p.sf[(size_t)r * (p.I / per) + i / per] =
-          (uint8_t)(p.mode == 1 ? (uint32_t)(mx_scale_exp(m) + 127) : nv_scale_code(m));
+    reinterpret_cast<uint32_t*>(p.q + (size_t)r * (p.I >> 1))[i >> 3] = codes;
+    constexpr int kSh = MODE == 1 ? 5 : 4;  // log2 of the elements per block
+    if ((i & ((1 << kSh) - 1)) == 0)
+      p.sf[(size_t)r * (p.I >> kSh) + (i >> kSh)] =
+          (uint8_t)(MODE == 1 ? (uint32_t)(mx_scale_exp(m) + 127) : nv_scale_code(m));
   }
   if (bad) atomicOr(p.health, kHealthActRange);
 }
@@ -127,7 +128,9 @@ cudaError_t launch_act_quant(const ActQuantParams& p, cudaStream_t s, bool pdl) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return p.mode ? cudaLaunchKernelEx(&cfg, k_act_fp4, p) : cudaLaunchKernelEx(&cfg, k_act_quant, p);
+  if (p.mode == 1) return cudaLaunchKernelEx(&cfg, k_act_fp4<1>, p);
+  if (p.mode == 2) return cudaLaunchKernelEx(&cfg, k_act_fp4<2>, p);
+  return cudaLaunchKernelEx(&cfg, k_act_quant, p);
 }
 
 // ---- tail: post-expert norm of each route, router weight, sum over k ------

@@ -65,7 +65,8 @@ struct FrontParams {
   // block applies the pre-expert RMSNorm to the block's rows of y
   const uint16_t* w_pre_norm;  // bf16 [M]
   int pre_norm, quant;
-  int act4;             // W4A4: h_op / h_sf hold h rounded to MXFP4 (1) or NVFP4 (2)
+  int act4;             // W4A4 (1 MXFP4, 2 NVFP4): the norm writes h only (no operand);
+                        // the forward rounds h into h_op / h_sf next
   float norm_eps;
   uint16_t* h;          // bf16 [rows, M]
   uint8_t* h_op;        // f16 [rows, M] (FP4), e4m3 [rows, M] (FP8), W4A4: e2m1 codes [rows, M / 2]
@@ -149,8 +150,9 @@ size_t expert_part_bytes(int grid, int nt);
 size_t expert_tickets(int max_groups, int quant, int role, int K, int N);
 
 // FP8 only: per-route dynamic e4m3 quantization of the bf16 activation.
-// W4A4 (mode 1 MXFP4, 2 NVFP4): per-route FP4 rounding of the bf16
-// activation into w2's operand: e2m1 codes and block scales.
+// W4A4 (mode 1 MXFP4, 2 NVFP4): per-row FP4 rounding of a bf16 operand,
+// w2's activation per route (and w13's h per token), into e2m1 codes and
+// block scales.
 struct ActQuantParams {
   const uint16_t* act;  // bf16 [routes, I]
   uint8_t* q;           // mode 0: e4m3 [routes, I]; modes 1, 2: e2m1 codes [routes, I / 2]

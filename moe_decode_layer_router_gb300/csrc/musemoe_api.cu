@@ -242,6 +242,22 @@ bool use_dense_tc(const musemoe_handle* h, int rows) {
   return h->dense_part != nullptr && rows >= kTcMinRows;
 }
 
+// W4A4: h (bf16, written by the pooler's norm) rounded per token to the
+// weights' FP4 format, e2m1 codes into h_op and block scales into h_sf (the
+// per-route rounding kernel, one warp per 256 elements of a row).
+cudaError_t launch_h_fp4(const musemoe_handle* h, int rows, cudaStream_t s, bool pdl) {
+  ActQuantParams q{};
+  q.act = h->h;
+  q.q = h->h_op;
+  q.sf = h->h_sf;
+  q.routes = rows;
+  q.I = h->d.pooled;
+  q.mode = h->act4;
+  q.health = h->health;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? launch_act_quant(q, s, pdl) : e;
+}
+
 // Whether a forward of `rows` runs its experts on the tensor-core kernels.
 bool use_tc(const musemoe_handle* h, int rows) {
   if (h->act4) return true;  // W4A4: the FP4 tensor cores at every size
@@ -360,14 +376,18 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     dp.health = h->health;
     dp.grid = h->sms;
     // one "pool" stage of the taps' events: the GEMM and the norm launch
+    // (W4A4: and the FP4 rounding of h)
     before();
     cudaError_t r = launch_dense_tc(dp, s, pdl);
     if (r == cudaSuccess) r = cudaGetLastError();
     if (r == cudaSuccess) r = launch_pool_norm(fp, s, pdl);
+    if (r == cudaSuccess && h->act4) r = launch_h_fp4(h, rows, s, pdl);
     if (!after(r, "pool")) return MUSEMOE_ECUDA;
   } else {
     before();
-    if (!after(launch_front(fp, ntf, s, pdl), "pool")) return MUSEMOE_ECUDA;
+    cudaError_t r = launch_front(fp, ntf, s, pdl);
+    if (r == cudaSuccess && h->act4) r = launch_h_fp4(h, rows, s, pdl);
+    if (!after(r, "pool")) return MUSEMOE_ECUDA;
   }
 
   // 3. w13 + SiLU * up
