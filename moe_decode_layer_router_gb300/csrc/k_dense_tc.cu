@@ -5,20 +5,28 @@
 // "vllm.models.muse_spark.nvidia.specialized_decode.runtime.providers",
 // MoEProvider: the pooler GEMM and the unpooler GEMM of the routed MoE).
 //
-// One CTA per SM (persistent), Stream-K over units = (token block of up to
-// 256 rows, tile of 128 weight rows, 64-element K block). The MMA is
-// D[128 weight rows x N tokens] += W_tile[128 x 64] X_block[N x 64]^T with N
-// the block's rows rounded up to 16. A producer lane loads both operands
-// with 2-D tensor copies (128-byte swizzle: the canonical K-major layout the
-// MMA reads); an MMA lane issues 4 MMAs per unit; 4 epilogue warps read the
-// accumulators (two, so a tile's epilogue overlaps the next tile's MMAs) and
-// store Y, or a partial sum when the tile's K blocks span several CTAs; the
-// contributors of a split tile then share its final sums (below), each
-// adding all partials in CTA order, so results do not depend on scheduling.
-// Rows past the end are zero-filled by the tensor copy and never stored.
+// Split K across a thread-block cluster: one cluster per work item (a tile of
+// 128 weight rows x a token block of up to 256 rows), its C CTAs each
+// accumulate a disjoint range of the 64-element K blocks. C is the largest
+// size (at most 8, at most the K blocks, at most the SMs' share per item) at
+// which all the items' clusters are resident at once, so the launch is one
+// wave. The MMA is D[128 weight rows x N tokens] +=
+// W_tile[128 x 64] X_block[N x 64]^T with N the block's rows rounded up to
+// 16. A producer lane loads both operands with 2-D tensor copies (128-byte
+// swizzle: the canonical K-major layout the MMA reads) into a 4-stage ring;
+// an MMA lane issues 4 MMAs per K block into one tensor-memory accumulator.
+// The partial sums never leave the cluster: after a cluster barrier (every
+// CTA's MMAs done, its stages free) the 4 epilogue warps write each row of
+// their accumulator into the stage memory of the row's owner (rank r owns
+// rows [ceil(128 r / C), ceil(128 (r + 1) / C))) through distributed shared
+// memory; after a second barrier each owner adds the C slots of its rows in
+// rank order and stores Y (8 rows x 4 tokens per warp step), so results do
+// not depend on scheduling. Rows past
+// the end are zero-filled by the tensor copy and never stored.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pipeline.cuh"
@@ -38,64 +46,48 @@ constexpr int kDStage = kDStageA + kDStageB;   // 48 KB
 constexpr int kDSmem = 1024 + kDStages * kDStage;
 constexpr int kDEpi = 4;
 constexpr int kDThreads = (kDEpi + 2) * 32;    // epilogue, producer, MMA
-constexpr int kDTmemCols = 512;                // two accumulators of up to 256 columns
-
-__device__ __forceinline__ int d_cta_of(long long u, long long U, int G) {
-  return (int)(((u + 1) * G - 1) / U);
+constexpr int kDTmemCols = kDN;                // one accumulator of up to 256 columns
+constexpr int kDMaxCluster = 8;
+// A slot row (one output row's N fp32) is N + 4 floats apart from the next:
+// the 32 lanes of a warp, one row each, then store to distinct banks, and
+// the summing threads (8 rows x 4 tokens per warp) load from distinct banks.
+constexpr int kDSlotPad = 4;
+// the exchange slots (C of them, each the owner's rows x N fp32) fit the stages
+constexpr bool dense_slots_fit() {
+  for (int c = 1; c <= kDMaxCluster; ++c)
+    if (c * ((kDM + c - 1) / c) * (kDN + kDSlotPad) * 4 > kDStages * kDStage) return false;
+  return true;
 }
-__device__ __forceinline__ long long d_start(int c, long long U, int G) { return U * c / G; }
+static_assert(dense_slots_fit(), "exchange slots within the stage memory");
 
-struct DRange {
-  int U0, U1, b0, b1, KS, PG, tiles;
-  __device__ void init(long long u0, long long u1, int ks, int tl) {
-    U0 = (int)u0;
-    U1 = (int)u1;
-    KS = ks;
-    tiles = tl;
-    PG = ks * tl;
-    b0 = (U0 + KS - 1) / KS * KS;
-    b1 = U1 / KS * KS;
-    if (b0 > b1) b0 = b1 = U0;
-  }
-  __device__ int lo(int i) const { return i == 0 ? b0 : (i == 1 ? b1 : U0); }
-  __device__ int hi(int i) const { return i == 0 ? b1 : (i == 1 ? U1 : b0); }
-};
-// units in processing order: whole tiles, then the leading part (leave a
-// partial), then the trailing part (own the tile): no wait depends on a
-// waiting CTA
-struct DWalk {
-  int u, blk, tile, kb, lo, hi, part, left;
-  __device__ void begin() {
-    part = -1;
-    left = 0;
-  }
-  __device__ void next(const DRange& R) {
-    if (left == 0) {
-      do {
-        ++part;
-      } while (part < 3 && R.hi(part) <= R.lo(part));
-      lo = R.lo(part);
-      hi = R.hi(part);
-      left = hi - lo;
-      u = lo;
-      blk = u / R.PG;
-      const int rem = u - blk * R.PG;
-      tile = rem / R.KS;
-      kb = rem - tile * R.KS;
-    } else {
-      ++u;
-      if (++kb == R.KS) {
-        kb = 0;
-        if (++tile == R.tiles) {
-          tile = 0;
-          ++blk;
-        }
-      }
-    }
-    --left;
-  }
-  __device__ bool closes(const DRange& R) const { return kb == R.KS - 1 || u + 1 == hi; }
-};
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster: release its earlier memory
+// operations, then acquire the others'
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// the shared::cluster address of a shared::cta address in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+// first row of the tile that rank r of C owns (ceil(128 r / C))
+__device__ __forceinline__ int own_first(int r, int C) { return (r * kDM + C - 1) / C; }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar, uint64_t pol) {
@@ -145,32 +137,28 @@ __global__ void __launch_bounds__(kDThreads, 1)
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) unsigned long long full_b[kDStages], empty_b[kDStages];
-  __shared__ __align__(8) unsigned long long accfull[2], accempty[2], drain_b;
+  __shared__ __align__(8) unsigned long long accfull, drain_b;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
 
+  const int C = (int)cluster_size(), r = (int)cluster_rank();
   const int tiles = (p.M + kDM - 1) / kDM;
+  const int item = blockIdx.x / C;  // one (token block, tile) per cluster
+  const int tile = item % tiles, blk = item / tiles;
   const int KS = p.K / kDK;
-  const int blocks = (p.rows + kDN - 1) / kDN;
-  const long long U = (long long)blocks * tiles * KS;
-  const int GE = (int)min((long long)gridDim.x, U);
-  const long long u0 = blockIdx.x < GE ? d_start(blockIdx.x, U, GE) : 0;
-  const long long u1 = blockIdx.x < GE ? d_start(blockIdx.x + 1, U, GE) : 0;
-  DRange R;
-  R.init(u0, u1, KS, tiles);
-  const int count = R.U1 - R.U0;
+  const int k0 = r * KS / C, nk = (r + 1) * KS / C - k0;  // this CTA's K blocks
+  const int nr = min(kDN, p.rows - blk * kDN);             // the block's rows
+  const int npad = (nr + 15) & ~15;
+  const int box_rows = min(kDN, (p.rows + 15) & ~15);      // rows of the token tensor copy
 
   if (tid == 0) {
     for (int i = 0; i < kDStages; ++i) {
       mbar_init(smem_u32(&full_b[i]), 1);
       mbar_init(smem_u32(&empty_b[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&accfull[i]), 1);
-      mbar_init(smem_u32(&accempty[i]), kDEpi);
-    }
+    mbar_init(smem_u32(&accfull), 1);
     mbar_init(smem_u32(&drain_b), 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -189,23 +177,19 @@ __global__ void __launch_bounds__(kDThreads, 1)
   auto wait = [&](unsigned long long* bar, uint32_t phase) -> bool {
     return mbar_wait_or_abort(smem_u32(bar), phase, &abort_flag);
   };
-  auto rows_of = [&](int blk) { return min(kDN, p.rows - blk * kDN); };
-  const int box_rows = min(kDN, (p.rows + 15) & ~15);  // rows of the token tensor copy
 
+  bool have = false;  // epilogue: the accumulator holds this CTA's partial
   if (warp == kDEpi) {
-    // ---------------- producer: weight tile and token rows of each unit ----------------
+    // ---------------- producer: weight tile and token rows of each K block ----------------
     if (lane == 0) {
-      int tlc = 0;
+      [[maybe_unused]] int tlc = 0;
       DTL(0, tlc, 0);
       const uint64_t pol_w = l2_policy_evict_first();
       uint64_t pol_x;
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol_x));
-      DWalk wk;
-      wk.begin();
       int issued = 0;
       bool waited = false;
-      for (int n = 0; n < count; ++n) {
-        wk.next(R);
+      for (int n = 0; n < nk; ++n) {
         const int st = n % kDStages, use = n / kDStages;
         if (use > 0 && !wait(&empty_b[st], (uint32_t)(use - 1) & 1u)) {
           fail();
@@ -215,15 +199,16 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const uint32_t dst = base + st * kDStage;
         mbar_expect_tx(bar, kDStageA + box_rows * 128);  // the copy writes the whole box
         // the weights never depend on the previous kernel; the token rows do
-        tma_load_2d(dst, &tw, wk.kb * kDK, wk.tile * kDM, bar, pol_w);
+        tma_load_2d(dst, &tw, (k0 + n) * kDK, tile * kDM, bar, pol_w);
         if (!waited) {
           pdl_wait();
           waited = true;
         }
-        tma_load_2d(dst + kDStageA, &tx, wk.kb * kDK, wk.blk * kDN, bar, pol_x);
+        tma_load_2d(dst + kDStageA, &tx, (k0 + n) * kDK, blk * kDN, bar, pol_x);
         issued = n + 1;
         DTL(0, tlc, 1);
       }
+      if (!waited) pdl_wait();
       for (int st = 0; st < kDStages && st < issued; ++st) {
         const int last = st + ((issued - 1 - st) / kDStages) * kDStages;
         const unsigned long long t0 = globaltimer();
@@ -234,21 +219,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
   } else if (warp == kDEpi + 1) {
     // ---------------- MMA issue (one lane) ----------------
     if (lane == 0) {
-      int tlc = 0;
+      [[maybe_unused]] int tlc = 0;
       DTL(1, tlc, 0);
-      DWalk wk;
-      wk.begin();
-      int acc = 0, acc_use = 0;
-      bool fresh = true;
-      for (int n = 0; n < count; ++n) {
-        wk.next(R);
-        if (fresh) {
-          if (acc_use > 1 && !wait(&accempty[acc], (uint32_t)((acc_use >> 1) - 1) & 1u)) {
-            fail();
-            break;
-          }
-          tc::fence_after_sync();
-        }
+      const uint32_t idesc = tc::instr_desc(tc::kBF16, tc::kBF16, kDM, npad);
+      int n = 0;
+      for (; n < nk; ++n) {
         const int st = n % kDStages;
         if (!wait(&full_b[st], (uint32_t)(n / kDStages) & 1u)) {
           fail();
@@ -256,192 +231,108 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         DTL(1, tlc, 1);
         tc::fence_after_sync();
-        const int npad = (rows_of(wk.blk) + 15) & ~15;
-        const uint32_t idesc = tc::instr_desc(tc::kBF16, tc::kBF16, kDM, npad);
         const uint64_t da = tc::smem_desc(base + st * kDStage, 16, 1024, tc::kSw128);
         const uint64_t db = tc::smem_desc(base + st * kDStage + kDStageA, 16, 1024, tc::kSw128);
-        const uint32_t d_tmem = tmem + acc * kDN;
 #pragma unroll
         for (int j = 0; j < 4; ++j)  // K = 16 per MMA: 32 bytes further in the 128-byte rows
-          tc::mma_f16(d_tmem, da + (uint64_t)(2 * j), db + (uint64_t)(2 * j), idesc,
-                      (fresh && j == 0) ? 0u : 1u);
+          tc::mma_f16(tmem, da + (uint64_t)(2 * j), db + (uint64_t)(2 * j), idesc,
+                      (n == 0 && j == 0) ? 0u : 1u);
         tc::commit(smem_u32(&empty_b[st]));
-        fresh = false;
-        if (wk.closes(R)) {
-          tc::commit(smem_u32(&accfull[acc]));
-          acc ^= 1;
-          ++acc_use;
-          fresh = true;
-        }
       }
-      tc::commit(smem_u32(&drain_b));
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(smem_u32(&drain_b), 0u))
-        if (globaltimer() - t0 > kWaitLimitNs) break;
+      // the accumulator is complete (or, after a timeout, abandoned)
+      tc::commit(smem_u32(n == nk ? &accfull : &drain_b));
+      if (n != nk) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&drain_b), 0u))
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+      }
     }
   } else {
-    // ---------------- epilogue (warps 0..3): tensor memory -> Y ----------------
-    // A tile finished inside this CTA is stored directly. A tile whose K
-    // blocks span several CTAs: every contributor stores its partial and
-    // signals the tile's ticket as soon as its part closes; only after all of
-    // its own parts does it wait for the tile's other contributors, then sums
-    // its share of the tile's 16-column chunks (chunk cc goes to contributor
-    // cc mod n) over all partials in CTA order. Every signal comes before
-    // every wait, so no wait depends on a waiting CTA; the sums do not
-    // depend on scheduling.
+    // ---------------- epilogue (warps 0..3), part 1: the accumulator is complete ----------------
     pdl_wait();  // Y's previous readers are done
-    const int row = warp * 32 + lane;  // weight row within the tile
-    const uint32_t t_row = (uint32_t)(warp * 32) << 16;
-    int tlc = 0;
-    if (tid == 0) DTL(2, tlc, 0);
-    DWalk wk;
-    wk.begin();
-    int acc = 0, acc_use = 0;
-    float4* part = reinterpret_cast<float4*>(p.part);
-    const int slot_f4 = kDM * kDN / 4;
-    auto slot_of = [&](int c, int tb) -> int {
-      const int which = (d_start(c, U, GE) >= tb) ? 0 : 1;  // the CTA's first or last tile
-      return (c * 2 + which) * slot_f4;
-    };
-    int nsplit = 0;
-    int sp_blk[2] = {0, 0}, sp_tile[2] = {0, 0}, sp_tb[2] = {0, 0};
-    bool good = true;
-    for (int n = 0; n < count && good; ++n) {
-      wk.next(R);
-      if (!wk.closes(R)) continue;
-      if (!__all_sync(0xffffffffu, wait(&accfull[acc], (uint32_t)(acc_use >> 1) & 1u))) {
-        if (lane == 0) fail();
-        good = false;
-        break;
-      }
-      if (tid == 0) DTL(2, tlc, 1);
-      tc::fence_after_sync();
-      const int nr = rows_of(wk.blk);
-      const int ncol = (nr + 15) >> 4;
-      const int tb = wk.u - wk.kb;
-      const bool whole = (wk.kb == KS - 1) && tb >= wk.lo;
-      const uint32_t tsrc = tmem + acc * kDN + t_row;
-      const int m = wk.tile * kDM + row;
-      // 32 columns (two 16-column chunks) per tensor-memory load and wait
-      for (int c2 = 0; c2 < ncol; c2 += 2) {
-        float v2[32];
-        tc::ld_32x32b_x32(tsrc + c2 * 16, v2);
-        tc::wait_ld();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int cc = c2 + h;
-          if (cc >= ncol) break;
-          const float* v = v2 + 16 * h;
-          if (!whole) {
-            float4* dst = part + slot_of(blockIdx.x, tb) + (cc * kDM + row) * 4;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          } else if (m < p.M) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              const int tok = cc * 16 + t;
-              if (tok < nr) p.y[(size_t)(wk.blk * kDN + tok) * p.M + m] = v[t];
-            }
-          }
-        }
-      }
-      if (!whole) {
-        __syncwarp();  // orders the lanes' partial stores before lane 0's release
-        int32_t* flag = p.tickets + (((size_t)wk.blk * tiles + wk.tile) * kDEpi + warp) * 2;
-        if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;\n" ::"l"(flag) : "memory");
-        sp_blk[nsplit] = wk.blk;
-        sp_tile[nsplit] = wk.tile;
-        sp_tb[nsplit] = tb;
-        ++nsplit;
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&accempty[acc]));
-      if (tid == 0) DTL(2, tlc, 3 + (whole ? 0 : 1));
-      acc ^= 1;
-      ++acc_use;
+    if (nk > 0) {
+      have = __all_sync(0xffffffffu, wait(&accfull, 0u));
+      if (!have && lane == 0) fail();
     }
-    // the split tiles' sums: this CTA's share of each
-    for (int k = 0; k < nsplit && good; ++k) {
-      const int blk = sp_blk[k], tile = sp_tile[k], tb = sp_tb[k];
-      const int c_first = d_cta_of(tb, U, GE), c_last = d_cta_of(tb + KS - 1, U, GE);
-      const int ncon = c_last - c_first + 1;  // contributors, this CTA among them
-      int32_t* flag = p.tickets + (((size_t)blk * tiles + tile) * kDEpi + warp) * 2;
-      int got = 1;
-      if (lane == 0) {
-        int v = 0;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
-        if (v < ncon) {
-          const unsigned long long t0 = globaltimer();
-          do {
-            __nanosleep(128);
-            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
-          } while (v < ncon && globaltimer() - t0 <= kWaitLimitNs && !abort_flag);
-        }
-        got = (v >= ncon);
+    tc::fence_after_sync();
+  }
+  [[maybe_unused]] int etl = 0;
+  if (tid == 0) DTL(2, etl, 1);
+
+  // every CTA of the cluster has finished its MMAs: its stage memory is free
+  // for the exchange (all warps of every CTA reach both barriers on every path)
+  __syncwarp();
+  cluster_sync();
+  if (tid == 0) DTL(2, etl, 5);
+
+  const int R = (kDM + C - 1) / C;  // rows per owner slot
+  const int ss = npad + kDSlotPad;    // floats from one slot row to the next
+  if (warp < kDEpi) {
+    // part 2: each row of this CTA's partial goes to slot r of the row's owner
+    const int row = warp * 32 + lane;
+    int o = 0;
+    while (o + 1 < C && own_first(o + 1, C) <= row) ++o;
+    const int lr = row - own_first(o, C);
+    const uint32_t slot = peer_addr(base + (uint32_t)(((r * R + lr) * ss) * 4), (uint32_t)o);
+    const uint32_t tsrc = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int c0 = 0; c0 < npad; c0 += 32) {
+      float v[32];
+      if (c0 + 16 < npad) {
+        tc::ld_32x32b_x32(tsrc + c0, v);
+      } else {
+        float h[16];
+        tc::ld_32x32b_x16(tsrc + c0, h);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = h[i];
       }
-      if (!__shfl_sync(0xffffffffu, got, 0)) {
-        if (lane == 0) fail();
-        good = false;
-        break;
-      }
-      if (tid == 0) DTL(2, tlc, 2);
-      const int nr = rows_of(blk);
-      const int ncol = (nr + 15) >> 4;
-      const int m = tile * kDM + row;
-      for (int cc = (int)blockIdx.x - c_first; cc < ncol; cc += ncon) {
-        float s[16];
+      tc::wait_ld();
+      const int nc = min(32, npad - c0);
+      if (!have || nk == 0)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = 0.f;
-        int c = c_first;
-        // four contributors' loads in flight at a time, added in CTA order
-        for (; c + 4 <= c_last + 1; c += 4) {
-          float4 x[4][4];
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;  // no K blocks (or abandoned): contributes zeros
 #pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[a][i] = __ldcg(part + slot_of(c + a, tb) + (cc * kDM + row) * 4 + i);
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              s[4 * i] += x[a][i].x;
-              s[4 * i + 1] += x[a][i].y;
-              s[4 * i + 2] += x[a][i].z;
-              s[4 * i + 3] += x[a][i].w;
-            }
-        }
-        for (; c <= c_last; ++c)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 x = __ldcg(part + slot_of(c, tb) + (cc * kDM + row) * 4 + i);
-            s[4 * i] += x.x;
-            s[4 * i + 1] += x.y;
-            s[4 * i + 2] += x.z;
-            s[4 * i + 3] += x.w;
-          }
-        if (m < p.M) {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int tok = cc * 16 + t;
-            if (tok < nr) p.y[(size_t)(blk * kDN + tok) * p.M + m] = s[t];
-          }
-        }
-      }
-      // the last contributor done with the tile zeroes its tickets for the next launch
-      __syncwarp();
-      if (lane == 0) {
-        int d = 0;
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(d) : "l"(flag + 1) : "memory");
-        if (d == ncon - 1) {
-          flag[0] = 0;
-          flag[1] = 0;
-        }
-      }
-      if (tid == 0) DTL(2, tlc, 5);
+      for (int i = 0; i < 32; i += 4)
+        if (i < nc) st_cluster_v4(slot + (uint32_t)((c0 + i) * 4), v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
   }
+  if (tid == 0) DTL(2, etl, 2);
+  tc::fence_before_sync();
+  __syncwarp();
+  cluster_sync();
+  if (tid == 0) DTL(2, etl, 3);
+
+  {
+    // part 3: this CTA's rows, the C slots added in rank order, by every warp
+    // of the CTA. A warp takes 8 rows x 4 token quads at a time: each lane
+    // loads its row's quad from the C slots (16 bytes, distinct banks) and
+    // stores 4 tokens; a token's 8 rows m are one 32-byte sector of y.
+    const int rf = own_first(r, C), rn = own_first(r + 1, C) - rf;
+    const int nq = (nr + 3) >> 2, rb = (rn + 7) >> 3, qb = (nq + 3) >> 2;
+    const float* sl = reinterpret_cast<const float*>(smem_raw + (base - smem_u32(smem_raw)));
+    for (int b = warp; b < rb * qb; b += kDThreads / 32) {
+      const int lr = (b % rb) * 8 + (lane & 7), qd = (b / rb) * 4 + (lane >> 3);
+      const int m = tile * kDM + rf + lr;
+      if (lr >= rn || qd >= nq || m >= p.M) continue;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kDMaxCluster; ++q) {
+        if (q < C) {
+          const float4 v = *reinterpret_cast<const float4*>(sl + (q * R + lr) * ss + 4 * qd);
+          a.x += v.x;
+          a.y += v.y;
+          a.z += v.z;
+          a.w += v.w;
+        }
+      }
+      float* yo = p.y + (size_t)(blk * kDN + 4 * qd) * p.M + m;
+      const int nt = nr - 4 * qd;  // tokens of this quad in the block
+      yo[0] = a.x;
+      if (nt > 1) yo[p.M] = a.y;
+      if (nt > 2) yo[2 * (size_t)p.M] = a.z;
+      if (nt > 3) yo[3 * (size_t)p.M] = a.w;
+    }
+  }
+  if (tid == 0) DTL(2, etl, 4);
 
   tc::fence_before_sync();
   __syncthreads();
@@ -478,8 +369,36 @@ cudaError_t map_2d(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, 
 }
 }  // namespace
 
+// How many clusters of C CTAs of this kernel (one per SM: its shared
+// memory) can be resident at once (a cluster must fit one GPC); asked once
+// per size.
+int clusters_resident(int C) {
+  static int known[kDMaxCluster + 1] = {0};  // 0 unknown, else count + 1
+  if (known[C] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = kDSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_dense_tc, &cfg);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    known[C] = n + 1;
+  }
+  return known[C] - 1;
+}
+
 cudaError_t launch_dense_tc(const DenseParams& p, cudaStream_t s, bool pdl) {
-  if (p.K % kDK || p.rows < 1) return cudaErrorInvalidValue;
+  if (p.K % kDK || p.rows < 1 || p.M < 1) return cudaErrorInvalidValue;
   CUtensorMap tw{}, tx{};
   const int box_rows = std::min(kDN, (p.rows + 15) & ~15);
   cudaError_t e = map_2d(&tw, p.w, (uint64_t)p.K, (uint64_t)p.M, kDM);
@@ -487,22 +406,31 @@ cudaError_t launch_dense_tc(const DenseParams& p, cudaStream_t s, bool pdl) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_dense_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
   if (e != cudaSuccess) return e;
+  // one cluster per (token block, tile); as many K-splitting CTAs per
+  // cluster as fill the SMs (p.grid), at most 8 and at most the K blocks
+  const int items = ((p.rows + kDN - 1) / kDN) * ((p.M + kDM - 1) / kDM);
+  // the largest cluster (at most 8 CTAs, at most the K blocks, at most the
+  // SMs' share) whose clusters all fit at once: one wave
+  int C = std::max(1, std::min(std::min(kDMaxCluster, p.K / kDK), p.grid / items));
+  while (C > 1 && clusters_resident(C) < items) --C;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
+  cfg.gridDim = dim3(items * C);
   cfg.blockDim = dim3(kDThreads);
   cfg.dynamicSmemBytes = kDSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_dense_tc, tw, tx, p);
 }
 
-size_t dense_tc_part_bytes(int grid) { return (size_t)grid * 2 * kDM * kDN * sizeof(float); }
-size_t dense_tc_tickets(int rows, int M) {
-  return (size_t)((rows + kDN - 1) / kDN) * ((M + kDM - 1) / kDM) * kDEpi * 2;
-}
+// the cluster kernel keeps its partial sums on chip: no workspace beyond a
+// token (a non-null pointer marks the dense path as available)
 
 }  // namespace musemoe

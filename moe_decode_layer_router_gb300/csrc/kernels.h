@@ -87,22 +87,18 @@ cudaError_t launch_front(const FrontParams& p, int nt, cudaStream_t s, bool pdl)
 cudaError_t launch_pool_norm(const FrontParams& p, cudaStream_t s, bool pdl);
 
 // ---- dense bf16 GEMM on the tensor cores (pooler / unpooler, larger buckets)
-// y[rows, M] = x[rows, K] w[M, K]^T, fp32; K a multiple of 64; grid CTAs (one
-// per SM); partial sums in dense_tc_part_bytes(grid), tickets
-// dense_tc_tickets(rows, M) int32 (zero between launches).
+// y[rows, M] = x[rows, K] w[M, K]^T, fp32; K a multiple of 64; split K over
+// thread-block clusters of at most `grid` CTAs in all, the partial sums
+// exchanged in distributed shared memory (no global workspace).
 struct DenseParams {
   const uint16_t* x;  // bf16 [rows, K]
   const uint16_t* w;  // bf16 [M, K]
   float* y;           // fp32 [rows, M]
   int rows, M, K;
-  float* part;
-  int32_t* tickets;
   int32_t* health;
-  int grid;
+  int grid;  // CTAs the launch may use (the SMs)
 };
 cudaError_t launch_dense_tc(const DenseParams& p, cudaStream_t s, bool pdl);
-size_t dense_tc_part_bytes(int grid);
-size_t dense_tc_tickets(int rows, int M);
 cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl);          // router
 int front_gemv_ctas(int M, int rows, int nt);
 int front_ctas_per_sm(int K, int nt);

@@ -71,8 +71,6 @@ struct musemoe_handle {
   float *h_raw = nullptr, *u = nullptr;
   float *y = nullptr, *stream_stage = nullptr, *expert_part = nullptr;
   int32_t* expert_tickets[2] = {nullptr, nullptr};
-  float* dense_part = nullptr;                     // dense tensor-core GEMMs (rows above 32)
-  int32_t* dense_tickets[2] = {nullptr, nullptr};  // pooler, unpooler
   size_t expert_ticket_bytes[2] = {0, 0};
   size_t block_ticket_bytes = 0;  // norm_ticket and route_ticket, each
   int32_t* norm_ticket = nullptr;
@@ -149,11 +147,6 @@ void plan(musemoe_handle* h, Layout& L) {
   h->expert_ticket_bytes[1] = expert_tickets(h->max_groups, h->quant, 1, d.inter, d.pooled) * 4;
   L.add(&h->expert_tickets[0], h->expert_ticket_bytes[0]);
   L.add(&h->expert_tickets[1], h->expert_ticket_bytes[1]);
-  if (d.max_rows >= kTcMinRows) {
-    L.add(&h->dense_part, dense_tc_part_bytes(h->sms));
-    L.add(&h->dense_tickets[0], dense_tc_tickets(d.max_rows, d.pooled) * 4);
-    L.add(&h->dense_tickets[1], dense_tc_tickets(d.max_rows, d.hidden) * 4);
-  }
   L.add(&h->moe_out, R * P * 2);
   L.add(&h->x_stage, R * H * 2);
   L.add(&h->stream_stage, R * H * 4);
@@ -238,9 +231,7 @@ std::string check_weights(const musemoe_handle* h, const musemoe_weights* w, boo
 
 // Whether a forward of `rows` runs the pooler and unpooler as dense
 // tensor-core GEMMs (the same rows as the expert kernels' dense buckets).
-bool use_dense_tc(const musemoe_handle* h, int rows) {
-  return h->dense_part != nullptr && rows >= kTcMinRows;
-}
+bool use_dense_tc(int rows) { return rows >= kTcMinRows; }
 
 // W4A4: h (bf16, written by the pooler's norm) rounded per token to the
 // weights' FP4 format, e2m1 codes into h_op and block scales into h_sf (the
@@ -362,7 +353,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   // 2. pooler GEMV (its weight copies overlap the router); the last CTA of
   // each token block applies the pre-expert norm to the block's rows. Above
   // 32 rows: a dense tensor-core GEMM, then the norm as its own launch
-  const bool dense = use_dense_tc(h, rows);
+  const bool dense = use_dense_tc(rows);
   if (dense) {
     DenseParams dp{};
     dp.x = x;
@@ -371,8 +362,6 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     dp.rows = rows;
     dp.M = d.pooled;
     dp.K = d.hidden;
-    dp.part = h->dense_part;
-    dp.tickets = h->dense_tickets[0];
     dp.health = h->health;
     dp.grid = h->sms;
     // one "pool" stage of the taps' events: the GEMM and the norm launch
@@ -511,7 +500,7 @@ musemoe_status launch_back(musemoe_handle* h, const musemoe_weights* w, float* s
                            const std::function<bool(cudaError_t, const char*)>& after) {
   const musemoe_dims& d = h->d;
   const int ntf = nt_front(rows);
-  const bool dense = use_dense_tc(h, rows);
+  const bool dense = use_dense_tc(rows);
   // 6. unpooler GEMV
   FrontParams up{};
   up.x = h->moe_out;
@@ -531,8 +520,6 @@ musemoe_status launch_back(musemoe_handle* h, const musemoe_weights* w, float* s
     dp.rows = rows;
     dp.M = d.hidden;
     dp.K = d.pooled;
-    dp.part = h->dense_part;
-    dp.tickets = h->dense_tickets[1];
     dp.health = h->health;
     dp.grid = h->sms;
     before();

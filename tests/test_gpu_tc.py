@@ -152,3 +152,17 @@ def test_dense_tc_front_every_form(quant, rows):
     x, st = synth.activations(cfg)
     g = _run_path(cfg, w, x, st, mm.MUSEMOE_PATH_AUTO)
     H.compare(cfg, w, x, st, g)
+
+
+@pytest.mark.parametrize("rows,hidden", [(40, 1088), (300, 5120)])
+def test_dense_tc_cluster_shapes(rows, hidden):
+    # the split-K cluster sizes at their edges: 1088 unpooler rows end in a
+    # half tile (rows past the end never stored) and split 4 ways; 40 tiles x
+    # 2 token blocks are more items than 76, so the unpooler runs one CTA per
+    # item, while its pooler splits 8 ways
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=rows, hidden=hidden, pooled=256,
+                              inter=128, quant=synth.MXFP4, seed=37)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    g = _run_path(cfg, w, x, st, mm.MUSEMOE_PATH_AUTO)
+    H.compare(cfg, w, x, st, g)
