@@ -136,7 +136,9 @@ def compare(cfg: synth.Config, w: dict, x, st, g: dict, pre_norm: bool = True) -
     np.testing.assert_allclose(g["weights"], ref["weights"], rtol=WEIGHT_RTOL, atol=0)
     stage = stage_errors(g, ref, b, k)
     assert_stage_parity(stage, ref, b * cfg.pooled, b * k * cfg.inter)
-    e2e = {key: rel_err(g[key], ind[key]) for key in ("moe_out", "stream", "out")}
+    e2e = {"moe_out": rel_err_bf16(g["moe_out"], ind["moe_out"]),
+           "stream": rel_err(g["stream"], ind["stream"]),
+           "out": rel_err_bf16(g["out"], ind["out"])}
     bound = e2e_bound(cfg)
     assert max(e2e["stream"], e2e["out"]) <= bound, (e2e, bound)
     rep = {"stage_" + k_: v for k_, v in stage.items()}
@@ -286,3 +288,20 @@ FP8_E2E_TOL = 1e-1
 def rel_err(gpu, ref):
     rms = float(np.sqrt(np.mean(np.square(ref))))
     return float(np.max(np.abs(np.asarray(gpu, np.float64) - ref))) / max(rms, 1e-30)
+
+
+def bf16_step(v):
+    """The spacing of bf16 values at |v|: 2^(e - 7) for |v| in [2^e, 2^(e+1))."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 2.0 ** -126)))
+    return np.exp2(np.maximum(e, -126.0) - 7.0)
+
+
+def rel_err_bf16(gpu, ref):
+    """rel_err of a bf16-rounded output, one bf16 step per element allowed:
+    an independent run that differs from the GPU in the last fp32 bits
+    upstream may round any element the other way, and at an element of 4x the
+    RMS that one step alone is 3 % of the RMS."""
+    g, r = np.asarray(gpu, np.float64), np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(np.square(r))))
+    return float(np.max(np.maximum(np.abs(g - r) - bf16_step(r), 0.0))) / max(rms, 1e-30)

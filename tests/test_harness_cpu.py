@@ -36,6 +36,23 @@ def test_planted_mistakes_fail_the_comparison(tensor):
         H.compare(cfg, w, x, st, g)
 
 
+def test_bf16_output_error_allows_one_step_only():
+    # the independent check of a bf16 output forgives one bf16 step per
+    # element (a rounding that went the other way) at any magnitude, and no
+    # more: two steps at an element of 4x the RMS still fail the 2e-2 bound
+    ref = np.concatenate([[4.3125], np.tile([-0.5, 0.25, 1.0, -1.0, 0.75, -1.25, 0.0078125], 20)])
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert H.bf16_step(4.3125) == 2.0 ** -5 and H.bf16_step(-0.5) == 2.0 ** -8
+    assert H.bf16_step(4.0) == 2.0 ** -5 and H.bf16_step(3.984375) == 2.0 ** -6
+    one = ref + np.sign(ref) * H.bf16_step(ref)
+    assert H.rel_err_bf16(one, ref) == 0.0
+    assert H.rel_err(one, ref) > H.OUT_TOL  # what the plain metric would say
+    two = ref.copy()
+    two[0] += 2 * H.bf16_step(ref[0])
+    assert H.rel_err_bf16(two, ref) == pytest.approx(2.0 ** -5 / rms)
+    assert H.rel_err_bf16(two, ref) > H.OUT_TOL
+
+
 @pytest.mark.parametrize("quant", [synth.MXFP4_A4, synth.NVFP4_A4])
 def test_w4a4_without_activation_rounding_fails_the_comparison(quant):
     # a forward that skipped the FP4 rounding of the expert inputs (the W4A16
