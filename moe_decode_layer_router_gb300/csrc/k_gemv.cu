@@ -104,8 +104,11 @@ __device__ __noinline__ void router_route_tail(const FrontParams& p, int tb, int
     __threadfence();
     last_s = atomicAdd(p.route_ticket + tb, 1) == ctas_per_block - 1;
     if (last_s) {
-      p.route_ticket[tb] = 0;  // for the next launch
+      // the fence orders the other CTAs' logits (released before their
+      // tickets) before this CTA's reads; the reset after it (for the next
+      // launch) leaves the fence no store of its own to wait for
       __threadfence();
+      p.route_ticket[tb] = 0;
     }
   }
   __syncthreads();
@@ -128,8 +131,8 @@ __device__ __noinline__ void router_route_tail(const FrontParams& p, int tb, int
     __threadfence();
     last_s = atomicAdd(p.route_done, 1) == nblk - 1;
     if (last_s) {
-      *p.route_done = 0;
       __threadfence();
+      *p.route_done = 0;  // for the next launch
     }
   }
   __syncthreads();
@@ -564,19 +567,25 @@ __device__ __forceinline__ void gemv_cta(const CUtensorMap* tw, const FrontParam
         if (globaltimer() - t0 > kWaitLimitNs) break;
     }
   }
-  if constexpr (POOL) {
+  if (POOL && !p.norm_in_tail) {
+    // the norm is the next launch; this one completes only after the router
+    pdl_wait();
+    pdl_launch_dependents();
+  } else if constexpr (POOL) {
     // the CTA that stores a token block's last tile (atomic ticket, no
     // waiting) normalizes the block's rows: the barrier orders the CTA's y
     // stores before thread 0's fence and ticket; the last CTA's thread 0
-    // fences after the ticket, and the barrier orders its reads after that
+    // fences after the ticket (before its reset for the next launch, so the
+    // fence has no store of its own to wait for), and the barrier orders
+    // its reads after that
     __shared__ int last;
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
       last = (atomicAdd(p.norm_ticket + tbk, 1) == tiles - 1);
       if (last) {
-        p.norm_ticket[tbk] = 0;  // for the next launch
         __threadfence();
+        p.norm_ticket[tbk] = 0;
       }
     }
     __syncthreads();

@@ -61,8 +61,10 @@ struct FrontParams {
   int32_t* health;
   int M, K;
   int gemv_ctas;
-  // pooler only (skipped when h == nullptr): the last CTA of each token
-  // block applies the pre-expert RMSNorm to the block's rows of y
+  // pooler only (skipped when h == nullptr): with norm_in_tail the last CTA
+  // of each token block applies the pre-expert RMSNorm to the block's rows
+  // of y; without, launch_pool_norm follows (eight rows per CTA)
+  int norm_in_tail;
   const uint16_t* w_pre_norm;  // bf16 [M]
   int pre_norm, quant;
   int act4;             // W4A4 (1 MXFP4, 2 NVFP4): the norm writes h only (no operand);
@@ -72,7 +74,7 @@ struct FrontParams {
   uint8_t* h_op;        // f16 [rows, M] (FP4), e4m3 [rows, M] (FP8), W4A4: e2m1 codes [rows, M / 2]
   float* h_scale;       // [rows] (FP8)
   uint8_t* h_sf;        // W4A4: block scales [rows, M / 32] (UE8M0) or [rows, M / 16] (e4m3)
-  int32_t* norm_ticket; // [token blocks], zero between launches
+  int32_t* norm_ticket; // [token blocks], zero between launches (norm_in_tail)
   // router only (route_tail != 0): the last router CTA of each 8-token block
   // routes the block's rows, and the last block to finish builds the permute
   int route_tail;

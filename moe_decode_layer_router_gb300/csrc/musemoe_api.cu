@@ -322,6 +322,9 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   fp.h_sf = h->h_sf;
   fp.h_scale = h->h_scale;
   fp.norm_ticket = h->norm_ticket;
+  // one CTA normalizes a token block in the GEMV's tail only for 8 rows;
+  // wider blocks (16 or 32 rows) take the norm launch, eight rows per CTA
+  fp.norm_in_tail = ntf == 1;
   fp.route_tail = 1;
   fp.route_ticket = h->route_ticket;
   fp.route_done = h->route_done;
@@ -350,9 +353,10 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   before();
   if (!after(launch_router(fp, s, pdl), "router")) return MUSEMOE_ECUDA;
 
-  // 2. pooler GEMV (its weight copies overlap the router); the last CTA of
-  // each token block applies the pre-expert norm to the block's rows. Above
-  // 32 rows: a dense tensor-core GEMM, then the norm as its own launch
+  // 2. pooler GEMV (its weight copies overlap the router); for 8 rows the
+  // last CTA applies the pre-expert norm to them, for 16 or 32 rows the norm
+  // is its own launch. Above 32 rows: a dense tensor-core GEMM, then the
+  // norm launch
   const bool dense = use_dense_tc(rows);
   if (dense) {
     DenseParams dp{};
@@ -375,6 +379,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
   } else {
     before();
     cudaError_t r = launch_front(fp, ntf, s, pdl);
+    if (r == cudaSuccess && !fp.norm_in_tail) r = launch_pool_norm(fp, s, pdl);
     if (r == cudaSuccess && h->act4) r = launch_h_fp4(h, rows, s, pdl);
     if (!after(r, "pool")) return MUSEMOE_ECUDA;
   }
