@@ -198,9 +198,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const uint32_t bar = smem_u32(&full_b[st]);
         const uint32_t dst = base + st * kDStage;
         mbar_expect_tx(bar, kDStageA + box_rows * 128);  // the copy writes the whole box
-        // the weights never depend on the previous kernel; the token rows do
+        // the weights never depend on the previous kernel; the token rows
+        // do, unless they are final before the launch (x_ready)
         tma_load_2d(dst, &tw, (k0 + n) * kDK, tile * kDM, bar, pol_w);
-        if (!waited) {
+        if (!waited && !p.x_ready) {
           pdl_wait();
           waited = true;
         }
@@ -208,7 +209,6 @@ __global__ void __launch_bounds__(kDThreads, 1)
         issued = n + 1;
         DTL(0, tlc, 1);
       }
-      if (!waited) pdl_wait();
       for (int st = 0; st < kDStages && st < issued; ++st) {
         const int last = st + ((issued - 1 - st) / kDStages) * kDStages;
         const unsigned long long t0 = globaltimer();
@@ -249,7 +249,6 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 0..3), part 1: the accumulator is complete ----------------
-    pdl_wait();  // Y's previous readers are done
     if (nk > 0) {
       have = __all_sync(0xffffffffu, wait(&accfull, 0u));
       if (!have && lane == 0) fail();
@@ -301,6 +300,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
   cluster_sync();
   if (tid == 0) DTL(2, etl, 3);
 
+  // Y is stored, and the launch completes, only after the previous kernel
+  // (the pooler's: the router, whose routing the expert kernels read before
+  // their own wait once this launch and the norm after it are done)
+  pdl_wait();
   {
     // part 3: this CTA's rows, the C slots added in rank order, by every warp
     // of the CTA. A warp takes 8 rows x 4 token quads at a time: each lane

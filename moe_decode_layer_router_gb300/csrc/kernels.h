@@ -97,6 +97,8 @@ struct DenseParams {
   const uint16_t* w;  // bf16 [M, K]
   float* y;           // fp32 [rows, M]
   int rows, M, K;
+  int x_ready;  // x is final when the launch starts (the pooler's input, which
+                // the router before it only reads): its copies do not wait
   int32_t* health;
   int grid;  // CTAs the launch may use (the SMs)
 };

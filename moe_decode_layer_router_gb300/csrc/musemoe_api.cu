@@ -366,6 +366,7 @@ musemoe_status launch_chain(musemoe_handle* h, const musemoe_weights* w, const u
     dp.rows = rows;
     dp.M = d.pooled;
     dp.K = d.hidden;
+    dp.x_ready = 1;  // x is the router's input, final before the router's launch
     dp.health = h->health;
     dp.grid = h->sms;
     // one "pool" stage of the taps' events: the GEMM and the norm launch
