@@ -186,8 +186,10 @@ const char *musemoe_last_error(const musemoe_handle *handle);
 size_t musemoe_workspace_bytes(const musemoe_dims *dims, int32_t quant);
 
 /* Stages one musemoe_forward runs for this quant (for taps->events): one
- * kernel each, except that above 32 rows the "pool" stage is two launches
- * (the dense tensor-core GEMM, then the pre-expert norm), timed together. */
+ * kernel each, except that above 8 rows the "pool" stage is two launches
+ * (the pooler GEMV, or above 32 rows the dense tensor-core GEMM, then the
+ * pre-expert norm), and for W4A4 one more (h rounded to FP4), timed
+ * together. */
 int32_t musemoe_num_kernels(int32_t quant);
 /* Name of stage i of the forward ("router", "pool", "w13", ...). */
 const char *musemoe_kernel_name(int32_t quant, int32_t i);
