@@ -90,6 +90,18 @@ def test_ragged_rows(rows):
         run.close()
 
 
+@pytest.mark.parametrize("quant,rows", [(synth.MXFP4, 24), (synth.FP8, 12), (synth.MXFP4_A4, 20),
+                                        (synth.NVFP4_A4, 31)])
+def test_wide_pooler_token_blocks_every_form(quant, rows):
+    # 9..32 rows: the pooler GEMV takes 16- or 32-row token blocks and the
+    # pre-expert norm runs as its own launch (8 rows per CTA, a ragged last
+    # CTA), before the FP8 or W4A4 rounding of h
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], rows=rows, quant=quant, seed=12)
+    w = synth.layer_tensors(cfg)
+    x, st = synth.activations(cfg)
+    _compare_block(cfg, w, x, st)
+
+
 @pytest.mark.parametrize("top_k", [1, 16])
 def test_top_k_extremes(top_k):
     cfg = dataclasses.replace(synth.CONFIGS["tiny"], top_k=top_k, seed=6)
