@@ -21,8 +21,11 @@
 // rows [ceil(128 r / C), ceil(128 (r + 1) / C))) through distributed shared
 // memory; after a second barrier each owner adds the C slots of its rows in
 // rank order and stores Y (8 rows x 4 tokens per warp step), so results do
-// not depend on scheduling. Rows past
-// the end are zero-filled by the tensor copy and never stored.
+// not depend on scheduling. Rows past the end are zero-filled by the tensor
+// copy and never stored. The weight copies never wait for the previous
+// kernel; the token rows' copies do unless x_ready (the pooler's input, final
+// before the router launches), and every thread waits before it stores Y, so
+// the launch completes only after its predecessor.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
