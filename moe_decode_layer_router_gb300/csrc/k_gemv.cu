@@ -681,11 +681,6 @@ cudaError_t launch_t(const FrontParams& p, cudaStream_t s, bool pdl) {
 int front_gemv_ctas(int M, int rows, int nt) {
   return ((M + kGTileRows - 1) / kGTileRows) * ((rows + 8 * nt - 1) / (8 * nt));
 }
-int front_ctas_per_sm(int K, int nt) {
-  const size_t per = g_smem_bytes(K, nt);
-  const size_t budget = 227 * 1024;
-  return (int)std::max<size_t>(1, std::min<size_t>(budget / per, 2048 / kGThreads));
-}
 int front_max_k() { return kGMaxK; }
 
 cudaError_t launch_pool_norm(const FrontParams& p, cudaStream_t s, bool pdl) {

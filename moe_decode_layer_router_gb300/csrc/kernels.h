@@ -105,7 +105,6 @@ struct DenseParams {
 cudaError_t launch_dense_tc(const DenseParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const FrontParams& p, cudaStream_t s, bool pdl);          // router
 int front_gemv_ctas(int M, int rows, int nt);
-int front_ctas_per_sm(int K, int nt);
 int front_max_k();
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
